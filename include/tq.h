@@ -1,0 +1,223 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) rotated Lloyd-Max KV-cache codec and
+ * the fused decode attention that reads it.
+ *
+ * The codec stores each K/V head vector x (head_dim d, bf16) as
+ *   n = ||x|| (f32);  y = H (s . x/n) / sqrt(d)   (s: seeded +-1 signs, H:
+ *   Sylvester Walsh-Hadamard);  code_j = index of the nearest of 2^b Gaussian
+ *   Lloyd-Max centroids for N(0, 1/d);  codes bit-packed; optionally the
+ *   coordinates with |y_j| > T/sqrt(d) kept as (u16 index, bf16 value).
+ * Sources: "v1.3 PPL on vLLM" (LLM-KV--Cache-compress PR #15), M4 Phase A/B and
+ * M5 commits (rotate = H.D.x, per-row scale, Lloyd-Max argmin, outlier
+ * overrides applied before the inverse WHT); larql PR #196, turbo-quant note
+ * (one N(0,1) table per bit width scaled by 1/sqrt(d), append-only encode);
+ * "feat(v4): TurboQuant KV storage for DeepSeek-V4" (arc PR #98), "What landed"
+ * (packed records with the norm inside, 260 B/token at d = 512, b = 4),
+ * "Eviction is chunked, on purpose" (EVICT_CHUNK = 128; tail bound
+ * window + max(t_q-1, margin) + chunk), "Also: two silently-ignored kernel
+ * parameters" (query stride honoured; no silent no-op on an unsupported head
+ * dim).
+ *
+ * Conventions for every call:
+ *  - Pointers named d_* or documented "device" are device addresses; the
+ *    caller owns every buffer (inputs, outputs, workspaces).  The library
+ *    allocates no memory and keeps no state between calls.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on that stream unless stated otherwise.
+ *  - Arguments are validated on the host before anything is launched; on an
+ *    error nothing is launched and the status says why.  A launch failure
+ *    returns TQ_ERR_CUDA.  There is no CPU fallback and no silent no-op.
+ *  - bf16 data are raw 16-bit patterns; f32 little-endian.
+ *
+ * Record format (one record = 128 consecutive tokens of one stream):
+ *   offset 0           codes: 128 rows of d*b/8 bytes; row i = token slot i;
+ *                      code j occupies bits [j*b, j*b + b) of the row's
+ *                      little-endian bitstream (bit k = bit k%8 of byte k/8)
+ *   128*d*b/8          norms: 128 x f32
+ *   when outlier_T != 0:
+ *   + 512              ocount: 128 x u8, entries stored for each slot
+ *   + 128              entries: outlier_cap x {u16 index, u16 bf16 value},
+ *                      in (slot, index) order; a slot stores at most 255 and
+ *                      a record at most outlier_cap; the rest keep their code
+ *   The size is a multiple of 16 bytes (tq_record_bytes).  Slots not yet
+ *   written (a partially filled last record) are unspecified.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or stride */
+  TQ_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128,256,512}, bits not in 1..4, ... */
+  TQ_ERR_WORKSPACE = 3,   /* workspace or scratch smaller than required */
+  TQ_ERR_CUDA = 4         /* a CUDA call or launch failed */
+} tq_status;
+
+#define TQ_CHUNK 128
+
+/* Human-readable name of a status code (static storage). */
+const char* tq_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int tq_version(void);
+
+/*
+ * Codec description, passed by pointer and read on the host at every call.
+ * Filled by tq_make_codebook; plain data, copy freely.
+ */
+typedef struct {
+  int32_t head_dim;       /* d: 64, 128, 256 or 512 */
+  int32_t bits;           /* b: 1..4 */
+  uint64_t sign_seed;     /* seed of the SplitMix64 sign diagonal */
+  float outlier_T;        /* 0: no outlier section; > 0: keep |y_j| > T/sqrt(d) (may be +inf) */
+  int32_t outlier_cap;    /* outlier entries per record (multiple of 4) */
+  float centroids[16];    /* 2^b ascending f32 centroids of N(0, 1/d) */
+  float boundaries[15];   /* 2^b - 1 f32 midpoints of consecutive centroids */
+  uint32_t sign_bits[16]; /* bit j%32 of word j/32 set <=> s_j = -1 */
+} tq_codec;
+
+/* Device scratch tq_make_codebook needs (bytes). */
+size_t tq_codebook_scratch_bytes(void);
+
+/*
+ * a1/a2: Gaussian Lloyd-Max table and sign diagonal.  Runs the 1-D Lloyd
+ * iteration t_k = (c_k + c_{k+1})/2, c_k = E[X | t_{k-1} < X <= t_k] on the
+ * N(0,1) density in fp64 on the device until no centroid moves by more than
+ * 1e-14, scales by 1/sqrt(d), rounds to f32 and derives the f32 midpoints;
+ * draws the signs s_j from SplitMix64(sign_seed) (top bit set -> -1).
+ *   d_scratch: device buffer of tq_codebook_scratch_bytes(), 16-byte aligned.
+ *   outlier_cap: 0 selects 4*ceil(0.08*128*d/4) (8% of a record's coordinates).
+ *   out: host; filled on success.  mse_out: host, nullable: E[(X-Q(X))^2] of
+ *   the unit-variance table.
+ * SYNCHRONISES `stream` (the table is returned in host memory).
+ */
+tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float outlier_T,
+                           int outlier_cap, void* d_scratch, size_t scratch_bytes, tq_codec* out,
+                           double* mse_out, void* stream);
+
+/* Bytes of one 128-token record of this codec; 0 if the codec is invalid. */
+size_t tq_record_bytes(const tq_codec* codec);
+
+/*
+ * a3: encode.  n_groups independent streams of n_vec bf16 vectors each;
+ * vector i of group g is read at src + g*src_group_stride + i*src_vec_stride
+ * (elements) and written as token first_vec + i of the record array at
+ * dst + g*dst_group_stride (bytes).
+ *   src: device, 16-byte aligned; strides multiples of 8 elements.
+ *   dst: device, 16-byte aligned; dst_group_stride multiple of 16.
+ *   With outliers, first_vec must be a multiple of 128 (a record's outlier
+ *   section is written whole by one call).  Encoding is append-only: records
+ *   and slots outside the written range are not touched.
+ */
+tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, int64_t n_vec,
+                    int64_t src_vec_stride, int64_t src_group_stride, void* dst,
+                    int64_t dst_group_stride, int64_t first_vec, void* stream);
+
+/*
+ * a5: decode.  Tokens [first_vec, first_vec + n_vec) of each group's record
+ * array (at src + g*src_group_stride bytes) to f32 vectors
+ *   xhat = n * s . H(yhat) / sqrt(d),  yhat_j = centroid[code_j], replaced by
+ *   the stored value at outlier coordinates,
+ * written at dst + g*dst_group_stride + i*dst_vec_stride (elements).
+ *   src: device, 16-byte aligned.  dst: device, 16-byte aligned, strides
+ *   multiples of 4 elements.
+ */
+tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, int64_t n_vec,
+                    int64_t src_group_stride, int64_t first_vec, float* dst,
+                    int64_t dst_vec_stride, int64_t dst_group_stride, void* stream);
+
+/*
+ * a4: chunked eviction from dense bf16 ring-buffer tails into records, for
+ * n_layers x batch x n_kv_heads streams in one launch (plus one small
+ * bookkeeping launch), with every decision taken on the device (no host
+ * synchronisation).  For each (layer, batch) with counters
+ *   len = tail_len[l][b], start = tail_start[l][b], n = n_chunks[l][b]:
+ *   floor = window + max(t_q - 1, margin);  k = len >= floor + 128 ?
+ *   min((len - floor) / 128, max_evict) : 0;
+ * tokens at ring slots (start + e*128 + i) % tail_cap, e < k, i < 128, are
+ * encoded into record n + e of every kv head, then n += k, start advances by
+ * 128k (mod tail_cap), len -= 128k.  Records that would reach rec_cap are not
+ * written and the counters of that (layer, batch) are left unchanged.
+ */
+typedef struct {
+  int32_t n_layers, batch, n_kv_heads;
+  /* records: layer l, batch b, head h, record r at
+   *   k_rec + l*k_rec_layer_stride + ((b*n_kv_heads + h)*rec_cap + r)*record_bytes */
+  void* k_rec;
+  void* v_rec; /* may equal k_rec with v codec == k codec: keys and values share records */
+  int64_t k_rec_layer_stride, v_rec_layer_stride; /* bytes, multiples of 16 */
+  int32_t rec_cap;
+  /* tails: bf16 [L][B][Hkv][tail_cap][d] at k_tail + l*tail_layer_stride (elements) */
+  const void* k_tail;
+  const void* v_tail;
+  int64_t tail_layer_stride;
+  int32_t tail_cap;
+  int32_t* n_chunks;   /* device [L][B] */
+  int32_t* tail_start; /* device [L][B] */
+  int32_t* tail_len;   /* device [L][B] */
+  int32_t window, margin, t_q;
+  int32_t max_evict;   /* upper bound on records written per (layer, batch) per call */
+} tq_evict_args;
+
+tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_evict_args* args,
+                   void* stream);
+
+/*
+ * a6-a10: fused decode attention for one group of layers sharing codecs and
+ * geometry.  For layer l, batch b, query head h (kv head h / (Hq/Hkv)):
+ *   out = sum_i softmax_i(scale * q . k_i) v_i  over the layer's compressed
+ * tokens (records 0..n_chunks-1, scored in the rotated basis against
+ * q~ = H(s_k . q)/sqrt(d) from a shared-memory centroid table, values
+ * accumulated as sum p_i n_i yhat_i and brought back by one inverse
+ * transform) and its dense bf16 tokens (ring slots (tail_start + t) % tail_cap,
+ * t < tail_len), with split-K over context and a merge of the splits.
+ * Layers without records (k_codec == NULL) are dense bf16 layers: set
+ * k_rec = v_rec = NULL, n_chunks = tail_start = NULL and pass the whole cache
+ * as the "tail" (tail_len = context length).
+ */
+typedef struct {
+  int32_t n_layers, batch, n_q_heads, n_kv_heads, head_dim;
+  float scale; /* softmax scale applied to q . k */
+  /* q: bf16, element (l, b, h, j) at q + l*q_layer_stride + b*q_batch_stride + h*d + j */
+  const void* q;
+  int64_t q_layer_stride, q_batch_stride; /* elements, multiples of 8 */
+  /* out: f32 [L][B][Hq][d], contiguous, 16-byte aligned */
+  float* out;
+  const void* k_rec; /* records as in tq_evict_args; NULL for dense layers */
+  const void* v_rec;
+  int64_t k_rec_layer_stride, v_rec_layer_stride;
+  int32_t rec_cap;
+  const void* k_tail; /* bf16 [L][B][Hkv][tail_cap][d]; NULL when there is no dense part */
+  const void* v_tail;
+  int64_t tail_layer_stride; /* elements */
+  int32_t tail_cap;
+  const int32_t* n_chunks;   /* device [L][B]; NULL = 0 */
+  const int32_t* tail_start; /* device [L][B]; NULL = 0 */
+  const int32_t* tail_len;   /* device [L][B]; NULL = 0 */
+  int32_t max_chunks;        /* host upper bound of n_chunks (sizes the grid) */
+  int32_t max_tail;          /* host upper bound of tail_len */
+  int32_t splits;            /* splits per (layer, batch, kv head); 0 = automatic */
+} tq_attn_args;
+
+/* Workspace bytes tq_decode_attn needs for these arguments (0 on invalid args). */
+size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k_codec,
+                                     const tq_codec* v_codec);
+
+/* workspace: device, 256-byte aligned, >= tq_decode_attn_workspace_size bytes.
+ * Its contents need no initialisation and are garbage afterwards.  An empty
+ * context (no compressed and no dense token) yields a zero output row. */
+tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
+                         const tq_codec* v_codec, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H_ */

@@ -1,0 +1,465 @@
+// The C ABI (include/tq.h): host-side validation, codec resolution, split
+// planning and kernel dispatch.  Every argument is checked before anything is
+// launched; there is no CPU fallback and no silent no-op (arc PR #98, "Also:
+// two silently-ignored kernel parameters": an unsupported head dim must fail,
+// not return early leaving the output uninitialised).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/tq.h"
+#include "tq_params.h"
+
+using namespace tq;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool dim_ok(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+
+int default_cap(int d) { return 4 * ((8 * TQ_CHUNK * d + 399) / 400); }
+
+// record layout: codes, norms, [counts, entries]
+int record_layout(int d, int bits, bool outl, int cap, int* off_norm, int* off_count, int* off_ent) {
+  const int codes = TQ_CHUNK * d * bits / 8;
+  *off_norm = codes;
+  *off_count = codes + 4 * TQ_CHUNK;
+  *off_ent = *off_count + TQ_CHUNK;
+  return outl ? *off_ent + 4 * cap : *off_count;
+}
+
+tq_status resolve_codec(const tq_codec* c, CodecDev* o) {
+  if (!c) return TQ_ERR_INVALID_ARG;
+  const int d = c->head_dim, b = c->bits;
+  if (!dim_ok(d) || b < 1 || b > 4) return TQ_ERR_UNSUPPORTED;
+  if (!(c->outlier_T >= 0.f)) return TQ_ERR_INVALID_ARG;  // negative or NaN
+  const bool outl = c->outlier_T != 0.f;
+  if (outl && (c->outlier_cap <= 0 || c->outlier_cap % 4 != 0 || c->outlier_cap > 65536))
+    return TQ_ERR_INVALID_ARG;
+  const int K = 1 << b;
+  for (int k = 0; k + 1 < K; ++k) {
+    if (!(c->centroids[k] < c->boundaries[k] && c->boundaries[k] < c->centroids[k + 1]))
+      return TQ_ERR_INVALID_ARG;  // not ascending / boundaries not between centroids
+    if (c->boundaries[k] != -c->boundaries[K - 2 - k]) return TQ_ERR_UNSUPPORTED;  // asymmetric table
+  }
+  std::memset(o, 0, sizeof(*o));
+  o->d = d;
+  o->bits = b;
+  o->has_outl = outl ? 1 : 0;
+  o->cap = outl ? c->outlier_cap : 0;
+  o->rec_bytes = record_layout(d, b, outl, o->cap, &o->off_norm, &o->off_count, &o->off_entries);
+  o->thr_out = outl ? (float)((double)c->outlier_T / std::sqrt((double)d)) : INFINITY;
+  o->inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  o->sqrt_d = (float)std::sqrt((double)d);
+  for (int k = 0; k < 16; ++k) o->centroids[k] = c->centroids[k & (K - 1)];
+  for (int k = 0; k < 15; ++k) o->boundaries[k] = k + 1 < K ? c->boundaries[k] : 0.f;
+  for (int w = 0; w < 16; ++w) o->signs[w] = w < d / 32 ? c->sign_bits[w] : 0u;
+  return TQ_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+int max_dyn_smem() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 227 * 1024;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 227 * 1024;
+  return n;
+}
+
+// ----------------------------------------------------------------- attention plan
+struct Plan {
+  int D, G, GT, n_hg, S, Sc, cps, tps;
+  int64_t rows;
+  size_t ws_acc_bytes, ws_bytes;
+  CodecDev kc, vc;
+  bool has_rec, has_tail, shared;
+};
+
+tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec* vcod, Plan* pl) {
+  if (!a) return TQ_ERR_INVALID_ARG;
+  std::memset(pl, 0, sizeof(*pl));
+  const int D = a->head_dim;
+  if (!dim_ok(D)) return TQ_ERR_UNSUPPORTED;
+  if (a->n_layers <= 0 || a->n_layers > 65535 || a->batch <= 0 || a->n_q_heads <= 0 ||
+      a->n_kv_heads <= 0 || a->n_q_heads % a->n_kv_heads != 0)
+    return TQ_ERR_INVALID_ARG;
+  if (!a->q || !a->out || !aligned(a->q, 16) || !aligned(a->out, 16)) return TQ_ERR_INVALID_ARG;
+  if (a->q_layer_stride < 0 || a->q_batch_stride < 0 || a->q_layer_stride % 8 || a->q_batch_stride % 8)
+    return TQ_ERR_INVALID_ARG;
+  if (!(std::isfinite(a->scale))) return TQ_ERR_INVALID_ARG;
+  if (a->max_chunks < 0 || a->max_tail < 0 || a->splits < 0) return TQ_ERR_INVALID_ARG;
+  pl->D = D;
+  pl->G = a->n_q_heads / a->n_kv_heads;
+  const int cand[5] = {8, 6, 4, 2, 1};
+  for (int c : cand)
+    if (pl->G % c == 0) { pl->GT = c; break; }
+  pl->n_hg = pl->G / pl->GT;
+  if ((int64_t)a->batch * a->n_kv_heads * pl->n_hg > 65535) return TQ_ERR_UNSUPPORTED;
+
+  pl->has_rec = a->k_rec != nullptr;
+  if (pl->has_rec) {
+    if (!kcod || !vcod || !a->v_rec) return TQ_ERR_INVALID_ARG;
+    tq_status st = resolve_codec(kcod, &pl->kc);
+    if (st != TQ_OK) return st;
+    st = resolve_codec(vcod, &pl->vc);
+    if (st != TQ_OK) return st;
+    if (pl->kc.d != D || pl->vc.d != D) return TQ_ERR_INVALID_ARG;
+    pl->shared = a->v_rec == a->k_rec;
+    if (pl->shared && std::memcmp(kcod, vcod, sizeof(tq_codec)) != 0) return TQ_ERR_INVALID_ARG;
+    if (!aligned(a->k_rec, 16) || !aligned(a->v_rec, 16) || a->k_rec_layer_stride % 16 ||
+        a->v_rec_layer_stride % 16 || a->rec_cap <= 0 || a->max_chunks > a->rec_cap || !a->n_chunks)
+      return TQ_ERR_INVALID_ARG;
+  } else {
+    if (a->v_rec || a->n_chunks) return TQ_ERR_INVALID_ARG;
+    if (vcod) {  // the merge uses the value codec's signs only for compressed splits
+      tq_status st = resolve_codec(vcod, &pl->vc);
+      if (st != TQ_OK) return st;
+    }
+  }
+  pl->has_tail = a->k_tail != nullptr;
+  if (pl->has_tail) {
+    if (!a->v_tail || !aligned(a->k_tail, 16) || !aligned(a->v_tail, 16) || a->tail_layer_stride % 8 ||
+        a->tail_cap <= 0 || a->max_tail > a->tail_cap || !a->tail_len)
+      return TQ_ERR_INVALID_ARG;
+  } else if (a->v_tail || a->tail_len || a->tail_start) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  const int64_t comp_tiles = pl->has_rec ? a->max_chunks : 0;
+  const int TT = 4096 / D;
+  const int64_t max_tail = pl->has_tail ? a->max_tail : 0;
+  const int64_t tail_tiles = cdiv(max_tail, TT);
+  const int64_t units = (int64_t)a->n_layers * a->batch * a->n_kv_heads * pl->n_hg;
+  int64_t want = a->splits > 0 ? a->splits : std::max<int64_t>(1, cdiv(4LL * num_sms(), units));
+  want = std::min<int64_t>(want, 1024);
+  const int64_t tok_c = comp_tiles * TQ_CHUNK, tok_t = max_tail;
+  int64_t Sc = 0, St = 0;
+  if (comp_tiles > 0) {
+    Sc = tok_t > 0 ? (want * tok_c + (tok_c + tok_t) / 2) / (tok_c + tok_t) : want;
+    Sc = std::max<int64_t>(1, std::min(Sc, comp_tiles));
+  }
+  if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want - Sc, tail_tiles));
+  int64_t cps = 1, tps = TT;
+  if (Sc > 0) {
+    cps = cdiv(comp_tiles, Sc);
+    Sc = cdiv(comp_tiles, cps);
+  }
+  if (St > 0) {
+    tps = TT * cdiv(tail_tiles, St);
+    St = cdiv(max_tail, tps);
+  }
+  if (Sc + St == 0) St = 1;  // empty context: one empty split, zero output
+  pl->Sc = (int)Sc;
+  pl->S = (int)(Sc + St);
+  pl->cps = (int)cps;
+  pl->tps = (int)tps;
+  pl->rows = (int64_t)a->n_layers * a->batch * a->n_q_heads;
+  pl->ws_acc_bytes = (size_t)(((pl->rows * pl->S * D * 4) + 255) / 256 * 256);
+  pl->ws_bytes = pl->ws_acc_bytes + (size_t)pl->rows * pl->S * 2 * 4;
+  return TQ_OK;
+}
+
+}  // namespace
+
+namespace tq {
+
+void attn_smem_layout(AttnParams& p, int D, int GT) {
+  const int GTP = GT == 6 ? 8 : GT;
+  const int QS = 32 * GTP + (GTP < 4 ? GTP : 4);
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  int off = 0;
+  p.sm_q = off;
+  off = al(off + (D / 32) * QS * 4, 16);
+  p.sm_lut = off;
+  off += 32 * 4;
+  p.sm_red = off;
+  off += 2 * 4 * GTP * 4;
+  p.sm_logit = off;
+  off = al(off + TQ_CHUNK * GTP * 4, 16);
+  p.sm_corr = off;
+  off = al(off + (p.vout ? D * GTP * 4 : 0), 16);
+  const bool anyout = p.kout || p.vout;
+  p.sm_pre = off;
+  off = al(off + (anyout ? 2 * 2 * 129 * 4 : 0), 16);
+  const int vcap = p.shared_kv ? p.kcap : p.vcap;
+  p.sm_slot = off;
+  off = al(off + (p.vout ? 2 * vcap : 0), 16);
+  p.sm_ent_stage = (p.kout ? p.kcap * 4 : 0) + (p.vout && !p.shared_kv ? p.vcap * 4 : 0);
+  p.sm_ent = off;
+  off = al(off + 2 * p.sm_ent_stage, 128);
+  int stage = p.krec ? p.k_main + (p.shared_kv ? 0 : p.v_main) : 0;
+  if (p.ktail) stage = std::max(stage, 2 * (4096 / D) * D * 2);
+  const int part = (128 / (D / 4)) * D * GTP * 4;  // token-lane partials at the end
+  stage = std::max(stage, (part + 2) / 3);
+  p.sm_stage = al(stage, 128);
+  p.sm_main = off;
+  off += 3 * p.sm_stage;
+  p.sm_total = off;
+}
+
+}  // namespace tq
+
+extern "C" {
+
+const char* tq_status_string(int status) {
+  switch (status) {
+    case TQ_OK: return "TQ_OK";
+    case TQ_ERR_INVALID_ARG: return "TQ_ERR_INVALID_ARG: null, misaligned or out-of-range argument";
+    case TQ_ERR_UNSUPPORTED: return "TQ_ERR_UNSUPPORTED: head_dim/bits/table/geometry not supported";
+    case TQ_ERR_WORKSPACE: return "TQ_ERR_WORKSPACE: workspace or scratch too small";
+    case TQ_ERR_CUDA: return "TQ_ERR_CUDA: a CUDA call or kernel launch failed";
+    default: return "unknown tq_status";
+  }
+}
+
+int tq_version(void) { return kVersion; }
+
+size_t tq_codebook_scratch_bytes(void) { return sizeof(CodebookOut); }
+
+tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float outlier_T, int outlier_cap,
+                           void* d_scratch, size_t scratch_bytes, tq_codec* out, double* mse_out,
+                           void* stream) {
+  if (bits < 1 || bits > 4 || !dim_ok(head_dim)) return TQ_ERR_UNSUPPORTED;
+  if (!out || !d_scratch || !aligned(d_scratch, 16)) return TQ_ERR_INVALID_ARG;
+  if (!(outlier_T >= 0.f) || outlier_cap < 0 || outlier_cap % 4 != 0 || outlier_cap > 65536)
+    return TQ_ERR_INVALID_ARG;
+  if (scratch_bytes < sizeof(CodebookOut)) return TQ_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_codebook(bits, head_dim, sign_seed, d_scratch, s) != cudaSuccess) return TQ_ERR_CUDA;
+  CodebookOut h;
+  if (cudaMemcpyAsync(&h, d_scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
+  std::memset(out, 0, sizeof(*out));
+  out->head_dim = head_dim;
+  out->bits = bits;
+  out->sign_seed = sign_seed;
+  out->outlier_T = outlier_T;
+  out->outlier_cap = outlier_cap ? outlier_cap : default_cap(head_dim);
+  const int K = 1 << bits;
+  for (int k = 0; k < K; ++k) out->centroids[k] = h.c[k];
+  for (int k = 0; k + 1 < K; ++k) out->boundaries[k] = h.t[k];
+  for (int w = 0; w < head_dim / 32; ++w) out->sign_bits[w] = h.signs[w];
+  if (mse_out) *mse_out = h.mse;
+  return TQ_OK;
+}
+
+size_t tq_record_bytes(const tq_codec* codec) {
+  CodecDev c;
+  if (resolve_codec(codec, &c) != TQ_OK) return 0;
+  return (size_t)c.rec_bytes;
+}
+
+tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, int64_t n_vec,
+                    int64_t src_vec_stride, int64_t src_group_stride, void* dst, int64_t dst_group_stride,
+                    int64_t first_vec, void* stream) {
+  EncodeParams p;
+  tq_status st = resolve_codec(codec, &p.c);
+  if (st != TQ_OK) return st;
+  if (n_groups < 0 || n_vec < 0 || first_vec < 0) return TQ_ERR_INVALID_ARG;
+  if (n_groups == 0 || n_vec == 0) return TQ_OK;
+  if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16)) return TQ_ERR_INVALID_ARG;
+  if (src_vec_stride < p.c.d || src_vec_stride % 8 || src_group_stride < 0 || src_group_stride % 8 ||
+      dst_group_stride < 0 || dst_group_stride % 16)
+    return TQ_ERR_INVALID_ARG;
+  if (p.c.has_outl && first_vec % TQ_CHUNK) return TQ_ERR_INVALID_ARG;
+  p.src = (const uint16_t*)src;
+  p.src_vs = src_vec_stride;
+  p.src_gs = src_group_stride;
+  p.dst = (uint8_t*)dst;
+  p.dst_gs = dst_group_stride;
+  p.n_groups = n_groups;
+  p.n_vec = n_vec;
+  p.first_vec = first_vec;
+  p.first_chunk = first_vec / TQ_CHUNK;
+  p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
+  const int64_t tasks = n_groups * p.chunks_per_group;
+  const int grid = (int)std::min<int64_t>(tasks, 8LL * num_sms());
+  return launch_encode(p, grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, int64_t n_vec,
+                    int64_t src_group_stride, int64_t first_vec, float* dst, int64_t dst_vec_stride,
+                    int64_t dst_group_stride, void* stream) {
+  DecodeParams p;
+  tq_status st = resolve_codec(codec, &p.c);
+  if (st != TQ_OK) return st;
+  if (n_groups < 0 || n_vec < 0 || first_vec < 0) return TQ_ERR_INVALID_ARG;
+  if (n_groups == 0 || n_vec == 0) return TQ_OK;
+  if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16)) return TQ_ERR_INVALID_ARG;
+  if (src_group_stride < 0 || src_group_stride % 16 || dst_vec_stride < p.c.d || dst_vec_stride % 4 ||
+      dst_group_stride < 0 || dst_group_stride % 4)
+    return TQ_ERR_INVALID_ARG;
+  p.src = (const uint8_t*)src;
+  p.src_gs = src_group_stride;
+  p.dst = dst;
+  p.dst_vs = dst_vec_stride;
+  p.dst_gs = dst_group_stride;
+  p.n_groups = n_groups;
+  p.n_vec = n_vec;
+  p.first_vec = first_vec;
+  p.first_chunk = first_vec / TQ_CHUNK;
+  p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
+  const int64_t tasks = n_groups * p.chunks_per_group;
+  const int grid = (int)std::min<int64_t>(tasks, 8LL * num_sms());
+  return launch_decode(p, grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_evict_args* a, void* stream) {
+  if (!a) return TQ_ERR_INVALID_ARG;
+  CodecDev kc, vc;
+  tq_status st = resolve_codec(k_codec, &kc);
+  if (st != TQ_OK) return st;
+  const bool shared = a->v_rec == a->k_rec;
+  if (shared) {
+    if (v_codec && std::memcmp(k_codec, v_codec, sizeof(tq_codec)) != 0) return TQ_ERR_INVALID_ARG;
+    vc = kc;
+  } else {
+    st = resolve_codec(v_codec, &vc);
+    if (st != TQ_OK) return st;
+  }
+  const int D = kc.d;
+  if (vc.d != D) return TQ_ERR_INVALID_ARG;
+  if (a->n_layers <= 0 || a->n_layers > 65535 || a->batch <= 0 || a->n_kv_heads <= 0 ||
+      (int64_t)a->batch * a->n_kv_heads > 65535 || a->max_evict <= 0 || a->max_evict > 65535)
+    return TQ_ERR_INVALID_ARG;
+  if (!a->k_rec || !a->v_rec || !a->k_tail || !a->v_tail || !a->n_chunks || !a->tail_start || !a->tail_len)
+    return TQ_ERR_INVALID_ARG;
+  if (!aligned(a->k_rec, 16) || !aligned(a->v_rec, 16) || !aligned(a->k_tail, 16) || !aligned(a->v_tail, 16) ||
+      a->k_rec_layer_stride % 16 || a->v_rec_layer_stride % 16 || a->tail_layer_stride % 8)
+    return TQ_ERR_INVALID_ARG;
+  if (a->rec_cap <= 0 || a->tail_cap <= 0 || a->window < 0 || a->margin < 0 || a->t_q < 1)
+    return TQ_ERR_INVALID_ARG;
+  if (kc.has_outl || vc.has_outl) {
+    // records of outlier codecs are always written whole, so nothing more to check
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int floor_ = a->window + std::max(a->t_q - 1, a->margin);
+  EvictParams p;
+  p.rec_cap = a->rec_cap;
+  p.tail_ls = a->tail_layer_stride;
+  p.tail_cap = a->tail_cap;
+  p.n_chunks = a->n_chunks;
+  p.tail_start = a->tail_start;
+  p.tail_len = a->tail_len;
+  p.L = a->n_layers;
+  p.B = a->batch;
+  p.Hkv = a->n_kv_heads;
+  p.floor_ = floor_;
+  p.max_evict = a->max_evict;
+  p.c = kc;
+  p.rec = (uint8_t*)a->k_rec;
+  p.rec_ls = a->k_rec_layer_stride;
+  p.tail = (const uint16_t*)a->k_tail;
+  if (launch_evict(p, s) != cudaSuccess) return TQ_ERR_CUDA;
+  if (!shared) {
+    p.c = vc;
+    p.rec = (uint8_t*)a->v_rec;
+    p.rec_ls = a->v_rec_layer_stride;
+    p.tail = (const uint16_t*)a->v_tail;
+    if (launch_evict(p, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  EvictCommitParams cp;
+  cp.n_chunks = a->n_chunks;
+  cp.tail_start = a->tail_start;
+  cp.tail_len = a->tail_len;
+  cp.LB = a->n_layers * a->batch;
+  cp.floor_ = floor_;
+  cp.max_evict = a->max_evict;
+  cp.tail_cap = a->tail_cap;
+  cp.rec_cap = a->rec_cap;
+  return launch_evict_commit(cp, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k_codec,
+                                     const tq_codec* v_codec) {
+  Plan pl;
+  if (make_plan(args, k_codec, v_codec, &pl) != TQ_OK) return 0;
+  return pl.ws_bytes;
+}
+
+tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const tq_codec* v_codec,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  Plan pl;
+  tq_status st = make_plan(a, k_codec, v_codec, &pl);
+  if (st != TQ_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return TQ_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.ws_bytes) return TQ_ERR_WORKSPACE;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.L = a->n_layers;
+  p.B = a->batch;
+  p.Hq = a->n_q_heads;
+  p.Hkv = a->n_kv_heads;
+  p.G = pl.G;
+  p.n_hg = pl.n_hg;
+  p.sscale = (float)((double)a->scale * 1.4426950408889634074);
+  p.q = (const uint16_t*)a->q;
+  p.q_ls = a->q_layer_stride;
+  p.q_bs = a->q_batch_stride;
+  if (pl.has_rec) {
+    p.krec = (const uint8_t*)a->k_rec;
+    p.vrec = (const uint8_t*)a->v_rec;
+    p.krec_ls = a->k_rec_layer_stride;
+    p.vrec_ls = a->v_rec_layer_stride;
+    p.rec_cap = a->rec_cap;
+    p.krec_bytes = pl.kc.rec_bytes;
+    p.vrec_bytes = pl.vc.rec_bytes;
+    p.kb = pl.kc.bits;
+    p.vb = pl.vc.bits;
+    p.kout = pl.kc.has_outl;
+    p.vout = pl.vc.has_outl;
+    p.kcap = pl.kc.cap;
+    p.vcap = pl.vc.cap;
+    p.shared_kv = pl.shared ? 1 : 0;
+    p.k_off_norm = pl.kc.off_norm;
+    p.v_off_norm = pl.vc.off_norm;
+    p.k_off_count = pl.kc.off_count;
+    p.v_off_count = pl.vc.off_count;
+    p.k_off_ent = pl.kc.off_entries;
+    p.v_off_ent = pl.vc.off_entries;
+    p.k_main = pl.kc.off_count + (pl.kc.has_outl ? TQ_CHUNK : 0);
+    p.v_main = pl.vc.off_count + (pl.vc.has_outl ? TQ_CHUNK : 0);
+    std::memcpy(p.kc, pl.kc.centroids, sizeof(p.kc));
+    std::memcpy(p.vc, pl.vc.centroids, sizeof(p.vc));
+    std::memcpy(p.ksign, pl.kc.signs, sizeof(p.ksign));
+    p.n_chunks = a->n_chunks;
+  }
+  if (pl.has_tail) {
+    p.ktail = (const uint16_t*)a->k_tail;
+    p.vtail = (const uint16_t*)a->v_tail;
+    p.tail_ls = a->tail_layer_stride;
+    p.tail_cap = a->tail_cap;
+    p.tail_start = a->tail_start;
+    p.tail_len = a->tail_len;
+  }
+  p.S = pl.S;
+  p.Sc = pl.Sc;
+  p.cps = pl.cps;
+  p.tps = pl.tps;
+  p.ws_acc = (float*)workspace;
+  p.ws_ml = (float*)((char*)workspace + pl.ws_acc_bytes);
+  attn_smem_layout(p, pl.D, pl.GT);
+  if (p.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  dim3 grid(pl.S, a->batch * a->n_kv_heads * pl.n_hg, a->n_layers);
+  if (launch_attn(p, pl.D, pl.GT, grid, s) != cudaSuccess) return TQ_ERR_CUDA;
+  MergeParams m;
+  m.ws_acc = p.ws_acc;
+  m.ws_ml = p.ws_ml;
+  m.out = a->out;
+  m.rows = (int)pl.rows;
+  m.S = pl.S;
+  m.Sc = pl.Sc;
+  m.inv_sqrt_d = (float)(1.0 / std::sqrt((double)pl.D));
+  std::memcpy(m.vsign, pl.vc.signs, sizeof(m.vsign));
+  return launch_merge(m, pl.D, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // extern "C"

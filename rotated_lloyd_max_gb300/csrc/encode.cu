@@ -1,0 +1,292 @@
+// a3/a4: encode bf16 head vectors into 128-token records, and chunked
+// eviction from dense ring-buffer tails into records.
+//
+// Per vector ("v1.3 PPL on vLLM", M4 Phase A/B commits: rotate = H.D.x,
+// per-row scale, Lloyd-Max argmin, outliers; larql PR #196 turbo-quant note:
+// N(0,1) table scaled by 1/sqrt(d)):
+//   n = ||x||;  w = H(s . x) (unnormalised FWHT);  y = w / (n sqrt(d));
+//   code_j = #{k : y_j > t_k};  outlier_j = |y_j| > T/sqrt(d), value bf16(y_j).
+// Thread mapping: a vector is spread over L = d/32 lanes, each holding 32
+// consecutive coordinates (64 B of bf16, four 16-byte loads), so the first five
+// FWHT stages run in registers and log2(L) stages via warp shuffles; the 32
+// codes of a lane are exactly b 32-bit words of the packed row.
+// A CTA (4 warps) owns one record at a time and walks its 128 slots in passes
+// of 4*32/L vectors; with outliers, each pass is followed by a CTA-wide prefix
+// sum so that entries land in (slot, index) order.
+#include "tq_common.cuh"
+#include "tq_params.h"
+
+namespace tq {
+
+template <int D, int B, bool OUTL>
+struct Enc {
+  static constexpr int L = D / 32;       // lanes per vector
+  static constexpr int VPW = 32 / L;     // vectors per warp pass
+  static constexpr int VPC = 4 * VPW;    // vectors per CTA pass
+  static constexpr int HALF = 1 << (B - 1);
+  static constexpr int NPOS = HALF - 1;  // boundaries strictly above zero
+  static constexpr int RB = D * B / 8;   // packed row bytes
+};
+
+struct EncSmem {
+  int cnt[kChunk];
+  int off[kChunk];
+  int running;
+};
+
+// Encode slots [s_begin, s_end) of the record at `rec`; row(slot) gives the
+// bf16 source of a slot.  Must be called by all 128 threads of the CTA.
+template <int D, int B, bool OUTL, class RowFn>
+__device__ __forceinline__ void encode_record(const CodecDev& c, RowFn row, uint8_t* rec,
+                                              int s_begin, int s_end, EncSmem* sm) {
+  using E = Enc<D, B, OUTL>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lg = lane % E::L;   // lane within the vector's group
+  const int vi = lane / E::L;   // vector within the warp pass
+  const uint32_t sbits = c.signs[lg];
+  uint32_t tpos[E::NPOS > 0 ? E::NPOS : 1];
+#pragma unroll
+  for (int k = 0; k < E::NPOS; ++k) tpos[k] = __float_as_uint(c.boundaries[E::HALF + k]);
+  if (OUTL && threadIdx.x == 0) sm->running = 0;
+  if (OUTL) __syncthreads();
+
+  for (int base = s_begin; base < s_end; base += E::VPC) {
+    const int pslot = warp * E::VPW + vi;  // slot index within the pass
+    const int slot = base + pslot;
+    const bool valid = slot < s_end;
+    float x[32];
+    {
+      uint4 w[4] = {};
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(row(slot) + lg * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = __ldg(src + k);
+      }
+      const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t lo = (ww[k] << 16) ^ (((sbits >> (2 * k)) & 1u) << 31);
+        const uint32_t hi = (ww[k] & 0xFFFF0000u) ^ (((sbits >> (2 * k + 1)) & 1u) << 31);
+        x[2 * k] = __uint_as_float(lo);
+        x[2 * k + 1] = __uint_as_float(hi);
+      }
+    }
+    // ||x||^2 by a pairwise tree (squares of bf16 values are exact in f32)
+    float sq[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) sq[k] = fmaf(x[2 * k], x[2 * k], x[2 * k + 1] * x[2 * k + 1]);
+#pragma unroll
+    for (int h = 8; h; h >>= 1)
+#pragma unroll
+      for (int k = 0; k < h; ++k) sq[k] += sq[k + h];
+    float ss = sq[0];
+#pragma unroll
+    for (int m = 1; m < E::L; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float n = sqrtf(ss);
+    const float inv = n > 0.f ? 1.0f / (n * c.sqrt_d) : 0.f;
+
+    fwht_regs<32>(x);
+    fwht_lanes<32>(x, lane, E::L);
+
+    // quantise (mirror of the symmetric table around t = 0) and pack LSB-first
+    uint32_t wd[B];
+#pragma unroll
+    for (int q = 0; q < B; ++q) wd[q] = 0u;
+    uint32_t omask = 0u;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const float y = x[r] * inv;
+      const bool pos = y > 0.f;
+      // non-positive side counts t <= |y| as |y| + 1ulp > t (exact tie rule)
+      const uint32_t a = (__float_as_uint(y) & 0x7FFFFFFFu) + (pos ? 0u : 1u);
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int k = 0; k < E::NPOS; ++k) cnt += (a > tpos[k]) ? 1u : 0u;
+      const uint32_t code = (E::HALF + cnt) ^ (pos ? 0u : (uint32_t)((1 << B) - 1));
+      const int bit = r * B;
+      wd[bit >> 5] |= code << (bit & 31);
+      if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
+      if (OUTL) omask |= (fabsf(y) > c.thr_out ? 1u : 0u) << r;
+    }
+    if (valid) {
+      uint8_t* dstrow = rec + (size_t)slot * E::RB + lg * 4 * B;
+      if constexpr (B == 4) {
+        *reinterpret_cast<uint4*>(dstrow) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      } else if constexpr (B == 2) {
+        *reinterpret_cast<uint2*>(dstrow) = make_uint2(wd[0], wd[1]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < B; ++q) reinterpret_cast<uint32_t*>(dstrow)[q] = wd[q];
+      }
+      if (lg == 0) reinterpret_cast<float*>(rec + c.off_norm)[slot] = n;
+    }
+    if (OUTL) {
+      // per-vector count (slot stores at most 255), then a CTA prefix sum
+      int lc = __popc(valid ? omask : 0u);
+      int incl = lc;
+#pragma unroll
+      for (int m = 1; m < E::L; m <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, m, E::L);
+        if (lg >= m) incl += o;
+      }
+      const int excl = incl - lc;  // entries in lanes before this one
+      const int vtot = __shfl_sync(0xffffffffu, incl, E::L - 1, E::L);
+      const int nslot = min(vtot, 255);
+      if (lg == 0) sm->cnt[pslot] = valid ? nslot : 0;
+      __syncthreads();
+      if (warp == 0) {
+        // exclusive prefix over the pass's VPC slots (VPC <= 64)
+        int run = sm->running;
+        for (int k0 = 0; k0 < E::VPC; k0 += 32) {
+          const int v = (k0 + lane < E::VPC) ? sm->cnt[k0 + lane] : 0;
+          int inc = v;
+#pragma unroll
+          for (int m = 1; m < 32; m <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, inc, m);
+            if (lane >= m) inc += o;
+          }
+          if (k0 + lane < E::VPC) sm->off[k0 + lane] = run + inc - v;
+          run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        __syncwarp();
+        if (lane == 0) sm->running = run;
+      }
+      __syncthreads();
+      if (valid) {
+        const int off = sm->off[pslot];
+        const int stored = max(0, min(nslot, c.cap - off));
+        uint32_t* ent = reinterpret_cast<uint32_t*>(rec + c.off_entries);
+        int k = excl;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          if ((omask >> r) & 1u) {
+            if (k < stored) {
+              const uint32_t idx = (uint32_t)(lg * 32 + r);
+              const uint32_t v = f32_to_bf16_rne(x[r] * inv);
+              ent[off + k] = idx | (v << 16);
+            }
+            ++k;
+          }
+        }
+        if (lg == 0) rec[c.off_count + slot] = (uint8_t)stored;
+      }
+      // the next pass rewrites cnt[] only before its first barrier and off[]
+      // only after it, so no barrier is needed here
+    }
+  }
+}
+
+template <int D, int B, bool OUTL>
+__global__ void __launch_bounds__(kThreads) encode_kernel(const __grid_constant__ EncodeParams p) {
+  __shared__ EncSmem sm;
+  const int64_t n_tasks = p.n_groups * p.chunks_per_group;
+  for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+    const int64_t g = task / p.chunks_per_group;
+    const int64_t ci = p.first_chunk + task % p.chunks_per_group;
+    const int64_t lo = max(p.first_vec, ci * kChunk), hi = min(p.first_vec + p.n_vec, (ci + 1) * kChunk);
+    uint8_t* rec = p.dst + g * p.dst_gs + ci * (int64_t)p.c.rec_bytes;
+    const uint16_t* src_g = p.src + g * p.src_gs;
+    const int64_t vs = p.src_vs, v0 = ci * kChunk - p.first_vec;
+    auto row = [&](int slot) { return src_g + (v0 + slot) * vs; };
+    encode_record<D, B, OUTL>(p.c, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
+  }
+}
+
+// Eviction: CTA (e, b*Hkv + h, l) encodes the e-th due chunk of stream (l, b, h).
+template <int D, int B, bool OUTL>
+__global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__ EvictParams p) {
+  __shared__ EncSmem sm;
+  const int e = blockIdx.x;
+  const int h = blockIdx.y % p.Hkv, b = blockIdx.y / p.Hkv, l = blockIdx.z;
+  const int lb = l * p.B + b;
+  const int len = p.tail_len[lb], nch = p.n_chunks[lb];
+  const int start = ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap;
+  const int k = len >= p.floor_ + kChunk ? min((len - p.floor_) / kChunk, p.max_evict) : 0;
+  if (e >= k || nch < 0 || nch + k > p.rec_cap) return;
+  uint8_t* rec = p.rec + l * p.rec_ls +
+                 ((int64_t)(b * p.Hkv + h) * p.rec_cap + nch + e) * (int64_t)p.c.rec_bytes;
+  const uint16_t* tail = p.tail + l * p.tail_ls + (int64_t)(b * p.Hkv + h) * p.tail_cap * D;
+  const int first = start + e * kChunk;
+  const int cap = p.tail_cap;
+  auto row = [&](int slot) { return tail + (int64_t)((first + slot) % cap) * D; };
+  encode_record<D, B, OUTL>(p.c, row, rec, 0, kChunk, &sm);
+}
+
+__global__ void evict_commit_kernel(const EvictCommitParams p) {
+  for (int lb = blockIdx.x * blockDim.x + threadIdx.x; lb < p.LB; lb += gridDim.x * blockDim.x) {
+    const int len = p.tail_len[lb];
+    const int k = len >= p.floor_ + kChunk ? min((len - p.floor_) / kChunk, p.max_evict) : 0;
+    if (k == 0 || p.n_chunks[lb] < 0 || p.n_chunks[lb] + k > p.rec_cap) continue;
+    const int start = ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap;
+    p.n_chunks[lb] += k;
+    p.tail_start[lb] = (start + k * kChunk) % p.tail_cap;
+    p.tail_len[lb] = len - k * kChunk;
+  }
+}
+
+template <int D, int B, bool OUTL>
+static cudaError_t enc_launch(const EncodeParams& p, int grid, cudaStream_t s) {
+  encode_kernel<D, B, OUTL><<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+template <int D, int B, bool OUTL>
+static cudaError_t ev_launch(const EvictParams& p, cudaStream_t s) {
+  dim3 grid(p.max_evict, p.B * p.Hkv, p.L);
+  evict_kernel<D, B, OUTL><<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+#define TQ_DISPATCH_DBO(FN, D_, B_, O_, ...)                                      \
+  do {                                                                           \
+    switch (D_ * 100 + B_ * 10 + (O_ ? 1 : 0)) {                                 \
+      case 6410: return FN<64, 1, false>(__VA_ARGS__);                           \
+      case 6411: return FN<64, 1, true>(__VA_ARGS__);                            \
+      case 6420: return FN<64, 2, false>(__VA_ARGS__);                           \
+      case 6421: return FN<64, 2, true>(__VA_ARGS__);                            \
+      case 6430: return FN<64, 3, false>(__VA_ARGS__);                           \
+      case 6431: return FN<64, 3, true>(__VA_ARGS__);                            \
+      case 6440: return FN<64, 4, false>(__VA_ARGS__);                           \
+      case 6441: return FN<64, 4, true>(__VA_ARGS__);                            \
+      case 12810: return FN<128, 1, false>(__VA_ARGS__);                         \
+      case 12811: return FN<128, 1, true>(__VA_ARGS__);                          \
+      case 12820: return FN<128, 2, false>(__VA_ARGS__);                         \
+      case 12821: return FN<128, 2, true>(__VA_ARGS__);                          \
+      case 12830: return FN<128, 3, false>(__VA_ARGS__);                         \
+      case 12831: return FN<128, 3, true>(__VA_ARGS__);                          \
+      case 12840: return FN<128, 4, false>(__VA_ARGS__);                         \
+      case 12841: return FN<128, 4, true>(__VA_ARGS__);                          \
+      case 25610: return FN<256, 1, false>(__VA_ARGS__);                         \
+      case 25611: return FN<256, 1, true>(__VA_ARGS__);                          \
+      case 25620: return FN<256, 2, false>(__VA_ARGS__);                         \
+      case 25621: return FN<256, 2, true>(__VA_ARGS__);                          \
+      case 25630: return FN<256, 3, false>(__VA_ARGS__);                         \
+      case 25631: return FN<256, 3, true>(__VA_ARGS__);                          \
+      case 25640: return FN<256, 4, false>(__VA_ARGS__);                         \
+      case 25641: return FN<256, 4, true>(__VA_ARGS__);                          \
+      case 51210: return FN<512, 1, false>(__VA_ARGS__);                         \
+      case 51211: return FN<512, 1, true>(__VA_ARGS__);                          \
+      case 51220: return FN<512, 2, false>(__VA_ARGS__);                         \
+      case 51221: return FN<512, 2, true>(__VA_ARGS__);                          \
+      case 51230: return FN<512, 3, false>(__VA_ARGS__);                         \
+      case 51231: return FN<512, 3, true>(__VA_ARGS__);                          \
+      case 51240: return FN<512, 4, false>(__VA_ARGS__);                         \
+      case 51241: return FN<512, 4, true>(__VA_ARGS__);                          \
+      default: return cudaErrorInvalidValue;                                     \
+    }                                                                            \
+  } while (0)
+
+cudaError_t launch_encode(const EncodeParams& p, int grid, cudaStream_t s) {
+  TQ_DISPATCH_DBO(enc_launch, p.c.d, p.c.bits, p.c.has_outl, p, grid, s);
+}
+
+cudaError_t launch_evict(const EvictParams& p, cudaStream_t s) {
+  TQ_DISPATCH_DBO(ev_launch, p.c.d, p.c.bits, p.c.has_outl, p, s);
+}
+
+cudaError_t launch_evict_commit(const EvictCommitParams& p, cudaStream_t s) {
+  const int threads = 128, grid = (p.LB + threads - 1) / threads;
+  evict_commit_kernel<<<grid, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

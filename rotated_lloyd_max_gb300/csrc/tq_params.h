@@ -1,0 +1,125 @@
+// Kernel parameter blocks and launcher declarations shared between the C ABI
+// (abi.cu) and the kernel translation units.  Host-visible plain structs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+// What a kernel needs of a codec, resolved on the host.
+struct CodecDev {
+  int d, bits, has_outl, cap;
+  int rec_bytes, off_norm, off_count, off_entries;
+  float thr_out;     // T / sqrt(d) in f32 (+inf when T is +inf)
+  float inv_sqrt_d;  // f32(1/sqrt(d))
+  float sqrt_d;      // f32(sqrt(d))
+  float centroids[16];
+  float boundaries[15];
+  uint32_t signs[16];
+};
+
+struct EncodeParams {
+  CodecDev c;
+  const uint16_t* src;
+  int64_t src_vs, src_gs;  // elements
+  uint8_t* dst;
+  int64_t dst_gs;  // bytes
+  int64_t n_groups, n_vec, first_vec;
+  int64_t first_chunk, chunks_per_group;
+};
+
+struct EvictParams {
+  CodecDev c;               // codec of the stream this launch encodes
+  uint8_t* rec;
+  int64_t rec_ls;           // bytes
+  int rec_cap;
+  const uint16_t* tail;
+  int64_t tail_ls;          // elements
+  int tail_cap;
+  const int32_t* n_chunks;
+  const int32_t* tail_start;
+  const int32_t* tail_len;
+  int L, B, Hkv, floor_, max_evict;
+};
+
+struct EvictCommitParams {
+  int32_t* n_chunks;
+  int32_t* tail_start;
+  int32_t* tail_len;
+  int LB, floor_, max_evict, tail_cap, rec_cap;
+};
+
+struct DecodeParams {
+  CodecDev c;
+  const uint8_t* src;
+  int64_t src_gs;  // bytes
+  float* dst;
+  int64_t dst_vs, dst_gs;  // elements
+  int64_t n_groups, n_vec, first_vec;
+  int64_t first_chunk, chunks_per_group;
+};
+
+struct AttnParams {
+  int L, B, Hq, Hkv, G, n_hg;
+  float sscale;  // softmax scale * log2(e)
+  const uint16_t* q;
+  int64_t q_ls, q_bs;
+  const uint8_t* krec;
+  const uint8_t* vrec;
+  int64_t krec_ls, vrec_ls;
+  int rec_cap;
+  int krec_bytes, vrec_bytes;
+  int kb, vb, kout, vout, kcap, vcap, shared_kv;
+  int k_off_norm, v_off_norm, k_off_count, v_off_count, k_off_ent, v_off_ent;
+  int k_main, v_main;  // bytes staged per record (codes, norms, counts)
+  float kc[16], vc[16];
+  uint32_t ksign[16];
+  const uint16_t* ktail;
+  const uint16_t* vtail;
+  int64_t tail_ls;
+  int tail_cap;
+  const int32_t* n_chunks;
+  const int32_t* tail_start;
+  const int32_t* tail_len;
+  int S, Sc, cps, tps;
+  float* ws_acc;
+  float* ws_ml;
+  // dynamic shared memory carve-up (bytes)
+  int sm_q, sm_lut, sm_red, sm_logit, sm_main, sm_stage, sm_ent, sm_ent_stage, sm_pre, sm_slot,
+      sm_corr, sm_total;
+};
+
+struct MergeParams {
+  const float* ws_acc;
+  const float* ws_ml;
+  float* out;
+  int rows, S, Sc;
+  float inv_sqrt_d;
+  uint32_t vsign[16];
+};
+
+// launchers (return the launch status)
+cudaError_t launch_codebook(int bits, int d, uint64_t seed, void* scratch, cudaStream_t s);
+cudaError_t launch_encode(const EncodeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_evict(const EvictParams& p, cudaStream_t s);
+cudaError_t launch_evict_commit(const EvictCommitParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
+
+// Dynamic shared memory of the attention kernel for head dim D and head group GT
+// (everything but the record-size dependent parts is fixed by D and GT).
+void attn_smem_layout(AttnParams& p, int D, int GT);
+
+// The codebook kernel writes this block into the caller's scratch.
+struct CodebookOut {
+  float c[16];
+  float t[16];
+  uint32_t signs[16];
+  double mse;
+  int iters;
+  int pad;
+};
+
+}  // namespace tq

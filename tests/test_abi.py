@@ -1,0 +1,139 @@
+"""The C-ABI library builds, loads and exports every entry point include/tq.h
+declares; host-side validation rejects bad arguments with a status (no silent
+no-op, no launch).  Runs without a GPU: only calls that fail validation before
+touching the device are made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rotated_lloyd_max_gb300 import build
+    path = build.build()
+    import rotated_lloyd_max_gb300 as tq
+    return tq, ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b(tq_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for want in ["tq_make_codebook", "tq_encode", "tq_decode", "tq_evict", "tq_decode_attn",
+                 "tq_decode_attn_workspace_size", "tq_record_bytes", "tq_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    _, raw = lib
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in tq.h but not exported"
+
+
+def test_status_strings(lib):
+    tq, _ = lib
+    for s in range(5):
+        assert tq.status_string(s).startswith("TQ_")
+    assert tq.load().tq_version() >= 10000
+
+
+def _codec(tq, d=128, bits=3, T=0.0, cap=0):
+    c = tq.tq_codec()
+    c.head_dim, c.bits, c.outlier_T, c.outlier_cap = d, bits, T, cap
+    if not 1 <= bits <= 4:
+        return c
+    K = 1 << bits
+    # a valid symmetric ascending table (values are irrelevant to validation)
+    for k in range(K):
+        c.centroids[k] = (k - (K - 1) / 2) / 10
+    for k in range(K - 1):
+        c.boundaries[k] = (c.centroids[k] + c.centroids[k + 1]) / 2
+    c.boundaries[K // 2 - 1] = 0.0
+    return c
+
+
+def test_record_bytes_and_rejections(lib):
+    tq, raw = lib
+    L = tq.load()
+    assert L.tq_record_bytes(ctypes.byref(_codec(tq, 128, 3))) == 128 * 52
+    assert L.tq_record_bytes(ctypes.byref(_codec(tq, 512, 4))) == 128 * 260
+    assert L.tq_record_bytes(ctypes.byref(_codec(tq, 128, 4, 2.0, 1312))) == 128 * 68 + 128 + 4 * 1312
+    for bad in [_codec(tq, 96, 3), _codec(tq, 320, 3), _codec(tq, 128, 5), _codec(tq, 128, 0)]:
+        assert L.tq_record_bytes(ctypes.byref(bad)) == 0
+    asym = _codec(tq, 128, 2)
+    asym.boundaries[0] = asym.boundaries[0] * 0.9
+    assert L.tq_record_bytes(ctypes.byref(asym)) == 0
+    bad_cap = _codec(tq, 128, 3, 2.0, 6)   # not a multiple of 4
+    assert L.tq_record_bytes(ctypes.byref(bad_cap)) == 0
+
+
+def test_calls_fail_loudly_on_bad_arguments(lib):
+    tq, _ = lib
+    L = tq.load()
+    good = _codec(tq, 128, 3)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    # unsupported head dims: a status, not a silent return
+    assert L.tq_encode(ctypes.byref(_codec(tq, 96, 3)), fake, 1, 128, 96, 0, fake, 0, 0, None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_decode(ctypes.byref(_codec(tq, 320, 3)), fake, 1, 128, 0, 0, fake, 320, 0, None) == tq.TQ_ERR_UNSUPPORTED
+    # null / misaligned pointers, bad strides
+    assert L.tq_encode(ctypes.byref(good), None, 1, 128, 128, 0, fake, 0, 0, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_encode(ctypes.byref(good), ctypes.c_void_p(0x10002), 1, 128, 128, 0, fake, 0, 0, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_encode(ctypes.byref(good), fake, 1, 128, 100, 0, fake, 0, 0, None) == tq.TQ_ERR_INVALID_ARG
+    # outliers need record-aligned starts
+    outl = _codec(tq, 128, 3, 2.0, 1312)
+    assert L.tq_encode(ctypes.byref(outl), fake, 1, 10, 128, 0, fake, 0, 5, None) == tq.TQ_ERR_INVALID_ARG
+    # empty work is a successful no-op that launches nothing
+    assert L.tq_encode(ctypes.byref(good), fake, 0, 128, 128, 0, fake, 0, 0, None) == tq.TQ_OK
+    # codebook: unsupported shapes and a too-small scratch
+    out = tq.tq_codec()
+    assert L.tq_make_codebook(5, 128, 1, 0.0, 0, fake, 4096, ctypes.byref(out), None, None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_make_codebook(3, 96, 1, 0.0, 0, fake, 4096, ctypes.byref(out), None, None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_make_codebook(3, 128, 1, 0.0, 0, fake, 8, ctypes.byref(out), None, None) == tq.TQ_ERR_WORKSPACE
+    # attention: Hq % Hkv != 0, bad head dim, missing pointers
+    a = tq.tq_attn_args()
+    a.n_layers, a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim, a.scale = 1, 1, 6, 4, 128, 1.0
+    a.q, a.out = 0x10000, 0x20000
+    assert L.tq_decode_attn(ctypes.byref(a), None, None, fake, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
+    a.n_kv_heads, a.head_dim = 2, 96
+    assert L.tq_decode_attn(ctypes.byref(a), None, None, fake, 1 << 20, None) == tq.TQ_ERR_UNSUPPORTED
+    a.head_dim = 128
+    a.k_rec = 0x30000   # records without codecs
+    assert L.tq_decode_attn(ctypes.byref(a), None, None, fake, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_decode_attn_workspace_size(ctypes.byref(a), None, None) == 0
+    # eviction: null counters
+    e = tq.tq_evict_args()
+    e.n_layers, e.batch, e.n_kv_heads, e.max_evict, e.rec_cap, e.tail_cap, e.t_q = 1, 1, 1, 1, 4, 272, 1
+    assert L.tq_evict(ctypes.byref(good), ctypes.byref(good), ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARG
+
+
+def test_struct_layouts_match_header(lib, tmp_path):
+    """The ctypes mirrors of the C structs have the C compiler's size and field
+    offsets (checked by compiling a probe against include/tq.h with gcc)."""
+    import subprocess
+    tq, _ = lib
+    structs = {"tq_codec": tq.tq_codec, "tq_evict_args": tq.tq_evict_args, "tq_attn_args": tq.tq_attn_args}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{name}.{fname} %zu\\n", offsetof({name}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.check_call(["gcc", str(src), "-o", str(exe)])
+    got = dict(l.split() for l in subprocess.check_output([str(exe)], text=True).splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for fname, _ in cls._fields_:
+            assert int(got[f"{name}.{fname}"]) == getattr(cls, fname).offset, f"{name}.{fname}"

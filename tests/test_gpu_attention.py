@@ -1,0 +1,167 @@
+"""GPU parity of the fused decode attention (tq_decode_attn) against the
+oracle's brute-force softmax attention over fully dequantised vectors.
+
+Two comparisons per case: (1) the oracle attends the GPU's own records (this
+isolates the attention numerics, bar 2e-3 max-abs), (2) end to end, the oracle
+encodes the same inputs itself and attends its own records (bar 2e-3 too;
+boundary-band code flips are the only other difference)."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+import tq_testlib as tl
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rotated_lloyd_max_gb300 import build
+    build.build()
+    import rotated_lloyd_max_gb300 as m
+    m.load()
+    return m
+
+
+def _ocodec(orc, c):
+    return orc.Codec(d=c.head_dim, bits=c.bits, seed=int(c.c.sign_seed), T=float(c.c.outlier_T),
+                     cap=int(c.c.outlier_cap) if c.c.outlier_T else 0)
+
+
+def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=False, dense=False,
+             tail_cap=None, splits=0, seed=0, q_pad=0, k_outlier_frac=0.0, end_to_end=True, scale=1.0):
+    """chunks[b], tails[b]: compressed records and dense tail tokens of batch b
+    (the same for every layer).  Returns (gpu_out, oracle_out, oracle_e2e_out)."""
+    import torch
+    dev = "cuda"
+    Hq = G * Hkv
+    max_chunks = max(chunks) if not dense else 0
+    rec_cap = max(max_chunks, 1)
+    tail_cap = tail_cap or max(max(tails), 1)
+    kc = tq.tq_make_codebook(kb, d, sign_seed=1, outlier_T=T)
+    vc = kc if shared else tq.tq_make_codebook(vb, d, sign_seed=1, outlier_T=T)
+    okc, ovc = _ocodec(orc, kc), _ocodec(orc, vc)
+    ntok = rec_cap * 128
+    kx = synth.gaussian_bf16((L, B, Hkv, ntok, d), seed + 1, outlier_frac=k_outlier_frac,
+                             lognormal_sigma=0.3)
+    vx = kx if shared else synth.gaussian_bf16((L, B, Hkv, ntok, d), seed + 2)
+    kt = synth.gaussian_bf16((L, B, Hkv, tail_cap, d), seed + 3)
+    vt = kt if shared else synth.gaussian_bf16((L, B, Hkv, tail_cap, d), seed + 4)
+    qb = synth.gaussian_bf16((L, B, Hq + q_pad, d), seed + 5, scale=1 / math.sqrt(d))
+    rng = np.random.default_rng(seed)
+    tstart = rng.integers(0, tail_cap, size=(L, B)).astype(np.int32)
+    n_chunks = np.tile(np.array(chunks, np.int32), (L, 1))
+    tail_len = np.tile(np.array(tails, np.int32), (L, 1))
+
+    q = tl.to_bf16_tensor(qb, dev)[:, :, :Hq, :]          # batch stride (Hq + q_pad) * d
+    out = torch.full((L, B, Hq, d), float("nan"), dtype=torch.float32, device=dev)
+    kw = dict(q=q, out=out, scale=scale)
+    rec_np = {}
+    if not dense:
+        krec = torch.zeros((L, B, Hkv, rec_cap, kc.record_bytes), dtype=torch.uint8, device=dev)
+        tq.tq_encode(kc, tl.to_bf16_tensor(kx, dev).reshape(L * B * Hkv, ntok, d),
+                     krec.view(L * B * Hkv, rec_cap, kc.record_bytes))
+        if shared:
+            vrec = krec
+        else:
+            vrec = torch.zeros((L, B, Hkv, rec_cap, vc.record_bytes), dtype=torch.uint8, device=dev)
+            tq.tq_encode(vc, tl.to_bf16_tensor(vx, dev).reshape(L * B * Hkv, ntok, d),
+                         vrec.view(L * B * Hkv, rec_cap, vc.record_bytes))
+        kw.update(k_rec=krec, v_rec=vrec, n_chunks=torch.from_numpy(n_chunks).to(dev), max_chunks=max_chunks)
+        rec_np["k"], rec_np["v"] = krec.cpu().numpy(), vrec.cpu().numpy()
+    if max(tails) > 0:
+        kw.update(k_tail=tl.to_bf16_tensor(kt, dev), v_tail=tl.to_bf16_tensor(vt, dev),
+                  tail_start=torch.from_numpy(tstart).to(dev), tail_len=torch.from_numpy(tail_len).to(dev),
+                  max_tail=max(tails))
+    kw["n_kv_heads"] = Hkv
+    tq.decode_attn(k_codec=None if dense else kc, v_codec=None if dense else vc, splits=splits, **kw)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+
+    want = np.zeros_like(got, dtype=np.float64)
+    want_e2e = np.zeros_like(want) if (end_to_end and not dense) else None
+    for l in range(L):
+        for b in range(B):
+            for h in range(Hkv):
+                nc = 0 if dense else chunks[b]
+                slots = (tstart[l, b] + np.arange(tails[b])) % tail_cap
+                kd, vd = kt[l, b, h, slots], vt[l, b, h, slots]
+                qh = qb[l, b, h * G:(h + 1) * G]
+                kr = rec_np["k"][l, b, h] if not dense else None
+                vr = rec_np["v"][l, b, h] if not dense else None
+                want[l, b, h * G:(h + 1) * G] = orc.unit_attention(qh, okc, ovc, kr, vr, nc * 128, kd, vd, scale)
+                if want_e2e is not None:
+                    okr = orc.encode_records(kx[l, b, h, :nc * 128], okc) if nc else None
+                    ovr = orc.encode_records(vx[l, b, h, :nc * 128], ovc) if nc else None
+                    want_e2e[l, b, h * G:(h + 1) * G] = orc.unit_attention(qh, okc, ovc, okr, ovr, nc * 128,
+                                                                           kd, vd, scale)
+    return got, want, want_e2e
+
+
+def _assert_close(got, want, tol=TOL):
+    assert np.all(np.isfinite(got))
+    err = np.max(np.abs(got - want))
+    assert err <= tol, f"max abs err {err}"
+    return err
+
+
+CASES = {
+    "tiny_gqa4_tail": dict(d=64, G=4, Hkv=2, B=2, L=2, chunks=[3, 1], tails=[50, 0], kb=3, vb=2),
+    "qwen_like_gqa6": dict(d=128, G=6, Hkv=2, B=1, L=2, chunks=[16], tails=[0], kb=3, vb=2),
+    "outliers_gqa4": dict(d=128, G=4, Hkv=2, B=2, L=1, chunks=[4, 2], tails=[0, 0], kb=4, vb=3, T=2.0,
+                          k_outlier_frac=0.02),
+    "mqa_shared_d512": dict(d=512, G=64, Hkv=1, B=1, L=1, chunks=[5], tails=[256], kb=4, vb=4, shared=True,
+                            tail_cap=272),
+    "d256_mha_b1": dict(d=256, G=1, Hkv=4, B=1, L=1, chunks=[2], tails=[70], kb=1, vb=4),
+    "d128_gqa2_b4b1": dict(d=128, G=2, Hkv=2, B=3, L=1, chunks=[2, 0, 3], tails=[10, 64, 0], kb=4, vb=1),
+    "gqa8_q_stride": dict(d=128, G=8, Hkv=1, B=2, L=1, chunks=[3, 3], tails=[20, 5], kb=2, vb=3, q_pad=3),
+    "gqa3_odd_group": dict(d=64, G=3, Hkv=2, B=1, L=1, chunks=[2], tails=[9], kb=3, vb=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_attention_cases(tq, orc, name):
+    got, want, e2e = run_case(tq, orc, **CASES[name])
+    _assert_close(got, want)
+    if e2e is not None:
+        _assert_close(got, e2e)
+
+
+def test_dense_boundary_layers(tq, orc):
+    """bf16 layers: no records, the whole cache passed as the dense part."""
+    got, want, _ = run_case(tq, orc, d=128, G=6, Hkv=2, B=1, L=2, chunks=[0], tails=[2048], kb=3, vb=2,
+                            dense=True)
+    _assert_close(got, want)
+
+
+def test_split_count_invariance(tq, orc):
+    cfg = dict(d=128, G=4, Hkv=2, B=1, L=1, chunks=[12], tails=[100], kb=3, vb=2, end_to_end=False)
+    a, want, _ = run_case(tq, orc, splits=1, **cfg)
+    b, _, _ = run_case(tq, orc, splits=40, **cfg)
+    _assert_close(a, want)
+    assert np.max(np.abs(a - b)) <= 1e-5
+
+
+def test_empty_context_gives_zero(tq):
+    import torch
+    L, B, Hq, Hkv, d = 1, 2, 4, 2, 128
+    q = torch.randn(L, B, Hq, d, device="cuda").to(torch.bfloat16)
+    out = torch.full((L, B, Hq, d), float("nan"), device="cuda")
+    kt = torch.zeros((L, B, Hkv, 16, d), dtype=torch.bfloat16, device="cuda")
+    zero = torch.zeros((L, B), dtype=torch.int32, device="cuda")
+    tq.decode_attn(q=q, out=out, scale=1.0, k_tail=kt, v_tail=kt, tail_start=zero, tail_len=zero, max_tail=16)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+def test_single_token_returns_its_value(tq, orc):
+    """One dense token: the output is that token's value (bf16 -> f32 exactly)."""
+    got, want, _ = run_case(tq, orc, d=128, G=2, Hkv=1, B=1, L=1, chunks=[0], tails=[1], kb=3, vb=3,
+                            end_to_end=False)
+    _assert_close(got, want, tol=1e-6)
