@@ -217,6 +217,29 @@ tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
                          const tq_codec* v_codec, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * Allocation-free variant of tq_decode_attn.  The pages describe no such
+ * call; it exists for callers that cannot allocate device memory at the time
+ * they run attention (their device memory is reserved up front by a host
+ * framework or pooling allocator, a plugin enqueue step that must not
+ * allocate, or a latency-critical loop that cannot take cudaMalloc's implicit
+ * synchronisation).
+ *   Same arguments and results as tq_decode_attn, but the split-K workspace is
+ *   a fixed device array inside the library of TQ_NOALLOC_WORKSPACE_BYTES
+ *   (8 MiB), present on every GPU that loads the library until the process
+ *   exits.  A call needing more (tq_decode_attn_workspace_size) is rejected
+ *   with TQ_ERR_WORKSPACE; lower `splits` or use tq_decode_attn.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  Nothing in the array needs to start at zero, and each
+ *   call overwrites what the previous one left.  All calls share the one
+ *   array: calls whose executions overlap on the GPU (different streams,
+ *   concurrent graph branches) race and corrupt each other's results.
+ */
+#define TQ_NOALLOC_WORKSPACE_BYTES (8u << 20)
+tq_status tq_decode_attn_noalloc(const tq_attn_args* args, const tq_codec* k_codec,
+                                 const tq_codec* v_codec, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

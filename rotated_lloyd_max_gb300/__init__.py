@@ -68,7 +68,11 @@ _SIGS = {
                                                         ctypes.POINTER(tq_codec)]),
     "tq_decode_attn": (ctypes.c_int, [ctypes.POINTER(tq_attn_args), ctypes.POINTER(tq_codec),
                                       ctypes.POINTER(tq_codec), c_p, ctypes.c_size_t, c_p]),
+    "tq_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(tq_attn_args), ctypes.POINTER(tq_codec),
+                                              ctypes.POINTER(tq_codec), c_p]),
 }
+
+NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lib = None
 
@@ -263,6 +267,17 @@ def tq_decode_attn(args: tq_attn_args, k_codec: Codec | None, v_codec: Codec | N
     _check("tq_decode_attn", load().tq_decode_attn(ctypes.byref(args), kc, vc, _ptr(workspace),
                                                    workspace.numel() * workspace.element_size(),
                                                    _stream(stream)))
+
+
+def tq_decode_attn_noalloc(args: tq_attn_args, k_codec: Codec | None, v_codec: Codec | None,
+                           stream=None):
+    """tq_decode_attn with the library's own fixed workspace (no allocation by
+    caller or library).  Calls that overlap on the GPU share that workspace and
+    race."""
+    kc = ctypes.byref(k_codec.c) if k_codec is not None else None
+    vc = ctypes.byref(v_codec.c) if v_codec is not None else None
+    _check("tq_decode_attn_noalloc", load().tq_decode_attn_noalloc(ctypes.byref(args), kc, vc,
+                                                                   _stream(stream)))
 
 
 def decode_attn(*, k_codec=None, v_codec=None, workspace=None, stream=None, **kw):
