@@ -138,7 +138,7 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   const int64_t tail_tiles = cdiv(max_tail, TT);
   const int64_t units = (int64_t)a->n_layers * a->batch * a->n_kv_heads * pl->n_hg;
   int64_t want = a->splits > 0 ? a->splits : std::max<int64_t>(1, cdiv(4LL * num_sms(), units));
-  want = std::min<int64_t>(want, 1024);
+  want = std::min<int64_t>(want, 1000);  // the merge keeps <= 1024 split weights
   const int64_t tok_c = comp_tiles * TQ_CHUNK, tok_t = max_tail;
   int64_t Sc = 0, St = 0;
   if (comp_tiles > 0) {
@@ -279,9 +279,8 @@ tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, in
   p.first_vec = first_vec;
   p.first_chunk = first_vec / TQ_CHUNK;
   p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
-  const int64_t tasks = n_groups * p.chunks_per_group;
-  const int grid = (int)std::min<int64_t>(tasks, 8LL * num_sms());
-  return launch_encode(p, grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  // the launcher caps the grid at the number of tasks of the kernel it picks
+  return launch_encode(p, 8 * num_sms(), (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, int64_t n_vec,

@@ -196,6 +196,102 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     return;
   }
 
+  const int n_tiles_c = t_end - t_begin;
+  // ---- compressed splits: record staging (3-deep cp.async ring)
+  const uint8_t* kb0 = !comp ? nullptr : p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
+  const uint8_t* vb0 = (!comp || p.shared_kv) ? kb0
+                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  const bool anyout = p.kout || p.vout;
+  const int vcap = p.shared_kv ? p.kcap : p.vcap;
+  auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
+  auto entb = [&](int i) { return reinterpret_cast<uint32_t*>(sm + p.sm_ent + (i & 1) * p.sm_ent_stage); };
+  auto issue_main = [&](int i) {
+    if (i < n_tiles_c) {
+      const int64_t c = t_begin + i;
+      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+    }
+    cp_async_commit();
+  };
+  auto prefix = [&](int i) {
+    if (i >= n_tiles_c || !anyout || warp >= 2) return;
+    const bool isk = warp == 0;
+    if (isk ? !p.kout : (!p.vout || p.shared_kv)) return;
+    const unsigned char* cnts = isk ? stage(i) + p.k_off_count : stage(i) + p.k_main + p.v_off_count;
+    int* pr = pre + ((i & 1) * 2 + (isk ? 0 : 1)) * 129;
+    const uint32_t c4 = reinterpret_cast<const uint32_t*>(cnts)[lane];  // slots 4*lane .. 4*lane+3
+    const int n0 = c4 & 0xff, n1 = (c4 >> 8) & 0xff, n2 = (c4 >> 16) & 0xff, n3 = c4 >> 24;
+    const int tot = n0 + n1 + n2 + n3;
+    int inc = tot;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, m);
+      if (lane >= m) inc += o;
+    }
+    const int ex = inc - tot;
+    pr[4 * lane] = ex;
+    pr[4 * lane + 1] = ex + n0;
+    pr[4 * lane + 2] = ex + n0 + n1;
+    pr[4 * lane + 3] = ex + n0 + n1 + n2;
+    if (lane == 31) pr[128] = inc;
+    const bool vmap = !isk || p.shared_kv;  // value corrections need entry -> slot
+    if (vmap && p.vout) {
+      uint8_t* so = slotof + (i & 1) * vcap;
+      int e = ex;
+      const int ns[4] = {n0, n1, n2, n3};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        for (int k = 0; k < ns[q]; ++k, ++e)
+          if (e < vcap) so[e] = (uint8_t)(4 * lane + q);
+    }
+  };
+  auto issue_ent = [&](int i) {
+    if (i < n_tiles_c && anyout) {
+      const int64_t c = t_begin + i;
+      uint32_t* eb = entb(i);
+      if (p.kout) {
+        const int E = min(pre[((i & 1) * 2) * 129 + 128], p.kcap);
+        cta_copy_async(eb, kb0 + c * p.krec_bytes + p.k_off_ent, (E * 4 + 15) & ~15);
+      }
+      if (p.vout && !p.shared_kv) {
+        const int E = min(pre[((i & 1) * 2 + 1) * 129 + 128], p.vcap);
+        cta_copy_async(eb + p.kcap * p.kout, vb0 + c * p.vrec_bytes + p.v_off_ent, (E * 4 + 15) & ~15);
+      }
+    }
+    cp_async_commit();
+  };
+
+  // ---- dense splits: bf16 tile staging
+  const int tstart = (!comp && p.tail_start) ? ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap : 0;
+  const uint16_t* kt0 = comp ? nullptr : p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+  const uint16_t* vt0 = comp ? nullptr : p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+  const int n_tiles = (n_tiles_c + TT - 1) / TT;
+  constexpr int TB = TT * D * 2;  // bytes of one stream's tile
+  auto issue_dense = [&](int i) {
+    if (i < n_tiles) {
+      const int tok0 = t_begin + i * TT;
+      const int cnt = min(TT, t_end - tok0);
+      unsigned char* s = stage(i);
+      for (int pc = tid; pc < TT * (D / 8); pc += kThreads) {
+        const int tok = pc / (D / 8), part = pc % (D / 8);
+        if (tok < cnt) {
+          const int64_t slot = (tstart + tok0 + tok) % p.tail_cap;
+          cp_async16(s + (tok * D + part * 8) * 2, kt0 + slot * D + part * 8);
+          cp_async16(s + TB + (tok * D + part * 8) * 2, vt0 + slot * D + part * 8);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  // the first copies go out before the query work so their latency overlaps it
+  if (comp) {
+    issue_main(0);
+    issue_main(1);
+  } else {
+    issue_dense(0);
+    issue_dense(1);
+  }
+
   // ---- query: load, rotate (compressed split), store as [slice][32][GTP]
   for (int hh = warp; hh < GT; hh += 4) {
     constexpr int R = D / 32;
@@ -296,74 +392,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       }
   };
 
-  const int n_tiles_c = t_end - t_begin;
   if (comp) {
-    // ------------------------------------------------------------ records
-    const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-    const uint8_t* vb0 = p.shared_kv ? kb0
-                                     : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
-    const bool anyout = p.kout || p.vout;
-    const int vcap = p.shared_kv ? p.kcap : p.vcap;
-    auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
-    auto entb = [&](int i) { return reinterpret_cast<uint32_t*>(sm + p.sm_ent + (i & 1) * p.sm_ent_stage); };
-    auto issue_main = [&](int i) {
-      if (i < n_tiles_c) {
-        const int64_t c = t_begin + i;
-        cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
-        if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
-      }
-      cp_async_commit();
-    };
-    auto prefix = [&](int i) {
-      if (i >= n_tiles_c || !anyout || warp >= 2) return;
-      const bool isk = warp == 0;
-      if (isk ? !p.kout : (!p.vout || p.shared_kv)) return;
-      const unsigned char* cnts = isk ? stage(i) + p.k_off_count : stage(i) + p.k_main + p.v_off_count;
-      int* pr = pre + ((i & 1) * 2 + (isk ? 0 : 1)) * 129;
-      const uint32_t c4 = reinterpret_cast<const uint32_t*>(cnts)[lane];  // slots 4*lane .. 4*lane+3
-      const int n0 = c4 & 0xff, n1 = (c4 >> 8) & 0xff, n2 = (c4 >> 16) & 0xff, n3 = c4 >> 24;
-      const int tot = n0 + n1 + n2 + n3;
-      int inc = tot;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, m);
-        if (lane >= m) inc += o;
-      }
-      const int ex = inc - tot;
-      pr[4 * lane] = ex;
-      pr[4 * lane + 1] = ex + n0;
-      pr[4 * lane + 2] = ex + n0 + n1;
-      pr[4 * lane + 3] = ex + n0 + n1 + n2;
-      if (lane == 31) pr[128] = inc;
-      const bool vmap = !isk || p.shared_kv;  // value corrections need entry -> slot
-      if (vmap && p.vout) {
-        uint8_t* so = slotof + (i & 1) * vcap;
-        int e = ex;
-        const int ns[4] = {n0, n1, n2, n3};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          for (int k = 0; k < ns[q]; ++k, ++e)
-            if (e < vcap) so[e] = (uint8_t)(4 * lane + q);
-      }
-    };
-    auto issue_ent = [&](int i) {
-      if (i < n_tiles_c && anyout) {
-        const int64_t c = t_begin + i;
-        uint32_t* eb = entb(i);
-        if (p.kout) {
-          const int E = min(pre[((i & 1) * 2) * 129 + 128], p.kcap);
-          cta_copy_async(eb, kb0 + c * p.krec_bytes + p.k_off_ent, (E * 4 + 15) & ~15);
-        }
-        if (p.vout && !p.shared_kv) {
-          const int E = min(pre[((i & 1) * 2 + 1) * 129 + 128], p.vcap);
-          cta_copy_async(eb + p.kcap * p.kout, vb0 + c * p.vrec_bytes + p.v_off_ent, (E * 4 + 15) & ~15);
-        }
-      }
-      cp_async_commit();
-    };
-
-    issue_main(0);
-    issue_main(1);
     cp_async_wait<1>();
     __syncthreads();
     prefix(0);
@@ -453,33 +482,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       __syncthreads();
     }
   } else {
-    // ------------------------------------------------------------ dense bf16 tokens
-    const int tstart = p.tail_start ? ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap : 0;
-    const uint16_t* kt0 = p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
-    const uint16_t* vt0 = p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
-    const int n_tiles = (n_tiles_c + TT - 1) / TT;
-    constexpr int TB = TT * D * 2;  // bytes of one stream's tile
-    auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
-    auto issue = [&](int i) {
-      if (i < n_tiles) {
-        const int tok0 = t_begin + i * TT;
-        const int cnt = min(TT, t_end - tok0);
-        unsigned char* s = stage(i);
-        for (int pc = tid; pc < TT * (D / 8); pc += kThreads) {
-          const int tok = pc / (D / 8), part = pc % (D / 8);
-          if (tok < cnt) {
-            const int64_t slot = (tstart + tok0 + tok) % p.tail_cap;
-            cp_async16(s + (tok * D + part * 8) * 2, kt0 + slot * D + part * 8);
-            cp_async16(s + TB + (tok * D + part * 8) * 2, vt0 + slot * D + part * 8);
-          }
-        }
-      }
-      cp_async_commit();
-    };
-    issue(0);
-    issue(1);
     for (int i = 0; i < n_tiles; ++i) {
-      issue(i + 2);
+      issue_dense(i + 2);
       cp_async_wait<2>();
       __syncthreads();
       const int ntok = min(TT, t_end - (t_begin + i * TT));

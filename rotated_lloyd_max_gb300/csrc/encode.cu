@@ -16,6 +16,8 @@
 #include "tq_common.cuh"
 #include "tq_params.h"
 
+#include <algorithm>
+
 namespace tq {
 
 template <int D, int B, bool OUTL>
@@ -34,150 +36,198 @@ struct EncSmem {
   int running;
 };
 
-// Encode slots [s_begin, s_end) of the record at `rec`; row(slot) gives the
+// Per-thread constants of the encoder (signs of the lane's 32 coordinates and
+// the positive boundaries as integer bit patterns).
+template <int D, int B, bool OUTL>
+struct EncLane {
+  using E = Enc<D, B, OUTL>;
+  int lane, warp, lg, vi;
+  uint32_t sbits;
+  uint32_t tpos[E::NPOS > 0 ? E::NPOS : 1];
+  __device__ __forceinline__ explicit EncLane(const CodecDev& c) {
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    lg = lane % E::L;
+    vi = lane / E::L;
+    sbits = c.signs[lg];
+#pragma unroll
+    for (int k = 0; k < E::NPOS; ++k) tpos[k] = __float_as_uint(c.boundaries[E::HALF + k]);
+  }
+};
+
+// The lane's 32 bf16 coordinates of a vector (zeros for an invalid slot).
+__device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4 (&w)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(rowp);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __ldg(src + k);
+  }
+}
+
+// Encode one vector spread over the L lanes of a group: norm, FWHT, codes,
+// packed store, and (OUTL) the outlier mask and the lane's y values.
+template <int D, int B, bool OUTL>
+__device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B, OUTL>& ln,
+                                           const uint4 (&w)[4], bool valid, uint8_t* rec, int slot,
+                                           float (&x)[32], float& inv, uint32_t& omask) {
+  using E = Enc<D, B, OUTL>;
+  {
+    const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t lo = (ww[k] << 16) ^ (((ln.sbits >> (2 * k)) & 1u) << 31);
+      const uint32_t hi = (ww[k] & 0xFFFF0000u) ^ (((ln.sbits >> (2 * k + 1)) & 1u) << 31);
+      x[2 * k] = __uint_as_float(lo);
+      x[2 * k + 1] = __uint_as_float(hi);
+    }
+  }
+  // ||x||^2 by a pairwise tree (squares of bf16 values are exact in f32)
+  float sq[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) sq[k] = fmaf(x[2 * k], x[2 * k], x[2 * k + 1] * x[2 * k + 1]);
+#pragma unroll
+  for (int h = 8; h; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) sq[k] += sq[k + h];
+  float ss = sq[0];
+#pragma unroll
+  for (int m = 1; m < E::L; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  const float n = sqrtf(ss);
+  inv = n > 0.f ? 1.0f / (n * c.sqrt_d) : 0.f;
+
+  fwht_regs<32>(x);
+  fwht_lanes<32>(x, ln.lane, E::L);
+
+  // quantise (mirror of the symmetric table around t = 0) and pack LSB-first
+  uint32_t wd[B];
+#pragma unroll
+  for (int q = 0; q < B; ++q) wd[q] = 0u;
+  omask = 0u;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const float y = x[r] * inv;
+    const bool pos = y > 0.f;
+    // non-positive side counts t <= |y| as |y| + 1ulp > t (exact tie rule)
+    const uint32_t a = (__float_as_uint(y) & 0x7FFFFFFFu) + (pos ? 0u : 1u);
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int k = 0; k < E::NPOS; ++k) cnt += (a > ln.tpos[k]) ? 1u : 0u;
+    const uint32_t code = (E::HALF + cnt) ^ (pos ? 0u : (uint32_t)((1 << B) - 1));
+    const int bit = r * B;
+    wd[bit >> 5] |= code << (bit & 31);
+    if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
+    if (OUTL) omask |= (fabsf(y) > c.thr_out ? 1u : 0u) << r;
+  }
+  if (valid) {
+    uint8_t* dstrow = rec + (size_t)slot * E::RB + ln.lg * 4 * B;
+    if constexpr (B == 4) {
+      *reinterpret_cast<uint4*>(dstrow) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    } else if constexpr (B == 2) {
+      *reinterpret_cast<uint2*>(dstrow) = make_uint2(wd[0], wd[1]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < B; ++q) reinterpret_cast<uint32_t*>(dstrow)[q] = wd[q];
+    }
+    if (ln.lg == 0) reinterpret_cast<float*>(rec + c.off_norm)[slot] = n;
+  } else {
+    omask = 0u;
+  }
+}
+
+// Outlier entries of one pass, in (slot, index) order: per-vector counts, a
+// CTA prefix sum over the pass (continuing the record's running total), then
+// each lane writes its entries.  All 128 threads must call it.
+template <int D, int B>
+__device__ __forceinline__ void enc_outliers(const CodecDev& c, const EncLane<D, B, true>& ln,
+                                             const float (&x)[32], float inv, uint32_t omask, bool valid,
+                                             uint8_t* rec, int slot, int pslot, EncSmem* sm) {
+  using E = Enc<D, B, true>;
+  const int lane = ln.lane, lg = ln.lg;
+  const int lc = __popc(omask);
+  int incl = lc;
+#pragma unroll
+  for (int m = 1; m < E::L; m <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, m, E::L);
+    if (lg >= m) incl += o;
+  }
+  const int excl = incl - lc;  // entries in lanes before this one
+  const int vtot = __shfl_sync(0xffffffffu, incl, E::L - 1, E::L);
+  const int nslot = min(vtot, 255);
+  if (lg == 0) sm->cnt[pslot] = valid ? nslot : 0;
+  __syncthreads();
+  if (ln.warp == 0) {
+    int run = sm->running;
+    for (int k0 = 0; k0 < E::VPC; k0 += 32) {
+      const int v = (k0 + lane < E::VPC) ? sm->cnt[k0 + lane] : 0;
+      int inc = v;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, m);
+        if (lane >= m) inc += o;
+      }
+      if (k0 + lane < E::VPC) sm->off[k0 + lane] = run + inc - v;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    __syncwarp();
+    if (lane == 0) sm->running = run;
+  }
+  __syncthreads();
+  if (valid) {
+    const int off = sm->off[pslot];
+    const int stored = max(0, min(nslot, c.cap - off));
+    uint32_t* ent = reinterpret_cast<uint32_t*>(rec + c.off_entries);
+    int k = excl;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if ((omask >> r) & 1u) {
+        if (k < stored) {
+          const uint32_t idx = (uint32_t)(lg * 32 + r);
+          const uint32_t v = f32_to_bf16_rne(x[r] * inv);
+          ent[off + k] = idx | (v << 16);
+        }
+        ++k;
+      }
+    }
+    if (lg == 0) rec[c.off_count + slot] = (uint8_t)stored;
+  }
+  // the next pass rewrites cnt[] only before its first barrier and off[] only
+  // after it, so no barrier is needed here
+}
+
+// Encode slots [s_begin, s_end) of the record at `rec`, one pass of VPC
+// vectors at a time with the next pass's loads in flight; row(slot) gives the
 // bf16 source of a slot.  Must be called by all 128 threads of the CTA.
 template <int D, int B, bool OUTL, class RowFn>
 __device__ __forceinline__ void encode_record(const CodecDev& c, RowFn row, uint8_t* rec,
                                               int s_begin, int s_end, EncSmem* sm) {
   using E = Enc<D, B, OUTL>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int lg = lane % E::L;   // lane within the vector's group
-  const int vi = lane / E::L;   // vector within the warp pass
-  const uint32_t sbits = c.signs[lg];
-  uint32_t tpos[E::NPOS > 0 ? E::NPOS : 1];
-#pragma unroll
-  for (int k = 0; k < E::NPOS; ++k) tpos[k] = __float_as_uint(c.boundaries[E::HALF + k]);
+  const EncLane<D, B, OUTL> ln(c);
   if (OUTL && threadIdx.x == 0) sm->running = 0;
   if (OUTL) __syncthreads();
-
+  const int pslot = ln.warp * E::VPW + ln.vi;  // slot index within a pass
+  uint4 wn[4];
+  enc_load(row(s_begin + pslot) + ln.lg * 32, s_begin + pslot < s_end, wn);
   for (int base = s_begin; base < s_end; base += E::VPC) {
-    const int pslot = warp * E::VPW + vi;  // slot index within the pass
     const int slot = base + pslot;
     const bool valid = slot < s_end;
+    uint4 w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = wn[k];
+    const int nslot = slot + E::VPC;
+    enc_load(row(nslot) + ln.lg * 32, nslot < s_end, wn);
     float x[32];
-    {
-      uint4 w[4] = {};
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(row(slot) + lg * 32);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[k] = __ldg(src + k);
-      }
-      const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t lo = (ww[k] << 16) ^ (((sbits >> (2 * k)) & 1u) << 31);
-        const uint32_t hi = (ww[k] & 0xFFFF0000u) ^ (((sbits >> (2 * k + 1)) & 1u) << 31);
-        x[2 * k] = __uint_as_float(lo);
-        x[2 * k + 1] = __uint_as_float(hi);
-      }
-    }
-    // ||x||^2 by a pairwise tree (squares of bf16 values are exact in f32)
-    float sq[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) sq[k] = fmaf(x[2 * k], x[2 * k], x[2 * k + 1] * x[2 * k + 1]);
-#pragma unroll
-    for (int h = 8; h; h >>= 1)
-#pragma unroll
-      for (int k = 0; k < h; ++k) sq[k] += sq[k + h];
-    float ss = sq[0];
-#pragma unroll
-    for (int m = 1; m < E::L; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    const float n = sqrtf(ss);
-    const float inv = n > 0.f ? 1.0f / (n * c.sqrt_d) : 0.f;
-
-    fwht_regs<32>(x);
-    fwht_lanes<32>(x, lane, E::L);
-
-    // quantise (mirror of the symmetric table around t = 0) and pack LSB-first
-    uint32_t wd[B];
-#pragma unroll
-    for (int q = 0; q < B; ++q) wd[q] = 0u;
-    uint32_t omask = 0u;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const float y = x[r] * inv;
-      const bool pos = y > 0.f;
-      // non-positive side counts t <= |y| as |y| + 1ulp > t (exact tie rule)
-      const uint32_t a = (__float_as_uint(y) & 0x7FFFFFFFu) + (pos ? 0u : 1u);
-      uint32_t cnt = 0;
-#pragma unroll
-      for (int k = 0; k < E::NPOS; ++k) cnt += (a > tpos[k]) ? 1u : 0u;
-      const uint32_t code = (E::HALF + cnt) ^ (pos ? 0u : (uint32_t)((1 << B) - 1));
-      const int bit = r * B;
-      wd[bit >> 5] |= code << (bit & 31);
-      if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
-      if (OUTL) omask |= (fabsf(y) > c.thr_out ? 1u : 0u) << r;
-    }
-    if (valid) {
-      uint8_t* dstrow = rec + (size_t)slot * E::RB + lg * 4 * B;
-      if constexpr (B == 4) {
-        *reinterpret_cast<uint4*>(dstrow) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-      } else if constexpr (B == 2) {
-        *reinterpret_cast<uint2*>(dstrow) = make_uint2(wd[0], wd[1]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < B; ++q) reinterpret_cast<uint32_t*>(dstrow)[q] = wd[q];
-      }
-      if (lg == 0) reinterpret_cast<float*>(rec + c.off_norm)[slot] = n;
-    }
-    if (OUTL) {
-      // per-vector count (slot stores at most 255), then a CTA prefix sum
-      int lc = __popc(valid ? omask : 0u);
-      int incl = lc;
-#pragma unroll
-      for (int m = 1; m < E::L; m <<= 1) {
-        int o = __shfl_up_sync(0xffffffffu, incl, m, E::L);
-        if (lg >= m) incl += o;
-      }
-      const int excl = incl - lc;  // entries in lanes before this one
-      const int vtot = __shfl_sync(0xffffffffu, incl, E::L - 1, E::L);
-      const int nslot = min(vtot, 255);
-      if (lg == 0) sm->cnt[pslot] = valid ? nslot : 0;
-      __syncthreads();
-      if (warp == 0) {
-        // exclusive prefix over the pass's VPC slots (VPC <= 64)
-        int run = sm->running;
-        for (int k0 = 0; k0 < E::VPC; k0 += 32) {
-          const int v = (k0 + lane < E::VPC) ? sm->cnt[k0 + lane] : 0;
-          int inc = v;
-#pragma unroll
-          for (int m = 1; m < 32; m <<= 1) {
-            int o = __shfl_up_sync(0xffffffffu, inc, m);
-            if (lane >= m) inc += o;
-          }
-          if (k0 + lane < E::VPC) sm->off[k0 + lane] = run + inc - v;
-          run += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        __syncwarp();
-        if (lane == 0) sm->running = run;
-      }
-      __syncthreads();
-      if (valid) {
-        const int off = sm->off[pslot];
-        const int stored = max(0, min(nslot, c.cap - off));
-        uint32_t* ent = reinterpret_cast<uint32_t*>(rec + c.off_entries);
-        int k = excl;
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          if ((omask >> r) & 1u) {
-            if (k < stored) {
-              const uint32_t idx = (uint32_t)(lg * 32 + r);
-              const uint32_t v = f32_to_bf16_rne(x[r] * inv);
-              ent[off + k] = idx | (v << 16);
-            }
-            ++k;
-          }
-        }
-        if (lg == 0) rec[c.off_count + slot] = (uint8_t)stored;
-      }
-      // the next pass rewrites cnt[] only before its first barrier and off[]
-      // only after it, so no barrier is needed here
-    }
+    float inv;
+    uint32_t omask;
+    enc_vector<D, B, OUTL>(c, ln, w, valid, rec, slot, x, inv, omask);
+    if constexpr (OUTL) enc_outliers<D, B>(c, ln, x, inv, omask, valid, rec, slot, pslot, sm);
   }
 }
 
-template <int D, int B, bool OUTL>
-__global__ void __launch_bounds__(kThreads) encode_kernel(const __grid_constant__ EncodeParams p) {
+// Record-aligned encode with outliers: one CTA per record (grid-stride).
+template <int D, int B>
+__global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_constant__ EncodeParams p) {
   __shared__ EncSmem sm;
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
@@ -188,7 +238,45 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(const __grid_constant_
     const uint16_t* src_g = p.src + g * p.src_gs;
     const int64_t vs = p.src_vs, v0 = ci * kChunk - p.first_vec;
     auto row = [&](int slot) { return src_g + (v0 + slot) * vs; };
-    encode_record<D, B, OUTL>(p.c, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
+    encode_record<D, B, true>(p.c, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
+  }
+}
+
+// Encode without outliers: every (group, record, pass) is an independent task
+// of VPC vectors; CTAs stride over tasks with the next task's loads in flight.
+template <int D, int B>
+__global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_constant__ EncodeParams p) {
+  using E = Enc<D, B, false>;
+  constexpr int PPR = kChunk / E::VPC;  // passes per record
+  const EncLane<D, B, false> ln(p.c);
+  const int pslot = ln.warp * E::VPW + ln.vi;
+  const int64_t per_group = p.chunks_per_group * PPR;
+  const int64_t n_tasks = p.n_groups * per_group;
+  const int64_t v_end = p.first_vec + p.n_vec;
+  // task -> (group, token index, validity)
+  auto locate = [&](int64_t task, int64_t& g, int64_t& tok) {
+    g = task / per_group;
+    const int64_t r = task % per_group;
+    tok = (p.first_chunk + r / PPR) * kChunk + (r % PPR) * E::VPC + pslot;
+    return task < n_tasks && tok >= p.first_vec && tok < v_end;
+  };
+  int64_t g, tok;
+  bool valid = locate(blockIdx.x, g, tok);
+  uint4 wn[4];
+  enc_load(p.src + g * p.src_gs + (tok - p.first_vec) * p.src_vs + ln.lg * 32, valid, wn);
+  for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+    uint4 w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = wn[k];
+    const int64_t cg = g, ctok = tok;
+    const bool cvalid = valid;
+    valid = locate(task + gridDim.x, g, tok);
+    enc_load(p.src + g * p.src_gs + (tok - p.first_vec) * p.src_vs + ln.lg * 32, valid, wn);
+    uint8_t* rec = p.dst + cg * p.dst_gs + (ctok / kChunk) * (int64_t)p.c.rec_bytes;
+    float x[32];
+    float inv;
+    uint32_t omask;
+    enc_vector<D, B, false>(p.c, ln, w, cvalid, rec, (int)(ctok % kChunk), x, inv, omask);
   }
 }
 
@@ -208,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   const uint16_t* tail = p.tail + l * p.tail_ls + (int64_t)(b * p.Hkv + h) * p.tail_cap * D;
   const int first = start + e * kChunk;
   const int cap = p.tail_cap;
-  auto row = [&](int slot) { return tail + (int64_t)((first + slot) % cap) * D; };
+  auto row = [&](int slot) { return tail + (int64_t)((first + min(slot, kChunk - 1)) % cap) * D; };
   encode_record<D, B, OUTL>(p.c, row, rec, 0, kChunk, &sm);
 }
 
@@ -226,7 +314,13 @@ __global__ void evict_commit_kernel(const EvictCommitParams p) {
 
 template <int D, int B, bool OUTL>
 static cudaError_t enc_launch(const EncodeParams& p, int grid, cudaStream_t s) {
-  encode_kernel<D, B, OUTL><<<grid, kThreads, 0, s>>>(p);
+  if constexpr (OUTL) {
+    const int64_t tasks = p.n_groups * p.chunks_per_group;
+    encode_record_kernel<D, B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+  } else {
+    const int64_t tasks = p.n_groups * p.chunks_per_group * (kChunk / Enc<D, B, false>::VPC);
+    encode_pass_kernel<D, B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 template <int D, int B, bool OUTL>
