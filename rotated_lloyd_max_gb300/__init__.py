@@ -248,6 +248,8 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     a.tail_start = _ptr(tail_start)
     a.tail_len = _ptr(tail_len)
     a.max_chunks, a.max_tail, a.splits = max_chunks, max_tail, splits
+    # the struct holds raw device pointers: keep the tensors alive with it
+    a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len)
     return a
 
 

@@ -204,6 +204,38 @@ void attn_smem_layout(AttnParams& p, int D, int GT) {
   p.sm_total = off;
 }
 
+void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
+  const int GTP = GT == 6 ? 8 : GT;
+  const int QS = 32 * GTP + (GTP < 4 ? GTP : 4);
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  const bool anyout = p.kout || p.vout;
+  const int vcap = p.shared_kv ? p.kcap : p.vcap;
+  int off = 0;
+  p.sm_q = off;
+  off = al(off + (D / 32) * QS * 4, 16);
+  p.sm_lut = off;
+  off += 32 * 4;
+  p.sm_red = off;
+  off += 2 * 4 * GTP * 4;
+  p.sm_logit = off;
+  off = al(off + 4 * 32 * GTP * 4, 16);
+  p.sm_corr = off;
+  off = al(off + (p.vout ? 4 * D * GTP * 4 : 0), 16);
+  p.sm_pre = off;
+  off = al(off + (anyout ? 2 * 2 * 129 * 4 : 0), 16);
+  p.sm_slot = off;
+  off = al(off + (anyout ? 2 * (p.kcap + vcap) : 0), 16);
+  p.sm_ent_stage = (p.kout ? p.kcap * 4 : 0) + (p.vout && !p.shared_kv ? p.vcap * 4 : 0);
+  p.sm_ent = off;
+  off = al(off + 2 * p.sm_ent_stage, 128);
+  int stage = p.k_main + (p.shared_kv ? 0 : p.v_main);
+  stage = std::max(stage, (4 * D * GTP * 4 + 2) / 3);  // the warps' partials at the end
+  p.sm_stage = al(stage, 128);
+  p.sm_main = off;
+  off += 3 * p.sm_stage;
+  p.sm_total = off;
+}
+
 }  // namespace tq
 
 extern "C" {
@@ -444,11 +476,26 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.tps = pl.tps;
   p.ws_acc = (float*)workspace;
   p.ws_ml = (float*)((char*)workspace + pl.ws_acc_bytes);
-  attn_smem_layout(p, pl.D, pl.GT);
-  if (p.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
-  dim3 grid(pl.S, a->batch * a->n_kv_heads * pl.n_hg, a->n_layers);
-  if (launch_attn(p, pl.D, pl.GT, grid, s) != cudaSuccess) return TQ_ERR_CUDA;
+  const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
+  const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
+  if (rec_kernel) {
+    // compressed splits: warp-local kernel; dense splits: general kernel
+    AttnParams pr = p;
+    attn_rec_smem_layout(pr, pl.D, pl.GT);
+    AttnParams pd = p;
+    pd.split_base = pl.Sc;
+    attn_smem_layout(pd, pl.D, pl.GT);
+    if (pr.sm_total > max_dyn_smem() || pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+    if (launch_attn_rec(pr, pl.D, pl.GT, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (pl.S > pl.Sc &&
+        launch_attn(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), s) != cudaSuccess)
+      return TQ_ERR_CUDA;
+  } else {
+    attn_smem_layout(p, pl.D, pl.GT);
+    if (p.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+    if (launch_attn(p, pl.D, pl.GT, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
   MergeParams m;
   m.ws_acc = p.ws_acc;
   m.ws_ml = p.ws_ml;

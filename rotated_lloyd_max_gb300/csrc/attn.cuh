@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   const int hg = rem % p.n_hg;
   rem /= p.n_hg;
   const int kvh = rem % p.Hkv, b = rem / p.Hkv;
-  const int split = blockIdx.x;
+  const int split = blockIdx.x + p.split_base;
   const int h0 = kvh * p.G + hg * GT;
   const bool comp = split < p.Sc;
   const int lb = l * p.B + b;

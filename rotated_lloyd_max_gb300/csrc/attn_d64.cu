@@ -1,5 +1,6 @@
-// Decode-attention instantiations for head dim 64 (query-head groups of 1, 2, 4, 6, 8).
-#include "attn.cuh"
+// Decode-attention instantiations for head dim 64 (query-head groups of 1, 2, 4, 6, 8):
+// the general kernel and the warp-local kernel for the compressed splits.
+#include "attn_rec.cuh"
 
 namespace tq {
 cudaError_t launch_attn_d64(const AttnParams& p, int GT, dim3 grid, cudaStream_t s) {
@@ -9,6 +10,16 @@ cudaError_t launch_attn_d64(const AttnParams& p, int GT, dim3 grid, cudaStream_t
     case 4: return attn_launch_t<64, 4>(p, grid, s);
     case 6: return attn_launch_t<64, 6>(p, grid, s);
     case 8: return attn_launch_t<64, 8>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+cudaError_t launch_attn_rec_d64(const AttnParams& p, int GT, dim3 grid, cudaStream_t s) {
+  switch (GT) {
+    case 1: return attn_rec_launch_t<64, 1>(p, grid, s);
+    case 2: return attn_rec_launch_t<64, 2>(p, grid, s);
+    case 4: return attn_rec_launch_t<64, 4>(p, grid, s);
+    case 6: return attn_rec_launch_t<64, 6>(p, grid, s);
+    case 8: return attn_rec_launch_t<64, 8>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

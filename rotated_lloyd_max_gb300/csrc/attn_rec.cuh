@@ -1,0 +1,481 @@
+// a6-a8: decode attention over the compressed records (head dims 64 and 128),
+// warp-local variant.
+//
+// Same arithmetic as attn.cuh (q~ = H(s_k . q)/sqrt(d) once per CTA; a record
+// token scores as n_i * q~ . c[codes] from a shared-memory LUT; values
+// accumulate p_i n_i yhat_i in the rotated basis), organised so that a record
+// costs one CTA barrier:
+//  * the CTA stages records global -> shared with cp.async in a 3-deep ring;
+//    warps 0 and 1 turn a record's per-slot outlier counts into prefix sums and
+//    fetch just the used entries, one record ahead;
+//  * each warp owns 32 of the record's 128 tokens end to end: scores (a lane
+//    holds 4 tokens x one 32-coordinate slice, so a q~ load serves 4 tokens,
+//    then a transposed shuffle reduction leaves each lane with one token's
+//    logits), an online softmax whose running max only moves when a logit
+//    exceeds it by 2^8 (warp vote), and the value accumulation (a lane holds 4
+//    coordinates x GT heads in registers);
+//  * outlier entries are applied as deltas (stored value - centroid) through
+//    per-warp shared-memory atomics on the logits and on a value correction
+//    buffer;
+//  * at the end the 4 warps' (m, l, acc) are merged in shared memory into the
+//    split's partial.
+#pragma once
+
+#include "attn.cuh"
+
+namespace tq {
+
+template <int D, int GT>
+struct RCfg {
+  static constexpr int SL = D / 32;          // lanes per token in the score phase
+  static constexpr int TPL = SL;             // tokens per lane in the score phase
+  static constexpr int QR = 32 / SL;         // token rows per warp in the score phase
+  static constexpr int GTP = (GT == 6) ? 8 : GT;
+  static constexpr int GH = (GT + 1) / 2;
+  static constexpr int QPAD = GTP < 4 ? GTP : 4;
+  static constexpr int QS = 32 * GTP + QPAD;  // floats per slice of q~
+  static constexpr int LPT = D / 4;           // value phase: lanes per token
+  static constexpr int TLW = 32 / LPT;        // value phase: token lanes per warp
+};
+
+// Transposed reduction of a[TPL][GH] over the SL lanes of a token group:
+// afterwards lane s of the group holds the full sums of its token s.
+template <int SL, int GH>
+__device__ __forceinline__ void reduce_transpose(float2 (&a)[SL][GH], int s, float2 (&out)[GH]) {
+  if constexpr (SL == 4) {
+    const bool h1 = (s >> 1) & 1, h0 = s & 1;
+    float2 b[2][GH];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+      for (int k = 0; k < GH; ++k) {
+        const float2 send = h1 ? a[kk][k] : a[2 + kk][k];
+        const float2 keep = h1 ? a[2 + kk][k] : a[kk][k];
+        float2 r;
+        r.x = __shfl_xor_sync(0xffffffffu, send.x, 2);
+        r.y = __shfl_xor_sync(0xffffffffu, send.y, 2);
+        b[kk][k] = add2(keep, r);
+      }
+#pragma unroll
+    for (int k = 0; k < GH; ++k) {
+      const float2 send = h0 ? b[0][k] : b[1][k];
+      const float2 keep = h0 ? b[1][k] : b[0][k];
+      float2 r;
+      r.x = __shfl_xor_sync(0xffffffffu, send.x, 1);
+      r.y = __shfl_xor_sync(0xffffffffu, send.y, 1);
+      out[k] = add2(keep, r);
+    }
+  } else {  // SL == 2
+    const bool h0 = s & 1;
+#pragma unroll
+    for (int k = 0; k < GH; ++k) {
+      const float2 send = h0 ? a[0][k] : a[1][k];
+      const float2 keep = h0 ? a[1][k] : a[0][k];
+      float2 r;
+      r.x = __shfl_xor_sync(0xffffffffu, send.x, 1);
+      r.y = __shfl_xor_sync(0xffffffffu, send.y, 1);
+      out[k] = add2(keep, r);
+    }
+  }
+}
+
+// Score partials of TPL tokens x one 32-coordinate slice.
+template <int B, int GT, int GTP, int TPL>
+__device__ __forceinline__ void score_tokens(const unsigned char* kcodes, int rb, const int (&tok)[TPL],
+                                             int slice, const float* qs, const float* lut,
+                                             float2 (&a)[TPL][(GT + 1) / 2]) {
+  uint32_t w[TPL][B];
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) load_words<B>(kcodes + tok[i] * rb + slice * 4 * B, w[i]);
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    float2 q[(GT + 1) / 2];
+    load_heads<GT>(qs + r * GTP, q);
+#pragma unroll
+    for (int i = 0; i < TPL; ++i) {
+      const float cv = lut[code_of<B>(w[i], r)];
+#pragma unroll
+      for (int k = 0; k < (GT + 1) / 2; ++k) a[i][k] = fma2(make_float2(cv, cv), q[k], a[i][k]);
+    }
+  }
+}
+
+// Value accumulation of the warp's tokens tl, tl + TLW, ... < 32 for the
+// lane's 4 coordinates 4g..4g+3.
+template <int B, int GT, int GTP, int TLW>
+__device__ __forceinline__ void pv_tokens(const unsigned char* vrows, int rb, const float* pw,
+                                          const float* lut, int g, int tl,
+                                          float2 (&acc)[4][(GT + 1) / 2]) {
+  const int bit0 = 4 * g * B, wi = bit0 >> 5, sh = bit0 & 31;
+#pragma unroll 4
+  for (int t = tl; t < 32; t += TLW) {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(vrows + t * rb);
+    uint32_t v;
+    if constexpr (B == 3) {
+      v = __funnelshift_r(row[wi], row[wi + 1], sh);
+    } else {
+      v = row[wi] >> sh;
+    }
+    float2 pp[(GT + 1) / 2];
+    load_heads<GT>(pw + t * GTP, pp);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float val = lut[(v >> (c * B)) & ((1u << B) - 1u)];
+#pragma unroll
+      for (int k = 0; k < (GT + 1) / 2; ++k) acc[c][k] = fma2(make_float2(val, val), pp[k], acc[c][k]);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t code_in_row(const unsigned char* row, int idx, int b) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(row);
+  const int bit = idx * b;
+  return __funnelshift_r(r[bit >> 5], r[(bit >> 5) + 1], bit & 31) & ((1u << b) - 1u);
+}
+
+template <int D, int GT>
+__global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constant__ AttnParams p) {
+  using C = RCfg<D, GT>;
+  constexpr int GTP = C::GTP, GH = C::GH, SL = C::SL, TPL = C::TPL, QR = C::QR, LPT = C::LPT, TLW = C::TLW;
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* qv = reinterpret_cast<float*>(sm + p.sm_q);
+  float* lutk = reinterpret_cast<float*>(sm + p.sm_lut);
+  float* lutv = lutk + 16;
+  float* pbuf = reinterpret_cast<float*>(sm + p.sm_logit);  // [4][32][GTP]
+  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);   // [4][D][GTP]
+  int* pre = reinterpret_cast<int*>(sm + p.sm_pre);         // [2][2][129]
+  uint8_t* slotof = sm + p.sm_slot;                        // [2][2][cap]
+  unsigned char* mainb = sm + p.sm_main;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int l = blockIdx.z;
+  int rem = blockIdx.y;
+  const int hg = rem % p.n_hg;
+  rem /= p.n_hg;
+  const int kvh = rem % p.Hkv, b = rem / p.Hkv;
+  const int split = blockIdx.x;
+  const int h0 = kvh * p.G + hg * GT;
+  const int lb = l * p.B + b;
+  const int64_t qh0 = (int64_t)lb * p.Hq + h0;
+  const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
+  const int t_begin = split * p.cps, t_end = min(t_begin + p.cps, nch);
+  if (t_begin >= t_end) {
+    if (tid < GT) {
+      float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+    }
+    return;
+  }
+  const int n = t_end - t_begin;
+  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
+  const uint8_t* vb0 = p.shared_kv ? kb0
+                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  const int kcap = p.kcap, vcap = p.shared_kv ? p.kcap : p.vcap;
+  const bool kout = p.kout, vout = p.vout;
+  auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
+  auto entk = [&](int i) { return reinterpret_cast<uint32_t*>(sm + p.sm_ent + (i & 1) * p.sm_ent_stage); };
+  auto entv = [&](int i) { return p.shared_kv ? entk(i) : entk(i) + kcap * p.kout; };
+  auto prek = [&](int i) { return pre + ((i & 1) * 2) * 129; };
+  auto prev = [&](int i) { return p.shared_kv ? prek(i) : pre + ((i & 1) * 2 + 1) * 129; };
+  auto slotk = [&](int i) { return slotof + (i & 1) * (kcap + vcap); };
+  auto slotv = [&](int i) { return p.shared_kv ? slotk(i) : slotk(i) + kcap; };
+
+  auto issue_main = [&](int i) {
+    if (i < n) {
+      const int64_t c = t_begin + i;
+      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+    }
+    cp_async_commit();
+  };
+  // warps 0 (keys) and 1 (values): prefix sums of the per-slot counts, the
+  // entry -> slot map, and the copy of exactly the used entries
+  auto prefix_issue = [&](int i) {
+    const bool isk = warp == 0;
+    if (i < n && warp < 2 && (isk ? kout : (vout && !p.shared_kv))) {
+      const unsigned char* cnts = isk ? stage(i) + p.k_off_count : stage(i) + p.k_main + p.v_off_count;
+      int* pr = isk ? prek(i) : pre + ((i & 1) * 2 + 1) * 129;
+      uint8_t* so = isk ? slotk(i) : slotk(i) + kcap;
+      const int cap = isk ? kcap : p.vcap;
+      const uint32_t c4 = reinterpret_cast<const uint32_t*>(cnts)[lane];
+      const int n0 = c4 & 0xff, n1 = (c4 >> 8) & 0xff, n2 = (c4 >> 16) & 0xff, n3 = c4 >> 24;
+      const int tot = n0 + n1 + n2 + n3;
+      int inc = tot;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, m);
+        if (lane >= m) inc += o;
+      }
+      const int ex = inc - tot;
+      pr[4 * lane] = ex;
+      pr[4 * lane + 1] = ex + n0;
+      pr[4 * lane + 2] = ex + n0 + n1;
+      pr[4 * lane + 3] = ex + n0 + n1 + n2;
+      if (lane == 31) pr[128] = inc;
+      int e = ex;
+      const int ns[4] = {n0, n1, n2, n3};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        for (int k = 0; k < ns[q]; ++k, ++e)
+          if (e < cap) so[e] = (uint8_t)(4 * lane + q);
+      const int E = min(__shfl_sync(0xffffffffu, inc, 31), cap);
+      const int64_t c = t_begin + i;
+      const unsigned char* src = isk ? kb0 + c * p.krec_bytes + p.k_off_ent : vb0 + c * p.vrec_bytes + p.v_off_ent;
+      char* dst = reinterpret_cast<char*>(isk ? entk(i) : entk(i) + kcap * p.kout);
+      const int bytes = (E * 4 + 15) & ~15;
+      for (int off = lane * 16; off < bytes; off += 32 * 16) cp_async16(dst + off, src + off);
+    }
+    cp_async_commit();
+  };
+
+  // first records go out before the query work so their latency overlaps it
+  issue_main(0);
+  issue_main(1);
+
+  // ---- query: load, rotate, store as [slice][32][GTP]
+  for (int hh = warp; hh < GT; hh += 4) {
+    constexpr int R = D / 32;
+    const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + hh) * D + lane * R;
+    float x[R];
+#pragma unroll
+    for (int r = 0; r < R; r += 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + r);
+      x[r] = bf16_lo(w);
+      x[r + 1] = bf16_hi(w);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int j = lane * R + r;
+      if ((p.ksign[j >> 5] >> (j & 31)) & 1u) x[r] = -x[r];
+    }
+    fwht_regs<R>(x);
+    fwht_lanes<R>(x, lane, 32);
+    const float f = inv_sqrt_dim<D>();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int j = lane * R + r;
+      qv[(j >> 5) * C::QS + (j & 31) * GTP + hh] = x[r] * f;
+    }
+  }
+  if (GTP != GT)
+    for (int i = tid; i < D; i += kThreads)
+#pragma unroll
+      for (int hh = GT; hh < GTP; ++hh) qv[(i >> 5) * C::QS + (i & 31) * GTP + hh] = 0.f;
+  if (tid < 16) {
+    lutk[tid] = p.kc[tid];
+    lutv[tid] = p.vc[tid];
+  }
+  if (vout)
+    for (int i = tid; i < 4 * D * GTP; i += kThreads) corr[i] = 0.f;
+
+  // per-warp state
+  float m_w[GT], l_ln[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    m_w[h] = -INFINITY;
+    l_ln[h] = 0.f;
+  }
+  float2 acc[4][GH];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < GH; ++k) acc[c][k] = make_float2(0.f, 0.f);
+  const int q = lane / SL, s = lane % SL;          // score phase
+  const int tl = lane / LPT, g = lane % LPT;       // value phase
+  const int tloc = q + QR * s;                     // the token whose logits this lane ends with
+  float* pw = pbuf + warp * 32 * GTP;
+  float* cw = corr + warp * D * GTP;
+  const int rbk = D * p.kb / 8, rbv = D * p.vb / 8;
+
+  cp_async_wait<0>();
+  __syncthreads();
+  prefix_issue(0);
+  for (int i = 0; i < n; ++i) {
+    cp_async_wait<0>();
+    __syncthreads();  // record i+1 and the entries of record i are in; record i-1 is done
+    issue_main(i + 2);
+    prefix_issue(i + 1);
+
+    const unsigned char* st = stage(i);
+    const unsigned char* kcodes = st + warp * 32 * rbk;  // the warp's 32 rows
+    const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + warp * 32;
+    const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
+    const unsigned char* vcodes = vbase + warp * 32 * rbv;
+    const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
+
+    // ---- scores
+    float lg[GT];
+    {
+      float2 a[TPL][GH];
+#pragma unroll
+      for (int i2 = 0; i2 < TPL; ++i2)
+#pragma unroll
+        for (int k = 0; k < GH; ++k) a[i2][k] = make_float2(0.f, 0.f);
+      int tok[TPL];
+#pragma unroll
+      for (int i2 = 0; i2 < TPL; ++i2) tok[i2] = q + QR * i2;
+      const float* qs = qv + s * C::QS;
+      switch (p.kb) {
+        case 1: score_tokens<1, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+        case 2: score_tokens<2, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+        case 3: score_tokens<3, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+        default: score_tokens<4, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+      }
+      float2 r[GH];
+      reduce_transpose<SL, GH>(a, s, r);
+      const float f = knorm[tloc] * p.sscale;
+#pragma unroll
+      for (int h = 0; h < GT; ++h) lg[h] = ((h & 1) ? r[h >> 1].y : r[h >> 1].x) * f;
+    }
+    if (kout) {
+      // keys' outlier entries of the warp's tokens: logit += (val - c) q~_idx n scale
+#pragma unroll
+      for (int h = 0; h < GT; ++h) pw[tloc * GTP + h] = lg[h];
+      __syncwarp();
+      const int* pk = prek(i);
+      const int e0 = min(pk[warp * 32], kcap), e1 = min(pk[warp * 32 + 32], kcap);
+      const uint32_t* ek = entk(i);
+      const uint8_t* sk = slotk(i);
+      const unsigned char* krows = st;
+      const float* kn = reinterpret_cast<const float*>(st + p.k_off_norm);
+      for (int e = e0 + lane; e < e1; e += 32) {
+        const uint32_t v = ek[e];
+        const int idx = (int)(v & 0xFFFFu) & (D - 1);
+        const int slot = sk[e];
+        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutk[code_in_row(krows + slot * rbk, idx, p.kb)];
+        const float f = delta * kn[slot] * p.sscale;
+        const float* qj = qv + (idx >> 5) * C::QS + (idx & 31) * GTP;
+#pragma unroll
+        for (int h = 0; h < GT; ++h) atomicAdd(&pw[(slot - warp * 32) * GTP + h], f * qj[h]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < GT; ++h) lg[h] = pw[tloc * GTP + h];
+    }
+
+    // ---- online softmax (warp-local, the max moves only when a logit passes it by 2^8)
+    {
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < GT; ++h) need |= lg[h] > m_w[h] + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        float al[GT];
+#pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          const float mn = fmaxf(m_w[h], warp_max(lg[h]));
+          al[h] = exp2f(m_w[h] - mn);
+          m_w[h] = mn;
+          l_ln[h] *= al[h];
+        }
+#pragma unroll
+        for (int k = 0; k < GH; ++k) {
+          const float2 a2 = make_float2(al[2 * k], (2 * k + 1 < GT) ? al[2 * k + 1] : 0.f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[c][k] = mul2(acc[c][k], a2);
+        }
+        if (vout) {
+          for (int j = lane; j < D; j += 32)
+#pragma unroll
+            for (int h = 0; h < GT; ++h) cw[j * GTP + h] *= al[h];
+        }
+      }
+      const float vn = vnorm[tloc];
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        const float pe = exp2f(lg[h] - m_w[h]);
+        l_ln[h] += pe;
+        pw[tloc * GTP + h] = pe * vn;
+      }
+      __syncwarp();
+    }
+
+    // ---- values
+    if (vout) {
+      const int* pv = prev(i);
+      const int e0 = min(pv[warp * 32], vcap), e1 = min(pv[warp * 32 + 32], vcap);
+      const uint32_t* ev = entv(i);
+      const uint8_t* sv = slotv(i);
+      for (int e = e0 + lane; e < e1; e += 32) {
+        const uint32_t v = ev[e];
+        const int idx = (int)(v & 0xFFFFu) & (D - 1);
+        const int slot = sv[e];
+        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vbase + slot * rbv, idx, p.vb)];
+        const float* pp = pw + (slot - warp * 32) * GTP;
+#pragma unroll
+        for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pp[h] * delta);
+      }
+    }
+    switch (p.vb) {
+      case 1: pv_tokens<1, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+      case 2: pv_tokens<2, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+      case 3: pv_tokens<3, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+      default: pv_tokens<4, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+    }
+  }
+
+  // ---- merge the warps' (m, l, acc) into the split's partial
+#pragma unroll
+  for (int h = 0; h < GT; ++h) l_ln[h] = warp_sum(l_ln[h]);
+  if constexpr (TLW == 2) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int k = 0; k < GH; ++k) {
+        acc[c][k].x += __shfl_xor_sync(0xffffffffu, acc[c][k].x, 16);
+        acc[c][k].y += __shfl_xor_sync(0xffffffffu, acc[c][k].y, 16);
+      }
+  }
+  __syncwarp();
+  cp_async_wait<0>();
+  __syncthreads();  // all records consumed: the staging ring becomes the merge buffer
+  float* red = reinterpret_cast<float*>(mainb);          // [4][D][GTP]
+  float* wml = reinterpret_cast<float*>(sm + p.sm_red);  // [4][2][GTP]
+  if (tl == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        float v = (h & 1) ? acc[c][h >> 1].y : acc[c][h >> 1].x;
+        if (vout) v += cw[(4 * g + c) * GTP + h];
+        red[(warp * D + 4 * g + c) * GTP + h] = v;
+      }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      wml[(warp * 2) * GTP + h] = m_w[h];
+      wml[(warp * 2 + 1) * GTP + h] = l_ln[h];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < GT * D; idx += kThreads) {
+    const int h = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 2) * GTP + h]);
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) v = fmaf(exp2f(wml[(w * 2) * GTP + h] - M), red[(w * D + j) * GTP + h], v);
+    p.ws_acc[((qh0 + h) * p.S + split) * D + j] = v;
+    if (j == 0) {
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) L = fmaf(exp2f(wml[(w * 2) * GTP + h] - M), wml[(w * 2 + 1) * GTP + h], L);
+      float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+      ml[0] = M;
+      ml[1] = L;
+    }
+  }
+}
+
+template <int D, int GT>
+cudaError_t attn_rec_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_rec_kernel<D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       p.sm_total);
+  if (e != cudaSuccess) return e;
+  attn_rec_kernel<D, GT><<<grid, kThreads, p.sm_total, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -111,6 +111,17 @@ cudaError_t launch_attn_d128(const AttnParams& p, int GT, dim3 grid, cudaStream_
 cudaError_t launch_attn_d256(const AttnParams& p, int GT, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_d512(const AttnParams& p, int GT, dim3 grid, cudaStream_t s);
 
+cudaError_t launch_attn_rec_d64(const AttnParams& p, int GT, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_rec_d128(const AttnParams& p, int GT, dim3 grid, cudaStream_t s);
+
+cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s) {
+  switch (D) {
+    case 64: return launch_attn_rec_d64(p, GT, grid, s);
+    case 128: return launch_attn_rec_d128(p, GT, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s) {
   switch (D) {
     case 64: return launch_attn_d64(p, GT, grid, s);

@@ -83,6 +83,7 @@ struct AttnParams {
   const int32_t* tail_start;
   const int32_t* tail_len;
   int S, Sc, cps, tps;
+  int split_base;  // index of the first split a launch covers (dense-only launches)
   float* ws_acc;
   float* ws_ml;
   // dynamic shared memory carve-up (bytes)
@@ -106,11 +107,14 @@ cudaError_t launch_evict(const EvictParams& p, cudaStream_t s);
 cudaError_t launch_evict_commit(const EvictCommitParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
+// warp-local kernel for the compressed splits (head dims 64 and 128)
+cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 
 // Dynamic shared memory of the attention kernel for head dim D and head group GT
 // (everything but the record-size dependent parts is fixed by D and GT).
 void attn_smem_layout(AttnParams& p, int D, int GT);
+void attn_rec_smem_layout(AttnParams& p, int D, int GT);
 
 // The codebook kernel writes this block into the caller's scratch.
 struct CodebookOut {

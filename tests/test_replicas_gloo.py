@@ -1,0 +1,48 @@
+"""The multi-GPU path is replicas only (the codec and attention have no
+cross-GPU exchange step): every rank runs the whole workload and the bench
+reports total work over the slowest rank.  This checks that host logic with
+two gloo ranks on CPU."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    import sys
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank), TQ_BENCH_BACKEND="gloo")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import bench
+    w, r, local, pg = bench.dist_init(world)
+    assert (w, r) == (world, rank)
+    # rank r "took" 1 + r seconds and processed 10 * (r + 1) bytes
+    t = bench.max_over_ranks(pg, 1.0 + rank, "cpu")
+    nb = bench.sum_over_ranks(pg, 10.0 * (rank + 1), "cpu")
+    bench.barrier(pg)
+    out.put((rank, t, nb))
+    pg.destroy_process_group()
+
+
+def test_two_rank_reduction_on_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
