@@ -137,15 +137,15 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   const int64_t max_tail = pl->has_tail ? a->max_tail : 0;
   const int64_t tail_tiles = cdiv(max_tail, TT);
   const int64_t units = (int64_t)a->n_layers * a->batch * a->n_kv_heads * pl->n_hg;
-  int64_t want = a->splits > 0 ? a->splits : std::max<int64_t>(1, cdiv(4LL * num_sms(), units));
-  want = std::min<int64_t>(want, 1000);  // the merge keeps <= 1024 split weights
-  const int64_t tok_c = comp_tiles * TQ_CHUNK, tok_t = max_tail;
+  // Splits per (layer, batch, kv head, head group): enough CTAs for several
+  // waves on every SM.  Records and dense tokens get their own budgets: a
+  // call may mix compressed layers with bf16 layers, whose splits then exit
+  // at once on the layers that lack that kind of token.
+  int64_t want = a->splits > 0 ? a->splits : std::max<int64_t>(1, cdiv(16LL * num_sms(), units));
+  want = std::min<int64_t>(want, 500);  // the merge keeps <= 1024 split weights
   int64_t Sc = 0, St = 0;
-  if (comp_tiles > 0) {
-    Sc = tok_t > 0 ? (want * tok_c + (tok_c + tok_t) / 2) / (tok_c + tok_t) : want;
-    Sc = std::max<int64_t>(1, std::min(Sc, comp_tiles));
-  }
-  if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want - Sc, tail_tiles));
+  if (comp_tiles > 0) Sc = std::max<int64_t>(1, std::min(want, comp_tiles));
+  if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want, tail_tiles));
   int64_t cps = 1, tps = TT;
   if (Sc > 0) {
     cps = cdiv(comp_tiles, Sc);
@@ -208,8 +208,6 @@ void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
   const int GTP = GT == 6 ? 8 : GT;
   const int QS = 32 * GTP + (GTP < 4 ? GTP : 4);
   auto al = [](int x, int a) { return (x + a - 1) / a * a; };
-  const bool anyout = p.kout || p.vout;
-  const int vcap = p.shared_kv ? p.kcap : p.vcap;
   int off = 0;
   p.sm_q = off;
   off = al(off + (D / 32) * QS * 4, 16);
@@ -220,19 +218,18 @@ void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
   p.sm_logit = off;
   off = al(off + 4 * 32 * GTP * 4, 16);
   p.sm_corr = off;
-  off = al(off + (p.vout ? 4 * D * GTP * 4 : 0), 16);
-  p.sm_pre = off;
-  off = al(off + (anyout ? 2 * 2 * 129 * 4 : 0), 16);
-  p.sm_slot = off;
-  off = al(off + (anyout ? 2 * (p.kcap + vcap) : 0), 16);
-  p.sm_ent_stage = (p.kout ? p.kcap * 4 : 0) + (p.vout && !p.shared_kv ? p.vcap * 4 : 0);
-  p.sm_ent = off;
-  off = al(off + 2 * p.sm_ent_stage, 128);
-  int stage = p.k_main + (p.shared_kv ? 0 : p.v_main);
-  stage = std::max(stage, (4 * D * GTP * 4 + 2) / 3);  // the warps' partials at the end
+  off = al(off + (p.vout ? 4 * D * GTP * 4 : 0), 128);
+  p.sm_pre = p.sm_slot = p.sm_ent = off;  // unused by this kernel
+  p.sm_ent_stage = 0;
+  int stage = p.krec ? p.k_main + (p.shared_kv ? 0 : p.v_main) : 0;
+  stage = std::max(stage, (4 * D * GTP * 4 + 1) / 2);  // the warps' partials at the end
+  if (p.ktail) {  // dense splits of the same launch: bf16 K/V tiles and their partials
+    stage = std::max(stage, 2 * (4096 / D) * D * 2);
+    stage = std::max(stage, ((128 / (D / 4)) * D * GTP * 4 + 1) / 2);
+  }
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
-  off += 3 * p.sm_stage;
+  off += 2 * p.sm_stage;
   p.sm_total = off;
 }
 
@@ -480,17 +477,11 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
   const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
   if (rec_kernel) {
-    // compressed splits: warp-local kernel; dense splits: general kernel
-    AttnParams pr = p;
-    attn_rec_smem_layout(pr, pl.D, pl.GT);
-    AttnParams pd = p;
-    pd.split_base = pl.Sc;
-    attn_smem_layout(pd, pl.D, pl.GT);
-    if (pr.sm_total > max_dyn_smem() || pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-    if (launch_attn_rec(pr, pl.D, pl.GT, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-    if (pl.S > pl.Sc &&
-        launch_attn(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), s) != cudaSuccess)
-      return TQ_ERR_CUDA;
+    // compressed splits on the warp-local path, dense splits on the general
+    // dense path, one launch
+    attn_rec_smem_layout(p, pl.D, pl.GT);
+    if (p.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+    if (launch_attn_rec(p, pl.D, pl.GT, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
   } else {
     attn_smem_layout(p, pl.D, pl.GT);
     if (p.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;

@@ -147,6 +147,182 @@ __device__ __forceinline__ void pv_codes(const unsigned char* vcodes, int rb, co
   }
 }
 
+// One dense split: bf16 tokens (a tail ring or a whole bf16 layer) attended
+// in the original basis, 4096/D tokens per tile staged by cp.async in a
+// 2-deep ring, online softmax across the CTA.  Writes the split's partial.
+template <int D, int GT>
+__device__ __forceinline__ void attn_dense_split(const AttnParams& p, unsigned char* sm, int l, int b,
+                                                 int kvh, int h0, int split, int64_t qh0, int t_begin,
+                                                 int t_end) {
+  using C = ACfg<D, GT>;
+  constexpr int GTP = C::GTP, GH = C::GH, SL = C::SL, TT = C::TT, CG = C::CG, TL = C::TL;
+  float* qv = reinterpret_cast<float*>(sm + p.sm_q);
+  float* redm = reinterpret_cast<float*>(sm + p.sm_red);
+  float* reds = redm + 4 * GTP;
+  float* logit = reinterpret_cast<float*>(sm + p.sm_logit);
+  unsigned char* mainb = sm + p.sm_main;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lb = l * p.B + b;
+  const int tstart = p.tail_start ? ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap : 0;
+  const uint16_t* kt0 = p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+  const uint16_t* vt0 = p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+  const int n_tiles = (t_end - t_begin + TT - 1) / TT;
+  constexpr int TB = TT * D * 2;  // bytes of one stream's tile
+  auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
+  auto issue = [&](int i) {
+    if (i < n_tiles) {
+      const int tok0 = t_begin + i * TT;
+      const int cnt = min(TT, t_end - tok0);
+      unsigned char* s = stage(i);
+      for (int pc = tid; pc < TT * (D / 8); pc += kThreads) {
+        const int tok = pc / (D / 8), part = pc % (D / 8);
+        if (tok < cnt) {
+          const int64_t slot = (tstart + tok0 + tok) % p.tail_cap;
+          cp_async16(s + (tok * D + part * 8) * 2, kt0 + slot * D + part * 8);
+          cp_async16(s + TB + (tok * D + part * 8) * 2, vt0 + slot * D + part * 8);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  // query (original basis) as [slice][32][GTP]
+  for (int hh = warp; hh < GT; hh += 4) {
+    constexpr int R = D / 32;
+    const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + hh) * D + lane * R;
+#pragma unroll
+    for (int r = 0; r < R; r += 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + r);
+      const int j = lane * R + r;
+      qv[(j >> 5) * C::QS + (j & 31) * GTP + hh] = bf16_lo(w);
+      qv[((j + 1) >> 5) * C::QS + ((j + 1) & 31) * GTP + hh] = bf16_hi(w);
+    }
+  }
+  if (GTP != GT)
+    for (int i = tid; i < D; i += kThreads)
+#pragma unroll
+      for (int hh = GT; hh < GTP; ++hh) qv[(i >> 5) * C::QS + (i & 31) * GTP + hh] = 0.f;
+
+  float m_run[GT], l_run[GT], alpha[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+  }
+  float2 acc[4][GH];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < GH; ++k) acc[c][k] = make_float2(0.f, 0.f);
+  const int g = tid % CG, tl = tid / CG;
+  const int stok = tid / SL, slice = tid % SL;
+  for (int i = 0; i < n_tiles; ++i) {
+    cp_async_wait<0>();
+    __syncthreads();  // tile i is in; tile i-1 is done with
+    issue(i + 1);
+    const int ntok = min(TT, t_end - (t_begin + i * TT));
+    const unsigned char* s = stage(i);
+    {
+      float2 a[GH];
+#pragma unroll
+      for (int k = 0; k < GH; ++k) a[k] = make_float2(0.f, 0.f);
+      if (stok < ntok) {
+        const uint4* kr = reinterpret_cast<const uint4*>(s + (stok * D + slice * 32) * 2);
+        const float* qs = qv + slice * C::QS;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint4 w = kr[k4];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float kv = (u & 1) ? bf16_hi(ww[u >> 1]) : bf16_lo(ww[u >> 1]);
+            float2 q[GH];
+            load_heads<GT>(qs + (k4 * 8 + u) * GTP, q);
+#pragma unroll
+            for (int k = 0; k < GH; ++k) a[k] = fma2(make_float2(kv, kv), q[k], a[k]);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < SL; m <<= 1)
+#pragma unroll
+        for (int k = 0; k < GH; ++k) {
+          a[k].x += __shfl_xor_sync(0xffffffffu, a[k].x, m);
+          a[k].y += __shfl_xor_sync(0xffffffffu, a[k].y, m);
+        }
+      if (slice == 0 && stok < ntok) {
+#pragma unroll
+        for (int h = 0; h < GT; ++h) logit[stok * GTP + h] = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * p.sscale;
+      }
+    }
+    __syncthreads();
+    // online softmax over the tile (CTA-wide)
+    {
+      float v[GT];
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        v[h] = tid < ntok ? logit[tid * GTP + h] : -INFINITY;
+        const float mx = warp_max(v[h]);
+        if (lane == 0) redm[warp * GTP + h] = mx;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        const float mx = fmaxf(fmaxf(redm[h], redm[GTP + h]), fmaxf(redm[2 * GTP + h], redm[3 * GTP + h]));
+        const float mnew = fmaxf(m_run[h], mx);
+        alpha[h] = exp2f(m_run[h] - mnew);
+        m_run[h] = mnew;
+        const float pe = tid < ntok ? exp2f(v[h] - mnew) : 0.f;
+        if (tid < ntok) logit[tid * GTP + h] = pe;
+        const float sum = warp_sum(pe);
+        if (lane == 0) reds[warp * GTP + h] = sum;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < GT; ++h)
+        l_run[h] = l_run[h] * alpha[h] + ((reds[h] + reds[GTP + h]) + (reds[2 * GTP + h] + reds[3 * GTP + h]));
+    }
+#pragma unroll
+    for (int k = 0; k < GH; ++k) {
+      const float2 a2 = make_float2(alpha[2 * k], (2 * k + 1 < GT) ? alpha[2 * k + 1] : 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c][k] = mul2(acc[c][k], a2);
+    }
+    for (int t = tl; t < ntok; t += TL) {
+      const uint2 w = *reinterpret_cast<const uint2*>(s + TB + (t * D + 4 * g) * 2);
+      const float vv[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+      float2 pp[GH];
+      load_heads<GT>(logit + t * GTP, pp);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < GH; ++k) acc[c][k] = fma2(make_float2(vv[c], vv[c]), pp[k], acc[c][k]);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  float* part = reinterpret_cast<float*>(mainb);  // [TL][D][GTP]
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int h = 0; h < GT; ++h) part[(tl * D + 4 * g + c) * GTP + h] = (h & 1) ? acc[c][h >> 1].y : acc[c][h >> 1].x;
+  __syncthreads();
+  for (int i = tid; i < GT * D; i += kThreads) {
+    const int h = i / D, j = i % D;
+    float sum = 0.f;
+#pragma unroll
+    for (int t = 0; t < TL; ++t) sum += part[(t * D + j) * GTP + h];
+    p.ws_acc[((qh0 + h) * p.S + split) * D + j] = sum;
+  }
+#pragma unroll
+  for (int h = 0; h < GT; ++h)
+    if (tid == h) {
+      float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+      ml[0] = m_run[h];
+      ml[1] = l_run[h];
+    }
+}
+
 template <int D, int GT>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = ACfg<D, GT>;
@@ -193,6 +369,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       ml[0] = -INFINITY;
       ml[1] = 0.f;
     }
+    return;
+  }
+  if (!comp) {
+    attn_dense_split<D, GT>(p, sm, l, b, kvh, h0, split, qh0, t_begin, t_end);
     return;
   }
 
@@ -261,36 +441,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     cp_async_commit();
   };
 
-  // ---- dense splits: bf16 tile staging
-  const int tstart = (!comp && p.tail_start) ? ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap : 0;
-  const uint16_t* kt0 = comp ? nullptr : p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
-  const uint16_t* vt0 = comp ? nullptr : p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
-  const int n_tiles = (n_tiles_c + TT - 1) / TT;
-  constexpr int TB = TT * D * 2;  // bytes of one stream's tile
-  auto issue_dense = [&](int i) {
-    if (i < n_tiles) {
-      const int tok0 = t_begin + i * TT;
-      const int cnt = min(TT, t_end - tok0);
-      unsigned char* s = stage(i);
-      for (int pc = tid; pc < TT * (D / 8); pc += kThreads) {
-        const int tok = pc / (D / 8), part = pc % (D / 8);
-        if (tok < cnt) {
-          const int64_t slot = (tstart + tok0 + tok) % p.tail_cap;
-          cp_async16(s + (tok * D + part * 8) * 2, kt0 + slot * D + part * 8);
-          cp_async16(s + TB + (tok * D + part * 8) * 2, vt0 + slot * D + part * 8);
-        }
-      }
-    }
-    cp_async_commit();
-  };
   // the first copies go out before the query work so their latency overlaps it
-  if (comp) {
-    issue_main(0);
-    issue_main(1);
-  } else {
-    issue_dense(0);
-    issue_dense(1);
-  }
+  issue_main(0);
+  issue_main(1);
 
   // ---- query: load, rotate (compressed split), store as [slice][32][GTP]
   for (int hh = warp; hh < GT; hh += 4) {
@@ -478,55 +631,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
               *cp = 0.f;
             }
         }
-      }
-      __syncthreads();
-    }
-  } else {
-    for (int i = 0; i < n_tiles; ++i) {
-      issue_dense(i + 2);
-      cp_async_wait<2>();
-      __syncthreads();
-      const int ntok = min(TT, t_end - (t_begin + i * TT));
-      const unsigned char* s = stage(i);
-      {
-        float2 a[GH];
-#pragma unroll
-        for (int k = 0; k < GH; ++k) a[k] = make_float2(0.f, 0.f);
-        if (stok < ntok) {
-          const uint4* kr = reinterpret_cast<const uint4*>(s + (stok * D + slice * 32) * 2);
-          const float* qs = qv + slice * C::QS;
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint4 w = kr[k4];
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float kv = (u & 1) ? bf16_hi(ww[u >> 1]) : bf16_lo(ww[u >> 1]);
-              float2 q[GH];
-              load_heads<GT>(qs + (k4 * 8 + u) * GTP, q);
-#pragma unroll
-              for (int k = 0; k < GH; ++k) a[k] = fma2(make_float2(kv, kv), q[k], a[k]);
-            }
-          }
-        }
-        reduce_slices(a);
-        if (slice == 0 && stok < ntok) {
-#pragma unroll
-          for (int h = 0; h < GT; ++h) logit[stok * GTP + h] = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * p.sscale;
-        }
-      }
-      __syncthreads();
-      softmax(ntok, nullptr);
-      rescale();
-      for (int t = tl; t < ntok; t += TL) {
-        const uint2 w = *reinterpret_cast<const uint2*>(s + TB + (t * D + 4 * g) * 2);
-        const float vv[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
-        float2 pp[GH];
-        load_heads<GT>(logit + t * GTP, pp);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int k = 0; k < GH; ++k) acc[c][k] = fma2(make_float2(vv[c], vv[c]), pp[k], acc[c][k]);
       }
       __syncthreads();
     }

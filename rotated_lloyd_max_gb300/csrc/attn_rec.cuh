@@ -1,6 +1,8 @@
 // a6-a8: decode attention over the compressed records (head dims 64 and 128),
 // warp-local variant.
 //
+// Dense splits of the same call (tail tokens, bf16 layers) run the general
+// dense path (attn_dense_split) inside this launch.
 // Same arithmetic as attn.cuh (q~ = H(s_k . q)/sqrt(d) once per CTA; a record
 // token scores as n_i * q~ . c[codes] from a shared-memory LUT; values
 // accumulate p_i n_i yhat_i in the rotated basis), organised so that a record
@@ -134,7 +136,7 @@ __device__ __forceinline__ uint32_t code_in_row(const unsigned char* row, int id
 }
 
 template <int D, int GT>
-__global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(const __grid_constant__ AttnParams p) {
   using C = RCfg<D, GT>;
   constexpr int GTP = C::GTP, GH = C::GH, SL = C::SL, TPL = C::TPL, QR = C::QR, LPT = C::LPT, TLW = C::TLW;
   extern __shared__ __align__(128) unsigned char sm[];
@@ -143,8 +145,6 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
   float* lutv = lutk + 16;
   float* pbuf = reinterpret_cast<float*>(sm + p.sm_logit);  // [4][32][GTP]
   float* corr = reinterpret_cast<float*>(sm + p.sm_corr);   // [4][D][GTP]
-  int* pre = reinterpret_cast<int*>(sm + p.sm_pre);         // [2][2][129]
-  uint8_t* slotof = sm + p.sm_slot;                        // [2][2][cap]
   unsigned char* mainb = sm + p.sm_main;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -157,6 +157,20 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
+  if (split >= p.Sc) {  // a dense split (tail ring or bf16 layer) in the same launch
+    const int tl = min(p.tail_len ? p.tail_len[lb] : 0, p.tail_cap);
+    const int d_begin = (split - p.Sc) * p.tps, d_end = min(d_begin + p.tps, tl);
+    if (d_begin >= d_end) {
+      if (tid < GT) {
+        float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
+        ml[0] = -INFINITY;
+        ml[1] = 0.f;
+      }
+      return;
+    }
+    attn_dense_split<D, GT>(p, sm, l, b, kvh, h0, split, qh0, d_begin, d_end);
+    return;
+  }
   const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
   const int t_begin = split * p.cps, t_end = min(t_begin + p.cps, nch);
   if (t_begin >= t_end) {
@@ -173,14 +187,7 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
                                    : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
   const int kcap = p.kcap, vcap = p.shared_kv ? p.kcap : p.vcap;
   const bool kout = p.kout, vout = p.vout;
-  auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
-  auto entk = [&](int i) { return reinterpret_cast<uint32_t*>(sm + p.sm_ent + (i & 1) * p.sm_ent_stage); };
-  auto entv = [&](int i) { return p.shared_kv ? entk(i) : entk(i) + kcap * p.kout; };
-  auto prek = [&](int i) { return pre + ((i & 1) * 2) * 129; };
-  auto prev = [&](int i) { return p.shared_kv ? prek(i) : pre + ((i & 1) * 2 + 1) * 129; };
-  auto slotk = [&](int i) { return slotof + (i & 1) * (kcap + vcap); };
-  auto slotv = [&](int i) { return p.shared_kv ? slotk(i) : slotk(i) + kcap; };
-
+  auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
   auto issue_main = [&](int i) {
     if (i < n) {
       const int64_t c = t_begin + i;
@@ -189,49 +196,8 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
     }
     cp_async_commit();
   };
-  // warps 0 (keys) and 1 (values): prefix sums of the per-slot counts, the
-  // entry -> slot map, and the copy of exactly the used entries
-  auto prefix_issue = [&](int i) {
-    const bool isk = warp == 0;
-    if (i < n && warp < 2 && (isk ? kout : (vout && !p.shared_kv))) {
-      const unsigned char* cnts = isk ? stage(i) + p.k_off_count : stage(i) + p.k_main + p.v_off_count;
-      int* pr = isk ? prek(i) : pre + ((i & 1) * 2 + 1) * 129;
-      uint8_t* so = isk ? slotk(i) : slotk(i) + kcap;
-      const int cap = isk ? kcap : p.vcap;
-      const uint32_t c4 = reinterpret_cast<const uint32_t*>(cnts)[lane];
-      const int n0 = c4 & 0xff, n1 = (c4 >> 8) & 0xff, n2 = (c4 >> 16) & 0xff, n3 = c4 >> 24;
-      const int tot = n0 + n1 + n2 + n3;
-      int inc = tot;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, m);
-        if (lane >= m) inc += o;
-      }
-      const int ex = inc - tot;
-      pr[4 * lane] = ex;
-      pr[4 * lane + 1] = ex + n0;
-      pr[4 * lane + 2] = ex + n0 + n1;
-      pr[4 * lane + 3] = ex + n0 + n1 + n2;
-      if (lane == 31) pr[128] = inc;
-      int e = ex;
-      const int ns[4] = {n0, n1, n2, n3};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        for (int k = 0; k < ns[q]; ++k, ++e)
-          if (e < cap) so[e] = (uint8_t)(4 * lane + q);
-      const int E = min(__shfl_sync(0xffffffffu, inc, 31), cap);
-      const int64_t c = t_begin + i;
-      const unsigned char* src = isk ? kb0 + c * p.krec_bytes + p.k_off_ent : vb0 + c * p.vrec_bytes + p.v_off_ent;
-      char* dst = reinterpret_cast<char*>(isk ? entk(i) : entk(i) + kcap * p.kout);
-      const int bytes = (E * 4 + 15) & ~15;
-      for (int off = lane * 16; off < bytes; off += 32 * 16) cp_async16(dst + off, src + off);
-    }
-    cp_async_commit();
-  };
-
-  // first records go out before the query work so their latency overlaps it
+  // the first record goes out before the query work so its latency overlaps it
   issue_main(0);
-  issue_main(1);
 
   // ---- query: load, rotate, store as [slice][32][GTP]
   for (int hh = warp; hh < GT; hh += 4) {
@@ -288,14 +254,29 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
   float* cw = corr + warp * D * GTP;
   const int rbk = D * p.kb / 8, rbv = D * p.vb / 8;
 
-  cp_async_wait<0>();
-  __syncthreads();
-  prefix_issue(0);
+  // Entry range of the lane's token in one stream's side list: a per-warp
+  // prefix sum of the record's per-slot counts (lane j <-> slot warp*32 + j).
+  auto token_entries = [&](const unsigned char* cnts, int cap, int& e_begin, int& e_cnt) {
+    int base = 0;
+    for (int u = 0; u < warp; ++u) base += cnts[u * 32 + lane];
+#pragma unroll
+    for (int m = 16; m; m >>= 1) base += __shfl_xor_sync(0xffffffffu, base, m);
+    const int c = cnts[warp * 32 + lane];
+    int inc = c;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, m);
+      if (lane >= m) inc += o;
+    }
+    e_begin = __shfl_sync(0xffffffffu, base + inc - c, tloc);
+    e_cnt = __shfl_sync(0xffffffffu, c, tloc);
+    e_cnt = max(0, min(e_cnt, cap - e_begin));
+  };
+
   for (int i = 0; i < n; ++i) {
     cp_async_wait<0>();
-    __syncthreads();  // record i+1 and the entries of record i are in; record i-1 is done
-    issue_main(i + 2);
-    prefix_issue(i + 1);
+    __syncthreads();  // record i is in; record i-1 is done with
+    issue_main(i + 1);
 
     const unsigned char* st = stage(i);
     const unsigned char* kcodes = st + warp * 32 * rbk;  // the warp's 32 rows
@@ -303,6 +284,24 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
     const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
     const unsigned char* vcodes = vbase + warp * 32 * rbv;
     const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
+    const int64_t c = t_begin + i;
+
+    // outlier entries of the lane's own token; the first 8 of each stream are
+    // fetched now so that their latency overlaps the scores
+    int ke0 = 0, kec = 0, ve0 = 0, vec = 0;
+    uint32_t kent[8], vent[8];
+    const uint32_t* kge = reinterpret_cast<const uint32_t*>(kb0 + c * p.krec_bytes + p.k_off_ent);
+    const uint32_t* vge = reinterpret_cast<const uint32_t*>(vb0 + c * p.vrec_bytes + p.v_off_ent);
+    if (kout) {
+      token_entries(st + p.k_off_count, kcap, ke0, kec);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) kent[k] = k < kec ? __ldg(kge + ke0 + k) : 0u;
+    }
+    if (vout) {
+      token_entries(vbase + p.v_off_count, vcap, ve0, vec);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) vent[k] = k < vec ? __ldg(vge + ve0 + k) : 0u;
+    }
 
     // ---- scores
     float lg[GT];
@@ -324,37 +323,33 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
       }
       float2 r[GH];
       reduce_transpose<SL, GH>(a, s, r);
-      const float f = knorm[tloc] * p.sscale;
 #pragma unroll
-      for (int h = 0; h < GT; ++h) lg[h] = ((h & 1) ? r[h >> 1].y : r[h >> 1].x) * f;
+      for (int h = 0; h < GT; ++h) lg[h] = (h & 1) ? r[h >> 1].y : r[h >> 1].x;
     }
     if (kout) {
-      // keys' outlier entries of the warp's tokens: logit += (val - c) q~_idx n scale
-#pragma unroll
-      for (int h = 0; h < GT; ++h) pw[tloc * GTP + h] = lg[h];
-      __syncwarp();
-      const int* pk = prek(i);
-      const int e0 = min(pk[warp * 32], kcap), e1 = min(pk[warp * 32 + 32], kcap);
-      const uint32_t* ek = entk(i);
-      const uint8_t* sk = slotk(i);
-      const unsigned char* krows = st;
-      const float* kn = reinterpret_cast<const float*>(st + p.k_off_norm);
-      for (int e = e0 + lane; e < e1; e += 32) {
-        const uint32_t v = ek[e];
+      // the stored value replaces the centroid: logit += (val - c[code]) q~_idx
+      const unsigned char* krow = kcodes + tloc * rbk;
+      auto kfix = [&](uint32_t v) {
         const int idx = (int)(v & 0xFFFFu) & (D - 1);
-        const int slot = sk[e];
-        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutk[code_in_row(krows + slot * rbk, idx, p.kb)];
-        const float f = delta * kn[slot] * p.sscale;
-        const float* qj = qv + (idx >> 5) * C::QS + (idx & 31) * GTP;
+        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutk[code_in_row(krow, idx, p.kb)];
+        float2 qq[GH];
+        load_heads<GT>(qv + (idx >> 5) * C::QS + (idx & 31) * GTP, qq);
 #pragma unroll
-        for (int h = 0; h < GT; ++h) atomicAdd(&pw[(slot - warp * 32) * GTP + h], f * qj[h]);
-      }
-      __syncwarp();
+        for (int h = 0; h < GT; ++h) lg[h] = fmaf(delta, (h & 1) ? qq[h >> 1].y : qq[h >> 1].x, lg[h]);
+      };
 #pragma unroll
-      for (int h = 0; h < GT; ++h) lg[h] = pw[tloc * GTP + h];
+      for (int k = 0; k < 8; ++k)
+        if (k < kec) kfix(kent[k]);
+      for (int k = 8; k < kec; ++k) kfix(__ldg(kge + ke0 + k));
+    }
+    {
+      const float f = knorm[tloc] * p.sscale;
+#pragma unroll
+      for (int h = 0; h < GT; ++h) lg[h] *= f;
     }
 
     // ---- online softmax (warp-local, the max moves only when a logit passes it by 2^8)
+    float pv[GT];
     {
       bool need = false;
 #pragma unroll
@@ -372,7 +367,7 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
         for (int k = 0; k < GH; ++k) {
           const float2 a2 = make_float2(al[2 * k], (2 * k + 1 < GT) ? al[2 * k + 1] : 0.f);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[c][k] = mul2(acc[c][k], a2);
+          for (int cc = 0; cc < 4; ++cc) acc[cc][k] = mul2(acc[cc][k], a2);
         }
         if (vout) {
           for (int j = lane; j < D; j += 32)
@@ -385,26 +380,26 @@ __global__ void __launch_bounds__(kThreads) attn_rec_kernel(const __grid_constan
       for (int h = 0; h < GT; ++h) {
         const float pe = exp2f(lg[h] - m_w[h]);
         l_ln[h] += pe;
-        pw[tloc * GTP + h] = pe * vn;
+        pv[h] = pe * vn;
+        pw[tloc * GTP + h] = pv[h];
       }
       __syncwarp();
     }
 
     // ---- values
     if (vout) {
-      const int* pv = prev(i);
-      const int e0 = min(pv[warp * 32], vcap), e1 = min(pv[warp * 32 + 32], vcap);
-      const uint32_t* ev = entv(i);
-      const uint8_t* sv = slotv(i);
-      for (int e = e0 + lane; e < e1; e += 32) {
-        const uint32_t v = ev[e];
+      // the stored value replaces the centroid: acc_idx += p' (val - c[code])
+      const unsigned char* vrow = vcodes + tloc * rbv;
+      auto vfix = [&](uint32_t v) {
         const int idx = (int)(v & 0xFFFFu) & (D - 1);
-        const int slot = sv[e];
-        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vbase + slot * rbv, idx, p.vb)];
-        const float* pp = pw + (slot - warp * 32) * GTP;
+        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)];
 #pragma unroll
-        for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pp[h] * delta);
-      }
+        for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pv[h] * delta);
+      };
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < vec) vfix(vent[k]);
+      for (int k = 8; k < vec; ++k) vfix(__ldg(vge + ve0 + k));
     }
     switch (p.vb) {
       case 1: pv_tokens<1, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
