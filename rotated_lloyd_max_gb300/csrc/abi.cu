@@ -223,10 +223,6 @@ void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
   p.sm_ent_stage = 0;
   int stage = p.krec ? p.k_main + (p.shared_kv ? 0 : p.v_main) : 0;
   stage = std::max(stage, (4 * D * GTP * 4 + 1) / 2);  // the warps' partials at the end
-  if (p.ktail) {  // dense splits of the same launch: bf16 K/V tiles and their partials
-    stage = std::max(stage, 2 * (4096 / D) * D * 2);
-    stage = std::max(stage, ((128 / (D / 4)) * D * GTP * 4 + 1) / 2);
-  }
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
   off += 2 * p.sm_stage;

@@ -157,22 +157,19 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
-  if (split >= p.Sc) {  // a dense split (tail ring or bf16 layer) in the same launch
-    const int tl = min(p.tail_len ? p.tail_len[lb] : 0, p.tail_cap);
-    const int d_begin = (split - p.Sc) * p.tps, d_end = min(d_begin + p.tps, tl);
-    if (d_begin >= d_end) {
-      if (tid < GT) {
-        float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
-        ml[0] = -INFINITY;
-        ml[1] = 0.f;
-      }
-      return;
-    }
-    attn_dense_split<D, GT>(p, sm, l, b, kvh, h0, split, qh0, d_begin, d_end);
-    return;
+  // a split is a run of whole records, or of dense tokens (a tail ring or a
+  // bf16 layer) handled by the warp-local dense path of the same launch
+  const bool dense = split >= p.Sc;
+  int t_begin, t_end;
+  if (dense) {
+    const int len = min(p.tail_len ? p.tail_len[lb] : 0, p.tail_cap);
+    t_begin = (split - p.Sc) * p.tps;
+    t_end = min(t_begin + p.tps, len);
+  } else {
+    const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
+    t_begin = split * p.cps;
+    t_end = min(t_begin + p.cps, nch);
   }
-  const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
-  const int t_begin = split * p.cps, t_end = min(t_begin + p.cps, nch);
   if (t_begin >= t_end) {
     if (tid < GT) {
       float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
@@ -182,11 +179,11 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     return;
   }
   const int n = t_end - t_begin;
-  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = p.shared_kv ? kb0
+  const uint8_t* kb0 = dense ? nullptr : p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
+  const uint8_t* vb0 = (dense || p.shared_kv) ? kb0
                                    : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
   const int kcap = p.kcap, vcap = p.shared_kv ? p.kcap : p.vcap;
-  const bool kout = p.kout, vout = p.vout;
+  const bool kout = p.kout && !dense, vout = p.vout && !dense;
   auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
   auto issue_main = [&](int i) {
     if (i < n) {
@@ -197,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     cp_async_commit();
   };
   // the first record goes out before the query work so its latency overlaps it
-  issue_main(0);
+  if (!dense) issue_main(0);
 
   // ---- query: load, rotate, store as [slice][32][GTP]
   for (int hh = warp; hh < GT; hh += 4) {
@@ -210,14 +207,17 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
       x[r] = bf16_lo(w);
       x[r + 1] = bf16_hi(w);
     }
+    float f = 1.f;
+    if (!dense) {  // records are scored against q~ = H(s_k . q)/sqrt(d)
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int j = lane * R + r;
-      if ((p.ksign[j >> 5] >> (j & 31)) & 1u) x[r] = -x[r];
+      for (int r = 0; r < R; ++r) {
+        const int j = lane * R + r;
+        if ((p.ksign[j >> 5] >> (j & 31)) & 1u) x[r] = -x[r];
+      }
+      fwht_regs<R>(x);
+      fwht_lanes<R>(x, lane, 32);
+      f = inv_sqrt_dim<D>();
     }
-    fwht_regs<R>(x);
-    fwht_lanes<R>(x, lane, 32);
-    const float f = inv_sqrt_dim<D>();
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int j = lane * R + r;
@@ -273,84 +273,76 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     e_cnt = max(0, min(e_cnt, cap - e_begin));
   };
 
-  for (int i = 0; i < n; ++i) {
-    cp_async_wait<0>();
-    __syncthreads();  // record i is in; record i-1 is done with
-    issue_main(i + 1);
-
-    const unsigned char* st = stage(i);
-    const unsigned char* kcodes = st + warp * 32 * rbk;  // the warp's 32 rows
-    const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + warp * 32;
-    const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
-    const unsigned char* vcodes = vbase + warp * 32 * rbv;
-    const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
-    const int64_t c = t_begin + i;
-
-    // outlier entries of the lane's own token; the first 8 of each stream are
-    // fetched now so that their latency overlaps the scores
-    int ke0 = 0, kec = 0, ve0 = 0, vec = 0;
-    uint32_t kent[8], vent[8];
-    const uint32_t* kge = reinterpret_cast<const uint32_t*>(kb0 + c * p.krec_bytes + p.k_off_ent);
-    const uint32_t* vge = reinterpret_cast<const uint32_t*>(vb0 + c * p.vrec_bytes + p.v_off_ent);
-    if (kout) {
-      token_entries(st + p.k_off_count, kcap, ke0, kec);
+  if (dense) {
+    // ---- dense tokens, warp-local: a warp takes TW tokens per step (lane =
+    // token x 32-coordinate slice for the scores, 4 coordinates for the
+    // values), loaded straight from global memory with the next step's keys
+    // in flight
+    constexpr int TW = 32 / SL;
+    const int tstart = p.tail_start ? ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap : 0;
+    const uint16_t* kt0 = p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+    const uint16_t* vt0 = p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * p.tail_cap * D;
+    const int steps = (n + 4 * TW - 1) / (4 * TW);
+    auto kload = [&](int kk, uint4 (&kw)[4]) {
+      const int t = t_begin + (kk * 4 + warp) * TW + q;
+      if (kk < steps && t < t_end) {
+        const int64_t slot = (tstart + t) % p.tail_cap;
+        const uint4* src = reinterpret_cast<const uint4*>(kt0 + slot * D + s * 32);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) kent[k] = k < kec ? __ldg(kge + ke0 + k) : 0u;
-    }
-    if (vout) {
-      token_entries(vbase + p.v_off_count, vcap, ve0, vec);
+        for (int k = 0; k < 4; ++k) kw[k] = __ldg(src + k);
+      } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) vent[k] = k < vec ? __ldg(vge + ve0 + k) : 0u;
-    }
-
-    // ---- scores
-    float lg[GT];
-    {
-      float2 a[TPL][GH];
-#pragma unroll
-      for (int i2 = 0; i2 < TPL; ++i2)
-#pragma unroll
-        for (int k = 0; k < GH; ++k) a[i2][k] = make_float2(0.f, 0.f);
-      int tok[TPL];
-#pragma unroll
-      for (int i2 = 0; i2 < TPL; ++i2) tok[i2] = q + QR * i2;
-      const float* qs = qv + s * C::QS;
-      switch (p.kb) {
-        case 1: score_tokens<1, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
-        case 2: score_tokens<2, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
-        case 3: score_tokens<3, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
-        default: score_tokens<4, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+        for (int k = 0; k < 4; ++k) kw[k] = make_uint4(0u, 0u, 0u, 0u);
       }
-      float2 r[GH];
-      reduce_transpose<SL, GH>(a, s, r);
+    };
+    uint4 kn[4];
+    kload(0, kn);
+    for (int kk = 0; kk < steps; ++kk) {
+      uint4 kc[4];
 #pragma unroll
-      for (int h = 0; h < GT; ++h) lg[h] = (h & 1) ? r[h >> 1].y : r[h >> 1].x;
-    }
-    if (kout) {
-      // the stored value replaces the centroid: logit += (val - c[code]) q~_idx
-      const unsigned char* krow = kcodes + tloc * rbk;
-      auto kfix = [&](uint32_t v) {
-        const int idx = (int)(v & 0xFFFFu) & (D - 1);
-        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutk[code_in_row(krow, idx, p.kb)];
-        float2 qq[GH];
-        load_heads<GT>(qv + (idx >> 5) * C::QS + (idx & 31) * GTP, qq);
+      for (int k = 0; k < 4; ++k) kc[k] = kn[k];
+      const int tb = t_begin + (kk * 4 + warp) * TW;
+      uint2 vc[TW / TLW];
 #pragma unroll
-        for (int h = 0; h < GT; ++h) lg[h] = fmaf(delta, (h & 1) ? qq[h >> 1].y : qq[h >> 1].x, lg[h]);
-      };
+      for (int j = 0; j < TW / TLW; ++j) {
+        const int t = tb + tl + j * TLW;
+        if (t < t_end) {
+          const int64_t slot = (tstart + t) % p.tail_cap;
+          vc[j] = __ldg(reinterpret_cast<const uint2*>(vt0 + slot * D + 4 * g));
+        } else {
+          vc[j] = make_uint2(0u, 0u);
+        }
+      }
+      kload(kk + 1, kn);
+      const bool valid = tb + q < t_end;
+      // scores
+      float2 a[GH];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (k < kec) kfix(kent[k]);
-      for (int k = 8; k < kec; ++k) kfix(__ldg(kge + ke0 + k));
-    }
-    {
-      const float f = knorm[tloc] * p.sscale;
+      for (int k = 0; k < GH; ++k) a[k] = make_float2(0.f, 0.f);
+      const float* qs = qv + s * C::QS;
 #pragma unroll
-      for (int h = 0; h < GT; ++h) lg[h] *= f;
-    }
-
-    // ---- online softmax (warp-local, the max moves only when a logit passes it by 2^8)
-    float pv[GT];
-    {
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint32_t ww[4] = {kc[k4].x, kc[k4].y, kc[k4].z, kc[k4].w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float kv = (u & 1) ? bf16_hi(ww[u >> 1]) : bf16_lo(ww[u >> 1]);
+          float2 qq[GH];
+          load_heads<GT>(qs + (k4 * 8 + u) * GTP, qq);
+#pragma unroll
+          for (int k = 0; k < GH; ++k) a[k] = fma2(make_float2(kv, kv), qq[k], a[k]);
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < SL; m <<= 1)
+#pragma unroll
+        for (int k = 0; k < GH; ++k) {
+          a[k].x += __shfl_xor_sync(0xffffffffu, a[k].x, m);
+          a[k].y += __shfl_xor_sync(0xffffffffu, a[k].y, m);
+        }
+      float lg[GT];
+#pragma unroll
+      for (int h = 0; h < GT; ++h) lg[h] = valid ? ((h & 1) ? a[h >> 1].y : a[h >> 1].x) * p.sscale : -INFINITY;
+      // online softmax (the SL lanes of a token hold the same logits)
       bool need = false;
 #pragma unroll
       for (int h = 0; h < GT; ++h) need |= lg[h] > m_w[h] + 8.f;
@@ -369,43 +361,165 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) acc[cc][k] = mul2(acc[cc][k], a2);
         }
-        if (vout) {
-          for (int j = lane; j < D; j += 32)
-#pragma unroll
-            for (int h = 0; h < GT; ++h) cw[j * GTP + h] *= al[h];
-        }
       }
-      const float vn = vnorm[tloc];
 #pragma unroll
       for (int h = 0; h < GT; ++h) {
-        const float pe = exp2f(lg[h] - m_w[h]);
-        l_ln[h] += pe;
-        pv[h] = pe * vn;
-        pw[tloc * GTP + h] = pv[h];
+        const float pe = valid ? exp2f(lg[h] - m_w[h]) : 0.f;
+        if (s == 0) {
+          l_ln[h] += pe;
+          pw[q * GTP + h] = pe;
+        }
+      }
+      __syncwarp();
+      // values
+#pragma unroll
+      for (int j = 0; j < TW / TLW; ++j) {
+        const int tt = tl + j * TLW;
+        const float vv[4] = {bf16_lo(vc[j].x), bf16_hi(vc[j].x), bf16_lo(vc[j].y), bf16_hi(vc[j].y)};
+        float2 pp[GH];
+        load_heads<GT>(pw + tt * GTP, pp);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int k = 0; k < GH; ++k) acc[cc][k] = fma2(make_float2(vv[cc], vv[cc]), pp[k], acc[cc][k]);
       }
       __syncwarp();
     }
+  } else {
+    for (int i = 0; i < n; ++i) {
+      cp_async_wait<0>();
+      __syncthreads();  // record i is in; record i-1 is done with
+      issue_main(i + 1);
 
-    // ---- values
-    if (vout) {
-      // the stored value replaces the centroid: acc_idx += p' (val - c[code])
-      const unsigned char* vrow = vcodes + tloc * rbv;
-      auto vfix = [&](uint32_t v) {
-        const int idx = (int)(v & 0xFFFFu) & (D - 1);
-        const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)];
-#pragma unroll
-        for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pv[h] * delta);
-      };
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (k < vec) vfix(vent[k]);
-      for (int k = 8; k < vec; ++k) vfix(__ldg(vge + ve0 + k));
-    }
-    switch (p.vb) {
-      case 1: pv_tokens<1, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
-      case 2: pv_tokens<2, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
-      case 3: pv_tokens<3, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
-      default: pv_tokens<4, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+      const unsigned char* st = stage(i);
+      const unsigned char* kcodes = st + warp * 32 * rbk;  // the warp's 32 rows
+      const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + warp * 32;
+      const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
+      const unsigned char* vcodes = vbase + warp * 32 * rbv;
+      const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
+      const int64_t c = t_begin + i;
+
+      // outlier entries of the lane's own token; the first 8 of each stream are
+      // fetched now so that their latency overlaps the scores
+      int ke0 = 0, kec = 0, ve0 = 0, vec = 0;
+      uint32_t kent[8], vent[8];
+      const uint32_t* kge = reinterpret_cast<const uint32_t*>(kb0 + c * p.krec_bytes + p.k_off_ent);
+      const uint32_t* vge = reinterpret_cast<const uint32_t*>(vb0 + c * p.vrec_bytes + p.v_off_ent);
+      if (kout) {
+        token_entries(st + p.k_off_count, kcap, ke0, kec);
+  #pragma unroll
+        for (int k = 0; k < 8; ++k) kent[k] = k < kec ? __ldg(kge + ke0 + k) : 0u;
+      }
+      if (vout) {
+        token_entries(vbase + p.v_off_count, vcap, ve0, vec);
+  #pragma unroll
+        for (int k = 0; k < 8; ++k) vent[k] = k < vec ? __ldg(vge + ve0 + k) : 0u;
+      }
+
+      // ---- scores
+      float lg[GT];
+      {
+        float2 a[TPL][GH];
+  #pragma unroll
+        for (int i2 = 0; i2 < TPL; ++i2)
+  #pragma unroll
+          for (int k = 0; k < GH; ++k) a[i2][k] = make_float2(0.f, 0.f);
+        int tok[TPL];
+  #pragma unroll
+        for (int i2 = 0; i2 < TPL; ++i2) tok[i2] = q + QR * i2;
+        const float* qs = qv + s * C::QS;
+        switch (p.kb) {
+          case 1: score_tokens<1, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+          case 2: score_tokens<2, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+          case 3: score_tokens<3, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+          default: score_tokens<4, GT, GTP, TPL>(kcodes, rbk, tok, s, qs, lutk, a); break;
+        }
+        float2 r[GH];
+        reduce_transpose<SL, GH>(a, s, r);
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) lg[h] = (h & 1) ? r[h >> 1].y : r[h >> 1].x;
+      }
+      if (kout) {
+        // the stored value replaces the centroid: logit += (val - c[code]) q~_idx
+        const unsigned char* krow = kcodes + tloc * rbk;
+        auto kfix = [&](uint32_t v) {
+          const int idx = (int)(v & 0xFFFFu) & (D - 1);
+          const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutk[code_in_row(krow, idx, p.kb)];
+          float2 qq[GH];
+          load_heads<GT>(qv + (idx >> 5) * C::QS + (idx & 31) * GTP, qq);
+  #pragma unroll
+          for (int h = 0; h < GT; ++h) lg[h] = fmaf(delta, (h & 1) ? qq[h >> 1].y : qq[h >> 1].x, lg[h]);
+        };
+  #pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < kec) kfix(kent[k]);
+        for (int k = 8; k < kec; ++k) kfix(__ldg(kge + ke0 + k));
+      }
+      {
+        const float f = knorm[tloc] * p.sscale;
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) lg[h] *= f;
+      }
+
+      // ---- online softmax (warp-local, the max moves only when a logit passes it by 2^8)
+      float pv[GT];
+      {
+        bool need = false;
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) need |= lg[h] > m_w[h] + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          float al[GT];
+  #pragma unroll
+          for (int h = 0; h < GT; ++h) {
+            const float mn = fmaxf(m_w[h], warp_max(lg[h]));
+            al[h] = exp2f(m_w[h] - mn);
+            m_w[h] = mn;
+            l_ln[h] *= al[h];
+          }
+  #pragma unroll
+          for (int k = 0; k < GH; ++k) {
+            const float2 a2 = make_float2(al[2 * k], (2 * k + 1 < GT) ? al[2 * k + 1] : 0.f);
+  #pragma unroll
+            for (int cc = 0; cc < 4; ++cc) acc[cc][k] = mul2(acc[cc][k], a2);
+          }
+          if (vout) {
+            for (int j = lane; j < D; j += 32)
+  #pragma unroll
+              for (int h = 0; h < GT; ++h) cw[j * GTP + h] *= al[h];
+          }
+        }
+        const float vn = vnorm[tloc];
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          const float pe = exp2f(lg[h] - m_w[h]);
+          l_ln[h] += pe;
+          pv[h] = pe * vn;
+          pw[tloc * GTP + h] = pv[h];
+        }
+        __syncwarp();
+      }
+
+      // ---- values
+      if (vout) {
+        // the stored value replaces the centroid: acc_idx += p' (val - c[code])
+        const unsigned char* vrow = vcodes + tloc * rbv;
+        auto vfix = [&](uint32_t v) {
+          const int idx = (int)(v & 0xFFFFu) & (D - 1);
+          const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)];
+  #pragma unroll
+          for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pv[h] * delta);
+        };
+  #pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < vec) vfix(vent[k]);
+        for (int k = 8; k < vec; ++k) vfix(__ldg(vge + ve0 + k));
+      }
+      switch (p.vb) {
+        case 1: pv_tokens<1, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+        case 2: pv_tokens<2, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+        case 3: pv_tokens<3, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+        default: pv_tokens<4, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
+      }
     }
   }
 

@@ -13,13 +13,13 @@ namespace tq {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ MergeParams p) {
-  // One CTA per (layer, batch, query head).  Split weights first (warp 0),
-  // then every thread sums its coordinates over all splits with independent
-  // loads, then warp 0 applies the inverse transform to the compressed part.
+  // One CTA per (layer, batch, query head).  Warp 0 turns the splits' (m, l)
+  // into weights; then warp w sums splits w, w+4, ... with a lane holding d/32
+  // consecutive coordinates (several vector loads in flight), the four warps'
+  // sums meet in shared memory, and warp 0 applies the inverse transform.
   constexpr int R = D / 32;
   __shared__ float w_s[1024];
-  __shared__ float acc_c[D];
-  __shared__ float acc_t[D];
+  __shared__ __align__(16) float part[2][4][D];
   __shared__ float s_W;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
@@ -43,33 +43,28 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
   }
   __syncthreads();
   const float W = s_W;
-  for (int j = tid; j < D; j += kThreads) {
-    float c0 = 0.f, c1 = 0.f, t0 = 0.f, t1 = 0.f;
-    int s = 0;
-    for (; s + 1 < p.Sc; s += 2) {
-      const float w0 = w_s[s], w1 = w_s[s + 1];
-      const float a0 = w0 > 0.f ? acc[(int64_t)s * D + j] : 0.f;
-      const float a1 = w1 > 0.f ? acc[(int64_t)(s + 1) * D + j] : 0.f;
-      c0 = fmaf(w0, a0, c0);
-      c1 = fmaf(w1, a1, c1);
+  float c[R], t[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) c[r] = t[r] = 0.f;
+  auto add_split = [&](int s, float (&dst)[R]) {
+    const float w = w_s[s];
+    if (!(w > 0.f)) return;
+    const float* a = acc + (int64_t)s * D + lane * R;
+#pragma unroll
+    for (int r = 0; r < R; r += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(a + r);
+      dst[r] = fmaf(w, v.x, dst[r]);
+      dst[r + 1] = fmaf(w, v.y, dst[r + 1]);
     }
-    for (; s < p.Sc; ++s) {
-      const float w0 = w_s[s];
-      c0 = fmaf(w0, w0 > 0.f ? acc[(int64_t)s * D + j] : 0.f, c0);
-    }
-    for (; s + 1 < p.S; s += 2) {
-      const float w0 = w_s[s], w1 = w_s[s + 1];
-      const float a0 = w0 > 0.f ? acc[(int64_t)s * D + j] : 0.f;
-      const float a1 = w1 > 0.f ? acc[(int64_t)(s + 1) * D + j] : 0.f;
-      t0 = fmaf(w0, a0, t0);
-      t1 = fmaf(w1, a1, t1);
-    }
-    for (; s < p.S; ++s) {
-      const float w0 = w_s[s];
-      t0 = fmaf(w0, w0 > 0.f ? acc[(int64_t)s * D + j] : 0.f, t0);
-    }
-    acc_c[j] = c0 + c1;
-    acc_t[j] = t0 + t1;
+  };
+#pragma unroll 4
+  for (int s = warp; s < p.Sc; s += 4) add_split(s, c);
+#pragma unroll 4
+  for (int s = p.Sc + ((warp - p.Sc) & 3); s < p.S; s += 4) add_split(s, t);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    part[0][warp][lane * R + r] = c[r];
+    part[1][warp][lane * R + r] = t[r];
   }
   __syncthreads();
   if (warp != 0) return;
@@ -77,20 +72,25 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     for (int j = lane; j < D; j += 32) out[j] = 0.f;
     return;
   }
-  float ar[R];
+  float ar[R], at[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) ar[r] = acc_c[lane * R + r];
+  for (int r = 0; r < R; ++r) {
+    const int j = lane * R + r;
+    ar[r] = (part[0][0][j] + part[0][1][j]) + (part[0][2][j] + part[0][3][j]);
+    at[r] = (part[1][0][j] + part[1][1][j]) + (part[1][2][j] + part[1][3][j]);
+  }
   if (p.Sc > 0) {
     fwht_regs<R>(ar);
     fwht_lanes<R>(ar, lane, 32);
   }
   const float invW = 1.0f / W;
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
+  for (int r = 0; r < R; r += 2) {
     const int j = lane * R + r;
-    const float f = ((p.vsign[j >> 5] >> (j & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
-    const float x = p.Sc > 0 ? ar[r] * f : 0.f;
-    out[j] = (x + acc_t[j]) * invW;
+    const float f0 = ((p.vsign[j >> 5] >> (j & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
+    const float f1 = ((p.vsign[(j + 1) >> 5] >> ((j + 1) & 31)) & 1u) ? -p.inv_sqrt_d : p.inv_sqrt_d;
+    const float x0 = p.Sc > 0 ? ar[r] * f0 : 0.f, x1 = p.Sc > 0 ? ar[r + 1] * f1 : 0.f;
+    *reinterpret_cast<float2*>(out + j) = make_float2((x0 + at[r]) * invW, (x1 + at[r + 1]) * invW);
   }
 }
 
