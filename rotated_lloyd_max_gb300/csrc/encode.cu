@@ -36,24 +36,39 @@ struct EncSmem {
   int running;
 };
 
-// Per-thread constants of the encoder (signs of the lane's 32 coordinates and
-// the positive boundaries as integer bit patterns).
+// Per-thread constants of the encoder: the signs of the lane's 32
+// coordinates as XOR masks on packed bf16 pairs (bits 15 and 31), and the
+// positive decision boundaries.
 template <int D, int B, bool OUTL>
 struct EncLane {
   using E = Enc<D, B, OUTL>;
   int lane, warp, lg, vi;
-  uint32_t sbits;
-  uint32_t tpos[E::NPOS > 0 ? E::NPOS : 1];
+  uint32_t smask[16];
+  float tpos[E::NPOS > 0 ? E::NPOS : 1];
   __device__ __forceinline__ explicit EncLane(const CodecDev& c) {
     lane = threadIdx.x & 31;
     warp = threadIdx.x >> 5;
     lg = lane % E::L;
     vi = lane / E::L;
-    sbits = c.signs[lg];
+    const uint32_t sb = c.signs[lg];
 #pragma unroll
-    for (int k = 0; k < E::NPOS; ++k) tpos[k] = __float_as_uint(c.boundaries[E::HALF + k]);
+    for (int k = 0; k < 16; ++k) smask[k] = (((sb >> (2 * k)) & 1u) << 15) | (((sb >> (2 * k + 1)) & 1u) << 31);
+#pragma unroll
+    for (int k = 0; k < E::NPOS; ++k) tpos[k] = c.boundaries[E::HALF + k];
   }
 };
+
+// 0xFFFFFFFF if a > b, else 0 (an f32 compare that yields an integer mask).
+__device__ __forceinline__ uint32_t mask_gt(float a, float b) {
+  uint32_t r;
+  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t mask_le(float a, float b) {
+  uint32_t r;
+  asm("set.le.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
 
 // The lane's 32 bf16 coordinates of a vector (zeros for an invalid slot).
 __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4 (&w)[4]) {
@@ -67,7 +82,15 @@ __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4
 }
 
 // Encode one vector spread over the L lanes of a group: norm, FWHT, codes,
-// packed store, and (OUTL) the outlier mask and the lane's y values.
+// packed store, and (OUTL) the outlier mask and the lane's unnormalised
+// transform values x with inv = 1/(n sqrt(d)), so that y = x * inv.
+//
+// The decisions compare the unnormalised transform w_j against the
+// boundaries scaled by sigma = n sqrt(d) (y_j > t_k  <=>  w_j > t_k sigma):
+// the two forms differ only within about one f32 ulp of a boundary.  A code
+// is the mirror of the count of positive boundaries below |w_j|:
+// HALF + cnt for w_j > 0, HALF - 1 - cnt otherwise (w = 0 gives HALF - 1,
+// the code of y = 0).
 template <int D, int B, bool OUTL>
 __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B, OUTL>& ln,
                                            const uint4 (&w)[4], bool valid, uint8_t* rec, int slot,
@@ -77,48 +100,51 @@ __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B
     const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const uint32_t lo = (ww[k] << 16) ^ (((ln.sbits >> (2 * k)) & 1u) << 31);
-      const uint32_t hi = (ww[k] & 0xFFFF0000u) ^ (((ln.sbits >> (2 * k + 1)) & 1u) << 31);
-      x[2 * k] = __uint_as_float(lo);
-      x[2 * k + 1] = __uint_as_float(hi);
+      const uint32_t v = ww[k] ^ ln.smask[k];
+      x[2 * k] = __uint_as_float(v << 16);
+      x[2 * k + 1] = __uint_as_float(v & 0xFFFF0000u);
     }
   }
   // ||x||^2 by a pairwise tree (squares of bf16 values are exact in f32)
-  float sq[16];
+  float2 sq[8];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) sq[k] = fmaf(x[2 * k], x[2 * k], x[2 * k + 1] * x[2 * k + 1]);
+  for (int k = 0; k < 8; ++k) {
+    const float2 a = f2(x[4 * k], x[4 * k + 1]), b2 = f2(x[4 * k + 2], x[4 * k + 3]);
+    sq[k] = fma2(a, a, mul2(b2, b2));
+  }
 #pragma unroll
-  for (int h = 8; h; h >>= 1)
+  for (int h = 4; h; h >>= 1)
 #pragma unroll
-    for (int k = 0; k < h; ++k) sq[k] += sq[k + h];
-  float ss = sq[0];
+    for (int k = 0; k < h; ++k) sq[k] = add2(sq[k], sq[k + h]);
+  float ss = sq[0].x + sq[0].y;
 #pragma unroll
   for (int m = 1; m < E::L; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
   const float n = sqrtf(ss);
-  inv = n > 0.f ? 1.0f / (n * c.sqrt_d) : 0.f;
+  const float sigma = n * c.sqrt_d;
+  inv = n > 0.f ? 1.0f / sigma : 0.f;
+  float T[E::NPOS > 0 ? E::NPOS : 1];
+#pragma unroll
+  for (int k = 0; k < E::NPOS; ++k) T[k] = ln.tpos[k] * sigma;
+  const float Tout = OUTL ? c.thr_out * sigma : 0.f;
 
   fwht_regs<32>(x);
   fwht_lanes<32>(x, ln.lane, E::L);
 
-  // quantise (mirror of the symmetric table around t = 0) and pack LSB-first
   uint32_t wd[B];
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
-    const float y = x[r] * inv;
-    const bool pos = y > 0.f;
-    // non-positive side counts t <= |y| as |y| + 1ulp > t (exact tie rule)
-    const uint32_t a = (__float_as_uint(y) & 0x7FFFFFFFu) + (pos ? 0u : 1u);
-    uint32_t cnt = 0;
+    const float aw = fabsf(x[r]);
+    uint32_t msum = 0u;  // -(number of positive boundaries below |w|)
 #pragma unroll
-    for (int k = 0; k < E::NPOS; ++k) cnt += (a > ln.tpos[k]) ? 1u : 0u;
-    const uint32_t code = (E::HALF + cnt) ^ (pos ? 0u : (uint32_t)((1 << B) - 1));
+    for (int k = 0; k < E::NPOS; ++k) msum += mask_gt(aw, T[k]);
+    const uint32_t code = ((uint32_t)E::HALF - msum) ^ (mask_le(x[r], 0.f) & ((1u << B) - 1u));
     const int bit = r * B;
-    wd[bit >> 5] |= code << (bit & 31);
-    if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
-    if (OUTL) omask |= (fabsf(y) > c.thr_out ? 1u : 0u) << r;
+    wd[bit >> 5] += code << (bit & 31);
+    if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code >> (32 - (bit & 31));
+    if (OUTL) omask |= mask_gt(aw, Tout) & (1u << r);
   }
   if (valid) {
     uint8_t* dstrow = rec + (size_t)slot * E::RB + ln.lg * 4 * B;
