@@ -204,6 +204,12 @@ typedef struct {
   int32_t max_chunks;        /* host upper bound of n_chunks (sizes the grid) */
   int32_t max_tail;          /* host upper bound of tail_len */
   int32_t splits;            /* splits per (layer, batch, kv head); 0 = automatic */
+  /* 0: automatic.  Compressed tokens at head dims 64 and 128 of codecs
+   * without outlier side lists run on the tensor cores (mma.sync, f16 hi/lo
+   * operand splits, f32 accumulation); everything else on the CUDA-core
+   * kernel (f32 FMA from the centroid table).  Nonzero: always the CUDA-core
+   * kernel.  Both meet the same tolerance. */
+  int32_t cuda_core_path;
 } tq_attn_args;
 
 /* Workspace bytes tq_decode_attn needs for these arguments (0 on invalid args). */
@@ -212,7 +218,12 @@ size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k
 
 /* workspace: device, 256-byte aligned, >= tq_decode_attn_workspace_size bytes.
  * Its contents need no initialisation and are garbage afterwards.  An empty
- * context (no compressed and no dense token) yields a zero output row. */
+ * context (no compressed and no dense token) yields a zero output row.
+ * When a call has both compressed tokens on the tensor-core kernel and dense
+ * tokens, the dense kernel runs on a library-owned stream of the current
+ * device (created, with two events, by the first such call), forked from and
+ * joined back to `stream` with events: the call's work stays ordered on
+ * `stream` like any other. */
 tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
                          const tq_codec* v_codec, void* workspace, size_t workspace_bytes,
                          void* stream);

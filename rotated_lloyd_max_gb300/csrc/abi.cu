@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/tq.h"
 #include "tq_params.h"
@@ -72,6 +73,32 @@ int max_dyn_smem() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 227 * 1024;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 227 * 1024;
   return n;
+}
+
+// One auxiliary stream and a fork/join event pair per device, created on first
+// use: a call whose compressed and dense splits run on different kernels
+// launches the dense kernel on the auxiliary stream so the two overlap.  The
+// mutex keeps a fork, its launches and its join together when several host
+// threads call at once.
+struct AuxStream {
+  bool ready = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_aux_mu;
+AuxStream g_aux[64];
+
+AuxStream* aux_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  AuxStream& a = g_aux[dev];
+  if (!a.ready) {
+    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    a.ready = true;
+  }
+  return &a;
 }
 
 // ----------------------------------------------------------------- attention plan
@@ -223,6 +250,31 @@ void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
   p.sm_ent_stage = 0;
   int stage = p.krec ? p.k_main + (p.shared_kv ? 0 : p.v_main) : 0;
   stage = std::max(stage, (4 * D * GTP * 4 + 1) / 2);  // the warps' partials at the end
+  p.sm_stage = al(stage, 128);
+  p.sm_main = off;
+  off += 2 * p.sm_stage;
+  p.sm_total = off;
+}
+
+void attn_mma_smem_layout(AttnParams& p, int D) {
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  int off = 0;
+  p.sm_kpair = off;  // the kernel addresses both pair tables at these fixed offsets
+  off += (1 << (2 * p.kb)) * 128;
+  p.sm_vpair = off;
+  off += (p.vb == 3 ? 120 : (1 << (2 * p.vb))) * 128;
+  p.sm_q = off;
+  off += 8 * D * 4;
+  p.sm_slot = off;   // centroid halves
+  off += 32 * 8;
+  p.sm_red = off;
+  off += 4 * 2 * 8 * 4;
+  p.sm_logit = off;  // query fragments [d/16][32 lanes][16 B]
+  off = al(off + (D / 16) * 32 * 16, 128);
+  p.sm_lut = p.sm_corr = p.sm_pre = p.sm_ent = off;  // unused by this kernel
+  p.sm_ent_stage = 0;
+  int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
+  stage = std::max(stage, (4 * 8 * (D + D / 8) * 4 + 1) / 2);  // the warps' partials at the end
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
   off += 2 * p.sm_stage;
@@ -471,8 +523,38 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.ws_ml = (float*)((char*)workspace + pl.ws_acc_bytes);
   cudaStream_t s = (cudaStream_t)stream;
   const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
+  // tensor cores for outlier-free codecs at head dims 64 and 128 (side-list
+  // corrections are latency-bound scatter work, better overlapped by the
+  // CUDA-core kernel's FMA work)
+  const bool mma_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0 && !a->cuda_core_path &&
+                          !pl.kc.has_outl && !pl.vc.has_outl;
   const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
-  if (rec_kernel) {
+  if (mma_kernel) {
+    // compressed splits on the tensor cores; dense splits (if any) on the
+    // warp-local kernel's dense path, on the auxiliary stream so that the two
+    // kernels overlap (fork and join through events on the caller's stream)
+    AttnParams pm = p;
+    attn_mma_smem_layout(pm, pl.D);
+    if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+    if (pl.S > pl.Sc) {
+      AttnParams pd = p;
+      pd.split_base = pl.Sc;
+      attn_rec_smem_layout(pd, pl.D, pl.GT);
+      if (pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+      std::lock_guard<std::mutex> lock(g_aux_mu);
+      AuxStream* ax = aux_stream();
+      if (!ax) return TQ_ERR_CUDA;
+      if (cudaEventRecord(ax->fork, s) != cudaSuccess || cudaStreamWaitEvent(ax->s, ax->fork, 0) != cudaSuccess)
+        return TQ_ERR_CUDA;
+      if (launch_attn_rec(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), ax->s) != cudaSuccess)
+        return TQ_ERR_CUDA;
+      if (launch_attn_mma(pm, pl.D, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+      if (cudaEventRecord(ax->join, ax->s) != cudaSuccess || cudaStreamWaitEvent(s, ax->join, 0) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    } else {
+      if (launch_attn_mma(pm, pl.D, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    }
+  } else if (rec_kernel) {
     // compressed splits on the warp-local path, dense splits on the general
     // dense path, one launch
     attn_rec_smem_layout(p, pl.D, pl.GT);

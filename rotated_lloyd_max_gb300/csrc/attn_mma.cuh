@@ -1,0 +1,538 @@
+// a6-a8 on the tensor cores: decode attention over the compressed records
+// (head dims 64 and 128, up to 8 query heads of one kv head per CTA).
+//
+// Same quantities as the warp-local kernel (q~ = H(s_k . q)/sqrt(d) once per
+// CTA; a token scores n_i * q~ . c[codes]; values accumulate p_i n_i c[codes]
+// in the rotated basis, inverted once by the merge), but both contractions
+// run as mma.sync.m16n8k16 (f16 operands, f32 accumulation):
+//   scores   C[token][head]  = K~[token][coord] . Q~^T[coord][head]
+//   values   O^T[coord][head] += V~^T[coord][token] . P'^T[token][head]
+// with the query heads (<= 8) as the MMA's n dimension.  f16 alone does not
+// hold an f32 centroid or q~ to the attention tolerance, so every operand is
+// split x = hi + lo (two f16, 22 significant bits) and a product is the three
+// MMAs hi.hi + hi.lo + lo.hi.  Centroids enter scaled by 2^16, q~ by a per-head
+// power of two and P' by a per-warp power of two, so that no f16 part is
+// subnormal or out of range; the scales are undone in f32.
+//
+// Dequantisation is one 64-bit shared-memory load per PAIR of codes from a
+// pair table (entry = hi pair, lo pair), replicated so that lane j of a
+// half-warp only ever touches bank pair j (conflict-free at any index).
+// Fragment coordinates are permuted so that a lane's codes are a contiguous
+// bit run of a packed row:
+//   score A (tokens x coords), k-step kk: fragment column 2t+e <-> coordinate
+//     (d/4) t + 4 kk + e, column 2t+8+e <-> (d/4) t + 4 kk + 2 + e;
+//   value A (coords x tokens), m-tile mc: fragment row g <-> coordinate
+//     (d/8) g + 2 mc, row g+8 <-> (d/8) g + 2 mc + 1.
+// (g = lane / 4, t = lane % 4: the mma.sync fragment coordinates.)
+//
+// A warp owns 32 of a record's 128 tokens (two m-tiles) end to end; records
+// are staged with cp.async in a two-deep ring, one CTA barrier per record;
+// the online softmax is warp-local (the running max moves only when a logit
+// passes it by 2^8).  Codecs with outlier side lists are not handled here:
+// their corrections are a latency-bound scatter (about 6 entries per token
+// and stream at T = 2) that the CUDA-core kernel overlaps with its FMA work at
+// twice this kernel's occupancy, so the host sends them there.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "attn.cuh"
+
+namespace tq {
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) -> f16 pairs hi = f16(x), lo = f16(x - hi); x0 in the low half.
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 r = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// floor(log2 x) for a normal positive float (-127 for zero).
+__device__ __forceinline__ int exp_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
+// 2^e as a float, e clamped to the normal range.
+__device__ __forceinline__ float pow2i(int e) {
+  e = max(-126, min(127, e));
+  return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// NB bits of a packed row starting at bit `off` (NB, off multiples of 32 when
+// ALIGNED), as ceil(NB/32) words, LSB-first.  The unaligned form reads one
+// word past the run: callers keep that inside the staged record.
+template <int NB, bool ALIGNED>
+__device__ __forceinline__ void load_run(const unsigned char* row, int off, uint32_t (&w)[(NB + 31) / 32]) {
+  constexpr int NW = (NB + 31) / 32;
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(row) + (off >> 5);
+  if constexpr (ALIGNED && NW == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(r);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (ALIGNED && NW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(r);
+    w[0] = v.x; w[1] = v.y;
+  } else if constexpr (ALIGNED) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = r[i];
+  } else {
+    const int sh = off & 31;
+    uint32_t tmp[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) tmp[i] = r[i];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(tmp[i], tmp[i + 1], sh);
+  }
+}
+
+// W bits at bit offset `off` (constant after unrolling) of a word run.
+template <int NW>
+__device__ __forceinline__ uint32_t run_bits(const uint32_t (&w)[NW], int off, int W) {
+  const int wi = off >> 5, sh = off & 31;
+  uint32_t v;
+  if (sh + W <= 32 || wi + 1 >= NW) v = w[wi] >> sh;
+  else v = __funnelshift_r(w[wi], w[wi + 1], sh);
+  return v & ((1u << W) - 1u);
+}
+
+// Shared-memory byte offset of the pair-table entry named by the W-bit field
+// at bit `off` of a word run: field * 128 + lane_off (lane_off < 128), i.e.
+// the field moved to bit 7 and or-ed with the lane's bank-pair offset.
+template <int NW>
+__device__ __forceinline__ uint32_t pair_off(const uint32_t (&w)[NW], int off, int W, uint32_t lane_off) {
+  const int wi = off >> 5, sh = off & 31;
+  uint32_t v;
+  if (sh + W <= 32 || wi + 1 >= NW) v = sh >= 7 ? (w[wi] >> (sh - 7)) : (w[wi] << (7 - sh));
+  else v = __funnelshift_r(w[wi], w[wi + 1], sh - 7);
+  return (v & (((1u << W) - 1u) << 7)) | lane_off;
+}
+
+// 3-bit codes -> one code per nibble (8 codes of a 24-bit field -> 32 bits).
+__device__ __forceinline__ uint32_t spread3(uint32_t x) {
+  x &= 0xFFFFFFu;
+  x = (x & 0xFFFu) | ((x << 4) & 0xFFF0000u);
+  x = (x & 0x003F003Fu) | ((x << 2) & 0x3F003F00u);
+  x = (x & 0x07070707u) | ((x << 1) & 0x70707070u);
+  return x;
+}
+
+template <int D>
+struct MCfg {
+  static constexpr int KS = D / 16;  // score k-steps = value m-tiles
+  static constexpr int KR = D / 4;   // coordinates of a lane's score run
+  static constexpr int VR = D / 8;   // coordinates of a lane group's value run
+};
+
+// Value pair-table index width: 2b bits, or two nibbles for b = 3.
+template <int VB>
+struct VIdx {
+  static constexpr int FW = (VB == 3) ? 4 : VB;   // field width after spreading
+  static constexpr int ENTRIES = (VB == 3) ? 120 : (1 << (2 * VB));
+};
+
+// Pair-index words for the value fragments of tokens (t0, t1): ze holds, per
+// 2*FW-bit field m, (code(t0, 2m) | code(t1, 2m) << FW); zo the same for the
+// odd coordinates.
+template <int VB, int NW>
+__device__ __forceinline__ void v_pair_words(const uint32_t (&r0)[NW], const uint32_t (&r1)[NW],
+                                             uint32_t (&ze)[(VB == 3) ? 2 * NW : NW],
+                                             uint32_t (&zo)[(VB == 3) ? 2 * NW : NW]) {
+  if constexpr (VB == 3) {
+    // spread to nibbles first (NW words of 3-bit codes hold at most 16 codes)
+    constexpr int NS = 2 * NW;
+    uint32_t s0[NS], s1[NS];
+    s0[0] = spread3(r0[0]);
+    s1[0] = spread3(r1[0]);
+    if constexpr (NS > 1) {
+      s0[1] = spread3(NW > 1 ? __funnelshift_r(r0[0], r0[1], 24) : (r0[0] >> 24));
+      s1[1] = spread3(NW > 1 ? __funnelshift_r(r1[0], r1[1], 24) : (r1[0] >> 24));
+    }
+#pragma unroll
+    for (int i = 2; i < NS; ++i) { s0[i] = 0u; s1[i] = 0u; }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      ze[i] = (s0[i] & 0x0F0F0F0Fu) | ((s1[i] << 4) & 0xF0F0F0F0u);
+      zo[i] = ((s0[i] >> 4) & 0x0F0F0F0Fu) | (s1[i] & 0xF0F0F0F0u);
+    }
+  } else {
+    constexpr uint32_t M = VB == 4 ? 0x0F0F0F0Fu : VB == 2 ? 0x33333333u : 0x55555555u;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      ze[i] = (r0[i] & M) | ((r1[i] << VB) & ~M);
+      zo[i] = ((r0[i] >> VB) & M) | (r1[i] & ~M);
+    }
+  }
+}
+
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_constant__ AttnParams p) {
+  using C = MCfg<D>;
+  constexpr int KS = C::KS, KR = C::KR, VR = C::VR;
+  constexpr int KNB = KR * KB, VNB = VR * VB;
+  constexpr int KNW = (KNB + 31) / 32, VNW = (VNB + 31) / 32;
+  constexpr bool KAL = (KNB % 32) == 0, VAL = (VNB % 32) == 0;
+  constexpr int FW = VIdx<VB>::FW;
+  constexpr int ZW = (VB == 3) ? 2 * VNW : VNW;
+  constexpr int EK = 1 << (2 * KB), EV = VIdx<VB>::ENTRIES;
+  constexpr int KP_OFF = 0, VP_OFF = EK * 128;  // pair tables at fixed offsets (immediate addressing)
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* qf = reinterpret_cast<float*>(sm + p.sm_q);      // [8][D] q~ (f32)
+  float* wml = reinterpret_cast<float*>(sm + p.sm_red);   // [4][2][8]
+  uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);  // [KS][32 lanes] (hi b0, hi b1, lo b0, lo b1)
+  uint2* cent = reinterpret_cast<uint2*>(sm + p.sm_slot); // [32] (hi|lo f16) of K then V centroids x 2^16
+  unsigned char* mainb = sm + p.sm_main;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int l = blockIdx.z;
+  int rem = blockIdx.y;
+  const int hg = rem % p.n_hg;
+  rem /= p.n_hg;
+  const int kvh = rem % p.Hkv, b = rem / p.Hkv;
+  const int split = blockIdx.x;
+  const int GT = p.G / p.n_hg;
+  const int h0 = kvh * p.G + hg * GT;
+  const int lb = l * p.B + b;
+  const int64_t qh0 = (int64_t)lb * p.Hq + h0;
+  const int nch = min(p.n_chunks[lb], p.rec_cap);
+  const int c_begin = split * p.cps;
+  const int c_end = min(c_begin + p.cps, nch);
+  if (c_begin >= c_end) {
+    if (tid < GT) {
+      float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+    }
+    return;
+  }
+  const int n = c_end - c_begin;
+  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
+  const uint8_t* vb0 = p.shared_kv ? kb0
+                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
+  auto issue_main = [&](int i) {
+    if (i < n) {
+      const int64_t c = c_begin + i;
+      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+    }
+    cp_async_commit();
+  };
+  issue_main(0);
+
+  // ---- q~ = H(s_k . q)/sqrt(d) of the CTA's heads (rows >= GT are zero)
+  for (int hh = warp; hh < 8; hh += 4) {
+    constexpr int R = D / 32;
+    float x[R];
+    if (hh < GT) {
+      const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + hh) * D + lane * R;
+#pragma unroll
+      for (int r = 0; r < R; r += 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + r);
+        x[r] = bf16_lo(w);
+        x[r + 1] = bf16_hi(w);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int j = lane * R + r;
+        if ((p.ksign[j >> 5] >> (j & 31)) & 1u) x[r] = -x[r];
+      }
+      fwht_regs<R>(x);
+      fwht_lanes<R>(x, lane, 32);
+#pragma unroll
+      for (int r = 0; r < R; ++r) x[r] *= inv_sqrt_dim<D>();
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) x[r] = 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) qf[hh * D + lane * R + r] = x[r];
+  }
+  // f16 halves of every centroid x 2^16: cent[i] = (hi, lo) of K centroid i,
+  // cent[16 + i] of V centroid i
+  if (tid < 32) {
+    const float v = (tid < 16 ? p.kc[tid] : p.vc[tid - 16]) * 65536.f;
+    const __half h = __float2half_rn(v);
+    const __half r = __float2half_rn(v - __half2float(h));
+    cent[tid] = make_uint2(__half_as_ushort(h), __half_as_ushort(r));
+  }
+  __syncthreads();  // q~ and the centroid halves complete
+  // pair tables: entry e at byte e*128 + (lane % 16)*8 holds (hi pair, lo pair)
+  // of its two centroids (first in the low half)
+  for (int i = tid; i < EK * 16; i += kThreads) {
+    const int e = i >> 4;
+    const uint2 a = cent[e & ((1 << KB) - 1)], c = cent[e >> KB];
+    *reinterpret_cast<uint2*>(sm + KP_OFF + i * 8) = make_uint2(__byte_perm(a.x, c.x, 0x5410), __byte_perm(a.y, c.y, 0x5410));
+  }
+  for (int i = tid; i < EV * 16; i += kThreads) {
+    const int e = i >> 4;
+    const int c0 = e & ((1 << FW) - 1), c1 = e >> FW;
+    uint2 v = make_uint2(0u, 0u);
+    if (c0 < (1 << VB) && c1 < (1 << VB)) {
+      const uint2 a = cent[16 + c0], c = cent[16 + c1];
+      v = make_uint2(__byte_perm(a.x, c.x, 0x5410), __byte_perm(a.y, c.y, 0x5410));
+    }
+    *reinterpret_cast<uint2*>(sm + VP_OFF + i * 8) = v;
+  }
+  __syncthreads();
+
+  // ---- query fragments: head g, coordinates (d/4) t + 4 kk + {0,1} / {2,3},
+  // scaled by 2^s_g so that the largest |q~| of the head is in [2^13, 2^14);
+  // stored per lane in shared memory (read once per k-step for both m-tiles)
+  float fq0, fq1;  // 2^-(s_h + 16) for the lane's score heads 2t, 2t+1
+  {
+    const float* qrow = qf + g * D + KR * t;
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < KR; ++j) mx = fmaxf(mx, fabsf(qrow[j]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int s = mx > 0.f ? 13 - exp_of(mx) : 0;
+    const float sc = pow2i(s);
+    for (int kk = warp; kk < KS; kk += 4) {
+      uint4 f;
+      split_f16x2(qrow[4 * kk] * sc, qrow[4 * kk + 1] * sc, f.x, f.z);
+      split_f16x2(qrow[4 * kk + 2] * sc, qrow[4 * kk + 3] * sc, f.y, f.w);
+      qfrag[kk * 32 + lane] = f;
+    }
+    const int s0 = __shfl_sync(0xffffffffu, s, 4 * (2 * t));
+    const int s1 = __shfl_sync(0xffffffffu, s, 4 * (2 * t + 1));
+    fq0 = pow2i(-s0 - 16);
+    fq1 = pow2i(-s1 - 16);
+  }
+  const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
+  const uint32_t loff = (lane & 15) * 8;
+  auto kpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + KP_OFF + o); };
+  auto vpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + VP_OFF + o); };
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float acc[KS][4];
+#pragma unroll
+  for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mc][e] = 0.f;
+  int kx = 127;  // P' f16 scale exponent of this warp (only ever decreases)
+  const int rbk = D * KB / 8, rbv = D * VB / 8;
+
+  for (int i = 0; i < n; ++i) {
+    cp_async_wait<0>();
+    __syncthreads();  // record i is in; record i-1 is done with
+    issue_main(i + 1);
+    const unsigned char* st = stage(i);
+    const unsigned char* kcodes = st + warp * 32 * rbk;
+    const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + warp * 32;
+    const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
+    const unsigned char* vcodes = vbase + warp * 32 * rbv;
+    const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
+
+    // ---- scores: tile mt holds tokens 16 mt + g (elements 0, 1) and + 8 (2, 3)
+    float sc[2][4];
+    {
+      uint32_t w[4][KNW];  // runs of tokens g, g + 8, 16 + g, 24 + g
+#pragma unroll
+      for (int r = 0; r < 4; ++r) load_run<KNB, KAL>(kcodes + (8 * r + g) * rbk, KNB * t, w[r]);
+      float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint4 f = qfrag[kk * 32 + lane];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t ah[4], al[4];
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int off = (4 * kk + 2 * hf) * KB;
+            const uint2 e0 = kpair_at(pair_off(w[2 * mt], off, 2 * KB, loff));
+            const uint2 e1 = kpair_at(pair_off(w[2 * mt + 1], off, 2 * KB, loff));
+            ah[2 * hf] = e0.x;
+            al[2 * hf] = e0.y;
+            ah[2 * hf + 1] = e1.x;
+            al[2 * hf + 1] = e1.y;
+          }
+          mma_f16(cc[mt], ah, f.x, f.y);
+          mma_f16(cc[mt], ah, f.z, f.w);
+          mma_f16(cc[mt], al, f.x, f.y);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        sc[mt][0] = cc[mt][0] * fq0;
+        sc[mt][1] = cc[mt][1] * fq1;
+        sc[mt][2] = cc[mt][2] * fq0;
+        sc[mt][3] = cc[mt][3] * fq1;
+      }
+    }
+    // logits (log2 domain)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float fa = knorm[16 * mt + g] * p.sscale, fb = knorm[16 * mt + g + 8] * p.sscale;
+      sc[mt][0] = hv0 ? sc[mt][0] * fa : -INFINITY;
+      sc[mt][1] = hv1 ? sc[mt][1] * fa : -INFINITY;
+      sc[mt][2] = hv0 ? sc[mt][2] * fb : -INFINITY;
+      sc[mt][3] = hv1 ? sc[mt][3] * fb : -INFINITY;
+    }
+    // ---- online softmax (the max moves only when a logit passes it by 2^8)
+    {
+      bool need = false;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+        need |= (sc[mt][0] > m0 + 8.f) | (sc[mt][2] > m0 + 8.f) | (sc[mt][1] > m1 + 8.f) | (sc[mt][3] > m1 + 8.f);
+      if (__any_sync(0xffffffffu, need)) {
+        float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+        float x1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+          x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, m));
+          x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, m));
+        }
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+        const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int mc = 0; mc < KS; ++mc) {
+          acc[mc][0] *= a0;
+          acc[mc][1] *= a1;
+          acc[mc][2] *= a0;
+          acc[mc][3] *= a1;
+        }
+      }
+    }
+    // p, l, p' = p * n_v (unscaled), in place of the logits
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float va = vnorm[16 * mt + g], vb = vnorm[16 * mt + g + 8];
+      const float p0 = hv0 ? exp2f(sc[mt][0] - m0) : 0.f, p1 = hv1 ? exp2f(sc[mt][1] - m1) : 0.f;
+      const float p2 = hv0 ? exp2f(sc[mt][2] - m0) : 0.f, p3 = hv1 ? exp2f(sc[mt][3] - m1) : 0.f;
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      sc[mt][0] = p0 * va;
+      sc[mt][1] = p1 * va;
+      sc[mt][2] = p2 * vb;
+      sc[mt][3] = p3 * vb;
+    }
+    // f16 range of P': p <= 2^8, so p' 2^kx <= 2^15 with kx = 6 - floor(log2 max n_v)
+    {
+      const float vmax = warp_max(vnorm[lane]);
+      if (vmax > 0.f) {
+        const int kn = 6 - exp_of(vmax);
+        if (kn < kx) {
+          const float r = pow2i(kn - kx);
+#pragma unroll
+          for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mc][e] *= r;
+          kx = kn;
+        }
+      }
+    }
+    const float psc = pow2i(kx);
+    // ---- values: k-step mt = the 16 tokens of score tile mt
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      uint32_t th, tl, bhw, blw;  // (p' hi / lo) of tokens g (top) and g + 8 (bottom)
+      split_f16x2(sc[mt][0] * psc, sc[mt][1] * psc, th, tl);
+      split_f16x2(sc[mt][2] * psc, sc[mt][3] * psc, bhw, blw);
+      const int sa = 4 * (2 * t) + (g >> 1), sb = sa + 4;
+      const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+      const uint32_t pb0h = __byte_perm(__shfl_sync(0xffffffffu, th, sa), __shfl_sync(0xffffffffu, th, sb), sel);
+      const uint32_t pb0l = __byte_perm(__shfl_sync(0xffffffffu, tl, sa), __shfl_sync(0xffffffffu, tl, sb), sel);
+      const uint32_t pb1h = __byte_perm(__shfl_sync(0xffffffffu, bhw, sa), __shfl_sync(0xffffffffu, bhw, sb), sel);
+      const uint32_t pb1l = __byte_perm(__shfl_sync(0xffffffffu, blw, sa), __shfl_sync(0xffffffffu, blw, sb), sel);
+      // value runs of tokens 2t, 2t+1 (k columns 2t, 2t+1) and 2t+8, 2t+9
+      uint32_t r0[VNW], r1[VNW], r2[VNW], r3[VNW];
+      const unsigned char* vt = vcodes + 16 * mt * rbv;
+      load_run<VNB, VAL>(vt + (2 * t) * rbv, VNB * g, r0);
+      load_run<VNB, VAL>(vt + (2 * t + 1) * rbv, VNB * g, r1);
+      load_run<VNB, VAL>(vt + (2 * t + 8) * rbv, VNB * g, r2);
+      load_run<VNB, VAL>(vt + (2 * t + 9) * rbv, VNB * g, r3);
+      uint32_t ze01[ZW], zo01[ZW], ze23[ZW], zo23[ZW];
+      v_pair_words<VB, VNW>(r0, r1, ze01, zo01);
+      v_pair_words<VB, VNW>(r2, r3, ze23, zo23);
+#pragma unroll
+      for (int mc = 0; mc < KS; ++mc) {
+        const int off = mc * 2 * FW;
+        const uint2 e0 = vpair_at(pair_off(ze01, off, 2 * FW, loff));
+        const uint2 e1 = vpair_at(pair_off(zo01, off, 2 * FW, loff));
+        const uint2 e2 = vpair_at(pair_off(ze23, off, 2 * FW, loff));
+        const uint2 e3 = vpair_at(pair_off(zo23, off, 2 * FW, loff));
+        const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x};
+        const uint32_t al[4] = {e0.y, e1.y, e2.y, e3.y};
+        mma_f16(acc[mc], ah, pb0h, pb1h);
+        mma_f16(acc[mc], ah, pb0l, pb1l);
+        mma_f16(acc[mc], al, pb0h, pb1h);
+      }
+    }
+  }
+
+  // ---- merge the warps' (m, l, acc) into the split's partial
+#pragma unroll
+  for (int m = 4; m < 32; m <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+  }
+  __syncwarp();
+  cp_async_wait<0>();
+  __syncthreads();  // all records consumed: the staging ring becomes the merge buffer
+  // merge buffer [4 warps][8 heads][D + D/8]: element (h, j) of a warp at
+  // h (D + D/8) + j + 4 (j / 32) + h / 2, so that a warp's 32 fragment stores
+  // (j = (d/8) g + const, h = 2t + const) hit 32 different banks
+  float* red = reinterpret_cast<float*>(mainb);
+  constexpr int RS = D + D / 8;
+  auto red_at = [&](int w, int h, int j) { return w * 8 * RS + h * RS + j + 4 * (j >> 5) + (h >> 1); };
+  {
+    const float un = pow2i(-16 - kx);
+#pragma unroll
+    for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = VR * g + 2 * mc + (e >> 1), h = 2 * t + (e & 1);
+        red[red_at(warp, h, j)] = acc[mc][e] * un;
+      }
+  }
+  if (g == 0) {
+    wml[(warp * 2) * 8 + 2 * t] = m0;
+    wml[(warp * 2) * 8 + 2 * t + 1] = m1;
+    wml[(warp * 2 + 1) * 8 + 2 * t] = l0;
+    wml[(warp * 2 + 1) * 8 + 2 * t + 1] = l1;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < GT * D; idx += kThreads) {
+    const int h = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 2) * 8 + h]);
+    float v = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw = wml[(w * 2) * 8 + h];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      v = fmaf(f, red[red_at(w, h, j)], v);
+      L = fmaf(f, wml[(w * 2 + 1) * 8 + h], L);
+    }
+    p.ws_acc[((qh0 + h) * p.S + split) * D + j] = v;
+    if (j == 0) {
+      float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+      ml[0] = M;
+      ml[1] = L;
+    }
+  }
+}
+
+template <int D, int KB, int VB>
+cudaError_t attn_mma_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       p.sm_total);
+  if (e != cudaSuccess) return e;
+  attn_mma_kernel<D, KB, VB><<<grid, kThreads, p.sm_total, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

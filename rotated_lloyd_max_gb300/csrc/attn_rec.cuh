@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   const int hg = rem % p.n_hg;
   rem /= p.n_hg;
   const int kvh = rem % p.Hkv, b = rem / p.Hkv;
-  const int split = blockIdx.x;
+  const int split = blockIdx.x + p.split_base;
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;

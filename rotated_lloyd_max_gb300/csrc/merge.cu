@@ -122,6 +122,31 @@ cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaS
   }
 }
 
+#define TQ_MMA_DECL(D_, K_) cudaError_t launch_attn_mma_d##D_##_k##K_(const AttnParams& p, dim3 grid, cudaStream_t s);
+TQ_MMA_DECL(64, 1)
+TQ_MMA_DECL(64, 2)
+TQ_MMA_DECL(64, 3)
+TQ_MMA_DECL(64, 4)
+TQ_MMA_DECL(128, 1)
+TQ_MMA_DECL(128, 2)
+TQ_MMA_DECL(128, 3)
+TQ_MMA_DECL(128, 4)
+#undef TQ_MMA_DECL
+
+cudaError_t launch_attn_mma(const AttnParams& p, int D, dim3 grid, cudaStream_t s) {
+  switch (D * 10 + p.kb) {
+    case 641: return launch_attn_mma_d64_k1(p, grid, s);
+    case 642: return launch_attn_mma_d64_k2(p, grid, s);
+    case 643: return launch_attn_mma_d64_k3(p, grid, s);
+    case 644: return launch_attn_mma_d64_k4(p, grid, s);
+    case 1281: return launch_attn_mma_d128_k1(p, grid, s);
+    case 1282: return launch_attn_mma_d128_k2(p, grid, s);
+    case 1283: return launch_attn_mma_d128_k3(p, grid, s);
+    case 1284: return launch_attn_mma_d128_k4(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s) {
   switch (D) {
     case 64: return launch_attn_d64(p, GT, grid, s);

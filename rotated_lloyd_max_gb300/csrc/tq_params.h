@@ -88,7 +88,7 @@ struct AttnParams {
   float* ws_ml;
   // dynamic shared memory carve-up (bytes)
   int sm_q, sm_lut, sm_red, sm_logit, sm_main, sm_stage, sm_ent, sm_ent_stage, sm_pre, sm_slot,
-      sm_corr, sm_total;
+      sm_corr, sm_kpair, sm_vpair, sm_total;
 };
 
 struct MergeParams {
@@ -109,12 +109,15 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
 // warp-local kernel for the compressed splits (head dims 64 and 128)
 cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
+// tensor-core kernel for the compressed splits (head dims 64 and 128)
+cudaError_t launch_attn_mma(const AttnParams& p, int D, dim3 grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 
 // Dynamic shared memory of the attention kernel for head dim D and head group GT
 // (everything but the record-size dependent parts is fixed by D and GT).
 void attn_smem_layout(AttnParams& p, int D, int GT);
 void attn_rec_smem_layout(AttnParams& p, int D, int GT);
+void attn_mma_smem_layout(AttnParams& p, int D);
 
 // The codebook kernel writes this block into the caller's scratch.
 struct CodebookOut {

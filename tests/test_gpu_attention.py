@@ -35,7 +35,8 @@ def _ocodec(orc, c):
 
 
 def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=False, dense=False,
-             tail_cap=None, splits=0, seed=0, q_pad=0, k_outlier_frac=0.0, end_to_end=True, scale=1.0):
+             tail_cap=None, splits=0, seed=0, q_pad=0, k_outlier_frac=0.0, end_to_end=True, scale=1.0,
+             cuda_core_path=False):
     """chunks[b], tails[b]: compressed records and dense tail tokens of batch b
     (the same for every layer).  Returns (gpu_out, oracle_out, oracle_e2e_out)."""
     import torch
@@ -80,7 +81,8 @@ def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=F
                   tail_start=torch.from_numpy(tstart).to(dev), tail_len=torch.from_numpy(tail_len).to(dev),
                   max_tail=max(tails))
     kw["n_kv_heads"] = Hkv
-    tq.decode_attn(k_codec=None if dense else kc, v_codec=None if dense else vc, splits=splits, **kw)
+    tq.decode_attn(k_codec=None if dense else kc, v_codec=None if dense else vc, splits=splits,
+                   cuda_core_path=cuda_core_path, **kw)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
 
@@ -122,15 +124,31 @@ CASES = {
     "d128_gqa2_b4b1": dict(d=128, G=2, Hkv=2, B=3, L=1, chunks=[2, 0, 3], tails=[10, 64, 0], kb=4, vb=1),
     "gqa8_q_stride": dict(d=128, G=8, Hkv=1, B=2, L=1, chunks=[3, 3], tails=[20, 5], kb=2, vb=3, q_pad=3),
     "gqa3_odd_group": dict(d=64, G=3, Hkv=2, B=1, L=1, chunks=[2], tails=[9], kb=3, vb=3),
+    "hot_logits_gqa6": dict(d=128, G=6, Hkv=1, B=1, L=1, chunks=[3], tails=[0], kb=3, vb=2, scale=4.0),
+    "outliers_both_d64": dict(d=64, G=8, Hkv=1, B=2, L=1, chunks=[2, 1], tails=[3, 0], kb=2, vb=4, T=1.5,
+                              k_outlier_frac=0.05),
 }
 
+PATHS = ["automatic", "cuda_core"]  # automatic = tensor cores where the kernel applies
 
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_attention_cases(tq, orc, name):
-    got, want, e2e = run_case(tq, orc, **CASES[name])
+def test_attention_cases(tq, orc, name, path):
+    got, want, e2e = run_case(tq, orc, cuda_core_path=(path == "cuda_core"), **CASES[name])
     _assert_close(got, want)
     if e2e is not None:
         _assert_close(got, e2e)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kb", [1, 2, 3, 4])
+@pytest.mark.parametrize("vb", [1, 2, 3, 4])
+def test_tensor_core_bit_widths(tq, orc, d, kb, vb):
+    """Every (key bits, value bits) pair of the tensor-core kernel, two records."""
+    got, want, _ = run_case(tq, orc, d=d, G=4, Hkv=1, B=1, L=1, chunks=[2], tails=[0], kb=kb, vb=vb,
+                            end_to_end=False, seed=kb * 10 + vb)
+    _assert_close(got, want)
 
 
 def test_dense_boundary_layers(tq, orc):
@@ -140,8 +158,10 @@ def test_dense_boundary_layers(tq, orc):
     _assert_close(got, want)
 
 
-def test_split_count_invariance(tq, orc):
-    cfg = dict(d=128, G=4, Hkv=2, B=1, L=1, chunks=[12], tails=[100], kb=3, vb=2, end_to_end=False)
+@pytest.mark.parametrize("path", PATHS)
+def test_split_count_invariance(tq, orc, path):
+    cfg = dict(d=128, G=4, Hkv=2, B=1, L=1, chunks=[12], tails=[100], kb=3, vb=2, end_to_end=False,
+               cuda_core_path=(path == "cuda_core"))
     a, want, _ = run_case(tq, orc, splits=1, **cfg)
     b, _, _ = run_case(tq, orc, splits=40, **cfg)
     _assert_close(a, want)
