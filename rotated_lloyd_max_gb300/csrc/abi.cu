@@ -6,7 +6,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "../../include/tq.h"
 #include "tq_params.h"
@@ -75,32 +74,6 @@ int max_dyn_smem() {
   return n;
 }
 
-// One auxiliary stream and a fork/join event pair per device, created on first
-// use: a call whose compressed and dense splits run on different kernels
-// launches the dense kernel on the auxiliary stream so the two overlap.  The
-// mutex keeps a fork, its launches and its join together when several host
-// threads call at once.
-struct AuxStream {
-  bool ready = false;
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_aux_mu;
-AuxStream g_aux[64];
-
-AuxStream* aux_stream() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  AuxStream& a = g_aux[dev];
-  if (!a.ready) {
-    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-    a.ready = true;
-  }
-  return &a;
-}
-
 // ----------------------------------------------------------------- attention plan
 struct Plan {
   int D, G, GT, n_hg, S, Sc, cps, tps;
@@ -108,6 +81,7 @@ struct Plan {
   size_t ws_acc_bytes, ws_bytes;
   CodecDev kc, vc;
   bool has_rec, has_tail, shared;
+  bool mma;  // tensor-core kernel (head dims 64/128, no outlier side lists)
 };
 
 tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec* vcod, Plan* pl) {
@@ -173,6 +147,13 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   int64_t Sc = 0, St = 0;
   if (comp_tiles > 0) Sc = std::max<int64_t>(1, std::min(want, comp_tiles));
   if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want, tail_tiles));
+  // Tensor cores for head dims 64 and 128 unless a codec has outlier side
+  // lists (their corrections are latency-bound scatter work, better
+  // overlapped by the CUDA-core kernel's FMA work) or the caller asks for the
+  // CUDA-core kernel.  Its CTAs take at least two records each, which
+  // amortises their per-CTA set-up (pair tables, query fragments).
+  pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
+  if (pl->mma && a->splits <= 0 && comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
   int64_t cps = 1, tps = TT;
   if (Sc > 0) {
     cps = cdiv(comp_tiles, Sc);
@@ -523,37 +504,14 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.ws_ml = (float*)((char*)workspace + pl.ws_acc_bytes);
   cudaStream_t s = (cudaStream_t)stream;
   const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
-  // tensor cores for outlier-free codecs at head dims 64 and 128 (side-list
-  // corrections are latency-bound scatter work, better overlapped by the
-  // CUDA-core kernel's FMA work)
-  const bool mma_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0 && !a->cuda_core_path &&
-                          !pl.kc.has_outl && !pl.vc.has_outl;
   const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
-  if (mma_kernel) {
-    // compressed splits on the tensor cores; dense splits (if any) on the
-    // warp-local kernel's dense path, on the auxiliary stream so that the two
-    // kernels overlap (fork and join through events on the caller's stream)
+  if (pl.mma) {
+    // tensor cores: compressed and dense splits in one launch
     AttnParams pm = p;
+    if (!pl.has_rec) pm.kb = pm.vb = 1;  // dense only: any instantiation (its tables go unused)
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-    if (pl.S > pl.Sc) {
-      AttnParams pd = p;
-      pd.split_base = pl.Sc;
-      attn_rec_smem_layout(pd, pl.D, pl.GT);
-      if (pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-      std::lock_guard<std::mutex> lock(g_aux_mu);
-      AuxStream* ax = aux_stream();
-      if (!ax) return TQ_ERR_CUDA;
-      if (cudaEventRecord(ax->fork, s) != cudaSuccess || cudaStreamWaitEvent(ax->s, ax->fork, 0) != cudaSuccess)
-        return TQ_ERR_CUDA;
-      if (launch_attn_rec(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), ax->s) != cudaSuccess)
-        return TQ_ERR_CUDA;
-      if (launch_attn_mma(pm, pl.D, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-      if (cudaEventRecord(ax->join, ax->s) != cudaSuccess || cudaStreamWaitEvent(s, ax->join, 0) != cudaSuccess)
-        return TQ_ERR_CUDA;
-    } else {
-      if (launch_attn_mma(pm, pl.D, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-    }
+    if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
   } else if (rec_kernel) {
     // compressed splits on the warp-local path, dense splits on the general
     // dense path, one launch

@@ -34,6 +34,7 @@
 // twice this kernel's occupancy, so the host sends them there.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "attn.cuh"
@@ -169,6 +170,228 @@ __device__ __forceinline__ void v_pair_words(const uint32_t (&r0)[NW], const uin
   }
 }
 
+// The 4 warps' (m, l, acc) of a split -> the split's partial in the
+// workspace.  acc is in the value-fragment layout (coordinate (d/8) g + 2 mc
+// (+1 for elements 2, 3), head 2t (+1 for odd elements)), scaled by 1/un.
+// mainb (the staging ring, free by now) holds the warps' partials.
+template <int D>
+__device__ __forceinline__ void mma_split_merge(const AttnParams& p, unsigned char* mainb, float* wml,
+                                                const float (&acc)[D / 16][4], float un, float m0, float m1,
+                                                float l0, float l1, int GT, int64_t qh0, int split) {
+  constexpr int KS = D / 16, VR = D / 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int m = 4; m < 32; m <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+  }
+  __syncwarp();
+  cp_async_wait<0>();
+  __syncthreads();  // all tokens consumed: the staging ring becomes the merge buffer
+  // merge buffer [4 warps][8 heads][D + D/8]: element (h, j) of a warp at
+  // h (D + D/8) + j + 4 (j / 32) + h / 2, so that a warp's 32 fragment stores
+  // (j = (d/8) g + const, h = 2t + const) hit 32 different banks
+  float* red = reinterpret_cast<float*>(mainb);
+  constexpr int RS = D + D / 8;
+  auto red_at = [&](int w, int h, int j) { return w * 8 * RS + h * RS + j + 4 * (j >> 5) + (h >> 1); };
+#pragma unroll
+  for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = VR * g + 2 * mc + (e >> 1), h = 2 * t + (e & 1);
+      red[red_at(warp, h, j)] = acc[mc][e] * un;
+    }
+  if (g == 0) {
+    wml[(warp * 2) * 8 + 2 * t] = m0;
+    wml[(warp * 2) * 8 + 2 * t + 1] = m1;
+    wml[(warp * 2 + 1) * 8 + 2 * t] = l0;
+    wml[(warp * 2 + 1) * 8 + 2 * t + 1] = l1;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < GT * D; idx += kThreads) {
+    const int h = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 2) * 8 + h]);
+    float v = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw = wml[(w * 2) * 8 + h];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      v = fmaf(f, red[red_at(w, h, j)], v);
+      L = fmaf(f, wml[(w * 2 + 1) * 8 + h], L);
+    }
+    p.ws_acc[((qh0 + h) * p.S + split) * D + j] = v;
+    if (j == 0) {
+      float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+      ml[0] = M;
+      ml[1] = L;
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) -> three bf16 pairs whose sum is x to 24 significant bits.
+__device__ __forceinline__ void split3_bf16x2(float x0, float x1, uint32_t (&w)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    const float2 hf = __bfloat1622float2(h);
+    x0 -= hf.x;
+    x1 -= hf.y;
+  }
+}
+
+// Dense split (tail ring tokens or a bf16 layer) of the tensor-core kernel:
+// the bf16 keys and values are exact MMA operands, and so is q (not rotated
+// here), so a score is one bf16 MMA per k-step; the probabilities are split
+// into three bf16 parts for the value MMAs.  Same fragment coordinate
+// permutations as the compressed path; a warp takes 16-token tiles.
+template <int D>
+__device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char* mainb, float* wml, int l, int b,
+                                             int kvh, int GT, int h0, int64_t qh0, int lb, int split) {
+  constexpr int KS = D / 16, KR = D / 4, VR = D / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  const int len = min(p.tail_len ? p.tail_len[lb] : 0, p.tail_cap);
+  const int t_begin = (split - p.Sc) * p.tps;
+  const int t_end = min(t_begin + p.tps, len);
+  if (t_begin >= t_end) {
+    if (threadIdx.x < GT) {
+      float* ml = p.ws_ml + ((qh0 + threadIdx.x) * p.S + split) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+    }
+    return;
+  }
+  const int n = t_end - t_begin;
+  const int cap = p.tail_cap;
+  const int tstart = p.tail_start ? ((p.tail_start[lb] % cap) + cap) % cap : 0;
+  const int first = (tstart + t_begin) % cap;
+  const uint16_t* kt0 = p.ktail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * cap * D;
+  const uint16_t* vt0 = p.vtail + l * p.tail_ls + (int64_t)(b * p.Hkv + kvh) * cap * D;
+  auto slot = [&](int i) { int s = first + i; return s >= cap ? s - cap : s; };  // i < n <= cap
+
+  // query fragments: head g (zero beyond GT), coordinates (d/4) t + 4 kk + {0,1} / {2,3}
+  uint32_t bq[KS][2];
+  {
+    const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + min(g, GT - 1)) * D + KR * t;
+#pragma unroll
+    for (int kk = 0; kk < KS; kk += 2) {
+      const uint4 w = *reinterpret_cast<const uint4*>(qp + 4 * kk);
+      bq[kk][0] = g < GT ? w.x : 0u;
+      bq[kk][1] = g < GT ? w.y : 0u;
+      bq[kk + 1][0] = g < GT ? w.z : 0u;
+      bq[kk + 1][1] = g < GT ? w.w : 0u;
+    }
+  }
+  const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float acc[KS][4];
+#pragma unroll
+  for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mc][e] = 0.f;
+
+  const int ntile = (n + 15) / 16;
+  for (int tile = warp; tile < ntile; tile += 4) {
+    const int tb = tile * 16;
+    // keys of tokens g, g + 8 (lane t's 32 coordinates), values of tokens
+    // 2t, 2t+1, 2t+8, 2t+9 (lane group g's 16 coordinates); zero past the end
+    uint32_t kw[2][KR / 2];
+    uint32_t vw[4][VR / 2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = tb + g + 8 * r;
+      const uint4* src = reinterpret_cast<const uint4*>(kt0 + (int64_t)slot(min(i, n - 1)) * D + KR * t);
+#pragma unroll
+      for (int k = 0; k < KR / 8; ++k) {
+        const uint4 v = i < n ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+        kw[r][4 * k] = v.x; kw[r][4 * k + 1] = v.y; kw[r][4 * k + 2] = v.z; kw[r][4 * k + 3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tb + 2 * t + (r & 1) + 8 * (r >> 1);
+      const uint4* src = reinterpret_cast<const uint4*>(vt0 + (int64_t)slot(min(i, n - 1)) * D + VR * g);
+#pragma unroll
+      for (int k = 0; k < VR / 8; ++k) {
+        const uint4 v = i < n ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+        vw[r][4 * k] = v.x; vw[r][4 * k + 1] = v.y; vw[r][4 * k + 2] = v.z; vw[r][4 * k + 3] = v.w;
+      }
+    }
+    // scores
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const uint32_t a[4] = {kw[0][2 * kk], kw[1][2 * kk], kw[0][2 * kk + 1], kw[1][2 * kk + 1]};
+      mma_bf16(sc, a, bq[kk][0], bq[kk][1]);
+    }
+    const bool va = tb + g < n, vb = tb + g + 8 < n;
+    sc[0] = (hv0 && va) ? sc[0] * p.sscale : -INFINITY;
+    sc[1] = (hv1 && va) ? sc[1] * p.sscale : -INFINITY;
+    sc[2] = (hv0 && vb) ? sc[2] * p.sscale : -INFINITY;
+    sc[3] = (hv1 && vb) ? sc[3] * p.sscale : -INFINITY;
+    // online softmax (lazy rescale)
+    const bool need = (sc[0] > m0 + 8.f) | (sc[2] > m0 + 8.f) | (sc[1] > m1 + 8.f) | (sc[3] > m1 + 8.f);
+    if (__any_sync(0xffffffffu, need)) {
+      float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, m));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, m));
+      }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+      const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int mc = 0; mc < KS; ++mc) {
+        acc[mc][0] *= a0;
+        acc[mc][1] *= a1;
+        acc[mc][2] *= a0;
+        acc[mc][3] *= a1;
+      }
+    }
+    const float p0 = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - m0);
+    const float p1 = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - m1);
+    const float p2 = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - m0);
+    const float p3 = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    // P^T fragments (three bf16 parts): tokens 2t, 2t+1 / 2t+8, 2t+9 of head g
+    uint32_t tw[3], bw[3];
+    split3_bf16x2(p0, p1, tw);
+    split3_bf16x2(p2, p3, bw);
+    const int sa = 4 * (2 * t) + (g >> 1), sb = sa + 4;
+    const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+    uint32_t pb0[3], pb1[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      pb0[k] = __byte_perm(__shfl_sync(0xffffffffu, tw[k], sa), __shfl_sync(0xffffffffu, tw[k], sb), sel);
+      pb1[k] = __byte_perm(__shfl_sync(0xffffffffu, bw[k], sa), __shfl_sync(0xffffffffu, bw[k], sb), sel);
+    }
+    // values: rows g / g + 8 <-> coordinates (d/8) g + 2 mc / + 1
+#pragma unroll
+    for (int mc = 0; mc < KS; ++mc) {
+      const uint32_t a[4] = {__byte_perm(vw[0][mc], vw[1][mc], 0x5410), __byte_perm(vw[0][mc], vw[1][mc], 0x7632),
+                             __byte_perm(vw[2][mc], vw[3][mc], 0x5410), __byte_perm(vw[2][mc], vw[3][mc], 0x7632)};
+#pragma unroll
+      for (int k = 0; k < 3; ++k) mma_bf16(acc[mc], a, pb0[k], pb1[k]);
+    }
+  }
+  mma_split_merge<D>(p, mainb, wml, acc, 1.f, m0, m1, l0, l1, GT, qh0, split);
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = MCfg<D>;
@@ -199,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
+  if (split >= p.Sc) {  // dense tokens (tail ring or bf16 layer)
+    mma_dense_split<D>(p, sm + p.sm_main, reinterpret_cast<float*>(sm + p.sm_red), l, b, kvh, GT, h0, qh0, lb,
+                       split);
+    return;
+  }
   const int nch = min(p.n_chunks[lb], p.rec_cap);
   const int c_begin = split * p.cps;
   const int c_end = min(c_begin + p.cps, nch);
@@ -472,58 +700,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
     }
   }
 
-  // ---- merge the warps' (m, l, acc) into the split's partial
-#pragma unroll
-  for (int m = 4; m < 32; m <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, m);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, m);
-  }
-  __syncwarp();
-  cp_async_wait<0>();
-  __syncthreads();  // all records consumed: the staging ring becomes the merge buffer
-  // merge buffer [4 warps][8 heads][D + D/8]: element (h, j) of a warp at
-  // h (D + D/8) + j + 4 (j / 32) + h / 2, so that a warp's 32 fragment stores
-  // (j = (d/8) g + const, h = 2t + const) hit 32 different banks
-  float* red = reinterpret_cast<float*>(mainb);
-  constexpr int RS = D + D / 8;
-  auto red_at = [&](int w, int h, int j) { return w * 8 * RS + h * RS + j + 4 * (j >> 5) + (h >> 1); };
-  {
-    const float un = pow2i(-16 - kx);
-#pragma unroll
-    for (int mc = 0; mc < KS; ++mc)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = VR * g + 2 * mc + (e >> 1), h = 2 * t + (e & 1);
-        red[red_at(warp, h, j)] = acc[mc][e] * un;
-      }
-  }
-  if (g == 0) {
-    wml[(warp * 2) * 8 + 2 * t] = m0;
-    wml[(warp * 2) * 8 + 2 * t + 1] = m1;
-    wml[(warp * 2 + 1) * 8 + 2 * t] = l0;
-    wml[(warp * 2 + 1) * 8 + 2 * t + 1] = l1;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < GT * D; idx += kThreads) {
-    const int h = idx / D, j = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 2) * 8 + h]);
-    float v = 0.f, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float mw = wml[(w * 2) * 8 + h];
-      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      v = fmaf(f, red[red_at(w, h, j)], v);
-      L = fmaf(f, wml[(w * 2 + 1) * 8 + h], L);
-    }
-    p.ws_acc[((qh0 + h) * p.S + split) * D + j] = v;
-    if (j == 0) {
-      float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
-      ml[0] = M;
-      ml[1] = L;
-    }
-  }
+  mma_split_merge<D>(p, mainb, wml, acc, pow2i(-16 - kx), m0, m1, l0, l1, GT, qh0, split);
 }
 
 template <int D, int KB, int VB>
