@@ -218,12 +218,7 @@ size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k
 
 /* workspace: device, 256-byte aligned, >= tq_decode_attn_workspace_size bytes.
  * Its contents need no initialisation and are garbage afterwards.  An empty
- * context (no compressed and no dense token) yields a zero output row.
- * When a call has both compressed tokens on the tensor-core kernel and dense
- * tokens, the dense kernel runs on a library-owned stream of the current
- * device (created, with two events, by the first such call), forked from and
- * joined back to `stream` with events: the call's work stays ordered on
- * `stream` like any other. */
+ * context (no compressed and no dense token) yields a zero output row. */
 tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
                          const tq_codec* v_codec, void* workspace, size_t workspace_bytes,
                          void* stream);
