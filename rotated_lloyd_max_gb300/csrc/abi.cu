@@ -151,9 +151,14 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   // lists (their corrections are latency-bound scatter work, better
   // overlapped by the CUDA-core kernel's FMA work) or the caller asks for the
   // CUDA-core kernel.  Its CTAs take at least two records each, which
-  // amortises their per-CTA set-up (pair tables, query fragments).
+  // amortises their per-CTA set-up (pair tables, query fragments)
   pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
-  if (pl->mma && a->splits <= 0 && comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
+  // (and dense CTAs at least 128 tokens: two 16-token tiles per warp), which
+  // also keeps the merge's split count down.
+  if (pl->mma && a->splits <= 0) {
+    if (comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
+    if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
+  }
   int64_t cps = 1, tps = TT;
   if (Sc > 0) {
     cps = cdiv(comp_tiles, Sc);

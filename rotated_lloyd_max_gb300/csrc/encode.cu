@@ -58,18 +58,6 @@ struct EncLane {
   }
 };
 
-// 0xFFFFFFFF if a > b, else 0 (an f32 compare that yields an integer mask).
-__device__ __forceinline__ uint32_t mask_gt(float a, float b) {
-  uint32_t r;
-  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t mask_le(float a, float b) {
-  uint32_t r;
-  asm("set.le.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
-  return r;
-}
-
 // The lane's 32 bf16 coordinates of a vector (zeros for an invalid slot).
 __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4 (&w)[4]) {
 #pragma unroll
@@ -396,6 +384,7 @@ static cudaError_t ev_launch(const EvictParams& p, cudaStream_t s) {
   } while (0)
 
 cudaError_t launch_encode(const EncodeParams& p, int grid, cudaStream_t s) {
+  if (p.c.d == 128) return launch_encode_mma(p, grid, s);  // Hadamard stage on the tensor cores
   TQ_DISPATCH_DBO(enc_launch, p.c.d, p.c.bits, p.c.has_outl, p, grid, s);
 }
 

@@ -1,0 +1,498 @@
+// a3 at head dim 128 with the Hadamard transform on the tensor cores.
+//
+// Same codes as the CUDA-core encoder (n = ||x||; w = H(s . x), the
+// unnormalised Sylvester transform; y = w / (n sqrt(d)); code_j = #{k : y_j > t_k},
+// taken from a table of decision cells; outliers |y_j| > T / sqrt(d), value
+// bf16(y_j)), computed as
+// H128 = H8 (x) H16 over a split of the 7 index bits: a coordinate is
+//   c = 32 t + 4 kb + 2 h + e      (t, kb, h, e: 2, 3, 1, 1 bits).
+// Stage 1 applies the 16-point transform over the bits (e, h, t) of every
+// block kb as one bf16 mma.sync (16 vectors x 16 coordinates x 16 outputs;
+// bf16 inputs and +-1 entries are exact, products are exact, sums are f32);
+// stage 2 applies the 8-point transform over kb in registers.  With
+//   fragment column 2t'+e+8h  <->  input coordinate 32 t' + 4 kb + 2 h + e,
+//   output column 2t''+e' of n-tile nt <-> output coordinate 32 t'' + 4 J + 2 nt + e',
+// lane (g, t) loads its vectors' coordinates 32 t .. 32 t + 31 with four
+// 16-byte loads straight into the A fragments, and after stage 2 holds the
+// same 32 coordinates of the output: its 32 codes are b words of the packed
+// row, as in the CUDA-core encoder.  A warp encodes 16 vectors at a time
+// (rows g and g + 8 of the MMA tile).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "tq_common.cuh"
+#include "tq_params.h"
+
+namespace tq {
+
+__device__ __forceinline__ void mma_bf16_e(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 +-1 pair of the permuted H16: entry (input in4, output out4) is
+// (-1)^popcount(in4 & out4), in4 = e | h<<1 | t'<<2, out4 = e' | nt<<1 | t''<<2.
+__device__ __forceinline__ uint32_t h16_pair(int in4a, int in4b, int out4) {
+  const uint32_t lo = (__popc(in4a & out4) & 1) ? 0xBF80u : 0x3F80u;
+  const uint32_t hi = (__popc(in4b & out4) & 1) ? 0xBF80u : 0x3F80u;
+  return lo | (hi << 16);
+}
+
+template <int B>
+struct EncM {
+  static constexpr int HALF = 1 << (B - 1);
+  static constexpr int NPOS = HALF - 1;
+  static constexpr int RB = 128 * B / 8;
+};
+
+// Lane state shared by the kernels: sign masks of the lane's 32 coordinates
+// (XOR on packed bf16 pairs) and the H16 fragments.
+template <int B>
+struct EncMLane {
+  int lane, warp, g, t;
+  uint32_t smask[16];
+  uint32_t hb[2][2];  // [n-tile][b0, b1]
+  __device__ __forceinline__ explicit EncMLane(const CodecDev& c) {
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    g = lane >> 2;
+    t = lane & 3;
+    const uint32_t sb = c.signs[t];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) smask[k] = (((sb >> (2 * k)) & 1u) << 15) | (((sb >> (2 * k + 1)) & 1u) << 31);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int out4 = (g & 1) | (nt << 1) | ((g >> 1) << 2);
+      hb[nt][0] = h16_pair(0 | (t << 2), 1 | (t << 2), out4);
+      hb[nt][1] = h16_pair(2 | (t << 2), 3 | (t << 2), out4);
+    }
+  }
+};
+
+// The lane's 32 bf16 coordinates (32 t .. 32 t + 31) of a vector, sign-flipped.
+__device__ __forceinline__ void encm_load(const uint16_t* row, bool valid, const uint32_t (&smask)[16],
+                                          uint32_t (&w)[16]) {
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldg(src + k);
+      w[4 * k] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = 0u;
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] ^= smask[k];
+}
+
+// cp.async staging of 16-vector tiles: a lane copies its own 64 bytes of
+// rows g and g + 8 and later reads back exactly those, so no other lane is
+// involved; its 4 chunks sit at swizzled positions so that the 16-byte reads
+// of a quarter-warp (g in {2q, 2q+1}, t in 0..3) hit 8 different bank groups.
+struct EncTile {
+  uint4 row[16][16];  // [tile row][16-byte chunk]
+};
+__device__ __forceinline__ int encm_chunk(int g, int t, int k) { return 4 * t + (k ^ (t >> 1) ^ ((g & 1) << 1)); }
+
+__device__ __forceinline__ void encm_issue(EncTile& tile, int g, int t, const uint16_t* ra, bool va,
+                                           const uint16_t* rb, bool vb) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (va) cp_async16(&tile.row[g][encm_chunk(g, t, k)], ra + 8 * k);
+    if (vb) cp_async16(&tile.row[g + 8][encm_chunk(g, t, k)], rb + 8 * k);
+  }
+}
+
+__device__ __forceinline__ void encm_read(const EncTile& tile, int r, int g, int t, bool valid,
+                                          const uint32_t (&smask)[16], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 v = valid ? tile.row[r][encm_chunk(g, t, k)] : make_uint4(0u, 0u, 0u, 0u);
+    w[4 * k] = v.x ^ smask[4 * k];
+    w[4 * k + 1] = v.y ^ smask[4 * k + 1];
+    w[4 * k + 2] = v.z ^ smask[4 * k + 2];
+    w[4 * k + 3] = v.w ^ smask[4 * k + 3];
+  }
+}
+
+// Sum of squares of 32 bf16 coordinates (exact squares, pairwise f32 tree).
+__device__ __forceinline__ float encm_sq(const uint32_t (&w)[16]) {
+  float2 sq[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 a = f2(__uint_as_float(w[2 * k] << 16), __uint_as_float(w[2 * k] & 0xFFFF0000u));
+    const float2 b = f2(__uint_as_float(w[2 * k + 1] << 16), __uint_as_float(w[2 * k + 1] & 0xFFFF0000u));
+    sq[k] = fma2(a, a, mul2(b, b));
+  }
+#pragma unroll
+  for (int h = 4; h; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) sq[k] = add2(sq[k], sq[k + h]);
+  return sq[0].x + sq[0].y;
+}
+
+// The full transform of two vectors (rows g, g + 8): wa, wb hold the lane's
+// loaded words; on return xa, xb hold the lane's 32 output coordinates.
+template <int B>
+__device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint32_t (&wa)[16],
+                                               const uint32_t (&wb)[16], float (&xa)[32], float (&xb)[32]) {
+  float cc[8][2][4];
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cc[kb][nt][e] = 0.f;
+      mma_bf16_e(cc[kb][nt], wa[2 * kb], wb[2 * kb], wa[2 * kb + 1], wb[2 * kb + 1], ln.hb[nt][0], ln.hb[nt][1]);
+    }
+  // 8-point transform over kb, on (element 0, 1) and (2, 3) pairs
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb)
+      if (!(kb & m))
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const float2 a = f2(cc[kb][nt][e], cc[kb][nt][e + 1]);
+            const float2 b = f2(cc[kb | m][nt][e], cc[kb | m][nt][e + 1]);
+            const float2 s = add2(a, b);
+            const float2 d = fma2(b, f2(-1.f, -1.f), a);
+            cc[kb][nt][e] = s.x;
+            cc[kb][nt][e + 1] = s.y;
+            cc[kb | m][nt][e] = d.x;
+            cc[kb | m][nt][e + 1] = d.y;
+          }
+#pragma unroll
+  for (int J = 0; J < 8; ++J)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        xa[4 * J + 2 * nt + e] = cc[J][nt][e];
+        xb[4 * J + 2 * nt + e] = cc[J][nt][2 + e];
+      }
+}
+
+// Decision cells: with z = y * 128 (y the normalised rotated value, |y| <= 1)
+// and i = round(z) + 128, cell i covers z in [i - 128.5, i - 127.5) and
+// holds (count of boundaries below the cell, the boundary inside it x 128 or
+// +huge); boundaries are >= 2/128 apart at d = 128 for b <= 4, so a cell holds
+// at most one.  |y| <= 1 keeps i in 0..256.  code = count + (z > boundary): the same code as
+// #{k : y > t_k} except within a couple of f32 ulp of a boundary.
+constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell (257.. = top cell's law)
+constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
+constexpr float kCellScale = 128.f;
+
+__device__ __forceinline__ void encm_build_cells(const CodecDev& c, float2* cells) {
+  const int nb = (1 << c.bits) - 1;
+  for (int i = threadIdx.x; i < kCells; i += kThreads) {
+    const float lo = ((float)(i - 128) - 0.5f) / kCellScale, hi = ((float)(i - 128) + 0.5f) / kCellScale;
+    int below = 0;
+    float inside = 3.0e38f;
+    for (int k = 0; k < nb; ++k) {
+      const float t = c.boundaries[k];
+      if (t < lo) ++below;
+      else if (t < hi) inside = t * kCellScale;
+    }
+    cells[i] = make_float2(inside, __int_as_float(below));
+    if (i == kPosCell && c.bits == 2) cells[i].x = c.boundaries[2] * kCellScale;
+  }
+}
+
+// Codes of the lane's 32 coordinates of one vector (x: unnormalised
+// transform, scale = 128 / (n sqrt(d)) or 0 for a zero vector), packed
+// LSB-first into B words; (OUTL) the outlier mask |y| > T / sqrt(d).
+template <int B, bool OUTL>
+__device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2* cells, float scale,
+                                              float thr_out, uint32_t (&wd)[B], uint32_t& omask) {
+  const float Tz = OUTL ? thr_out * kCellScale : 0.f;
+#pragma unroll
+  for (int q = 0; q < B; ++q) wd[q] = 0u;
+  omask = 0u;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const float z = x[r] * scale;
+    uint32_t code;
+    if constexpr (B <= 2) {
+      // at most one positive boundary: compare directly (the mirror of the
+      // positive side, HALF - 1 for z <= 0)
+      const uint32_t m = B == 2 ? mask_gt(fabsf(z), cells[kPosCell].x) : 0u;
+      code = ((uint32_t)(1 << (B - 1)) - m) ^ (mask_le(z, 0.f) & ((1u << B) - 1u));
+    } else {
+      const uint32_t ci = __float_as_uint(z + 8388736.0f) & 0x1FFu;  // round(z) + 128 (2^23 + 128 magic)
+      const float2 e = cells[ci];
+      code = (uint32_t)__float_as_int(e.y) - mask_gt(z, e.x);
+    }
+    const int bit = r * B;
+    wd[bit >> 5] += code << (bit & 31);
+    if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code >> (32 - (bit & 31));
+    if (OUTL) omask |= mask_gt(fabsf(z), Tz) & (1u << r);
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void encm_store_row(uint8_t* row, const uint32_t (&wd)[B]) {
+  if constexpr (B == 4) {
+    *reinterpret_cast<uint4*>(row) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  } else if constexpr (B == 2) {
+    *reinterpret_cast<uint2*>(row) = make_uint2(wd[0], wd[1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < B; ++q) reinterpret_cast<uint32_t*>(row)[q] = wd[q];
+  }
+}
+
+// Encode without outliers: every (group, record, 16-vector tile) is a task of
+// one warp; warps stride over the tasks with the next task's rows in flight
+// (cp.async, two buffers per warp).
+template <int B>
+__global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_constant__ EncodeParams p) {
+  using E = EncM<B>;
+  __shared__ float2 cells[kCells];
+  __shared__ EncTile tiles[4][2];
+  encm_build_cells(p.c, cells);
+  __syncthreads();
+  const EncMLane<B> ln(p.c);
+  const int64_t per_group = p.chunks_per_group * 8;
+  const int64_t n_tasks = p.n_groups * per_group;
+  const int64_t v_end = p.first_vec + p.n_vec;
+  struct Task {
+    int64_t grp, chunk, ta, tb;
+    int slot_a, slot_b;
+    bool va, vb;
+  };
+  auto locate = [&](int64_t task) {
+    Task k;
+    k.grp = task / per_group;
+    const int64_t r = task % per_group;
+    k.chunk = p.first_chunk + r / 8;
+    k.slot_a = (int)(r % 8) * 16 + ln.g;
+    k.slot_b = k.slot_a + 8;
+    k.ta = k.chunk * kChunk + k.slot_a;
+    k.tb = k.chunk * kChunk + k.slot_b;
+    k.va = task < n_tasks && k.ta >= p.first_vec && k.ta < v_end;
+    k.vb = task < n_tasks && k.tb >= p.first_vec && k.tb < v_end;
+    return k;
+  };
+  auto issue = [&](const Task& k, int buf) {
+    const uint16_t* src = p.src + k.grp * p.src_gs + ln.t * 32;
+    encm_issue(tiles[ln.warp][buf], ln.g, ln.t, src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs, k.va,
+               src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs, k.vb);
+    cp_async_commit();
+  };
+  const int64_t stride = (int64_t)gridDim.x * 4;
+  int64_t task = (int64_t)blockIdx.x * 4 + ln.warp;
+  Task cur = locate(task);
+  issue(cur, 0);
+  for (int it = 0; task < n_tasks; task += stride, ++it) {
+    const Task nxt = locate(task + stride);
+    issue(nxt, (it + 1) & 1);
+    cp_async_wait<1>();  // this lane's copies of the current tile are in
+    uint32_t wa[16], wb[16];
+    encm_read(tiles[ln.warp][it & 1], ln.g, ln.g, ln.t, cur.va, ln.smask, wa);
+    encm_read(tiles[ln.warp][it & 1], ln.g + 8, ln.g, ln.t, cur.vb, ln.smask, wb);
+    float sa = encm_sq(wa), sb = encm_sq(wb);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+    sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+    sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+    const float na = sqrtf(sa), nb = sqrtf(sb);
+    float xa[32], xb[32];
+    encm_transform<B>(ln, wa, wb, xa, xb);
+    uint8_t* rec = p.dst + cur.grp * p.dst_gs + cur.chunk * (int64_t)p.c.rec_bytes;
+    uint32_t wd[B], om;
+    encm_quantize<B, false>(xa, cells, na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f, 0.f, wd, om);
+    if (cur.va) encm_store_row<B>(rec + (size_t)cur.slot_a * E::RB + ln.t * 4 * B, wd);
+    encm_quantize<B, false>(xb, cells, nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f, 0.f, wd, om);
+    if (cur.vb) encm_store_row<B>(rec + (size_t)cur.slot_b * E::RB + ln.t * 4 * B, wd);
+    if (ln.t == 0) {
+      float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
+      if (cur.va) nrm[cur.slot_a] = na;
+      if (cur.vb) nrm[cur.slot_b] = nb;
+    }
+    cur = nxt;
+  }
+  cp_async_wait<0>();
+}
+
+// Encode with outliers: one CTA per record (grid-stride), two passes of 64
+// slots (warp w: tile w of the pass); entries land in (slot, index) order via
+// a quad prefix (a vector's lanes) and a CTA prefix over the pass's slots.
+template <int B>
+__global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __grid_constant__ EncodeParams p) {
+  using E = EncM<B>;
+  __shared__ int cnt_s[64];
+  __shared__ int off_s[64];
+  __shared__ int run_s;
+  __shared__ float2 cells[kCells];
+  __shared__ EncTile tiles[4][2];
+  encm_build_cells(p.c, cells);
+  const EncMLane<B> ln(p.c);
+  const int64_t n_tasks = p.n_groups * p.chunks_per_group;
+  const int64_t v_end = p.first_vec + p.n_vec;
+  // units u = (record task, pass): task blockIdx.x + (u / 2) gridDim.x, pass u % 2;
+  // warp w encodes slots 64 pass + 16 w + g (+ 8) of the record
+  struct Unit {
+    int64_t task, grp, chunk, ta, tb;
+    int pass, slot_a, slot_b;
+    bool va, vb;
+  };
+  auto locate = [&](int u) {
+    Unit k;
+    k.task = blockIdx.x + (int64_t)(u >> 1) * gridDim.x;
+    k.pass = u & 1;
+    k.grp = k.task / p.chunks_per_group;
+    k.chunk = p.first_chunk + k.task % p.chunks_per_group;
+    k.slot_a = 64 * k.pass + 16 * ln.warp + ln.g;
+    k.slot_b = k.slot_a + 8;
+    k.ta = k.chunk * kChunk + k.slot_a;
+    k.tb = k.chunk * kChunk + k.slot_b;
+    k.va = k.task < n_tasks && k.ta >= p.first_vec && k.ta < v_end;
+    k.vb = k.task < n_tasks && k.tb >= p.first_vec && k.tb < v_end;
+    return k;
+  };
+  auto issue = [&](const Unit& k, int buf) {
+    const uint16_t* src = p.src + k.grp * p.src_gs + ln.t * 32;
+    encm_issue(tiles[ln.warp][buf], ln.g, ln.t, src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs, k.va,
+               src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs, k.vb);
+    cp_async_commit();
+  };
+  Unit cur = locate(0);
+  issue(cur, 0);
+  for (int u = 0; cur.task < n_tasks; ++u) {
+    const Unit nxt = locate(u + 1);
+    issue(nxt, (u + 1) & 1);
+    if (cur.pass == 0 && threadIdx.x == 0) run_s = 0;
+    cp_async_wait<1>();
+    __syncthreads();  // run_s reset visible; the previous unit's off_s reads are done
+    uint8_t* rec = p.dst + cur.grp * p.dst_gs + cur.chunk * (int64_t)p.c.rec_bytes;
+    {
+      const int pa = 16 * ln.warp + ln.g, pb = pa + 8;  // slots within the pass
+      const int slot_a = cur.slot_a, slot_b = cur.slot_b;
+      const bool va = cur.va, vb = cur.vb;
+      uint32_t wa[16], wb[16];
+      encm_read(tiles[ln.warp][u & 1], ln.g, ln.g, ln.t, va, ln.smask, wa);
+      encm_read(tiles[ln.warp][u & 1], ln.g + 8, ln.g, ln.t, vb, ln.smask, wb);
+      float sa = encm_sq(wa), sb = encm_sq(wb);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+      const float na = sqrtf(sa), nb = sqrtf(sb);
+      float xa[32], xb[32];
+      encm_transform<B>(ln, wa, wb, xa, xb);
+      uint32_t wd[B], oma, omb;
+      encm_quantize<B, true>(xa, cells, na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f, p.c.thr_out, wd, oma);
+      if (va) encm_store_row<B>(rec + (size_t)slot_a * E::RB + ln.t * 4 * B, wd);
+      encm_quantize<B, true>(xb, cells, nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f, p.c.thr_out, wd, omb);
+      if (vb) encm_store_row<B>(rec + (size_t)slot_b * E::RB + ln.t * 4 * B, wd);
+      if (!va) oma = 0u;
+      if (!vb) omb = 0u;
+      if (ln.t == 0) {
+        float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
+        if (va) nrm[slot_a] = na;
+        if (vb) nrm[slot_b] = nb;
+      }
+      // entries before this lane within its vector (quad prefix over t)
+      const int ca = __popc(oma), cb = __popc(omb);
+      int ia = ca, ib = cb;
+#pragma unroll
+      for (int m = 1; m < 4; m <<= 1) {
+        const int oa = __shfl_up_sync(0xffffffffu, ia, m, 4);
+        const int ob = __shfl_up_sync(0xffffffffu, ib, m, 4);
+        if (ln.t >= m) {
+          ia += oa;
+          ib += ob;
+        }
+      }
+      const int tota = __shfl_sync(0xffffffffu, ia, 3, 4), totb = __shfl_sync(0xffffffffu, ib, 3, 4);
+      const int nsa = min(tota, 255), nsb = min(totb, 255);
+      if (ln.t == 0) {
+        cnt_s[pa] = va ? nsa : 0;
+        cnt_s[pb] = vb ? nsb : 0;
+      }
+      __syncthreads();
+      if (ln.warp == 0) {
+        const int run = run_s;
+        int v0 = cnt_s[ln.lane], v1 = cnt_s[32 + ln.lane];
+        int i0 = v0, i1 = v1;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+          const int o0 = __shfl_up_sync(0xffffffffu, i0, m), o1 = __shfl_up_sync(0xffffffffu, i1, m);
+          if (ln.lane >= m) {
+            i0 += o0;
+            i1 += o1;
+          }
+        }
+        const int half = __shfl_sync(0xffffffffu, i0, 31);
+        const int tot1 = __shfl_sync(0xffffffffu, i1, 31);  // all lanes: a full-mask shuffle
+        off_s[ln.lane] = run + i0 - v0;
+        off_s[32 + ln.lane] = run + half + i1 - v1;
+        __syncwarp();
+        if (ln.lane == 0) run_s = run + half + tot1;
+      }
+      __syncthreads();
+      uint32_t* ent = reinterpret_cast<uint32_t*>(rec + p.c.off_entries);
+      const float inva = na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f;
+      const float invb = nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f;
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const bool valid = v ? vb : va;
+        if (!valid) continue;
+        const int off = off_s[v ? pb : pa];
+        const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));
+        const uint32_t om = v ? omb : oma;
+        const float inv = v ? invb : inva;
+        int k = (v ? ib - cb : ia - ca);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          if ((om >> r) & 1u) {
+            if (k < stored) {
+              const float y = (v ? xb[r] : xa[r]) * inv;
+              ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)f32_to_bf16_rne(y) << 16);
+            }
+            ++k;
+          }
+        }
+        if (ln.t == 0) rec[p.c.off_count + (v ? slot_b : slot_a)] = (uint8_t)stored;
+      }
+    }
+    cur = nxt;
+  }
+  cp_async_wait<0>();
+}
+
+template <int B>
+static cudaError_t encm_launch(const EncodeParams& p, int grid, cudaStream_t s) {
+  if (p.c.has_outl) {
+    const int64_t tasks = p.n_groups * p.chunks_per_group;
+    encode_mma_outl_kernel<B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+  } else {
+    const int64_t tasks = (p.n_groups * p.chunks_per_group * 8 + 3) / 4;
+    encode_mma_kernel<B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_mma(const EncodeParams& p, int grid, cudaStream_t s) {
+  switch (p.c.bits) {
+    case 1: return encm_launch<1>(p, grid, s);
+    case 2: return encm_launch<2>(p, grid, s);
+    case 3: return encm_launch<3>(p, grid, s);
+    case 4: return encm_launch<4>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tq

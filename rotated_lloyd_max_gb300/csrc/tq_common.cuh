@@ -88,6 +88,18 @@ __device__ __forceinline__ void fwht_lanes(float (&x)[R], int lane, int lanes_pe
   }
 }
 
+// 0xFFFFFFFF if a > b, else 0 (an f32 compare that yields an integer mask).
+__device__ __forceinline__ uint32_t mask_gt(float a, float b) {
+  uint32_t r;
+  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t mask_le(float a, float b) {
+  uint32_t r;
+  asm("set.le.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 // ------------------------------------------------------------- SplitMix64
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t k) {
   // output k (0-based) of SplitMix64 seeded with `seed`
