@@ -124,6 +124,25 @@ __device__ __forceinline__ void encm_read(const EncTile& tile, int r, int g, int
   }
 }
 
+// The lane's 32 values x * inv as bf16 (round to nearest even), into its own
+// chunks of tile row r (which it has read already); and one of them back.
+__device__ __forceinline__ void encm_stash(EncTile& tile, int r, int g, int t, const float (&x)[32], float inv) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[8 * k + 2 * j] * inv, x[8 * k + 2 * j + 1] * inv);
+      w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    tile.row[r][encm_chunk(g, t, k)] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+__device__ __forceinline__ uint16_t encm_stashed(const EncTile& tile, int r, int g, int t, int c) {
+  const uint16_t* ch = reinterpret_cast<const uint16_t*>(&tile.row[r][encm_chunk(g, t, c >> 3)]);
+  return ch[c & 7];
+}
+
 // Sum of squares of 32 bf16 coordinates (exact squares, pairwise f32 tree).
 __device__ __forceinline__ float encm_sq(const uint32_t (&w)[16]) {
   float2 sq[8];
@@ -399,6 +418,13 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
       if (vb) encm_store_row<B>(rec + (size_t)slot_b * E::RB + ln.t * 4 * B, wd);
       if (!va) oma = 0u;
       if (!vb) omb = 0u;
+      // the lane's y values as bf16 (the stored outlier value), kept in its own
+      // chunks of the tile buffer it has just read, for the entry writes below
+      const float inva = na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f;
+      const float invb = nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f;
+      EncTile& tl = tiles[ln.warp][u & 1];
+      if (oma) encm_stash(tl, ln.g, ln.g, ln.t, xa, inva);
+      if (omb) encm_stash(tl, ln.g + 8, ln.g, ln.t, xb, invb);
       if (ln.t == 0) {
         float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
         if (va) nrm[slot_a] = na;
@@ -444,26 +470,20 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
       }
       __syncthreads();
       uint32_t* ent = reinterpret_cast<uint32_t*>(rec + p.c.off_entries);
-      const float inva = na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f;
-      const float invb = nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f;
 #pragma unroll
       for (int v = 0; v < 2; ++v) {
         const bool valid = v ? vb : va;
         if (!valid) continue;
         const int off = off_s[v ? pb : pa];
         const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));
-        const uint32_t om = v ? omb : oma;
-        const float inv = v ? invb : inva;
+        uint32_t om = v ? omb : oma;
         int k = (v ? ib - cb : ia - ca);
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          if ((om >> r) & 1u) {
-            if (k < stored) {
-              const float y = (v ? xb[r] : xa[r]) * inv;
-              ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)f32_to_bf16_rne(y) << 16);
-            }
-            ++k;
-          }
+        const int row = v ? ln.g + 8 : ln.g;
+        while (om) {
+          const int r = __ffs(om) - 1;
+          om &= om - 1;
+          if (k < stored) ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)encm_stashed(tl, row, ln.g, ln.t, r) << 16);
+          ++k;
         }
         if (ln.t == 0) rec[p.c.off_count + (v ? slot_b : slot_a)] = (uint8_t)stored;
       }
