@@ -493,8 +493,11 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
   cp_async_wait<0>();
 }
 
+// `grid` is 8 CTAs per SM; these kernels run 4 per SM (registers), so one
+// wave (grid / 2) of persistent CTAs, whose warps then prefetch their next task.
 template <int B>
 static cudaError_t encm_launch(const EncodeParams& p, int grid, cudaStream_t s) {
+  grid = std::max(1, grid / 2);
   if (p.c.has_outl) {
     const int64_t tasks = p.n_groups * p.chunks_per_group;
     encode_mma_outl_kernel<B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
