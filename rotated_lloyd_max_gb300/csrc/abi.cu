@@ -267,6 +267,31 @@ void attn_mma_smem_layout(AttnParams& p, int D) {
   p.sm_total = off;
 }
 
+void attn_mma512_smem_layout(AttnParams& p) {
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  int off = 0;
+  p.sm_kpair = off;  // fixed offsets, as in the d 64/128 kernel
+  off += (1 << (2 * p.kb)) * 128;
+  p.sm_vpair = off;
+  off += (p.vb == 3 ? 120 : (1 << (2 * p.vb))) * 128;
+  p.sm_logit = off;  // query fragments [32 k-steps][32 lanes][16 B]
+  off += 32 * 32 * 16;
+  p.sm_slot = off;   // centroid halves
+  off += 32 * 8;
+  p.sm_red = off;    // logits [128][8]
+  off += 128 * 8 * 4;
+  p.sm_corr = off;   // softmax state
+  off = al(off + 32 * 4, 128);
+  p.sm_q = p.sm_lut = p.sm_pre = p.sm_ent = off;  // unused by this kernel
+  p.sm_ent_stage = 0;
+  int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
+  stage = std::max(stage, 8 * 512 * 4);                       // q~ is built in the second buffer
+  p.sm_stage = al(stage, 128);
+  p.sm_main = off;
+  off += 2 * p.sm_stage;
+  p.sm_total = off;
+}
+
 }  // namespace tq
 
 extern "C" {
@@ -517,6 +542,21 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
     if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+  } else if (pl.D == 512 && pl.Sc > 0 && !a->cuda_core_path && !pl.kc.has_outl && !pl.vc.has_outl) {
+    // compressed splits on the d-512 tensor-core kernel, dense splits (if any)
+    // on the general kernel in a second launch
+    AttnParams pm = p;
+    attn_mma512_smem_layout(pm);
+    if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+    if (launch_attn_mma512(pm, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (pl.S > pl.Sc) {
+      AttnParams pd = p;
+      pd.split_base = pl.Sc;
+      attn_smem_layout(pd, pl.D, pl.GT);
+      if (pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+      if (launch_attn(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), s) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    }
   } else if (rec_kernel) {
     // compressed splits on the warp-local path, dense splits on the general
     // dense path, one launch

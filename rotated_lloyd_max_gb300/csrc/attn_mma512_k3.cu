@@ -1,0 +1,14 @@
+// Tensor-core decode attention, head dim 512, 3-bit keys (values of 1-4 bits).
+#include "attn_mma512.cuh"
+
+namespace tq {
+cudaError_t launch_attn_mma512_k3(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  switch (p.vb) {
+    case 1: return attn_mma512_launch_t<3, 1>(p, grid, s);
+    case 2: return attn_mma512_launch_t<3, 2>(p, grid, s);
+    case 3: return attn_mma512_launch_t<3, 3>(p, grid, s);
+    case 4: return attn_mma512_launch_t<3, 4>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+}  // namespace tq

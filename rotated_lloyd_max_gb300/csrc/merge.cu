@@ -147,6 +147,21 @@ cudaError_t launch_attn_mma(const AttnParams& p, int D, dim3 grid, cudaStream_t 
   }
 }
 
+cudaError_t launch_attn_mma512_k1(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_mma512_k2(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_mma512_k3(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_mma512_k4(const AttnParams& p, dim3 grid, cudaStream_t s);
+
+cudaError_t launch_attn_mma512(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  switch (p.kb) {
+    case 1: return launch_attn_mma512_k1(p, grid, s);
+    case 2: return launch_attn_mma512_k2(p, grid, s);
+    case 3: return launch_attn_mma512_k3(p, grid, s);
+    case 4: return launch_attn_mma512_k4(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s) {
   switch (D) {
     case 64: return launch_attn_d64(p, GT, grid, s);

@@ -112,6 +112,8 @@ cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStrea
 cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
 // tensor-core kernel for the compressed splits (head dims 64 and 128)
 cudaError_t launch_attn_mma(const AttnParams& p, int D, dim3 grid, cudaStream_t s);
+// tensor-core kernel for the compressed splits at head dim 512 (256 threads)
+cudaError_t launch_attn_mma512(const AttnParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 
 // Dynamic shared memory of the attention kernel for head dim D and head group GT
@@ -119,6 +121,7 @@ cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 void attn_smem_layout(AttnParams& p, int D, int GT);
 void attn_rec_smem_layout(AttnParams& p, int D, int GT);
 void attn_mma_smem_layout(AttnParams& p, int D);
+void attn_mma512_smem_layout(AttnParams& p);
 
 // The codebook kernel writes this block into the caller's scratch.
 struct CodebookOut {

@@ -151,6 +151,15 @@ def test_tensor_core_bit_widths(tq, orc, d, kb, vb):
     _assert_close(got, want)
 
 
+@pytest.mark.parametrize("kb,vb,G,shared", [(4, 4, 64, True), (2, 3, 4, False), (3, 1, 8, False), (1, 2, 6, False)])
+def test_tensor_core_d512(tq, orc, kb, vb, G, shared):
+    """Head dim 512 on its tensor-core kernel (8 query heads per CTA), with a
+    dense tail on the general kernel."""
+    got, want, _ = run_case(tq, orc, d=512, G=G, Hkv=1, B=1, L=1, chunks=[3], tails=[40], kb=kb, vb=kb if shared else vb,
+                            shared=shared, end_to_end=False, seed=kb * 10 + vb + G)
+    _assert_close(got, want)
+
+
 def test_dense_boundary_layers(tq, orc):
     """bf16 layers: no records, the whole cache passed as the dense part."""
     got, want, _ = run_case(tq, orc, d=128, G=6, Hkv=2, B=1, L=2, chunks=[0], tails=[2048], kb=3, vb=2,
