@@ -249,8 +249,8 @@ void attn_mma_smem_layout(AttnParams& p, int D) {
   off += (1 << (2 * p.kb)) * 128;
   p.sm_vpair = off;
   off += (p.vb == 3 ? 120 : (1 << (2 * p.vb))) * 128;
-  p.sm_q = off;
-  off += 8 * D * 4;
+  p.sm_q = off;      // q~ [8 heads][4 lane runs padded], see the kernel
+  off += 8 * 4 * (std::max(D / 4, 32) + 1) * 4;
   p.sm_slot = off;   // centroid halves
   off += 32 * 8;
   p.sm_red = off;
@@ -285,7 +285,7 @@ void attn_mma512_smem_layout(AttnParams& p) {
   p.sm_q = p.sm_lut = p.sm_pre = p.sm_ent = off;  // unused by this kernel
   p.sm_ent_stage = 0;
   int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
-  stage = std::max(stage, 8 * 512 * 4);                       // q~ is built in the second buffer
+  stage = std::max(stage, 8 * 516 * 4);                       // q~ is built in the second buffer
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
   off += 2 * p.sm_stage;

@@ -404,7 +404,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   constexpr int EK = 1 << (2 * KB), EV = VIdx<VB>::ENTRIES;
   constexpr int KP_OFF = 0, VP_OFF = EK * 128;  // pair tables at fixed offsets (immediate addressing)
   extern __shared__ __align__(128) unsigned char sm[];
-  float* qf = reinterpret_cast<float*>(sm + p.sm_q);      // [8][D] q~ (f32)
+  // q~ (f32): coordinate c of head h at h*4*ST + (c / KR)*ST + c % KR with
+  // ST = max(KR, 32) + 1, so the 32 lanes' runs start in 32 different banks
+  float* qf = reinterpret_cast<float*>(sm + p.sm_q);
+  constexpr int QST = (MCfg<D>::KR > 32 ? MCfg<D>::KR : 32) + 1;
+  auto qidx = [](int h, int c) { return h * 4 * QST + (c / MCfg<D>::KR) * QST + (c % MCfg<D>::KR); };
   float* wml = reinterpret_cast<float*>(sm + p.sm_red);   // [4][2][8]
   uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);  // [KS][32 lanes] (hi b0, hi b1, lo b0, lo b1)
   uint2* cent = reinterpret_cast<uint2*>(sm + p.sm_slot); // [32] (hi|lo f16) of K then V centroids x 2^16
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
       for (int r = 0; r < R; ++r) x[r] = 0.f;
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) qf[hh * D + lane * R + r] = x[r];
+    for (int r = 0; r < R; ++r) qf[qidx(hh, lane * R + r)] = x[r];
   }
   // f16 halves of every centroid x 2^16: cent[i] = (hi, lo) of K centroid i,
   // cent[16 + i] of V centroid i
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   // stored per lane in shared memory (read once per k-step for both m-tiles)
   float fq0, fq1;  // 2^-(s_h + 16) for the lane's score heads 2t, 2t+1
   {
-    const float* qrow = qf + g * D + KR * t;
+    const float* qrow = qf + qidx(g, KR * t);
     float mx = 0.f;
 #pragma unroll
     for (int j = 0; j < KR; ++j) mx = fmaxf(mx, fabsf(qrow[j]));
@@ -564,7 +568,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
       uint32_t w[4][KNW];  // runs of tokens g, g + 8, 16 + g, 24 + g
 #pragma unroll
       for (int r = 0; r < 4; ++r) load_run<KNB, KAL>(kcodes + (8 * r + g) * rbk, KNB * t, w[r]);
+      // hi.hi, hi.lo and lo.hi in separate accumulators: independent MMA chains
       float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float cl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float ch[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const uint4 f = qfrag[kk * 32 + lane];
@@ -582,10 +589,14 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
             al[2 * hf + 1] = e1.y;
           }
           mma_f16(cc[mt], ah, f.x, f.y);
-          mma_f16(cc[mt], ah, f.z, f.w);
-          mma_f16(cc[mt], al, f.x, f.y);
+          mma_f16(cl[mt], ah, f.z, f.w);
+          mma_f16(ch[mt], al, f.x, f.y);
         }
       }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cc[mt][e] += cl[mt][e] + ch[mt][e];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         sc[mt][0] = cc[mt][0] * fq0;

@@ -88,7 +88,10 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
 
   // ---- q~ of the CTA's heads into the second staging buffer (free until
   // record 1 is issued), rows >= GT zero
-  float* qf = reinterpret_cast<float*>(stage(1));  // [8][512]
+  // [8 heads][4 lane runs of 128, padded to 129][+1]: coordinate c of head h at
+  // h*516 + (c/128)*129 + c%128, so the 32 lanes' runs start in 32 different banks
+  float* qf = reinterpret_cast<float*>(stage(1));
+  auto qidx = [](int h, int c) { return h * 516 + (c >> 7) * 129 + (c & 127); };
   {
     constexpr int R = D / 32;
     const int hh = warp;  // 8 warps, 8 head rows
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
       for (int r = 0; r < R; ++r) x[r] = 0.f;
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) qf[hh * D + lane * R + r] = x[r];
+    for (int r = 0; r < R; ++r) qf[qidx(hh, lane * R + r)] = x[r];
   }
   if (tid < 32) {
     const float v = (tid < 16 ? p.kc[tid] : p.vc[tid - 16]) * 65536.f;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
   // query fragments (head g, lane t's coordinates), scaled per head
   float fq0, fq1;
   {
-    const float* qrow = qf + g * D + KR * t;
+    const float* qrow = qf + qidx(g, KR * t);
     float mx = 0.f;
 #pragma unroll 8
     for (int j = 0; j < KR; ++j) mx = fmaxf(mx, fabsf(qrow[j]));
@@ -191,7 +194,8 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     {
       const unsigned char* r0 = st + (16 * warp + g) * rbk;
       const unsigned char* r1 = r0 + 8 * rbk;
-      float cc[4] = {0.f, 0.f, 0.f, 0.f};
+      // hi.hi, hi.lo and lo.hi in separate accumulators: three independent MMA chains
+      float cc[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f}, ch[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
       for (int q8 = 0; q8 < 4; ++q8) {  // 8 k-steps = 32 coordinates = 32 KB bits of the lane's run
         constexpr int PB = 32 * KB;      // bits per 8 k-steps
@@ -214,10 +218,12 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
             al[2 * hf + 1] = e1.y;
           }
           mma_f16(cc, ah, f.x, f.y);
-          mma_f16(cc, ah, f.z, f.w);
-          mma_f16(cc, al, f.x, f.y);
+          mma_f16(cl, ah, f.z, f.w);
+          mma_f16(ch, al, f.x, f.y);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cc[e] += cl[e] + ch[e];
       const int ta = 16 * warp + g, tb = ta + 8;
       const float fa = knorm[ta] * p.sscale, fb = knorm[tb] * p.sscale;
       lg_s[ta * 8 + 2 * t] = hv0 ? cc[0] * fq0 * fa : -INFINITY;
