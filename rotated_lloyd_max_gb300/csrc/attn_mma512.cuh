@@ -232,35 +232,35 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
       lg_s[tb * 8 + 2 * t + 1] = hv1 ? cc[3] * fq1 * fb : -INFINITY;
     }
     __syncthreads();
-    // ---- warp 0: the record's max per head (lane (g, t): head g, tokens t + 4j),
-    // lazy rescale (only when a logit passes the max by 2^8), softmax
-    // denominator, P' scale exponent
-    if (warp == 0) {
-      float mx = -INFINITY;
-#pragma unroll 8
-      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, lg_s[(t + 4 * j) * 8 + g]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mo = st_s[g];
+    // ---- warp w: head w's max over the record (lane: tokens lane + 32j), lazy
+    // rescale (only when a logit passes the max by 2^8), softmax denominator;
+    // every warp also derives the same P' scale exponent from the norms
+    {
+      const int hw = warp;
+      float lv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lv[j] = lg_s[(lane + 32 * j) * 8 + hw];
+      const float mx = warp_max(fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3])));
+      const float mo = st_s[hw];
       const float mn = mx > mo + 8.f ? mx : mo;
       const float alpha = (mn == mo || mo == -INFINITY) ? (mo == -INFINITY ? 0.f : 1.f) : exp2f(mo - mn);
       float ls = 0.f;
       if (mn != -INFINITY) {
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) ls += exp2f(lg_s[(t + 4 * j) * 8 + g] - mn);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ls += exp2f(lv[j] - mn);
       }
-      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      ls = warp_sum(ls);
       const float vmax = warp_max(fmaxf(fmaxf(vnorm[lane], vnorm[32 + lane]), fmaxf(vnorm[64 + lane], vnorm[96 + lane])));
       int kn = kx;
       if (vmax > 0.f) kn = min(kx, 6 - exp_of(vmax));
       const float gamma = pow2i(kn - kx);
-      if (t == 0) {
-        st_s[g] = mn;
-        st_s[8 + g] = (mo == -INFINITY ? 1.f : alpha) * gamma;  // acc rescale (acc is 0 before the first record)
-        st_s[16 + g] = st_s[16 + g] * alpha + ls;
+      __syncwarp();
+      if (lane == 0) {
+        st_s[hw] = mn;
+        st_s[8 + hw] = (mo == -INFINITY ? 1.f : alpha) * gamma;  // acc rescale (acc is 0 before the first record)
+        st_s[16 + hw] = st_s[16 + hw] * alpha + ls;
+        if (hw == 0) st_s[24] = __int_as_float(kn);
       }
-      if (lane == 0) st_s[24] = __int_as_float(kn);
     }
     __syncthreads();
     kx = __float_as_int(st_s[24]);

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   float* lutk = reinterpret_cast<float*>(sm + p.sm_lut);
   float* lutv = lutk + 16;
   float* pbuf = reinterpret_cast<float*>(sm + p.sm_logit);  // [4][32][GTP]
-  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);   // [4][D][GTP]
+  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);   // [4][GTP][D] (head-major: atomics on random coordinates spread over the banks)
   unsigned char* mainb = sm + p.sm_main;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
           if (vout) {
             for (int j = lane; j < D; j += 32)
   #pragma unroll
-              for (int h = 0; h < GT; ++h) cw[j * GTP + h] *= al[h];
+              for (int h = 0; h < GT; ++h) cw[h * D + j] *= al[h];
           }
         }
         const float vn = vnorm[tloc];
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
           const int idx = (int)(v & 0xFFFFu) & (D - 1);
           const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)];
   #pragma unroll
-          for (int h = 0; h < GT; ++h) atomicAdd(&cw[idx * GTP + h], pv[h] * delta);
+          for (int h = 0; h < GT; ++h) atomicAdd(&cw[h * D + idx], pv[h] * delta);
         };
   #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
 #pragma unroll
       for (int h = 0; h < GT; ++h) {
         float v = (h & 1) ? acc[c][h >> 1].y : acc[c][h >> 1].x;
-        if (vout) v += cw[(4 * g + c) * GTP + h];
+        if (vout) v += cw[h * D + 4 * g + c];
         red[(warp * D + 4 * g + c) * GTP + h] = v;
       }
   }
