@@ -81,7 +81,8 @@ struct Plan {
   size_t ws_acc_bytes, ws_bytes;
   CodecDev kc, vc;
   bool has_rec, has_tail, shared;
-  bool mma;  // tensor-core kernel (head dims 64/128, no outlier side lists)
+  bool mma;     // tensor-core kernel (head dims 64/128, no outlier side lists)
+  bool mma512;  // tensor-core kernel at head dim 512
 };
 
 tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec* vcod, Plan* pl) {
@@ -133,6 +134,18 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   } else if (a->v_tail || a->tail_len || a->tail_start) {
     return TQ_ERR_INVALID_ARG;
   }
+  // Tensor cores for head dims 64 and 128 unless a codec has outlier side
+  // lists (their corrections are latency-bound scatter work, better
+  // overlapped by the CUDA-core kernel's FMA work) or the caller asks for the
+  // CUDA-core kernel; the same at head dim 512 for the compressed splits, with
+  // CTAs of 16 query heads where the group allows (each dequantised pair then
+  // feeds two n-tiles of MMAs).
+  pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
+  pl->mma512 = D == 512 && pl->has_rec && !a->cuda_core_path && !pl->kc.has_outl && !pl->vc.has_outl;
+  if (pl->mma512 && pl->G % 16 == 0) {
+    pl->GT = 16;
+    pl->n_hg = pl->G / 16;
+  }
   const int64_t comp_tiles = pl->has_rec ? a->max_chunks : 0;
   const int TT = 4096 / D;
   const int64_t max_tail = pl->has_tail ? a->max_tail : 0;
@@ -147,14 +160,10 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   int64_t Sc = 0, St = 0;
   if (comp_tiles > 0) Sc = std::max<int64_t>(1, std::min(want, comp_tiles));
   if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want, tail_tiles));
-  // Tensor cores for head dims 64 and 128 unless a codec has outlier side
-  // lists (their corrections are latency-bound scatter work, better
-  // overlapped by the CUDA-core kernel's FMA work) or the caller asks for the
-  // CUDA-core kernel.  Its CTAs take at least two records each, which
-  // amortises their per-CTA set-up (pair tables, query fragments)
-  pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
-  // (and dense CTAs at least 128 tokens: two 16-token tiles per warp), which
-  // also keeps the merge's split count down.
+  // Tensor-core kernels' CTAs take at least two records each, which amortises
+  // their per-CTA set-up (pair tables, query fragments), and dense CTAs at
+  // least 128 tokens (two 16-token tiles per warp), which also keeps the
+  // merge's split count down.
   if (pl->mma && a->splits <= 0) {
     if (comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
     if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
@@ -268,24 +277,25 @@ void attn_mma_smem_layout(AttnParams& p, int D) {
 }
 
 void attn_mma512_smem_layout(AttnParams& p) {
+  const int NT = (p.G / p.n_hg > 8) ? 2 : 1;  // n-tiles of 8 query heads per CTA
   auto al = [](int x, int a) { return (x + a - 1) / a * a; };
   int off = 0;
   p.sm_kpair = off;  // fixed offsets, as in the d 64/128 kernel
   off += (1 << (2 * p.kb)) * 128;
   p.sm_vpair = off;
   off += (p.vb == 3 ? 120 : (1 << (2 * p.vb))) * 128;
-  p.sm_logit = off;  // query fragments [32 k-steps][32 lanes][16 B]
-  off += 32 * 32 * 16;
+  p.sm_logit = off;  // query fragments [32 k-steps][NT][32 lanes][16 B]
+  off += 32 * NT * 32 * 16;
   p.sm_slot = off;   // centroid halves
   off += 32 * 8;
-  p.sm_red = off;    // logits [128][8]
-  off += 128 * 8 * 4;
-  p.sm_corr = off;   // softmax state
-  off = al(off + 32 * 4, 128);
+  p.sm_red = off;    // logits [128][8 NT]
+  off += 128 * 8 * NT * 4;
+  p.sm_corr = off;   // softmax state m[16] | scale[16] | l[16] | kx
+  off = al(off + 64 * 4, 128);
   p.sm_q = p.sm_lut = p.sm_pre = p.sm_ent = off;  // unused by this kernel
   p.sm_ent_stage = 0;
   int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
-  stage = std::max(stage, 8 * 516 * 4);                       // q~ is built in the second buffer
+  stage = std::max(stage, 8 * NT * 516 * 4);                  // q~ is built in the second buffer
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
   off += 2 * p.sm_stage;
@@ -542,9 +552,9 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
     if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-  } else if (pl.D == 512 && pl.Sc > 0 && !a->cuda_core_path && !pl.kc.has_outl && !pl.vc.has_outl) {
+  } else if (pl.mma512 && pl.Sc > 0) {
     // compressed splits on the d-512 tensor-core kernel, dense splits (if any)
-    // on the general kernel in a second launch
+    // on the general kernel in a second launch (groups of at most 8 heads)
     AttnParams pm = p;
     attn_mma512_smem_layout(pm);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
@@ -552,10 +562,15 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     if (pl.S > pl.Sc) {
       AttnParams pd = p;
       pd.split_base = pl.Sc;
-      attn_smem_layout(pd, pl.D, pl.GT);
+      int gt = pl.GT;
+      if (gt > 8) {
+        gt = 8;
+        pd.n_hg = pl.G / 8;
+      }
+      attn_smem_layout(pd, pl.D, gt);
       if (pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-      if (launch_attn(pd, pl.D, pl.GT, dim3(pl.S - pl.Sc, units_y, a->n_layers), s) != cudaSuccess)
-        return TQ_ERR_CUDA;
+      const int uy = a->batch * a->n_kv_heads * pd.n_hg;
+      if (launch_attn(pd, pl.D, gt, dim3(pl.S - pl.Sc, uy, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
     }
   } else if (rec_kernel) {
     // compressed splits on the warp-local path, dense splits on the general

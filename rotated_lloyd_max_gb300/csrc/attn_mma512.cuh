@@ -30,8 +30,9 @@ __device__ __forceinline__ void cta256_copy_async(void* smem, const void* gmem, 
   for (int off = threadIdx.x * 16; off < bytes; off += kT512 * 16) cp_async16(s + off, gp + off);
 }
 
-template <int KB, int VB>
+template <int KB, int VB, int NT>
 __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int HN = 8 * NT;  // query heads per CTA (NT n-tiles of 8)
   constexpr int D = 512, KS = 32, KR = 128;
   constexpr int KNB = KR * KB;                 // bits of a lane's score run (multiple of 32)
   constexpr int VNB = 8 * VB;                  // bits of a lane group's value run (8 codes)
@@ -42,10 +43,10 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
   constexpr int EK = 1 << (2 * KB), EV = VIdx<VB>::ENTRIES;
   constexpr int KP_OFF = 0, VP_OFF = EK * 128;
   extern __shared__ __align__(128) unsigned char sm[];
-  uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);   // [32 k-steps][32 lanes]
+  uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);   // [32 k-steps][NT][32 lanes]
   uint2* cent = reinterpret_cast<uint2*>(sm + p.sm_slot);     // [32] centroid halves x 2^16
-  float* lg_s = reinterpret_cast<float*>(sm + p.sm_red);      // [128 tokens][8 heads] logits
-  float* st_s = reinterpret_cast<float*>(sm + p.sm_corr);     // m[8] | scale[8] | l[8] | flag, kx
+  float* lg_s = reinterpret_cast<float*>(sm + p.sm_red);      // [128 tokens][HN heads] logits
+  float* st_s = reinterpret_cast<float*>(sm + p.sm_corr);     // m[16] | scale[16] | l[16] | kx
   unsigned char* mainb = sm + p.sm_main;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -88,13 +89,13 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
 
   // ---- q~ of the CTA's heads into the second staging buffer (free until
   // record 1 is issued), rows >= GT zero
-  // [8 heads][4 lane runs of 128, padded to 129][+1]: coordinate c of head h at
+  // [HN heads][4 lane runs of 128, padded to 129][+1]: coordinate c of head h at
   // h*516 + (c/128)*129 + c%128, so the 32 lanes' runs start in 32 different banks
   float* qf = reinterpret_cast<float*>(stage(1));
   auto qidx = [](int h, int c) { return h * 516 + (c >> 7) * 129 + (c & 127); };
   {
     constexpr int R = D / 32;
-    const int hh = warp;  // 8 warps, 8 head rows
+    for (int hh = warp; hh < HN; hh += 8) {
     float x[R];
     if (hh < GT) {
       const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + hh) * D + lane * R;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) qf[qidx(hh, lane * R + r)] = x[r];
+    }
   }
   if (tid < 32) {
     const float v = (tid < 16 ? p.kc[tid] : p.vc[tid - 16]) * 65536.f;
@@ -126,9 +128,9 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     const __half r = __float2half_rn(v - __half2float(h));
     cent[tid] = make_uint2(__half_as_ushort(h), __half_as_ushort(r));
   }
-  if (tid < 8) {
+  if (tid < 16) {
     st_s[tid] = -INFINITY;  // m
-    st_s[16 + tid] = 0.f;   // l
+    st_s[32 + tid] = 0.f;   // l
   }
   __syncthreads();
   for (int i = tid; i < EK * 16; i += kT512) {
@@ -146,10 +148,11 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     }
     *reinterpret_cast<uint2*>(sm + VP_OFF + i * 8) = v;
   }
-  // query fragments (head g, lane t's coordinates), scaled per head
-  float fq0, fq1;
-  {
-    const float* qrow = qf + qidx(g, KR * t);
+  // query fragments (head 8 nt + g, lane t's coordinates), scaled per head
+  float fq[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float* qrow = qf + qidx(8 * nt + g, KR * t);
     float mx = 0.f;
 #pragma unroll 8
     for (int j = 0; j < KR; ++j) mx = fmaxf(mx, fabsf(qrow[j]));
@@ -161,22 +164,24 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
       uint4 f;
       split_f16x2(qrow[4 * kk] * sc, qrow[4 * kk + 1] * sc, f.x, f.z);
       split_f16x2(qrow[4 * kk + 2] * sc, qrow[4 * kk + 3] * sc, f.y, f.w);
-      qfrag[kk * 32 + lane] = f;
+      qfrag[(kk * NT + nt) * 32 + lane] = f;
     }
     const int s0 = __shfl_sync(0xffffffffu, s, 4 * (2 * t));
     const int s1 = __shfl_sync(0xffffffffu, s, 4 * (2 * t + 1));
-    fq0 = pow2i(-s0 - 16);
-    fq1 = pow2i(-s1 - 16);
+    fq[nt][0] = pow2i(-s0 - 16);
+    fq[nt][1] = pow2i(-s1 - 16);
   }
-  const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
+  // head of element e of n-tile nt in the score / value fragments: 8 nt + 2t + (e & 1)
   const uint32_t loff = (lane & 15) * 8;
   auto kpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + KP_OFF + o); };
   auto vpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + VP_OFF + o); };
-  float acc[4][4];
+  float acc[4][NT][4];
 #pragma unroll
   for (int mc = 0; mc < 4; ++mc)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[mc][e] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mc][nt][e] = 0.f;
   int kx = 127;  // P' f16 scale exponent (CTA-wide, only decreases)
   const int rbk = D * KB / 8, rbv = D * VB / 8;
 
@@ -194,18 +199,21 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     {
       const unsigned char* r0 = st + (16 * warp + g) * rbk;
       const unsigned char* r1 = r0 + 8 * rbk;
-      // hi.hi, hi.lo and lo.hi in separate accumulators: three independent MMA chains
-      float cc[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f}, ch[4] = {0.f, 0.f, 0.f, 0.f};
+      // hi.hi, hi.lo and lo.hi in separate accumulators: independent MMA chains
+      float cc[NT][4], cl[NT][4], ch[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cc[nt][e] = cl[nt][e] = ch[nt][e] = 0.f;
 #pragma unroll 2
-      for (int q8 = 0; q8 < 4; ++q8) {  // 8 k-steps = 32 coordinates = 32 KB bits of the lane's run
-        constexpr int PB = 32 * KB;      // bits per 8 k-steps
+      for (int q8 = 0; q8 < 4; ++q8) {  // 8 k-steps = 32 coordinates of the lane's run
+        constexpr int PB = 32 * KB;
         uint32_t w0[PB / 32], w1[PB / 32];
         load_run<PB, true>(r0, KNB * t + PB * q8, w0);
         load_run<PB, true>(r1, KNB * t + PB * q8, w1);
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
           const int kk = 8 * q8 + k8;
-          const uint4 f = qfrag[kk * 32 + lane];
           uint32_t ah[4], al[4];
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -217,81 +225,94 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
             ah[2 * hf + 1] = e1.x;
             al[2 * hf + 1] = e1.y;
           }
-          mma_f16(cc, ah, f.x, f.y);
-          mma_f16(cl, ah, f.z, f.w);
-          mma_f16(ch, al, f.x, f.y);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint4 f = qfrag[(kk * NT + nt) * 32 + lane];
+            mma_f16(cc[nt], ah, f.x, f.y);
+            mma_f16(cl[nt], ah, f.z, f.w);
+            mma_f16(ch[nt], al, f.x, f.y);
+          }
         }
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cc[e] += cl[e] + ch[e];
       const int ta = 16 * warp + g, tb = ta + 8;
       const float fa = knorm[ta] * p.sscale, fb = knorm[tb] * p.sscale;
-      lg_s[ta * 8 + 2 * t] = hv0 ? cc[0] * fq0 * fa : -INFINITY;
-      lg_s[ta * 8 + 2 * t + 1] = hv1 ? cc[1] * fq1 * fa : -INFINITY;
-      lg_s[tb * 8 + 2 * t] = hv0 ? cc[2] * fq0 * fb : -INFINITY;
-      lg_s[tb * 8 + 2 * t + 1] = hv1 ? cc[3] * fq1 * fb : -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = 8 * nt + 2 * t;
+        const bool v0 = h < GT, v1 = h + 1 < GT;
+        lg_s[ta * HN + h] = v0 ? (cc[nt][0] + cl[nt][0] + ch[nt][0]) * fq[nt][0] * fa : -INFINITY;
+        lg_s[ta * HN + h + 1] = v1 ? (cc[nt][1] + cl[nt][1] + ch[nt][1]) * fq[nt][1] * fa : -INFINITY;
+        lg_s[tb * HN + h] = v0 ? (cc[nt][2] + cl[nt][2] + ch[nt][2]) * fq[nt][0] * fb : -INFINITY;
+        lg_s[tb * HN + h + 1] = v1 ? (cc[nt][3] + cl[nt][3] + ch[nt][3]) * fq[nt][1] * fb : -INFINITY;
+      }
     }
     __syncthreads();
-    // ---- warp w: head w's max over the record (lane: tokens lane + 32j), lazy
-    // rescale (only when a logit passes the max by 2^8), softmax denominator;
-    // every warp also derives the same P' scale exponent from the norms
+    // ---- warp w: heads w (and w + 8): max over the record (lane: tokens
+    // lane + 32j), lazy rescale (only when a logit passes the max by 2^8),
+    // softmax denominator; and the P' scale exponent from the norms
     {
-      const int hw = warp;
-      float lv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) lv[j] = lg_s[(lane + 32 * j) * 8 + hw];
-      const float mx = warp_max(fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3])));
-      const float mo = st_s[hw];
-      const float mn = mx > mo + 8.f ? mx : mo;
-      const float alpha = (mn == mo || mo == -INFINITY) ? (mo == -INFINITY ? 0.f : 1.f) : exp2f(mo - mn);
-      float ls = 0.f;
-      if (mn != -INFINITY) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) ls += exp2f(lv[j] - mn);
-      }
-      ls = warp_sum(ls);
       const float vmax = warp_max(fmaxf(fmaxf(vnorm[lane], vnorm[32 + lane]), fmaxf(vnorm[64 + lane], vnorm[96 + lane])));
       int kn = kx;
       if (vmax > 0.f) kn = min(kx, 6 - exp_of(vmax));
       const float gamma = pow2i(kn - kx);
-      __syncwarp();
-      if (lane == 0) {
-        st_s[hw] = mn;
-        st_s[8 + hw] = (mo == -INFINITY ? 1.f : alpha) * gamma;  // acc rescale (acc is 0 before the first record)
-        st_s[16 + hw] = st_s[16 + hw] * alpha + ls;
-        if (hw == 0) st_s[24] = __int_as_float(kn);
+#pragma unroll
+      for (int hw = warp; hw < HN; hw += 8) {
+        float lv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) lv[j] = lg_s[(lane + 32 * j) * HN + hw];
+        const float mx = warp_max(fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3])));
+        const float mo = st_s[hw];
+        const float mn = mx > mo + 8.f ? mx : mo;
+        const float alpha = (mn == mo || mo == -INFINITY) ? (mo == -INFINITY ? 0.f : 1.f) : exp2f(mo - mn);
+        float ls = 0.f;
+        if (mn != -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ls += exp2f(lv[j] - mn);
+        }
+        ls = warp_sum(ls);
+        __syncwarp();
+        if (lane == 0) {
+          st_s[hw] = mn;
+          st_s[16 + hw] = (mo == -INFINITY ? 1.f : alpha) * gamma;  // acc rescale (acc is 0 before the first record)
+          st_s[32 + hw] = st_s[32 + hw] * alpha + ls;
+        }
       }
+      if (tid == 0) st_s[48] = __int_as_float(kn);
     }
     __syncthreads();
-    kx = __float_as_int(st_s[24]);
-    {
-      const float s0 = st_s[8 + 2 * t], s1 = st_s[8 + 2 * t + 1];
+    kx = __float_as_int(st_s[48]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float s0 = st_s[16 + 8 * nt + 2 * t], s1 = st_s[16 + 8 * nt + 2 * t + 1];
 #pragma unroll
       for (int mc = 0; mc < 4; ++mc) {
-        acc[mc][0] *= s0;
-        acc[mc][1] *= s1;
-        acc[mc][2] *= s0;
-        acc[mc][3] *= s1;
+        acc[mc][nt][0] *= s0;
+        acc[mc][nt][1] *= s1;
+        acc[mc][nt][2] *= s0;
+        acc[mc][nt][3] *= s1;
       }
     }
     // ---- values: output coordinates 64 warp + 8 g + 2 mc (+1), all 128 tokens
     {
-      const float mg = st_s[g];
       const float psc = pow2i(kx);
-      const bool hvg = g < GT;
 #pragma unroll 2
       for (int ks = 0; ks < 8; ++ks) {
         const int tk = 16 * ks + 2 * t;
-        float pp[4];
+        uint32_t pbh[NT][2], pbl[NT][2];  // P'^T fragments of heads 8 nt + g
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int tok = tk + (r & 1) + 8 * (r >> 1);
-          const float lgv = lg_s[tok * 8 + g];
-          pp[r] = (hvg && lgv != -INFINITY) ? exp2f(lgv - mg) * vnorm[tok] * psc : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+          const int hg2 = 8 * nt + g;
+          const float mg = st_s[hg2];
+          float pp[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int tok = tk + (r & 1) + 8 * (r >> 1);
+            const float lgv = lg_s[tok * HN + hg2];
+            pp[r] = (hg2 < GT && lgv != -INFINITY) ? exp2f(lgv - mg) * vnorm[tok] * psc : 0.f;
+          }
+          split_f16x2(pp[0], pp[1], pbh[nt][0], pbl[nt][0]);
+          split_f16x2(pp[2], pp[3], pbh[nt][1], pbl[nt][1]);
         }
-        uint32_t pb0h, pb0l, pb1h, pb1l;
-        split_f16x2(pp[0], pp[1], pb0h, pb0l);
-        split_f16x2(pp[2], pp[3], pb1h, pb1l);
         uint32_t r0[VNW], r1[VNW], r2[VNW], r3[VNW];
         const int voff = (64 * warp + 8 * g) * VB;
         load_run<VNB, VAL>(vcodes + tk * rbv, voff, r0);
@@ -310,9 +331,12 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
           const uint2 e3 = vpair_at(pair_off(zo23, off, 2 * FW, loff));
           const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x};
           const uint32_t al[4] = {e0.y, e1.y, e2.y, e3.y};
-          mma_f16(acc[mc], ah, pb0h, pb1h);
-          mma_f16(acc[mc], ah, pb0l, pb1l);
-          mma_f16(acc[mc], al, pb0h, pb1h);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(acc[mc][nt], ah, pbh[nt][0], pbh[nt][1]);
+            mma_f16(acc[mc][nt], ah, pbl[nt][0], pbl[nt][1]);
+            mma_f16(acc[mc][nt], al, pbh[nt][0], pbh[nt][1]);
+          }
         }
       }
     }
@@ -323,24 +347,31 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
 #pragma unroll
   for (int mc = 0; mc < 4; ++mc)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = 64 * warp + 8 * g + 2 * mc + (e >> 1), h = 2 * t + (e & 1);
-      if (h < GT) p.ws_acc[((qh0 + h) * p.S + split) * D + j] = acc[mc][e] * un;
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 64 * warp + 8 * g + 2 * mc + (e >> 1), h = 8 * nt + 2 * t + (e & 1);
+        if (h < GT) p.ws_acc[((qh0 + h) * p.S + split) * D + j] = acc[mc][nt][e] * un;
+      }
   if (tid < GT) {
     float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
     ml[0] = st_s[tid];
-    ml[1] = st_s[16 + tid];
+    ml[1] = st_s[32 + tid];
   }
 }
 
-template <int KB, int VB>
-cudaError_t attn_mma512_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attn_mma512_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int KB, int VB, int NT>
+cudaError_t attn_mma512_launch_nt(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_mma512_kernel<KB, VB, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        p.sm_total);
   if (e != cudaSuccess) return e;
-  attn_mma512_kernel<KB, VB><<<grid, kT512, p.sm_total, s>>>(p);
+  attn_mma512_kernel<KB, VB, NT><<<grid, kT512, p.sm_total, s>>>(p);
   return cudaGetLastError();
+}
+// 16 heads per CTA (two n-tiles) when the group holds more than 8
+template <int KB, int VB>
+cudaError_t attn_mma512_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  return (p.G / p.n_hg > 8) ? attn_mma512_launch_nt<KB, VB, 2>(p, grid, s) : attn_mma512_launch_nt<KB, VB, 1>(p, grid, s);
 }
 
 }  // namespace tq

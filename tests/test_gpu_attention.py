@@ -151,7 +151,8 @@ def test_tensor_core_bit_widths(tq, orc, d, kb, vb):
     _assert_close(got, want)
 
 
-@pytest.mark.parametrize("kb,vb,G,shared", [(4, 4, 64, True), (2, 3, 4, False), (3, 1, 8, False), (1, 2, 6, False)])
+@pytest.mark.parametrize("kb,vb,G,shared", [(4, 4, 64, True), (2, 3, 4, False), (3, 1, 8, False), (1, 2, 6, False),
+                                             (3, 3, 32, False)])
 def test_tensor_core_d512(tq, orc, kb, vb, G, shared):
     """Head dim 512 on its tensor-core kernel (8 query heads per CTA), with a
     dense tail on the general kernel."""
