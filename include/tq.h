@@ -204,11 +204,15 @@ typedef struct {
   int32_t max_chunks;        /* host upper bound of n_chunks (sizes the grid) */
   int32_t max_tail;          /* host upper bound of tail_len */
   int32_t splits;            /* splits per (layer, batch, kv head); 0 = automatic */
-  /* 0: automatic.  Compressed tokens at head dims 64 and 128 of codecs
-   * without outlier side lists run on the tensor cores (mma.sync, f16 hi/lo
-   * operand splits, f32 accumulation); everything else on the CUDA-core
-   * kernel (f32 FMA from the centroid table).  Nonzero: always the CUDA-core
-   * kernel.  Both meet the same tolerance. */
+  /* 0: automatic.  Compressed tokens of codecs without outlier side lists
+   * run on the tensor cores with f16 hi/lo operand splits and f32
+   * accumulation: at head dim 512 with 16-64 query heads per kv head (a
+   * multiple of 8) or a multiple of 64, on the fifth-generation tensor cores
+   * (tcgen05, accumulators in tensor memory); at head dims 64, 128 and the
+   * other head-dim-512 groups on mma.sync.  Everything else runs on the
+   * CUDA-core kernel (f32 FMA from the centroid table).
+   * 1: always the CUDA-core kernel.  2: as 0 but never tcgen05 (the
+   * mma.sync kernels).  All paths meet the same tolerance. */
   int32_t cuda_core_path;
 } tq_attn_args;
 
@@ -218,7 +222,10 @@ size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k
 
 /* workspace: device, 256-byte aligned, >= tq_decode_attn_workspace_size bytes.
  * Its contents need no initialisation and are garbage afterwards.  An empty
- * context (no compressed and no dense token) yields a zero output row. */
+ * context (no compressed and no dense token) yields a zero output row.
+ * The tcgen05 kernel bounds every internal wait (about two seconds); if one
+ * expires (a fault of the device, not of the arguments) the call's outputs
+ * are NaN rather than wrong numbers. */
 tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
                          const tq_codec* v_codec, void* workspace, size_t workspace_bytes,
                          void* stream);

@@ -224,7 +224,7 @@ def tq_evict(k_codec: Codec, v_codec: Codec | None, *, k_rec, v_rec, k_tail, v_t
 def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None, v_tail=None,
                    n_chunks=None, tail_start=None, tail_len=None, max_chunks: int = 0,
                    max_tail: int = 0, splits: int = 0, n_kv_heads: int | None = None,
-                   cuda_core_path: bool = False) -> tq_attn_args:
+                   cuda_core_path: bool | int = False) -> tq_attn_args:
     """Build tq_attn_args from tensors.
     q: bf16 [L, B, Hq, d] (head and dim axes packed); out: f32 [L, B, Hq, d] contiguous;
     k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, bytes]; k_tail/v_tail: bf16 [L, B, Hkv, cap, d];
@@ -249,7 +249,7 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     a.tail_start = _ptr(tail_start)
     a.tail_len = _ptr(tail_len)
     a.max_chunks, a.max_tail, a.splits = max_chunks, max_tail, splits
-    a.cuda_core_path = 1 if cuda_core_path else 0
+    a.cuda_core_path = int(cuda_core_path)  # 0 automatic, 1 CUDA cores, 2 no tcgen05
     # the struct holds raw device pointers: keep the tensors alive with it
     a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len)
     return a

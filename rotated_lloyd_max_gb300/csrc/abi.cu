@@ -82,7 +82,9 @@ struct Plan {
   CodecDev kc, vc;
   bool has_rec, has_tail, shared;
   bool mma;     // tensor-core kernel (head dims 64/128, no outlier side lists)
-  bool mma512;  // tensor-core kernel at head dim 512
+  bool mma512;  // tensor-core kernel at head dim 512 (mma.sync)
+  bool umma512; // tcgen05 kernel at head dim 512 (groups of up to 64 heads per CTA)
+  size_t ws_status_off;
 };
 
 tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec* vcod, Plan* pl) {
@@ -141,8 +143,16 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   // CTAs of 16 query heads where the group allows (each dequantised pair then
   // feeds two n-tiles of MMAs).
   pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
-  pl->mma512 = D == 512 && pl->has_rec && !a->cuda_core_path && !pl->kc.has_outl && !pl->vc.has_outl;
-  if (pl->mma512 && pl->G % 16 == 0) {
+  pl->mma512 = D == 512 && pl->has_rec && a->cuda_core_path != 1 && !pl->kc.has_outl && !pl->vc.has_outl;
+  // tcgen05 for groups of 16-64 heads (multiples of 8, which the dense
+  // splits' 8-head CTAs need) or multiples of 64: one CTA keeps 64 heads
+  pl->umma512 = pl->mma512 && a->cuda_core_path == 0 && pl->G % 8 == 0 && pl->G >= 16 &&
+                (pl->G <= 64 || pl->G % 64 == 0) && tq::attn_umma512_smem() <= max_dyn_smem();
+  if (pl->umma512) {
+    pl->mma512 = false;
+    pl->GT = std::min(pl->G, 64);
+    pl->n_hg = pl->G / pl->GT;
+  } else if (pl->mma512 && pl->G % 16 == 0) {
     pl->GT = 16;
     pl->n_hg = pl->G / 16;
   }
@@ -168,6 +178,20 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
     if (comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
     if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
   }
+  if (pl->umma512 && a->splits <= 0 && comp_tiles > 0) {
+    // one CTA per SM: the split count that minimises waves x records per
+    // split (plus about two records' worth of per-CTA set-up and partials)
+    const int64_t sms = num_sms();
+    int64_t best = 1, best_cost = INT64_MAX;
+    for (int64_t sc = 1; sc <= std::min<int64_t>(comp_tiles, 500); ++sc) {
+      const int64_t cost = cdiv(units * sc, sms) * (cdiv(comp_tiles, sc) + 2);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = sc;
+      }
+    }
+    Sc = best;
+  }
   int64_t cps = 1, tps = TT;
   if (Sc > 0) {
     cps = cdiv(comp_tiles, Sc);
@@ -184,7 +208,8 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   pl->tps = (int)tps;
   pl->rows = (int64_t)a->n_layers * a->batch * a->n_q_heads;
   pl->ws_acc_bytes = (size_t)(((pl->rows * pl->S * D * 4) + 255) / 256 * 256);
-  pl->ws_bytes = pl->ws_acc_bytes + (size_t)pl->rows * pl->S * 2 * 4;
+  pl->ws_status_off = (pl->ws_acc_bytes + (size_t)pl->rows * pl->S * 2 * 4 + 15) / 16 * 16;
+  pl->ws_bytes = pl->ws_status_off + 16;  // + the launch status word
   return TQ_OK;
 }
 
@@ -545,6 +570,7 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   cudaStream_t s = (cudaStream_t)stream;
   const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
   const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
+  const int* status = nullptr;
   if (pl.mma) {
     // tensor cores: compressed and dense splits in one launch
     AttnParams pm = p;
@@ -552,13 +578,20 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
     if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-  } else if (pl.mma512 && pl.Sc > 0) {
-    // compressed splits on the d-512 tensor-core kernel, dense splits (if any)
+  } else if ((pl.mma512 || pl.umma512) && pl.Sc > 0) {
+    // compressed splits on a d-512 tensor-core kernel, dense splits (if any)
     // on the general kernel in a second launch (groups of at most 8 heads)
     AttnParams pm = p;
-    attn_mma512_smem_layout(pm);
-    if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-    if (launch_attn_mma512(pm, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (pl.umma512) {
+      pm.status = (int*)((char*)workspace + pl.ws_status_off);
+      if (cudaMemsetAsync(pm.status, 0, sizeof(int), s) != cudaSuccess) return TQ_ERR_CUDA;
+      if (launch_attn_umma512(pm, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+      status = pm.status;
+    } else {
+      attn_mma512_smem_layout(pm);
+      if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+      if (launch_attn_mma512(pm, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    }
     if (pl.S > pl.Sc) {
       AttnParams pd = p;
       pd.split_base = pl.Sc;
@@ -590,6 +623,7 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   m.rows = (int)pl.rows;
   m.S = pl.S;
   m.Sc = pl.Sc;
+  m.status = status;
   m.inv_sqrt_d = (float)(1.0 / std::sqrt((double)pl.D));
   std::memcpy(m.vsign, pl.vc.signs, sizeof(m.vsign));
   return launch_merge(m, pl.D, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

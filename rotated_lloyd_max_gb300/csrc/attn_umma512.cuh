@@ -1,0 +1,505 @@
+// a6-a10 at head dim 512 on the fifth-generation tensor cores (tcgen05.mma,
+// accumulators in tensor memory), for compressed records of codecs without
+// outlier side lists and groups of up to 64 query heads per kv head (MQA).
+//
+// Arithmetic (same contract as the mma.sync kernels): centroids x 2^16 and
+// q~ x 2^s (per head) are split into f16 hi + lo; every product is the sum
+// of the hi.hi, hi.lo and lo.hi MMAs with f32 accumulation; P' = p * n_V *
+// 2^kx is split likewise.  One CTA is one split of one (layer, batch, kv head,
+// group of <= 64 heads) and keeps all its heads, so each record is dequantised
+// once per pass for the whole group:
+//
+//  * scores, one 128-token record at a time: S^T[token][n] = K~ . B_q with
+//    B_q = [q~_hi (64 rows) | q~_lo (64 rows)] (N = 128, K-major, resident in
+//    shared memory) plus K~_lo . q~_hi (N = 64) into the same accumulator, so
+//    head h's logit is column h + column 64 + h of the token's TMEM lane;
+//  * softmax: a thread owns one token (its TMEM lane) and 32 heads; the
+//    running max per head moves only when a logit passes it by 2^8 (or the
+//    record's largest V norm needs a smaller P' scale), which is the one step
+//    that reduces across tokens and rescales the output accumulator;
+//  * values: O^T[coordinate][head] += V~^T . P' for four 128-coordinate
+//    blocks (A = the dequantised record, MN-major; B = P', MN-major, N = 64);
+//    O^T stays in tensor memory for the whole split.
+//
+// Warp roles (512 threads, four warps per SM sub-partition): warps 0-7
+// softmax and epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31, heads
+// 32 (w / 4) .. + 31); warps 8-15 dequantise records into a two-stage ring of
+// 32 KB operand tiles (16 stages per record: 8 score chunks of 64
+// coordinates, hi and lo; 8 value blocks of 128 coordinates, hi or lo); warp 8
+// also allocates tensor memory and its lane 0 issues each stage's MMAs once
+// all eight warps have written it.  Stages, scores, P' and outputs are handed over
+// through mbarriers; every wait is bounded and a CTA whose wait expires sets
+// the launch's status word and finishes without further waiting.
+#pragma once
+
+#include "attn_mma.cuh"
+#include "umma.cuh"
+
+namespace tq {
+
+constexpr int kU512Threads = 512;
+// shared memory (bytes from a 1024-aligned base)
+constexpr int kUQ = 0;          // q~ operand: [8 chunks of 64 coordinates][128 rows][128 B]
+constexpr int kUP = 131072;     // P' operand: hi [128 tokens][64 heads f16] | lo
+constexpr int kURing = 163840;  // 2 stages x 32 KB
+constexpr int kUMisc = 229376;
+constexpr int kUSmem = kUMisc + 2048 + 1024;  // + bookkeeping + alignment slack
+
+struct U512Misc {
+  uint64_t full[2], empty[2], s_full, p_full, o_done, fin;
+  uint32_t tbase;
+  int abort_;
+  int pad[2];
+  uint32_t ctab_k[16], ctab_v[16];  // centroid x 2^16 as f16 {hi, lo} per code
+  float qsc[64];                    // per head: softmax scale * log2(e) * 2^(-16 - s)
+  float mst[64];                    // running max per head (log2 units)
+  float scl[64];                    // output rescale per head (slow path)
+  float red[4][64];                 // cross-quarter reductions
+  float vmx[8];
+};
+static_assert(sizeof(U512Misc) <= 2048, "bookkeeping block");
+
+__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, "
+      "q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 8 codes of B bits: the m-th 8-code group of a packed row (B bytes)
+template <int B>
+__device__ __forceinline__ uint32_t group_word(const uint8_t* row, int m) {
+  if constexpr (B == 4) {
+    return __ldg(reinterpret_cast<const uint32_t*>(row) + m);
+  } else if constexpr (B == 2) {
+    return __ldg(reinterpret_cast<const uint16_t*>(row) + m);
+  } else if constexpr (B == 1) {
+    return __ldg(row + m);
+  } else {  // 3 bytes at 3m: two aligned words (the second may lie in the next row or the norms)
+    const int o = 3 * m;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + (o & ~3));
+    return __funnelshift_r(__ldg(w), __ldg(w + 1), 8 * (o & 3)) & 0xFFFFFFu;
+  }
+}
+
+// dequantise 8 codes into f16x2 hi / lo words (coordinate 2i in the low half)
+template <int B>
+__device__ __forceinline__ void deq8(uint32_t w, const uint32_t* tab, uint4& hi, uint4& lo) {
+  uint32_t e[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e[i] = tab[(w >> (B * i)) & ((1u << B) - 1u)];
+  hi = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410), __byte_perm(e[4], e[5], 0x5410),
+                  __byte_perm(e[6], e[7], 0x5410));
+  lo = make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632), __byte_perm(e[4], e[5], 0x7632),
+                  __byte_perm(e[6], e[7], 0x7632));
+}
+
+// 32 values per lane -> lane i holds the reduction over the warp of value i
+template <bool MAX>
+__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float keep = up ? v[half + i] : v[i];
+      const float give = up ? v[i] : v[half + i];
+      const float got = __shfl_xor_sync(0xffffffffu, give, half);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void set_status(const AttnParams& p, int code) {
+  if (p.status) atomicOr(p.status, code);
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int D = 512;
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+  U512Misc& ms = *reinterpret_cast<U512Misc*>(sm + kUMisc);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int l = blockIdx.z;
+  int rem = blockIdx.y;
+  const int hg = rem % p.n_hg;
+  rem /= p.n_hg;
+  const int kvh = rem % p.Hkv, b = rem / p.Hkv;
+  const int split = blockIdx.x;
+  const int GT = p.G / p.n_hg;  // <= 64
+  const int h0 = kvh * p.G + hg * GT;
+  const int lb = l * p.B + b;
+  const int64_t qh0 = (int64_t)lb * p.Hq + h0;
+  const int nch = min(p.n_chunks[lb], p.rec_cap);
+  const int c_begin = split * p.cps;
+  const int c_end = min(c_begin + p.cps, nch);
+  if (c_begin >= c_end) {
+    if (tid < GT) {
+      float* ml = p.ws_ml + ((qh0 + tid) * p.S + split) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+    }
+    return;
+  }
+  const int n = c_end - c_begin;
+  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
+  const uint8_t* vb0 = p.shared_kv ? kb0
+                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms.full[i], 8);
+      mbar_init(&ms.empty[i], 1);
+    }
+    mbar_init(&ms.s_full, 1);
+    mbar_init(&ms.p_full, 8);
+    mbar_init(&ms.o_done, 1);
+    mbar_init(&ms.fin, 1);
+    ms.abort_ = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 8) tmem_alloc(&ms.tbase, 512);
+  if (tid < 32) {
+    const int e = tid & 15, bits = tid < 16 ? KB : VB;
+    const float v = e < (1 << bits) ? (tid < 16 ? p.kc[e] : p.vc[e]) * 65536.f : 0.f;
+    const __half h = __float2half_rn(v);
+    const __half r = __float2half_rn(v - __half2float(h));
+    (tid < 16 ? ms.ctab_k : ms.ctab_v)[e] = (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(r) << 16);
+  }
+  if (tid < 64) ms.mst[tid] = -INFINITY;
+  // q~ rows (warps 0-15, four heads each): lane holds coordinates 16 lane .. + 15
+  if (warp < 16) {
+    for (int hh = warp; hh < 64; hh += 16) {
+      float x[16];
+      if (hh < GT) {
+        const uint16_t* qp = p.q + l * p.q_ls + b * p.q_bs + (int64_t)(h0 + hh) * D + lane * 16;
+#pragma unroll
+        for (int r = 0; r < 16; r += 2) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + r);
+          x[r] = bf16_lo(w);
+          x[r + 1] = bf16_hi(w);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const int j = lane * 16 + r;
+          if ((p.ksign[j >> 5] >> (j & 31)) & 1u) x[r] = -x[r];
+        }
+        fwht_regs<16>(x);
+        fwht_lanes<16>(x, lane, 32);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] *= inv_sqrt_dim<D>();
+      } else {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = 0.f;
+      }
+      float mx = 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) mx = fmaxf(mx, fabsf(x[r]));
+      mx = warp_max(mx);
+      const int s = mx > 0.f ? 13 - exp_of(mx) : 0;
+      const float sc = pow2i(s);
+      if (lane == 0) ms.qsc[hh] = hh < GT ? p.sscale * pow2i(-16 - s) : 0.f;
+      uint32_t hw[8], lw[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) split_f16x2(x[2 * e] * sc, x[2 * e + 1] * sc, hw[e], lw[e]);
+      unsigned char* qc = sm + kUQ + (lane >> 2) * 16384;
+      const int c16 = 2 * (lane & 3);
+      *reinterpret_cast<uint4*>(qc + sw128_off(hh, c16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(qc + sw128_off(hh, c16 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+      *reinterpret_cast<uint4*>(qc + sw128_off(64 + hh, c16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4*>(qc + sw128_off(64 + hh, c16 + 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tS = ms.tbase;        // scores: 128 columns
+  const uint32_t tO = ms.tbase + 128;  // O^T: 4 blocks x 64 columns
+  volatile int* abort_f = &ms.abort_;
+
+  if (warp >= 8) {
+    // ------------------------------------------------------------ dequantisation
+    // thread d: tokens 32 it + d / 8 (it = 0..3), 16-byte chunk d % 8 of every
+    // 64-coordinate chunk (coordinates 64 kc + 8 (d % 8) .. + 7)
+    const int d = tid - 256, c16 = d & 7, tk = d >> 3;
+    constexpr int RBK = D * KB / 8, RBV = D * VB / 8;
+    uint32_t kw[8][4], vw[8][4], kn[8][4];
+    auto load_k = [&](uint32_t (&w)[8][4], int rec) {
+      const uint8_t* base = kb0 + (int64_t)(c_begin + rec) * p.krec_bytes;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) w[kc][it] = group_word<KB>(base + (32 * it + tk) * RBK, 8 * kc + c16);
+    };
+    auto load_v = [&](uint32_t (&w)[8][4], int rec) {
+      const uint8_t* base = vb0 + (int64_t)(c_begin + rec) * p.vrec_bytes;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) w[kc][it] = group_word<VB>(base + (32 * it + tk) * RBV, 8 * kc + c16);
+    };
+    uint32_t g = 0;  // stages handed over so far
+    auto acquire = [&]() -> unsigned char* {
+      const uint32_t slot = g & 1;
+      mbar_wait(&ms.empty[slot], ((g >> 1) & 1) ^ 1, abort_f);
+      return sm + kURing + slot * 32768;
+    };
+    auto release = [&]() {
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.full[g & 1]);
+    };
+    // MMA issue (warp 8, lane 0): waits until all eight warps have written stage g
+    const bool issuer = warp == 8 && lane == 0;
+    const uint32_t qa = smem_u32(sm + kUQ), pa = smem_u32(sm + kUP), ra = smem_u32(sm + kURing);
+    auto stage_in = [&]() -> uint32_t {
+      const uint32_t slot = g & 1;
+      mbar_wait(&ms.full[slot], (g >> 1) & 1, abort_f);
+      tc_fence_after();
+      return ra + slot * 32768;
+    };
+    auto issue_scores = [&](int kc) {
+      constexpr uint32_t IS128 = idesc_f16(128, 128, false, false);
+      constexpr uint32_t IS64 = idesc_f16(128, 64, false, false);
+      const uint32_t st = stage_in();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t bq = sdesc_sw128(qa + kc * 16384 + 32 * ks, 16, 1024);
+        umma_f16(tS, sdesc_sw128(st + 32 * ks, 16, 1024), bq, IS128, (kc | ks) != 0);
+        umma_f16(tS, sdesc_sw128(st + 16384 + 32 * ks, 16, 1024), bq, IS64, 1);
+      }
+      umma_commit(&ms.empty[g & 1]);
+    };
+    auto issue_values = [&](int j, int part, bool first) {
+      constexpr uint32_t IV = idesc_f16(128, 64, true, true);
+      const uint32_t st = stage_in();
+      const uint32_t dO = tO + 64 * j;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t a = sdesc_sw128(st + 2048 * ks, 16384, 1024);
+        const uint64_t bh = sdesc_sw128(pa + 2048 * ks, 1024, 1024);
+        if (part == 0) {
+          umma_f16(dO, a, bh, IV, !(first && ks == 0));
+          umma_f16(dO, a, sdesc_sw128(pa + 16384 + 2048 * ks, 1024, 1024), IV, 1);
+        } else {
+          umma_f16(dO, a, bh, IV, 1);
+        }
+      }
+      umma_commit(&ms.empty[g & 1]);
+    };
+    load_k(kw, 0);
+    for (int r = 0; r < n; ++r) {
+      load_v(vw, r);
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        unsigned char* st = acquire();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          uint4 hi, lo;
+          deq8<KB>(kw[kc][it], ms.ctab_k, hi, lo);
+          const uint32_t o = sw128_off(32 * it + tk, c16);
+          *reinterpret_cast<uint4*>(st + o) = hi;
+          *reinterpret_cast<uint4*>(st + 16384 + o) = lo;
+        }
+        release();
+        if (issuer) {
+          issue_scores(kc);
+          if (kc == 7) umma_commit(&ms.s_full);
+        }
+        ++g;
+      }
+      if (r + 1 < n) load_k(kn, r + 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          unsigned char* st = acquire();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+              uint4 hi, lo;
+              deq8<VB>(vw[2 * j + hh][it], ms.ctab_v, hi, lo);
+              *reinterpret_cast<uint4*>(st + hh * 16384 + sw128_off(32 * it + tk, c16)) = part ? lo : hi;
+            }
+          release();
+          if (issuer) {
+            if (j == 0 && part == 0) {  // P' of this record is in shared memory
+              mbar_wait(&ms.p_full, r & 1, abort_f);
+              tc_fence_after();
+            }
+            issue_values(j, part, r == 0);
+            if (j == 3 && part == 1) umma_commit(&ms.o_done);
+          }
+          ++g;
+        }
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) kw[kc][it] = kn[kc][it];
+    }
+    if (issuer) umma_commit(&ms.fin);
+  } else {
+    // ------------------------------------------------------------ softmax, epilogue
+    const int q = warp & 3, hh = warp >> 2;
+    const int tok = 32 * q + lane;
+    const uint32_t lrow = (uint32_t)(32 * q) << 16;
+    float lacc = 0.f;  // softmax denominator of head 32 hh + lane over this warp's tokens
+    int kx = 127;  // P' scale exponent (only decreases)
+    auto norm_at = [&](const uint8_t* base, int bytes, int off, int rec) {
+      return __ldg(reinterpret_cast<const float*>(base + (int64_t)(c_begin + rec) * bytes + off) + tok);
+    };
+    float nk = norm_at(kb0, p.krec_bytes, p.k_off_norm, 0);
+    float nv = norm_at(vb0, p.vrec_bytes, p.v_off_norm, 0);
+    for (int r = 0; r < n; ++r) {
+      float nk1 = 0.f, nv1 = 0.f;
+      if (r + 1 < n) {
+        nk1 = norm_at(kb0, p.krec_bytes, p.k_off_norm, r + 1);
+        nv1 = norm_at(vb0, p.vrec_bytes, p.v_off_norm, r + 1);
+      }
+      mbar_wait(&ms.s_full, r & 1, abort_f);
+      tc_fence_after();
+      float t[32];
+      bool need = false;
+      {
+        uint32_t a[32], c[32];
+        tmem_ld32(tS + lrow + 32 * hh, a);
+        tmem_ld32(tS + lrow + 64 + 32 * hh, c);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int h = 32 * hh + i;
+          t[i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
+          need |= t[i] > ms.mst[h] + 8.f;
+        }
+      }
+      if (nv > 0.f && 6 - exp_of(nv) < kx) need = true;
+      bool owaited = false;
+      if (bar_or(1, 256, need)) {
+        // new running max per head (moves only past the 2^8 margin), rescale
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = t[i];
+        ms.red[q][32 * hh + lane] = transpose_reduce<true>(v, lane);
+        const float vm = warp_max(nv);
+        if (lane == 0) ms.vmx[warp] = vm;
+        bar_sync(1, 256);
+        if (q == 0) {
+          const int h = 32 * hh + lane;
+          const float mx = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+          const float mo = ms.mst[h];
+          const float mn = mx > mo + 8.f ? mx : mo;
+          ms.scl[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+          ms.mst[h] = mn;
+        }
+        float vmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) vmax = fmaxf(vmax, ms.vmx[w]);
+        int kn = kx;
+        if (vmax > 0.f) kn = min(kx, 6 - exp_of(vmax));
+        const float gamma = pow2i(kn - kx);
+        bar_sync(1, 256);
+        lacc *= ms.scl[32 * hh + lane];
+        if (r > 0) {
+          mbar_wait(&ms.o_done, (r - 1) & 1, abort_f);
+          tc_fence_after();
+          owaited = true;
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t o[32];
+            tmem_ld32(tO + lrow + 64 * j + 32 * hh, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * (ms.scl[32 * hh + i] * gamma));
+            tmem_st32(tO + lrow + 64 * j + 32 * hh, o);
+          }
+          tmem_st_wait();
+        }
+        kx = kn;
+      }
+      if (r > 0 && !owaited) {
+        mbar_wait(&ms.o_done, (r - 1) & 1, abort_f);
+        tc_fence_after();
+      }
+      // P' (hi, lo) of this token's 32 heads: row `tok` of the MN-major operand
+      {
+        const float vs = nv * pow2i(kx);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[i] = t[i] == -INFINITY ? 0.f : exp2f(t[i] - ms.mst[32 * hh + i]);
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) split_f16x2(t[2 * i] * vs, t[2 * i + 1] * vs, ph[i], pl[i]);
+        unsigned char* pb = sm + kUP;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t o = sw128_off(tok, 4 * hh + k);
+          *reinterpret_cast<uint4*>(pb + o) = make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
+          *reinterpret_cast<uint4*>(pb + 16384 + o) = make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.p_full);
+      lacc += transpose_reduce<false>(t, lane);
+      nk = nk1;
+      nv = nv1;
+    }
+    mbar_wait(&ms.o_done, (n - 1) & 1, abort_f);
+    tc_fence_after();
+    // the split's partial: softmax denominators and O^T (rotated basis)
+    ms.red[q][32 * hh + lane] = lacc;
+    bar_sync(1, 256);
+    const float un = pow2i(-16 - kx);
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o[32];
+      tmem_ld32(tO + lrow + 64 * j + 32 * hh, o);
+      tmem_ld_wait();
+      float* dst = p.ws_acc + ((qh0 + 32 * hh) * p.S + split) * D + 128 * j + tok;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (32 * hh + i < GT) dst[(int64_t)i * p.S * D] = __uint_as_float(o[i]) * un;
+    }
+    if (q == 0) {
+      const int h = 32 * hh + lane;
+      if (h < GT) {
+        float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+        ml[0] = ms.mst[h];
+        ml[1] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 8) {
+    // every MMA has completed (drain bounded independently of the abort flag)
+    volatile int drain = 0;
+    mbar_wait(&ms.fin, 0, &drain);
+    tc_fence_after();
+    tmem_dealloc(ms.tbase, 512);
+    if (lane == 0 && (*abort_f || drain)) set_status(p, 1);
+  }
+}
+
+template <int KB, int VB>
+cudaError_t attn_umma512_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_umma512_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e != cudaSuccess) return e;
+  attn_umma512_kernel<KB, VB><<<grid, kU512Threads, kUSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

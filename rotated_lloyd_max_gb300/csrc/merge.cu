@@ -68,6 +68,10 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
   }
   __syncthreads();
   if (warp != 0) return;
+  if (p.status && *reinterpret_cast<const volatile int*>(p.status) != 0) {  // failed launch: NaN row
+    for (int j = lane; j < D; j += 32) out[j] = __int_as_float(0x7fc00000);
+    return;
+  }
   if (!(W > 0.f)) {  // empty context: zero row
     for (int j = lane; j < D; j += 32) out[j] = 0.f;
     return;
@@ -151,6 +155,21 @@ cudaError_t launch_attn_mma512_k1(const AttnParams& p, dim3 grid, cudaStream_t s
 cudaError_t launch_attn_mma512_k2(const AttnParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_mma512_k3(const AttnParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_mma512_k4(const AttnParams& p, dim3 grid, cudaStream_t s);
+
+cudaError_t launch_attn_umma512_k1(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_umma512_k2(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_umma512_k3(const AttnParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_umma512_k4(const AttnParams& p, dim3 grid, cudaStream_t s);
+
+cudaError_t launch_attn_umma512(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  switch (p.kb) {
+    case 1: return launch_attn_umma512_k1(p, grid, s);
+    case 2: return launch_attn_umma512_k2(p, grid, s);
+    case 3: return launch_attn_umma512_k3(p, grid, s);
+    case 4: return launch_attn_umma512_k4(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_attn_mma512(const AttnParams& p, dim3 grid, cudaStream_t s) {
   switch (p.kb) {

@@ -86,6 +86,7 @@ struct AttnParams {
   int split_base;  // index of the first split a launch covers (dense-only launches)
   float* ws_acc;
   float* ws_ml;
+  int* status;  // sticky launch status in the workspace (nonzero: a bounded wait expired)
   // dynamic shared memory carve-up (bytes)
   int sm_q, sm_lut, sm_red, sm_logit, sm_main, sm_stage, sm_ent, sm_ent_stage, sm_pre, sm_slot,
       sm_corr, sm_kpair, sm_vpair, sm_total;
@@ -96,6 +97,7 @@ struct MergeParams {
   const float* ws_ml;
   float* out;
   int rows, S, Sc;
+  const int* status;  // nonzero: the attention launch failed, outputs are NaN (may be null)
   float inv_sqrt_d;
   uint32_t vsign[16];
 };
@@ -114,6 +116,9 @@ cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaS
 cudaError_t launch_attn_mma(const AttnParams& p, int D, dim3 grid, cudaStream_t s);
 // tensor-core kernel for the compressed splits at head dim 512 (256 threads)
 cudaError_t launch_attn_mma512(const AttnParams& p, dim3 grid, cudaStream_t s);
+// tcgen05 kernel for the compressed splits at head dim 512, up to 64 heads per CTA
+cudaError_t launch_attn_umma512(const AttnParams& p, dim3 grid, cudaStream_t s);
+int attn_umma512_smem();
 cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 
 // Dynamic shared memory of the attention kernel for head dim D and head group GT

@@ -154,11 +154,48 @@ def test_tensor_core_bit_widths(tq, orc, d, kb, vb):
 @pytest.mark.parametrize("kb,vb,G,shared", [(4, 4, 64, True), (2, 3, 4, False), (3, 1, 8, False), (1, 2, 6, False),
                                              (3, 3, 32, False)])
 def test_tensor_core_d512(tq, orc, kb, vb, G, shared):
-    """Head dim 512 on its tensor-core kernel (8 query heads per CTA), with a
-    dense tail on the general kernel."""
+    """Head dim 512 on its mma.sync kernel (8 or 16 query heads per CTA), with
+    a dense tail on the general kernel."""
     got, want, _ = run_case(tq, orc, d=512, G=G, Hkv=1, B=1, L=1, chunks=[3], tails=[40], kb=kb, vb=kb if shared else vb,
-                            shared=shared, end_to_end=False, seed=kb * 10 + vb + G)
+                            shared=shared, end_to_end=False, seed=kb * 10 + vb + G, cuda_core_path=2)
     _assert_close(got, want)
+
+
+@pytest.mark.parametrize("kb,vb,G,shared,chunks", [(4, 4, 64, True, [3]), (1, 1, 16, False, [2]),
+                                                    (2, 4, 48, False, [2]), (4, 2, 64, False, [4]),
+                                                    (3, 3, 64, True, [2]), (3, 2, 32, False, [1]),
+                                                    (4, 4, 128, True, [2])])
+def test_tcgen05_d512(tq, orc, kb, vb, G, shared, chunks):
+    """Head dim 512 with 16-128 query heads per kv head on the tcgen05 kernel
+    (64 heads per CTA, scores and outputs in tensor memory); dense tail on the
+    general kernel."""
+    got, want, _ = run_case(tq, orc, d=512, G=G, Hkv=1, B=1, L=1, chunks=chunks, tails=[40], kb=kb,
+                            vb=kb if shared else vb, shared=shared, end_to_end=False, seed=kb * 7 + vb + G)
+    _assert_close(got, want)
+
+
+def test_tcgen05_d512_multi_record_splits(tq, orc):
+    """Several records per CTA (the ring's phases wrap, the running max moves
+    lazily) on two batches and layers; one split per unit and three splits
+    give the same result."""
+    cfg = dict(d=512, G=64, Hkv=1, B=2, L=2, chunks=[6, 3], tails=[17, 0], kb=4, vb=4, shared=True,
+               end_to_end=False, seed=5)
+    a, want, _ = run_case(tq, orc, splits=1, **cfg)
+    b, _, _ = run_case(tq, orc, splits=3, **cfg)
+    _assert_close(a, want)
+    _assert_close(b, want)
+    assert np.max(np.abs(a - b)) <= 1e-5
+
+
+def test_tcgen05_d512_matches_mma_sync(tq, orc):
+    """The tcgen05 and mma.sync kernels agree (same operand splits) and both
+    meet the oracle, with two kv heads and separate K/V codecs."""
+    cfg = dict(d=512, G=32, Hkv=2, B=1, L=1, chunks=[3], tails=[0], kb=3, vb=2, end_to_end=False, seed=9)
+    a, want, _ = run_case(tq, orc, **cfg)
+    b, _, _ = run_case(tq, orc, cuda_core_path=2, **cfg)
+    _assert_close(a, want)
+    _assert_close(b, want)
+    assert np.max(np.abs(a - b)) <= 1e-4
 
 
 def test_dense_boundary_layers(tq, orc):
