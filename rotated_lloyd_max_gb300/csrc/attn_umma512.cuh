@@ -13,23 +13,25 @@
 //    B_q = [q~_hi (64 rows) | q~_lo (64 rows)] (N = 128, K-major, resident in
 //    shared memory) plus K~_lo . q~_hi (N = 64) into the same accumulator, so
 //    head h's logit is column h + column 64 + h of the token's TMEM lane;
-//  * softmax: a thread owns one token (its TMEM lane) and 32 heads; the
-//    running max per head moves only when a logit passes it by 2^8 (or the
-//    record's largest V norm needs a smaller P' scale), which is the one step
-//    that reduces across tokens and rescales the output accumulator;
+//    two score buffers let a record's scores run while the previous record's
+//    softmax is computed;
+//  * softmax: a thread owns one token (its TMEM lane) and all 64 heads, in two
+//    halves of 32; the running max per head moves only when a logit passes it
+//    by 2^8 (or the record's largest V norm needs a smaller P' scale), which is
+//    the one step that reduces across tokens and rescales the accumulator;
 //  * values: O^T[coordinate][head] += V~^T . P' for four 128-coordinate
 //    blocks (A = the dequantised record, MN-major; B = P', MN-major, N = 64);
 //    O^T stays in tensor memory for the whole split.
 //
-// Warp roles (512 threads, four warps per SM sub-partition): warps 0-7
-// softmax and epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31, heads
-// 32 (w / 4) .. + 31); warps 8-15 dequantise records into a two-stage ring of
-// 32 KB operand tiles (16 stages per record: 8 score chunks of 64
-// coordinates, hi and lo; 8 value blocks of 128 coordinates, hi or lo); warp 8
-// also allocates tensor memory and its lane 0 issues each stage's MMAs once
-// all eight warps have written it.  Stages, scores, P' and outputs are handed over
-// through mbarriers; every wait is bounded and a CTA whose wait expires sets
-// the launch's status word and finishes without further waiting.
+// Warp roles (640 threads, five warps per SM sub-partition): warps 0-3 softmax
+// and epilogue (warp w reads TMEM lanes 32 w .. 32 w + 31); warps 4-19
+// dequantise records into a two-stage ring of 32 KB operand tiles (16 stages
+// per record: 8 score chunks of 64 coordinates, hi and lo; 8 value blocks of
+// 128 coordinates, hi or lo); warp 4 also allocates tensor memory and its lane
+// 0 issues each stage's MMAs once all sixteen warps have written it.  Stages,
+// scores, P' and outputs are handed over through mbarriers; every wait is
+// bounded and a CTA whose wait expires sets the launch's status word and
+// finishes without further waiting.
 #pragma once
 
 #include "attn_mma.cuh"
@@ -37,7 +39,9 @@
 
 namespace tq {
 
-constexpr int kU512Threads = 512;
+constexpr int kU512Threads = 640;
+constexpr int kUSoftWarps = 4;
+constexpr int kUDeqWarps = 16;
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kUQ = 0;          // q~ operand: [8 chunks of 64 coordinates][128 rows][128 B]
 constexpr int kUP = 131072;     // P' operand: hi [128 tokens][64 heads f16] | lo
@@ -46,16 +50,15 @@ constexpr int kUMisc = 229376;
 constexpr int kUSmem = kUMisc + 2048 + 1024;  // + bookkeeping + alignment slack
 
 struct U512Misc {
-  uint64_t full[2], empty[2], s_full, p_full, o_done, fin;
+  uint64_t full[2], empty[2], s_full[2], p_full, o_done, fin;
   uint32_t tbase;
   int abort_;
-  int pad[2];
   uint32_t ctab_k[16], ctab_v[16];  // centroid x 2^16 as f16 {hi, lo} per code
   float qsc[64];                    // per head: softmax scale * log2(e) * 2^(-16 - s)
   float mst[64];                    // running max per head (log2 units)
   float scl[64];                    // output rescale per head (slow path)
   float red[4][64];                 // cross-quarter reductions
-  float vmx[8];
+  float vmx[4];
 };
 static_assert(sizeof(U512Misc) <= 2048, "bookkeeping block");
 
@@ -71,22 +74,6 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
 }
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// 8 codes of B bits: the m-th 8-code group of a packed row (B bytes)
-template <int B>
-__device__ __forceinline__ uint32_t group_word(const uint8_t* row, int m) {
-  if constexpr (B == 4) {
-    return __ldg(reinterpret_cast<const uint32_t*>(row) + m);
-  } else if constexpr (B == 2) {
-    return __ldg(reinterpret_cast<const uint16_t*>(row) + m);
-  } else if constexpr (B == 1) {
-    return __ldg(row + m);
-  } else {  // 3 bytes at 3m: two aligned words (the second may lie in the next row or the norms)
-    const int o = 3 * m;
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + (o & ~3));
-    return __funnelshift_r(__ldg(w), __ldg(w + 1), 8 * (o & 3)) & 0xFFFFFFu;
-  }
 }
 
 // dequantise 8 codes into f16x2 hi / lo words (coordinate 2i in the low half)
@@ -116,6 +103,71 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
     }
   }
   return v[0];
+}
+
+// Phase ph of a split of n records: S(0), then per record r S(r + 1) (when
+// r + 1 < n) and V(r).  kind 0 = scores, 1 = values.
+__device__ __forceinline__ void umma_phase(int ph, int n, int& kind, int& rec) {
+  if (ph == 0) {
+    kind = 0;
+    rec = 0;
+    return;
+  }
+  const int q = ph - 1, r = q >> 1;
+  if ((q & 1) == 0 && r + 1 < n) {
+    kind = 0;
+    rec = r + 1;
+  } else {
+    kind = 1;
+    rec = r;
+  }
+}
+
+// loads issued where they stand (the compiler does not sink them to their use)
+__device__ __forceinline__ uint32_t ldg_keep(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_keep16(const void* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ldg_keep2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+// words holding the 16-code unit u (coordinates 16 u .. 16 u + 15) of a packed row
+template <int B>
+__device__ __forceinline__ void load_unit(uint32_t (&w)[2], const uint8_t* row, int u) {
+  if constexpr (B == 4) {
+    const uint2 v = ldg_keep2(row + 8 * u);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else if constexpr (B == 2) {
+    w[0] = ldg_keep(row + 4 * u);
+  } else if constexpr (B == 1) {
+    w[0] = ldg_keep16(row + 2 * u);
+  } else {  // 6 bytes at 6u: the two words from 4-aligned (6u & ~3), still inside the row
+    const uint32_t* a = reinterpret_cast<const uint32_t*>(row + ((6 * u) & ~3));
+    w[0] = ldg_keep(a);
+    w[1] = ldg_keep(a + 1);
+  }
+}
+// codes 8 c .. 8 c + 7 (c = 0, 1) of the unit; sh = the unit's bit offset in w
+// (nonzero only for 3-bit codes)
+template <int B>
+__device__ __forceinline__ uint32_t codes8(const uint32_t (&w)[2], int c, int sh) {
+  if constexpr (B == 4) {
+    return w[c];
+  } else if constexpr (B == 3) {
+    const int o = sh + 24 * c;
+    return o < 32 ? __funnelshift_r(w[0], w[1], o) : (w[1] >> (o - 32));
+  } else {
+    return w[0] >> (8 * B * c);
+  }
 }
 
 __device__ __forceinline__ void set_status(const AttnParams& p, int code) {
@@ -159,17 +211,17 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms.full[i], 8);
+      mbar_init(&ms.full[i], kUDeqWarps);
       mbar_init(&ms.empty[i], 1);
+      mbar_init(&ms.s_full[i], 1);
     }
-    mbar_init(&ms.s_full, 1);
-    mbar_init(&ms.p_full, 8);
+    mbar_init(&ms.p_full, kUSoftWarps);
     mbar_init(&ms.o_done, 1);
     mbar_init(&ms.fin, 1);
     ms.abort_ = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 8) tmem_alloc(&ms.tbase, 512);
+  if (warp == kUSoftWarps) tmem_alloc(&ms.tbase, 512);
   if (tid < 32) {
     const int e = tid & 15, bits = tid < 16 ? KB : VB;
     const float v = e < (1 << bits) ? (tid < 16 ? p.kc[e] : p.vc[e]) * 65536.f : 0.f;
@@ -225,30 +277,33 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = ms.tbase;        // scores: 128 columns
-  const uint32_t tO = ms.tbase + 128;  // O^T: 4 blocks x 64 columns
+  const uint32_t tS = ms.tbase;        // scores: two buffers of 128 columns
+  const uint32_t tO = ms.tbase + 256;  // O^T: 4 blocks x 64 columns
   volatile int* abort_f = &ms.abort_;
 
-  if (warp >= 8) {
+  if (warp >= kUSoftWarps) {
     // ------------------------------------------------------------ dequantisation
-    // thread d: tokens 32 it + d / 8 (it = 0..3), 16-byte chunk d % 8 of every
-    // 64-coordinate chunk (coordinates 64 kc + 8 (d % 8) .. + 7)
-    const int d = tid - 256, c16 = d & 7, tk = d >> 3;
-    constexpr int RBK = D * KB / 8, RBV = D * VB / 8;
-    uint32_t kw[8][4], vw[8][4], kn[8][4];
-    auto load_k = [&](uint32_t (&w)[8][4], int rec) {
-      const uint8_t* base = kb0 + (int64_t)(c_begin + rec) * p.krec_bytes;
+    // Thread d owns token d / 4 and its 16-coordinate units u = 4 i + d % 4
+    // (i = 0..7): unit i feeds score chunk i (coordinates 64 i + 16 (d % 4) ..)
+    // and half i % 2 of value block i / 2, so the words loaded for a record
+    // serve both of its passes.  Phases run in the order S(0), S(1), V(0),
+    // S(2), V(1), ..., S(n-1), V(n-2), V(n-1) (scores one record ahead, into
+    // alternating score buffers); each phase's words are loaded one phase ahead.
+    const int d = tid - 32 * kUSoftWarps, tkn = d >> 2, sub = d & 3;
+    const int shk = KB == 3 ? 16 * (sub & 1) : 0, shv = VB == 3 ? 16 * (sub & 1) : 0;
+    uint32_t cur[8][2], nxt[8][2];
+    auto load_phase = [&](uint32_t (&w)[8][2], int ph) {
+      int kind, rec;
+      umma_phase(ph, n, kind, rec);
+      if (kind == 0) {
+        const uint8_t* row = kb0 + (int64_t)(c_begin + rec) * p.krec_bytes + tkn * (D * KB / 8);
 #pragma unroll
-      for (int kc = 0; kc < 8; ++kc)
+        for (int i = 0; i < 8; ++i) load_unit<KB>(w[i], row, 4 * i + sub);
+      } else {
+        const uint8_t* row = vb0 + (int64_t)(c_begin + rec) * p.vrec_bytes + tkn * (D * VB / 8);
 #pragma unroll
-        for (int it = 0; it < 4; ++it) w[kc][it] = group_word<KB>(base + (32 * it + tk) * RBK, 8 * kc + c16);
-    };
-    auto load_v = [&](uint32_t (&w)[8][4], int rec) {
-      const uint8_t* base = vb0 + (int64_t)(c_begin + rec) * p.vrec_bytes;
-#pragma unroll
-      for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-        for (int it = 0; it < 4; ++it) w[kc][it] = group_word<VB>(base + (32 * it + tk) * RBV, 8 * kc + c16);
+        for (int i = 0; i < 8; ++i) load_unit<VB>(w[i], row, 4 * i + sub);
+      }
     };
     uint32_t g = 0;  // stages handed over so far
     auto acquire = [&]() -> unsigned char* {
@@ -261,105 +316,127 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.full[g & 1]);
     };
-    // MMA issue (warp 8, lane 0): waits until all eight warps have written stage g
-    const bool issuer = warp == 8 && lane == 0;
-    const uint32_t qa = smem_u32(sm + kUQ), pa = smem_u32(sm + kUP), ra = smem_u32(sm + kURing);
-    auto stage_in = [&]() -> uint32_t {
-      const uint32_t slot = g & 1;
-      mbar_wait(&ms.full[slot], (g >> 1) & 1, abort_f);
+    // MMA issue (warp 4, lane 0): waits until all sixteen warps have written
+    // stage g.  Descriptors are built once; a byte offset o moves one by o / 16.
+    const bool issuer = warp == kUSoftWarps && lane == 0;
+    const uint32_t ra = smem_u32(sm + kURing);
+    const uint64_t dQ = sdesc_sw128(smem_u32(sm + kUQ), 16, 1024);
+    const uint64_t dP = sdesc_sw128(smem_u32(sm + kUP), 1024, 1024);
+    const uint64_t dK0 = sdesc_sw128(ra, 16, 1024), dK1 = sdesc_sw128(ra + 32768, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(ra, 16384, 1024), dV1 = sdesc_sw128(ra + 32768, 16384, 1024);
+    auto stage_in = [&]() {
+      mbar_wait(&ms.full[g & 1], (g >> 1) & 1, abort_f);
       tc_fence_after();
-      return ra + slot * 32768;
     };
-    auto issue_scores = [&](int kc) {
+    auto issue_scores = [&](int kc, uint32_t dS) {
       constexpr uint32_t IS128 = idesc_f16(128, 128, false, false);
       constexpr uint32_t IS64 = idesc_f16(128, 64, false, false);
-      const uint32_t st = stage_in();
+      stage_in();
+      const uint64_t a = (g & 1) ? dK1 : dK0;
+      const uint64_t bq = dQ + (uint64_t)(kc * 1024);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t bq = sdesc_sw128(qa + kc * 16384 + 32 * ks, 16, 1024);
-        umma_f16(tS, sdesc_sw128(st + 32 * ks, 16, 1024), bq, IS128, (kc | ks) != 0);
-        umma_f16(tS, sdesc_sw128(st + 16384 + 32 * ks, 16, 1024), bq, IS64, 1);
+        umma_f16(dS, a + 2 * ks, bq + 2 * ks, IS128, (kc | ks) != 0);
+        umma_f16(dS, a + 1024 + 2 * ks, bq + 2 * ks, IS64, 1);
       }
       umma_commit(&ms.empty[g & 1]);
     };
     auto issue_values = [&](int j, int part, bool first) {
       constexpr uint32_t IV = idesc_f16(128, 64, true, true);
-      const uint32_t st = stage_in();
+      stage_in();
+      const uint64_t a = (g & 1) ? dV1 : dV0;
       const uint32_t dO = tO + 64 * j;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t a = sdesc_sw128(st + 2048 * ks, 16384, 1024);
-        const uint64_t bh = sdesc_sw128(pa + 2048 * ks, 1024, 1024);
         if (part == 0) {
-          umma_f16(dO, a, bh, IV, !(first && ks == 0));
-          umma_f16(dO, a, sdesc_sw128(pa + 16384 + 2048 * ks, 1024, 1024), IV, 1);
+          umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, !(first && ks == 0));
+          umma_f16(dO, a + 128 * ks, dP + 1024 + 128 * ks, IV, 1);
         } else {
-          umma_f16(dO, a, bh, IV, 1);
+          umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, 1);
         }
       }
       umma_commit(&ms.empty[g & 1]);
     };
-    load_k(kw, 0);
-    for (int r = 0; r < n; ++r) {
-      load_v(vw, r);
+    load_phase(cur, 0);
+    for (int ph = 0; ph < 2 * n; ++ph) {
+      int kind, rec;
+      umma_phase(ph, n, kind, rec);
+      if (ph + 1 < 2 * n) load_phase(nxt, ph + 1);
+      if (kind == 0) {
+        // score chunk i: row tkn, 16-byte chunks 2 sub, 2 sub + 1 of its hi and lo tiles
 #pragma unroll
-      for (int kc = 0; kc < 8; ++kc) {
-        unsigned char* st = acquire();
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          uint4 hi, lo;
-          deq8<KB>(kw[kc][it], ms.ctab_k, hi, lo);
-          const uint32_t o = sw128_off(32 * it + tk, c16);
-          *reinterpret_cast<uint4*>(st + o) = hi;
-          *reinterpret_cast<uint4*>(st + 16384 + o) = lo;
-        }
-        release();
-        if (issuer) {
-          issue_scores(kc);
-          if (kc == 7) umma_commit(&ms.s_full);
-        }
-        ++g;
-      }
-      if (r + 1 < n) load_k(kn, r + 1);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int i = 0; i < 8; ++i) {
           unsigned char* st = acquire();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-              uint4 hi, lo;
-              deq8<VB>(vw[2 * j + hh][it], ms.ctab_v, hi, lo);
-              *reinterpret_cast<uint4*>(st + hh * 16384 + sw128_off(32 * it + tk, c16)) = part ? lo : hi;
-            }
+          for (int c = 0; c < 2; ++c) {
+            uint4 hi, lo;
+            deq8<KB>(codes8<KB>(cur[i], c, shk), ms.ctab_k, hi, lo);
+            const uint32_t o = sw128_off(tkn, 2 * sub + c);
+            *reinterpret_cast<uint4*>(st + o) = hi;
+            *reinterpret_cast<uint4*>(st + 16384 + o) = lo;
+          }
           release();
           if (issuer) {
-            if (j == 0 && part == 0) {  // P' of this record is in shared memory
-              mbar_wait(&ms.p_full, r & 1, abort_f);
-              tc_fence_after();
-            }
-            issue_values(j, part, r == 0);
-            if (j == 3 && part == 1) umma_commit(&ms.o_done);
+            issue_scores(i, tS + 128 * (rec & 1));
+            if (i == 7) umma_commit(&ms.s_full[rec & 1]);
           }
           ++g;
         }
+      } else {
+        // value block j: unit 2 j + e -> half e, chunks 2 sub, 2 sub + 1
 #pragma unroll
-      for (int kc = 0; kc < 8; ++kc)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int it = 0; it < 4; ++it) kw[kc][it] = kn[kc][it];
+          for (int part = 0; part < 2; ++part) {
+            unsigned char* st = acquire();
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint4 hi, lo;
+                deq8<VB>(codes8<VB>(cur[2 * j + e], c, shv), ms.ctab_v, hi, lo);
+                *reinterpret_cast<uint4*>(st + e * 16384 + sw128_off(tkn, 2 * sub + c)) = part ? lo : hi;
+              }
+            release();
+            if (issuer) {
+              if (j == 0 && part == 0) {  // P' of this record is in shared memory
+                mbar_wait(&ms.p_full, rec & 1, abort_f);
+                tc_fence_after();
+              }
+              issue_values(j, part, rec == 0);
+              if (j == 3 && part == 1) umma_commit(&ms.o_done);
+            }
+            ++g;
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cur[i][0] = nxt[i][0];
+        cur[i][1] = nxt[i][1];
+      }
     }
     if (issuer) umma_commit(&ms.fin);
   } else {
     // ------------------------------------------------------------ softmax, epilogue
-    const int q = warp & 3, hh = warp >> 2;
+    const int q = warp;  // TMEM lane quarter
     const int tok = 32 * q + lane;
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
-    float lacc = 0.f;  // softmax denominator of head 32 hh + lane over this warp's tokens
-    int kx = 127;  // P' scale exponent (only decreases)
+    float lacc[2] = {0.f, 0.f};  // softmax denominators of heads lane and 32 + lane over this warp's tokens
+    int kx = 127;                // P' scale exponent (only decreases)
     auto norm_at = [&](const uint8_t* base, int bytes, int off, int rec) {
       return __ldg(reinterpret_cast<const float*>(base + (int64_t)(c_begin + rec) * bytes + off) + tok);
+    };
+    // logits of heads 32 hh .. 32 hh + 31 of this token (-inf past the group)
+    auto logits = [&](uint32_t tSr, int hh, float nk, float (&t)[32]) {
+      uint32_t a[32], c[32];
+      tmem_ld32(tSr + lrow + 32 * hh, a);
+      tmem_ld32(tSr + lrow + 64 + 32 * hh, c);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int h = 32 * hh + i;
+        t[i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
+      }
     };
     float nk = norm_at(kb0, p.krec_bytes, p.k_off_norm, 0);
     float nv = norm_at(vb0, p.vrec_bytes, p.v_off_norm, 0);
@@ -369,61 +446,61 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
         nk1 = norm_at(kb0, p.krec_bytes, p.k_off_norm, r + 1);
         nv1 = norm_at(vb0, p.vrec_bytes, p.v_off_norm, r + 1);
       }
-      mbar_wait(&ms.s_full, r & 1, abort_f);
+      mbar_wait(&ms.s_full[r & 1], (r >> 1) & 1, abort_f);
       tc_fence_after();
-      float t[32];
-      bool need = false;
-      {
-        uint32_t a[32], c[32];
-        tmem_ld32(tS + lrow + 32 * hh, a);
-        tmem_ld32(tS + lrow + 64 + 32 * hh, c);
-        tmem_ld_wait();
+      const uint32_t tSr = tS + 128 * (r & 1);
+      bool need = nv > 0.f && 6 - exp_of(nv) < kx;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float t[32];
+        logits(tSr, hh, nk, t);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = 32 * hh + i;
-          t[i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
-          need |= t[i] > ms.mst[h] + 8.f;
-        }
+        for (int i = 0; i < 32; ++i) need |= t[i] > ms.mst[32 * hh + i] + 8.f;
       }
-      if (nv > 0.f && 6 - exp_of(nv) < kx) need = true;
       bool owaited = false;
-      if (bar_or(1, 256, need)) {
+      if (bar_or(1, 32 * kUSoftWarps, need)) {
         // new running max per head (moves only past the 2^8 margin), rescale
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = t[i];
-        ms.red[q][32 * hh + lane] = transpose_reduce<true>(v, lane);
-        const float vm = warp_max(nv);
-        if (lane == 0) ms.vmx[warp] = vm;
-        bar_sync(1, 256);
-        if (q == 0) {
-          const int h = 32 * hh + lane;
-          const float mx = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-          const float mo = ms.mst[h];
-          const float mn = mx > mo + 8.f ? mx : mo;
-          ms.scl[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-          ms.mst[h] = mn;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float t[32];
+          logits(tSr, hh, nk, t);
+          ms.red[q][32 * hh + lane] = transpose_reduce<true>(t, lane);
         }
-        float vmax = 0.f;
+        const float vm = warp_max(nv);
+        if (lane == 0) ms.vmx[q] = vm;
+        bar_sync(1, 32 * kUSoftWarps);
+        if (q == 0) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) vmax = fmaxf(vmax, ms.vmx[w]);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int h = 32 * hh + lane;
+            const float mx = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+            const float mo = ms.mst[h];
+            const float mn = mx > mo + 8.f ? mx : mo;
+            ms.scl[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+            ms.mst[h] = mn;
+          }
+        }
+        const float vmax = fmaxf(fmaxf(ms.vmx[0], ms.vmx[1]), fmaxf(ms.vmx[2], ms.vmx[3]));
         int kn = kx;
         if (vmax > 0.f) kn = min(kx, 6 - exp_of(vmax));
         const float gamma = pow2i(kn - kx);
-        bar_sync(1, 256);
-        lacc *= ms.scl[32 * hh + lane];
+        bar_sync(1, 32 * kUSoftWarps);
+        lacc[0] *= ms.scl[lane];
+        lacc[1] *= ms.scl[32 + lane];
         if (r > 0) {
           mbar_wait(&ms.o_done, (r - 1) & 1, abort_f);
           tc_fence_after();
           owaited = true;
 #pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 8; ++j) {  // block j / 2, heads 32 (j % 2) ..
+            const uint32_t col = 64 * (j >> 1) + 32 * (j & 1);
             uint32_t o[32];
-            tmem_ld32(tO + lrow + 64 * j + 32 * hh, o);
+            tmem_ld32(tO + lrow + col, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * (ms.scl[32 * hh + i] * gamma));
-            tmem_st32(tO + lrow + 64 * j + 32 * hh, o);
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * (ms.scl[32 * (j & 1) + i] * gamma));
+            tmem_st32(tO + lrow + col, o);
           }
           tmem_st_wait();
         }
@@ -433,58 +510,66 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
         mbar_wait(&ms.o_done, (r - 1) & 1, abort_f);
         tc_fence_after();
       }
-      // P' (hi, lo) of this token's 32 heads: row `tok` of the MN-major operand
-      {
-        const float vs = nv * pow2i(kx);
+      // P' (hi, lo): row `tok` of the MN-major operand, heads in 16-byte chunks
+      const float vs = nv * pow2i(kx);
+      unsigned char* pb = sm + kUP;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float t[32];
+        logits(tSr, hh, nk, t);
 #pragma unroll
         for (int i = 0; i < 32; ++i) t[i] = t[i] == -INFINITY ? 0.f : exp2f(t[i] - ms.mst[32 * hh + i]);
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) split_f16x2(t[2 * i] * vs, t[2 * i + 1] * vs, ph[i], pl[i]);
-        unsigned char* pb = sm + kUP;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t o = sw128_off(tok, 4 * hh + k);
           *reinterpret_cast<uint4*>(pb + o) = make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
           *reinterpret_cast<uint4*>(pb + 16384 + o) = make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
         }
+        lacc[hh] += transpose_reduce<false>(t, lane);
       }
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.p_full);
-      lacc += transpose_reduce<false>(t, lane);
       nk = nk1;
       nv = nv1;
     }
     mbar_wait(&ms.o_done, (n - 1) & 1, abort_f);
     tc_fence_after();
     // the split's partial: softmax denominators and O^T (rotated basis)
-    ms.red[q][32 * hh + lane] = lacc;
-    bar_sync(1, 256);
+    ms.red[q][lane] = lacc[0];
+    ms.red[q][32 + lane] = lacc[1];
+    bar_sync(1, 32 * kUSoftWarps);
     const float un = pow2i(-16 - kx);
 #pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
+      const int hb = 32 * (j & 1);
       uint32_t o[32];
-      tmem_ld32(tO + lrow + 64 * j + 32 * hh, o);
+      tmem_ld32(tO + lrow + 64 * (j >> 1) + hb, o);
       tmem_ld_wait();
-      float* dst = p.ws_acc + ((qh0 + 32 * hh) * p.S + split) * D + 128 * j + tok;
+      float* dst = p.ws_acc + ((qh0 + hb) * p.S + split) * D + 128 * (j >> 1) + tok;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (32 * hh + i < GT) dst[(int64_t)i * p.S * D] = __uint_as_float(o[i]) * un;
+        if (hb + i < GT) dst[(int64_t)i * p.S * D] = __uint_as_float(o[i]) * un;
     }
     if (q == 0) {
-      const int h = 32 * hh + lane;
-      if (h < GT) {
-        float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
-        ml[0] = ms.mst[h];
-        ml[1] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 32 * hh + lane;
+        if (h < GT) {
+          float* ml = p.ws_ml + ((qh0 + h) * p.S + split) * 2;
+          ml[0] = ms.mst[h];
+          ml[1] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+        }
       }
     }
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kUSoftWarps) {
     // every MMA has completed (drain bounded independently of the abort flag)
     volatile int drain = 0;
     mbar_wait(&ms.fin, 0, &drain);
