@@ -23,12 +23,13 @@
 //    blocks (A = the dequantised record, MN-major; B = P', MN-major, N = 64);
 //    O^T stays in tensor memory for the whole split.
 //
-// Warp roles (640 threads, five warps per SM sub-partition): warps 0-3 softmax
-// and epilogue (warp w reads TMEM lanes 32 w .. 32 w + 31); warps 4-19
-// dequantise records into a two-stage ring of 32 KB operand tiles (16 stages
-// per record: 8 score chunks of 64 coordinates, hi and lo; 8 value blocks of
-// 128 coordinates, hi or lo); warp 4 also allocates tensor memory and its lane
-// 0 issues each stage's MMAs once all sixteen warps have written it.  Stages,
+// Warp roles (672 threads): warps 0-3 softmax and epilogue (warp w reads TMEM
+// lanes 32 w .. 32 w + 31); warps 4-19 dequantise records into a two-stage
+// ring of 32 KB operand tiles (16 stages per record: 8 score chunks of 64
+// coordinates, hi and lo; 8 value blocks of 128 coordinates, hi or lo),
+// 4-bit codes through byte-plane tables held in registers (byte permutes, no
+// shared-memory lookups); warp 20 allocates tensor memory and its lane 0 only
+// issues MMAs, each stage's once all sixteen warps have written it.  Stages,
 // scores, P' and outputs are handed over through mbarriers; every wait is
 // bounded and a CTA whose wait expires sets the launch's status word and
 // finishes without further waiting.
@@ -39,9 +40,10 @@
 
 namespace tq {
 
-constexpr int kU512Threads = 640;
+constexpr int kU512Threads = 672;
 constexpr int kUSoftWarps = 4;
 constexpr int kUDeqWarps = 16;
+constexpr int kUIssueWarp = kUSoftWarps + kUDeqWarps;
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kUQ = 0;          // q~ operand: [8 chunks of 64 coordinates][128 rows][128 B]
 constexpr int kUP = 131072;     // P' operand: hi [128 tokens][64 heads f16] | lo
@@ -54,10 +56,10 @@ struct U512Misc {
   uint32_t tbase;
   int abort_;
   uint32_t ctab_k[16], ctab_v[16];  // centroid x 2^16 as f16 {hi, lo} per code
+  uint32_t plane_k[4][4], plane_v[4][4];  // the same as byte planes: hi.b0, hi.b1, lo.b0, lo.b1 of codes 4w..4w+3
   float qsc[64];                    // per head: softmax scale * log2(e) * 2^(-16 - s)
   float mst[64];                    // running max per head (log2 units)
-  float scl[64];                    // output rescale per head (slow path)
-  float red[4][64];                 // cross-quarter reductions
+  float red[4][64];                 // cross-quarter reductions; red[0] then holds the output rescale per head
   float vmx[4];
 };
 static_assert(sizeof(U512Misc) <= 2048, "bookkeeping block");
@@ -74,6 +76,38 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
 }
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// 16-entry byte plane lookup of four 4-bit codes (nibbles of sel): entries
+// 0-7 and 8-15 by index sel & 7, then per byte the half chosen by bit 3
+__device__ __forceinline__ uint32_t plane_lookup(const uint32_t (&P)[4], uint32_t sel7, uint32_t pick) {
+  return __byte_perm(__byte_perm(P[0], P[1], sel7), __byte_perm(P[2], P[3], sel7), pick);
+}
+// 8 four-bit codes -> f16x2 hi / lo words from byte planes in registers
+__device__ __forceinline__ void deq8_planes(uint32_t w, const uint32_t (&pl)[4][4], uint4& hi, uint4& lo) {
+  uint32_t out_h[4], out_l[4];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t sel = k ? (w >> 16) : w;
+    const uint32_t sel7 = sel & 0x7777u;
+    const uint32_t pick = 0x3210u + ((sel >> 3) & 0x1111u) * 4u;  // byte i from the low (i) or high (i + 4) lookup
+    const uint32_t h0 = plane_lookup(pl[0], sel7, pick), h1 = plane_lookup(pl[1], sel7, pick);
+    const uint32_t l0 = plane_lookup(pl[2], sel7, pick), l1 = plane_lookup(pl[3], sel7, pick);
+    out_h[2 * k] = __byte_perm(h0, h1, 0x5140);
+    out_h[2 * k + 1] = __byte_perm(h0, h1, 0x7362);
+    out_l[2 * k] = __byte_perm(l0, l1, 0x5140);
+    out_l[2 * k + 1] = __byte_perm(l0, l1, 0x7362);
+  }
+  hi = make_uint4(out_h[0], out_h[1], out_h[2], out_h[3]);
+  lo = make_uint4(out_l[0], out_l[1], out_l[2], out_l[3]);
 }
 
 // dequantise 8 codes into f16x2 hi / lo words (coordinate 2i in the low half)
@@ -221,13 +255,27 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
     ms.abort_ = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kUSoftWarps) tmem_alloc(&ms.tbase, 512);
+  if (warp == kUIssueWarp) tmem_alloc(&ms.tbase, 512);
   if (tid < 32) {
     const int e = tid & 15, bits = tid < 16 ? KB : VB;
     const float v = e < (1 << bits) ? (tid < 16 ? p.kc[e] : p.vc[e]) * 65536.f : 0.f;
     const __half h = __float2half_rn(v);
     const __half r = __float2half_rn(v - __half2float(h));
     (tid < 16 ? ms.ctab_k : ms.ctab_v)[e] = (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(r) << 16);
+  }
+  if (tid >= 32 && tid < 64) {  // byte planes: table (tid - 32) / 16, plane ((tid - 32) / 4) % 4, word (tid - 32) % 4
+    const int i = tid - 32, tb = i >> 4, pln = (i >> 2) & 3, wd = i & 3, bits = tb ? VB : KB;
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * wd + j;
+      const float v = e < (1 << bits) ? (tb ? p.vc[e] : p.kc[e]) * 65536.f : 0.f;
+      const __half h = __float2half_rn(v);
+      const __half r = __float2half_rn(v - __half2float(h));
+      const uint32_t hv = (pln < 2) ? __half_as_ushort(h) : __half_as_ushort(r);
+      word |= ((hv >> (8 * (pln & 1))) & 0xFFu) << (8 * j);
+    }
+    (tb ? ms.plane_v : ms.plane_k)[pln][wd] = word;
   }
   if (tid < 64) ms.mst[tid] = -INFINITY;
   // q~ rows (warps 0-15, four heads each): lane holds coordinates 16 lane .. + 15
@@ -281,7 +329,67 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
   const uint32_t tO = ms.tbase + 256;  // O^T: 4 blocks x 64 columns
   volatile int* abort_f = &ms.abort_;
 
-  if (warp >= kUSoftWarps) {
+  if (warp == kUIssueWarp) {
+    // ------------------------------------------------------------ MMA issue
+    // Descriptors are built once; a byte offset o moves one by o / 16.
+    if (lane == 0) {
+      const uint32_t ra = smem_u32(sm + kURing);
+      const uint64_t dQ = sdesc_sw128(smem_u32(sm + kUQ), 16, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(sm + kUP), 1024, 1024);
+      const uint64_t dK0 = sdesc_sw128(ra, 16, 1024), dK1 = sdesc_sw128(ra + 32768, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(ra, 16384, 1024), dV1 = sdesc_sw128(ra + 32768, 16384, 1024);
+      constexpr uint32_t IS128 = idesc_f16(128, 128, false, false);
+      constexpr uint32_t IS64 = idesc_f16(128, 64, false, false);
+      constexpr uint32_t IV = idesc_f16(128, 64, true, true);
+      uint32_t g = 0;
+      for (int ph = 0; ph < 2 * n; ++ph) {
+        int kind, rec;
+        umma_phase(ph, n, kind, rec);
+        if (kind == 0) {
+          const uint32_t dS = tS + 128 * (rec & 1);
+#pragma unroll 1
+          for (int kc = 0; kc < 8; ++kc, ++g) {
+            mbar_wait(&ms.full[g & 1], (g >> 1) & 1, abort_f);
+            tc_fence_after();
+            const uint64_t a = (g & 1) ? dK1 : dK0;
+            const uint64_t bq = dQ + (uint64_t)(kc * 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              umma_f16(dS, a + 2 * ks, bq + 2 * ks, IS128, (kc | ks) != 0);
+              umma_f16(dS, a + 1024 + 2 * ks, bq + 2 * ks, IS64, 1);
+            }
+            umma_commit(&ms.empty[g & 1]);
+          }
+          umma_commit(&ms.s_full[rec & 1]);
+        } else {
+          mbar_wait(&ms.p_full, rec & 1, abort_f);  // P' of this record is in shared memory
+          tc_fence_after();
+#pragma unroll 1
+          for (int st = 0; st < 8; ++st, ++g) {
+            const int j = st >> 1, part = st & 1;
+            mbar_wait(&ms.full[g & 1], (g >> 1) & 1, abort_f);
+            tc_fence_after();
+            const uint64_t a = (g & 1) ? dV1 : dV0;
+            const uint32_t dO = tO + 64 * j;
+            if (part == 0) {
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, !(rec == 0 && ks == 0));
+                umma_f16(dO, a + 128 * ks, dP + 1024 + 128 * ks, IV, 1);
+              }
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, 1);
+            }
+            umma_commit(&ms.empty[g & 1]);
+          }
+          umma_commit(&ms.o_done);
+        }
+      }
+      umma_commit(&ms.fin);
+    }
+    __syncwarp();
+  } else if (warp >= kUSoftWarps) {
     // ------------------------------------------------------------ dequantisation
     // Thread d owns token d / 4 and its 16-coordinate units u = 4 i + d % 4
     // (i = 0..7): unit i feeds score chunk i (coordinates 64 i + 16 (d % 4) ..)
@@ -315,53 +423,21 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.full[g & 1]);
-    };
-    // MMA issue (warp 4, lane 0): waits until all sixteen warps have written
-    // stage g.  Descriptors are built once; a byte offset o moves one by o / 16.
-    const bool issuer = warp == kUSoftWarps && lane == 0;
-    const uint32_t ra = smem_u32(sm + kURing);
-    const uint64_t dQ = sdesc_sw128(smem_u32(sm + kUQ), 16, 1024);
-    const uint64_t dP = sdesc_sw128(smem_u32(sm + kUP), 1024, 1024);
-    const uint64_t dK0 = sdesc_sw128(ra, 16, 1024), dK1 = sdesc_sw128(ra + 32768, 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(ra, 16384, 1024), dV1 = sdesc_sw128(ra + 32768, 16384, 1024);
-    auto stage_in = [&]() {
-      mbar_wait(&ms.full[g & 1], (g >> 1) & 1, abort_f);
-      tc_fence_after();
-    };
-    auto issue_scores = [&](int kc, uint32_t dS) {
-      constexpr uint32_t IS128 = idesc_f16(128, 128, false, false);
-      constexpr uint32_t IS64 = idesc_f16(128, 64, false, false);
-      stage_in();
-      const uint64_t a = (g & 1) ? dK1 : dK0;
-      const uint64_t bq = dQ + (uint64_t)(kc * 1024);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        umma_f16(dS, a + 2 * ks, bq + 2 * ks, IS128, (kc | ks) != 0);
-        umma_f16(dS, a + 1024 + 2 * ks, bq + 2 * ks, IS64, 1);
-      }
-      umma_commit(&ms.empty[g & 1]);
-    };
-    auto issue_values = [&](int j, int part, bool first) {
-      constexpr uint32_t IV = idesc_f16(128, 64, true, true);
-      stage_in();
-      const uint64_t a = (g & 1) ? dV1 : dV0;
-      const uint32_t dO = tO + 64 * j;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (part == 0) {
-          umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, !(first && ks == 0));
-          umma_f16(dO, a + 128 * ks, dP + 1024 + 128 * ks, IV, 1);
-        } else {
-          umma_f16(dO, a + 128 * ks, dP + 128 * ks, IV, 1);
-        }
-      }
-      umma_commit(&ms.empty[g & 1]);
+      ++g;
     };
     load_phase(cur, 0);
     for (int ph = 0; ph < 2 * n; ++ph) {
       int kind, rec;
       umma_phase(ph, n, kind, rec);
       if (ph + 1 < 2 * n) load_phase(nxt, ph + 1);
+      uint32_t pl[4][4];  // byte planes of this phase's codec (4-bit codes)
+      if constexpr (KB == 4 || VB == 4) {
+        const uint32_t(&src)[4][4] = kind == 0 ? ms.plane_k : ms.plane_v;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pl[a][c] = src[a][c];
+      }
       if (kind == 0) {
         // score chunk i: row tkn, 16-byte chunks 2 sub, 2 sub + 1 of its hi and lo tiles
 #pragma unroll
@@ -370,17 +446,16 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint4 hi, lo;
-            deq8<KB>(codes8<KB>(cur[i], c, shk), ms.ctab_k, hi, lo);
+            if constexpr (KB == 4) {
+              deq8_planes(codes8<KB>(cur[i], c, shk), pl, hi, lo);
+            } else {
+              deq8<KB>(codes8<KB>(cur[i], c, shk), ms.ctab_k, hi, lo);
+            }
             const uint32_t o = sw128_off(tkn, 2 * sub + c);
             *reinterpret_cast<uint4*>(st + o) = hi;
             *reinterpret_cast<uint4*>(st + 16384 + o) = lo;
           }
           release();
-          if (issuer) {
-            issue_scores(i, tS + 128 * (rec & 1));
-            if (i == 7) umma_commit(&ms.s_full[rec & 1]);
-          }
-          ++g;
         }
       } else {
         // value block j: unit 2 j + e -> half e, chunks 2 sub, 2 sub + 1
@@ -394,19 +469,14 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
                 uint4 hi, lo;
-                deq8<VB>(codes8<VB>(cur[2 * j + e], c, shv), ms.ctab_v, hi, lo);
+                if constexpr (VB == 4) {
+                  deq8_planes(codes8<VB>(cur[2 * j + e], c, shv), pl, hi, lo);
+                } else {
+                  deq8<VB>(codes8<VB>(cur[2 * j + e], c, shv), ms.ctab_v, hi, lo);
+                }
                 *reinterpret_cast<uint4*>(st + e * 16384 + sw128_off(tkn, 2 * sub + c)) = part ? lo : hi;
               }
             release();
-            if (issuer) {
-              if (j == 0 && part == 0) {  // P' of this record is in shared memory
-                mbar_wait(&ms.p_full, rec & 1, abort_f);
-                tc_fence_after();
-              }
-              issue_values(j, part, rec == 0);
-              if (j == 3 && part == 1) umma_commit(&ms.o_done);
-            }
-            ++g;
           }
       }
 #pragma unroll
@@ -415,7 +485,6 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
         cur[i][1] = nxt[i][1];
       }
     }
-    if (issuer) umma_commit(&ms.fin);
   } else {
     // ------------------------------------------------------------ softmax, epilogue
     const int q = warp;  // TMEM lane quarter
@@ -428,14 +497,17 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
     };
     // logits of heads 32 hh .. 32 hh + 31 of this token (-inf past the group)
     auto logits = [&](uint32_t tSr, int hh, float nk, float (&t)[32]) {
-      uint32_t a[32], c[32];
-      tmem_ld32(tSr + lrow + 32 * hh, a);
-      tmem_ld32(tSr + lrow + 64 + 32 * hh, c);
-      tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int h = 32 * hh + i;
-        t[i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
+      for (int x = 0; x < 2; ++x) {
+        uint32_t a[16], c[16];
+        tmem_ld16(tSr + lrow + 32 * hh + 16 * x, a);
+        tmem_ld16(tSr + lrow + 64 + 32 * hh + 16 * x, c);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = 32 * hh + 16 * x + i;
+          t[16 * x + i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
+        }
       }
     };
     float nk = norm_at(kb0, p.krec_bytes, p.k_off_norm, 0);
@@ -476,7 +548,7 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
             const float mx = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
             const float mo = ms.mst[h];
             const float mn = mx > mo + 8.f ? mx : mo;
-            ms.scl[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+            ms.red[0][h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
             ms.mst[h] = mn;
           }
         }
@@ -485,8 +557,8 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
         if (vmax > 0.f) kn = min(kx, 6 - exp_of(vmax));
         const float gamma = pow2i(kn - kx);
         bar_sync(1, 32 * kUSoftWarps);
-        lacc[0] *= ms.scl[lane];
-        lacc[1] *= ms.scl[32 + lane];
+        lacc[0] *= ms.red[0][lane];
+        lacc[1] *= ms.red[0][32 + lane];
         if (r > 0) {
           mbar_wait(&ms.o_done, (r - 1) & 1, abort_f);
           tc_fence_after();
@@ -499,7 +571,7 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * (ms.scl[32 * (j & 1) + i] * gamma));
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * (ms.red[0][32 * (j & 1) + i] * gamma));
             tmem_st32(tO + lrow + col, o);
           }
           tmem_st_wait();
@@ -569,7 +641,7 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == kUSoftWarps) {
+  if (warp == kUIssueWarp) {
     // every MMA has completed (drain bounded independently of the abort flag)
     volatile int drain = 0;
     mbar_wait(&ms.fin, 0, &drain);
