@@ -152,12 +152,13 @@ class ClockSampler:
 # workloads
 # ---------------------------------------------------------------------------
 def peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, "measured" | "fallback")."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 class QwenCache:
@@ -235,6 +236,8 @@ class QwenCache:
         self.enc_out = nc * B * Hkv * self.n_rec * (self.kc.record_bytes + self.vc.record_bytes)
         self.attn_bytes = (self.enc_out + nd * B * Hkv * ctx * 2 * d2 + L * B * Hq * d * 2
                            + L * B * Hq * d * 4)
+        # plain attention arithmetic: q.k and p.v per (query head, token), 2 flops per MAC
+        self.attn_flops = 4 * L * B * Hq * d * ctx
         self.step_bytes = self.enc_in + self.enc_out + self.attn_bytes
         self.vectors_per_step = 2 * n_vec_stream
         self.tokens_per_step = B  # one decode token per sequence through all layers
@@ -385,6 +388,7 @@ class BigCache:
             0 if self.shared else self._used_record_bytes(self.vrec, self.vc))
         self.attn_bytes = (self.enc_out + streams * L * B * Hkv * tail * d * 2 + L * B * Hq * d * 2
                            + L * B * Hq * d * 4)
+        self.attn_flops = 4 * L * B * Hq * d * (self.n_rec * 128 + tail)
         self.step_bytes = self.enc_in + self.enc_out + self.attn_bytes
         self.vectors_per_step = streams * n_vec
         self.tokens_per_step = B
@@ -510,11 +514,29 @@ def run_native(args, world, rank, local, pg):
         enc_launch = sum(t_enc) / (n_enc * K)    # average encode launch
         enc_bytes_per_launch = (wl.enc_in + wl.enc_out) / n_enc
     attn_region = sum(t_attn) / K
-    hbm, peak_kind = peaks()
+    hbm, tflops, peak_kind = peaks()
     enc_gbs = enc_bytes_per_launch / enc_launch / 1e9
     attn_gbs = wl.attn_bytes / attn_region / 1e9
     dominant = "tq_encode" if sum(t_enc) >= sum(t_attn) else "tq_decode_attn"
-    achieved, traffic = (enc_gbs, None) if dominant == "tq_encode" else (attn_gbs, None)
+    # attention is bound by the tensor cores when its arithmetic intensity
+    # (plain q.k + p.v flops per algorithmic byte) exceeds the ridge point
+    intensity = wl.attn_flops / wl.attn_bytes
+    ridge = tflops * 1e12 / (hbm * 1e9)
+    if dominant == "tq_encode":
+        roof = {"bound": "hbm", "achieved": round(enc_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(enc_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                "per_launch_bytes": enc_bytes_per_launch}
+    elif intensity <= ridge:
+        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(attn_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                "per_launch_bytes": wl.attn_bytes}
+    else:
+        attn_tf = wl.attn_flops / attn_region / 1e12
+        roof = {"bound": "tensor", "achieved": round(attn_tf, 2), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(attn_tf / tflops, 4),
+                "peak_kind": f"{peak_kind} dense bf16 GEMM (burst); the kernel's f16 MMAs run at the same rate",
+                "per_launch_flops": wl.attn_flops, "hbm_frac": round(attn_gbs / hbm, 4)}
+    roof.update({"intensity_flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1)})
     per_layer = (per_layer_attention(wl, stream, flush, max(3, min(200, K)))
                  if isinstance(wl, QwenCache) else attn_region)
     line = {
@@ -547,11 +569,8 @@ def run_native(args, world, rank, local, pg):
             "encode_us_per_step": round(sum(t_enc) / K * 1e6, 2),
             "step_algorithmic_bytes": wl.step_bytes,
         },
-        "roofline": {"bound": "hbm", "kernel": dominant + (" (K and V launches, concurrent)" if concurrent_enc and dominant == "tq_encode" else ""),
-                     "achieved": round(achieved, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
-                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "per_launch_bytes": enc_bytes_per_launch if dominant == "tq_encode" else wl.attn_bytes},
+        "roofline": {"kernel": dominant + (" (K and V launches, concurrent)" if concurrent_enc and dominant == "tq_encode" else ""),
+                     **roof, "traffic": None},
         "gpu_launches": wl.launches_per_step * K,
     }
     if clk:
