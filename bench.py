@@ -151,6 +151,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
+# captures of the current kernels (profiles/qwen2_1p5b_ctx2048_launches.md,
+# profiles/attn_umma512_v4flash_8layers.md); None where no capture exists.
+# The V4-Flash value is the 8-layer launch's 139.6 MB scaled to 43 layers
+# (traffic grows with the records read).
+MEASURED_TRAFFIC = {
+    ("qwen2_1p5b_ctx2048", "tq_encode"): 23_103_488 + 23_101_184,  # K and V launches of the phase
+    ("v4flash_mqa_ctx65536", "tq_decode_attn"): int((136.414976e6 + 3.229952e6) * 43 / 8),
+}
+
+
 def peaks():
     """(HBM GB/s, dense bf16 TFLOP/s burst, "measured" | "fallback")."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -570,7 +581,7 @@ def run_native(args, world, rank, local, pg):
             "step_algorithmic_bytes": wl.step_bytes,
         },
         "roofline": {"kernel": dominant + (" (K and V launches, concurrent)" if concurrent_enc and dominant == "tq_encode" else ""),
-                     **roof, "traffic": None},
+                     **roof, "traffic": MEASURED_TRAFFIC.get((wl.name, dominant))},
         "gpu_launches": wl.launches_per_step * K,
     }
     if clk:
