@@ -81,8 +81,8 @@ __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4
 // the code of y = 0).
 template <int D, int B, bool OUTL>
 __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B, OUTL>& ln,
-                                           const uint4 (&w)[4], bool valid, uint8_t* rec, int slot,
-                                           float (&x)[32], float& inv, uint32_t& omask) {
+                                           const float2* cells, const uint4 (&w)[4], bool valid, uint8_t* rec,
+                                           int slot, float (&x)[32], float& inv, uint32_t& omask) {
   using E = Enc<D, B, OUTL>;
   {
     const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
@@ -122,13 +122,22 @@ __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
+  const float zscale = n > 0.f ? kCellScale / sigma : 0.f;  // z = 128 y
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
     const float aw = fabsf(x[r]);
-    uint32_t msum = 0u;  // -(number of positive boundaries below |w|)
+    uint32_t code;
+    if constexpr (B >= 3) {  // decision cells (shared table)
+      const float z = x[r] * zscale;
+      const uint32_t ci = __float_as_uint(z + 8388736.0f) & 0x1FFu;  // round(z) + 128 (2^23 + 128 magic)
+      const float2 e = cells[ci];
+      code = (uint32_t)__float_as_int(e.y) - mask_gt(z, e.x);
+    } else {
+      uint32_t msum = 0u;  // -(number of positive boundaries below |w|)
 #pragma unroll
-    for (int k = 0; k < E::NPOS; ++k) msum += mask_gt(aw, T[k]);
-    const uint32_t code = ((uint32_t)E::HALF - msum) ^ (mask_le(x[r], 0.f) & ((1u << B) - 1u));
+      for (int k = 0; k < E::NPOS; ++k) msum += mask_gt(aw, T[k]);
+      code = ((uint32_t)E::HALF - msum) ^ (mask_le(x[r], 0.f) & ((1u << B) - 1u));
+    }
     const int bit = r * B;
     wd[bit >> 5] += code << (bit & 31);
     if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code >> (32 - (bit & 31));
@@ -214,7 +223,7 @@ __device__ __forceinline__ void enc_outliers(const CodecDev& c, const EncLane<D,
 // vectors at a time with the next pass's loads in flight; row(slot) gives the
 // bf16 source of a slot.  Must be called by all 128 threads of the CTA.
 template <int D, int B, bool OUTL, class RowFn>
-__device__ __forceinline__ void encode_record(const CodecDev& c, RowFn row, uint8_t* rec,
+__device__ __forceinline__ void encode_record(const CodecDev& c, const float2* cells, RowFn row, uint8_t* rec,
                                               int s_begin, int s_end, EncSmem* sm) {
   using E = Enc<D, B, OUTL>;
   const EncLane<D, B, OUTL> ln(c);
@@ -234,7 +243,7 @@ __device__ __forceinline__ void encode_record(const CodecDev& c, RowFn row, uint
     float x[32];
     float inv;
     uint32_t omask;
-    enc_vector<D, B, OUTL>(c, ln, w, valid, rec, slot, x, inv, omask);
+    enc_vector<D, B, OUTL>(c, ln, cells, w, valid, rec, slot, x, inv, omask);
     if constexpr (OUTL) enc_outliers<D, B>(c, ln, x, inv, omask, valid, rec, slot, pslot, sm);
   }
 }
@@ -243,6 +252,11 @@ __device__ __forceinline__ void encode_record(const CodecDev& c, RowFn row, uint
 template <int D, int B>
 __global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_constant__ EncodeParams p) {
   __shared__ EncSmem sm;
+  __shared__ float2 cells[B >= 3 ? kCells : 1];
+  if constexpr (B >= 3) {
+    build_cells(p.c, cells);
+    __syncthreads();
+  }
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
     const int64_t g = task / p.chunks_per_group;
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_co
     const uint16_t* src_g = p.src + g * p.src_gs;
     const int64_t vs = p.src_vs, v0 = ci * kChunk - p.first_vec;
     auto row = [&](int slot) { return src_g + (v0 + slot) * vs; };
-    encode_record<D, B, true>(p.c, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
+    encode_record<D, B, true>(p.c, cells, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
   }
 }
 
@@ -262,6 +276,11 @@ template <int D, int B>
 __global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_constant__ EncodeParams p) {
   using E = Enc<D, B, false>;
   constexpr int PPR = kChunk / E::VPC;  // passes per record
+  __shared__ float2 cells[B >= 3 ? kCells : 1];
+  if constexpr (B >= 3) {
+    build_cells(p.c, cells);
+    __syncthreads();
+  }
   const EncLane<D, B, false> ln(p.c);
   const int pslot = ln.warp * E::VPW + ln.vi;
   const int64_t per_group = p.chunks_per_group * PPR;
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_cons
     float x[32];
     float inv;
     uint32_t omask;
-    enc_vector<D, B, false>(p.c, ln, w, cvalid, rec, (int)(ctok % kChunk), x, inv, omask);
+    enc_vector<D, B, false>(p.c, ln, cells, w, cvalid, rec, (int)(ctok % kChunk), x, inv, omask);
   }
 }
 
@@ -305,13 +324,18 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   const int start = ((p.tail_start[lb] % p.tail_cap) + p.tail_cap) % p.tail_cap;
   const int k = len >= p.floor_ + kChunk ? min((len - p.floor_) / kChunk, p.max_evict) : 0;
   if (e >= k || nch < 0 || nch + k > p.rec_cap) return;
+  __shared__ float2 cells[B >= 3 ? kCells : 1];
+  if constexpr (B >= 3) {
+    build_cells(p.c, cells);
+    __syncthreads();
+  }
   uint8_t* rec = p.rec + l * p.rec_ls +
                  ((int64_t)(b * p.Hkv + h) * p.rec_cap + nch + e) * (int64_t)p.c.rec_bytes;
   const uint16_t* tail = p.tail + l * p.tail_ls + (int64_t)(b * p.Hkv + h) * p.tail_cap * D;
   const int first = start + e * kChunk;
   const int cap = p.tail_cap;
   auto row = [&](int slot) { return tail + (int64_t)((first + min(slot, kChunk - 1)) % cap) * D; };
-  encode_record<D, B, OUTL>(p.c, row, rec, 0, kChunk, &sm);
+  encode_record<D, B, OUTL>(p.c, cells, row, rec, 0, kChunk, &sm);
 }
 
 __global__ void evict_commit_kernel(const EvictCommitParams p) {

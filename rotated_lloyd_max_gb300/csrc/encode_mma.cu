@@ -203,32 +203,6 @@ __device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint
       }
 }
 
-// Decision cells: with z = y * 128 (y the normalised rotated value, |y| <= 1)
-// and i = round(z) + 128, cell i covers z in [i - 128.5, i - 127.5) and
-// holds (count of boundaries below the cell, the boundary inside it x 128 or
-// +huge); boundaries are >= 2/128 apart at d = 128 for b <= 4, so a cell holds
-// at most one.  |y| <= 1 keeps i in 0..256.  code = count + (z > boundary): the same code as
-// #{k : y > t_k} except within a couple of f32 ulp of a boundary.
-constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell (257.. = top cell's law)
-constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
-constexpr float kCellScale = 128.f;
-
-__device__ __forceinline__ void encm_build_cells(const CodecDev& c, float2* cells) {
-  const int nb = (1 << c.bits) - 1;
-  for (int i = threadIdx.x; i < kCells; i += kThreads) {
-    const float lo = ((float)(i - 128) - 0.5f) / kCellScale, hi = ((float)(i - 128) + 0.5f) / kCellScale;
-    int below = 0;
-    float inside = 3.0e38f;
-    for (int k = 0; k < nb; ++k) {
-      const float t = c.boundaries[k];
-      if (t < lo) ++below;
-      else if (t < hi) inside = t * kCellScale;
-    }
-    cells[i] = make_float2(inside, __int_as_float(below));
-    if (i == kPosCell && c.bits == 2) cells[i].x = c.boundaries[2] * kCellScale;
-  }
-}
-
 // Codes of the lane's 32 coordinates of one vector (x: unnormalised
 // transform, scale = 128 / (n sqrt(d)) or 0 for a zero vector), packed
 // LSB-first into B words; (OUTL) the outlier mask |y| > T / sqrt(d).
@@ -280,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
   using E = EncM<B>;
   __shared__ float2 cells[kCells];
   __shared__ EncTile tiles[4][2];
-  encm_build_cells(p.c, cells);
+  build_cells(p.c, cells);
   __syncthreads();
   const EncMLane<B> ln(p.c);
   const int64_t per_group = p.chunks_per_group * 8;
@@ -356,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
   __shared__ int run_s;
   __shared__ float2 cells[kCells];
   __shared__ EncTile tiles[4][2];
-  encm_build_cells(p.c, cells);
+  build_cells(p.c, cells);
   const EncMLane<B> ln(p.c);
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   const int64_t v_end = p.first_vec + p.n_vec;

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "../../include/tq.h"
+#include "tq_params.h"
 
 namespace tq {
 
@@ -151,6 +152,33 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[B], int r) {
     if (wi == k) { lo = w[k]; hi = (k + 1 < B) ? w[k + 1] : 0u; }
   uint64_t v = ((uint64_t)hi << 32) | lo;
   return (uint32_t)(v >> sh) & ((1u << B) - 1u);
+}
+
+// Decision cells (both encoders, b >= 3): with z = y * 128 (y the normalised rotated value, |y| <= 1)
+// and i = round(z) + 128, cell i covers z in [i - 128.5, i - 127.5) and
+// holds (count of boundaries below the cell, the boundary inside it x 128 or
+// +huge); boundaries are >= 1.4/128 apart for b <= 4 at every head dim up to
+// 512 (the closest pair, around 0 at b = 4, is 0.258/sqrt(d) apart), so a cell holds
+// at most one.  |y| <= 1 keeps i in 0..256.  code = count + (z > boundary): the same code as
+// #{k : y > t_k} except within a couple of f32 ulp of a boundary.
+constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell (257.. = top cell's law)
+constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
+constexpr float kCellScale = 128.f;
+
+__device__ __forceinline__ void build_cells(const CodecDev& c, float2* cells) {
+  const int nb = (1 << c.bits) - 1;
+  for (int i = threadIdx.x; i < kCells; i += kThreads) {
+    const float lo = ((float)(i - 128) - 0.5f) / kCellScale, hi = ((float)(i - 128) + 0.5f) / kCellScale;
+    int below = 0;
+    float inside = 3.0e38f;
+    for (int k = 0; k < nb; ++k) {
+      const float t = c.boundaries[k];
+      if (t < lo) ++below;
+      else if (t < hi) inside = t * kCellScale;
+    }
+    cells[i] = make_float2(inside, __int_as_float(below));
+    if (i == kPosCell && c.bits == 2) cells[i].x = c.boundaries[2] * kCellScale;
+  }
 }
 
 }  // namespace tq
