@@ -36,7 +36,7 @@ def _ocodec(orc, c):
 
 def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=False, dense=False,
              tail_cap=None, splits=0, seed=0, q_pad=0, k_outlier_frac=0.0, end_to_end=True, scale=1.0,
-             cuda_core_path=False):
+             cuda_core_path=False, zero_every=0):
     """chunks[b], tails[b]: compressed records and dense tail tokens of batch b
     (the same for every layer).  Returns (gpu_out, oracle_out, oracle_e2e_out)."""
     import torch
@@ -52,6 +52,12 @@ def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=F
     kx = synth.gaussian_bf16((L, B, Hkv, ntok, d), seed + 1, outlier_frac=k_outlier_frac,
                              lognormal_sigma=0.3)
     vx = kx if shared else synth.gaussian_bf16((L, B, Hkv, ntok, d), seed + 2)
+    if zero_every:  # zero-norm tokens (every zero_every-th token of K and of V)
+        kx = kx.copy()
+        kx[..., ::zero_every, :] = 0
+        vx = kx if shared else vx.copy()
+        if not shared:
+            vx[..., 3::zero_every, :] = 0
     kt = synth.gaussian_bf16((L, B, Hkv, tail_cap, d), seed + 3)
     vt = kt if shared else synth.gaussian_bf16((L, B, Hkv, tail_cap, d), seed + 4)
     qb = synth.gaussian_bf16((L, B, Hq + q_pad, d), seed + 5, scale=1 / math.sqrt(d))
@@ -185,6 +191,16 @@ def test_tcgen05_d512_multi_record_splits(tq, orc):
     _assert_close(a, want)
     _assert_close(b, want)
     assert np.max(np.abs(a - b)) <= 1e-5
+
+
+def test_tcgen05_d512_hot_logits_and_zero_tokens(tq, orc):
+    """Peaky softmax (scale 8: the running max moves, lazily, several times in
+    one split of six records) over a cache with zero-norm tokens (norm 0,
+    code of y = 0, decoded as exact zeros)."""
+    for shared, kb, vb in ((True, 4, 4), (False, 4, 2)):
+        got, want, _ = run_case(tq, orc, d=512, G=64, Hkv=1, B=1, L=1, chunks=[6], tails=[0], kb=kb, vb=vb,
+                                shared=shared, end_to_end=False, seed=11, splits=1, scale=8.0, zero_every=7)
+        _assert_close(got, want)
 
 
 def test_tcgen05_d512_matches_mma_sync(tq, orc):
