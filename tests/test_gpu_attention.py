@@ -231,6 +231,17 @@ def test_split_count_invariance(tq, orc, path):
     assert np.max(np.abs(a - b)) <= 1e-5
 
 
+def test_many_splits_one_record_each(tq, orc):
+    """70 records in 70 one-record splits (plus dense splits) against 4 splits:
+    both agree with the oracle and with each other."""
+    cfg = dict(d=64, G=2, Hkv=1, B=1, L=1, chunks=[70], tails=[20], kb=2, vb=2, end_to_end=False, seed=3)
+    a, want, _ = run_case(tq, orc, splits=80, **cfg)
+    b, _, _ = run_case(tq, orc, splits=4, **cfg)
+    _assert_close(a, want)
+    _assert_close(b, want)
+    assert np.max(np.abs(a - b)) <= 1e-5
+
+
 def test_empty_context_gives_zero(tq):
     import torch
     L, B, Hq, Hkv, d = 1, 2, 4, 2, 128
