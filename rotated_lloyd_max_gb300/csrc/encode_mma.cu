@@ -209,28 +209,40 @@ __device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint
 template <int B, bool OUTL>
 __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2* cells, float scale,
                                               float thr_out, uint32_t (&wd)[B], uint32_t& omask) {
-  const float Tz = OUTL ? thr_out * kCellScale : 0.f;
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
+  // b <= 2 and the outlier test compare |x| against thresholds scaled once per
+  // vector (z = x * scale > t * 128  <=>  x > t * 128 / scale); a zero vector
+  // (scale 0) has x = 0 and takes the y = 0 codes against threshold 0
+  const float inv = scale > 0.f ? 1.0f / scale : 0.f;
+  const float Tx = B == 2 ? cells[kPosCell].x * inv : 0.f;
+  const float Tox = OUTL ? (scale > 0.f ? thr_out * kCellScale * inv : INFINITY) : 0.f;
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const float z = x[r] * scale;
-    uint32_t code;
+  for (int r = 0; r < 32; r += 2) {
+    uint32_t code[2];
     if constexpr (B <= 2) {
       // at most one positive boundary: compare directly (the mirror of the
-      // positive side, HALF - 1 for z <= 0)
-      const uint32_t m = B == 2 ? mask_gt(fabsf(z), cells[kPosCell].x) : 0u;
-      code = ((uint32_t)(1 << (B - 1)) - m) ^ (mask_le(z, 0.f) & ((1u << B) - 1u));
+      // positive side, HALF - 1 for x <= 0)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t m = B == 2 ? mask_gt(fabsf(x[r + k]), Tx) : 0u;
+        code[k] = ((uint32_t)(1 << (B - 1)) - m) ^ (mask_le(x[r + k], 0.f) & ((1u << B) - 1u));
+      }
     } else {
-      const uint32_t ci = __float_as_uint(z + 8388736.0f) & 0x1FFu;  // round(z) + 128 (2^23 + 128 magic)
-      const float2 e = cells[ci];
-      code = (uint32_t)__float_as_int(e.y) - mask_gt(z, e.x);
+      const float2 z = mul2(f2(x[r], x[r + 1]), f2(scale, scale));
+      const float2 u = add2(z, f2(8388736.0f, 8388736.0f));  // round(z) + 128 in the low bits (2^23 + 128 magic)
+      const float2 e0 = cells[__float_as_uint(u.x) & 0x1FFu], e1 = cells[__float_as_uint(u.y) & 0x1FFu];
+      code[0] = (uint32_t)__float_as_int(e0.y) - mask_gt(z.x, e0.x);
+      code[1] = (uint32_t)__float_as_int(e1.y) - mask_gt(z.y, e1.x);
     }
-    const int bit = r * B;
-    wd[bit >> 5] += code << (bit & 31);
-    if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code >> (32 - (bit & 31));
-    if (OUTL) omask |= mask_gt(fabsf(z), Tz) & (1u << r);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int bit = (r + k) * B;
+      wd[bit >> 5] += code[k] << (bit & 31);
+      if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code[k] >> (32 - (bit & 31));
+      if (OUTL) omask |= mask_gt(fabsf(x[r + k]), Tox) & (1u << (r + k));
+    }
   }
 }
 
