@@ -58,6 +58,48 @@ struct EncLane {
   }
 };
 
+// The 16-point transform over the lane index of a d-512 vector (16 lanes x 32
+// coordinates) through shared memory instead of 128 shuffles per lane: the
+// lanes write their rows, lane l' takes coordinate pair (2 l', 2 l' + 1) of
+// all 16 rows, applies the butterflies in registers and writes the pair back,
+// and every lane reads its row again.  Rows are padded to 36 floats (row
+// writes and pair reads both at the minimum number of wavefronts); the
+// buffer holds the warp's two vectors.
+constexpr int kTRow = 36, kTVec = 16 * kTRow + 4;
+__device__ __forceinline__ void fwht16_lanes_smem(float (&x)[32], float* tb, int lane) {
+  float* base = tb + (lane >> 4) * kTVec;
+  float* row = base + (lane & 15) * kTRow;
+  const int pc = 2 * (lane & 15);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<float4*>(row + 4 * k) = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+  __syncwarp();
+  float2 y[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) y[i] = *reinterpret_cast<const float2*>(base + i * kTRow + pc);
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (!(i & m)) {
+        const float2 a = y[i], b = y[i | m];
+        y[i] = add2(a, b);
+        y[i | m] = fma2(b, f2(-1.f, -1.f), a);
+      }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) *reinterpret_cast<float2*>(base + i * kTRow + pc) = y[i];
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 v = *reinterpret_cast<const float4*>(row + 4 * k);
+    x[4 * k] = v.x;
+    x[4 * k + 1] = v.y;
+    x[4 * k + 2] = v.z;
+    x[4 * k + 3] = v.w;
+  }
+  __syncwarp();  // the buffer is written again for the warp's next vectors
+}
+
 // The lane's 32 bf16 coordinates of a vector (zeros for an invalid slot).
 __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4 (&w)[4]) {
 #pragma unroll
@@ -81,8 +123,8 @@ __device__ __forceinline__ void enc_load(const uint16_t* rowp, bool valid, uint4
 // the code of y = 0).
 template <int D, int B, bool OUTL>
 __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B, OUTL>& ln,
-                                           const float2* cells, const uint4 (&w)[4], bool valid, uint8_t* rec,
-                                           int slot, float (&x)[32], float& inv, uint32_t& omask) {
+                                           const float2* cells, float* tb, const uint4 (&w)[4], bool valid,
+                                           uint8_t* rec, int slot, float (&x)[32], float& inv, uint32_t& omask) {
   using E = Enc<D, B, OUTL>;
   {
     const uint32_t* ww = reinterpret_cast<const uint32_t*>(w);
@@ -116,7 +158,11 @@ __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B
   const float Tout = OUTL ? c.thr_out * sigma : 0.f;
 
   fwht_regs<32>(x);
-  fwht_lanes<32>(x, ln.lane, E::L);
+  if constexpr (D == 512) {
+    fwht16_lanes_smem(x, tb, ln.lane);
+  } else {
+    fwht_lanes<32>(x, ln.lane, E::L);
+  }
 
   uint32_t wd[B];
 #pragma unroll
@@ -223,8 +269,8 @@ __device__ __forceinline__ void enc_outliers(const CodecDev& c, const EncLane<D,
 // vectors at a time with the next pass's loads in flight; row(slot) gives the
 // bf16 source of a slot.  Must be called by all 128 threads of the CTA.
 template <int D, int B, bool OUTL, class RowFn>
-__device__ __forceinline__ void encode_record(const CodecDev& c, const float2* cells, RowFn row, uint8_t* rec,
-                                              int s_begin, int s_end, EncSmem* sm) {
+__device__ __forceinline__ void encode_record(const CodecDev& c, const float2* cells, float* tb, RowFn row,
+                                              uint8_t* rec, int s_begin, int s_end, EncSmem* sm) {
   using E = Enc<D, B, OUTL>;
   const EncLane<D, B, OUTL> ln(c);
   if (OUTL && threadIdx.x == 0) sm->running = 0;
@@ -243,7 +289,7 @@ __device__ __forceinline__ void encode_record(const CodecDev& c, const float2* c
     float x[32];
     float inv;
     uint32_t omask;
-    enc_vector<D, B, OUTL>(c, ln, cells, w, valid, rec, slot, x, inv, omask);
+    enc_vector<D, B, OUTL>(c, ln, cells, tb, w, valid, rec, slot, x, inv, omask);
     if constexpr (OUTL) enc_outliers<D, B>(c, ln, x, inv, omask, valid, rec, slot, pslot, sm);
   }
 }
@@ -252,6 +298,8 @@ __device__ __forceinline__ void encode_record(const CodecDev& c, const float2* c
 template <int D, int B>
 __global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_constant__ EncodeParams p) {
   __shared__ EncSmem sm;
+  __shared__ __align__(16) float tbuf[D == 512 ? (kThreads / 32) * 2 * kTVec : 4];
+  float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   __shared__ float2 cells[B >= 3 ? kCells : 1];
   if constexpr (B >= 3) {
     build_cells(p.c, cells);
@@ -266,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_co
     const uint16_t* src_g = p.src + g * p.src_gs;
     const int64_t vs = p.src_vs, v0 = ci * kChunk - p.first_vec;
     auto row = [&](int slot) { return src_g + (v0 + slot) * vs; };
-    encode_record<D, B, true>(p.c, cells, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
+    encode_record<D, B, true>(p.c, cells, tb, row, rec, (int)(lo - ci * kChunk), (int)(hi - ci * kChunk), &sm);
   }
 }
 
@@ -277,6 +325,8 @@ __global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_cons
   using E = Enc<D, B, false>;
   constexpr int PPR = kChunk / E::VPC;  // passes per record
   __shared__ float2 cells[B >= 3 ? kCells : 1];
+  __shared__ __align__(16) float tbuf[D == 512 ? (kThreads / 32) * 2 * kTVec : 4];
+  float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   if constexpr (B >= 3) {
     build_cells(p.c, cells);
     __syncthreads();
@@ -309,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_cons
     float x[32];
     float inv;
     uint32_t omask;
-    enc_vector<D, B, false>(p.c, ln, cells, w, cvalid, rec, (int)(ctok % kChunk), x, inv, omask);
+    enc_vector<D, B, false>(p.c, ln, cells, tb, w, cvalid, rec, (int)(ctok % kChunk), x, inv, omask);
   }
 }
 
@@ -325,6 +375,8 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   const int k = len >= p.floor_ + kChunk ? min((len - p.floor_) / kChunk, p.max_evict) : 0;
   if (e >= k || nch < 0 || nch + k > p.rec_cap) return;
   __shared__ float2 cells[B >= 3 ? kCells : 1];
+  __shared__ __align__(16) float tbuf[D == 512 ? (kThreads / 32) * 2 * kTVec : 4];
+  float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   if constexpr (B >= 3) {
     build_cells(p.c, cells);
     __syncthreads();
@@ -335,7 +387,7 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   const int first = start + e * kChunk;
   const int cap = p.tail_cap;
   auto row = [&](int slot) { return tail + (int64_t)((first + min(slot, kChunk - 1)) % cap) * D; };
-  encode_record<D, B, OUTL>(p.c, cells, row, rec, 0, kChunk, &sm);
+  encode_record<D, B, OUTL>(p.c, cells, tb, row, rec, 0, kChunk, &sm);
 }
 
 __global__ void evict_commit_kernel(const EvictCommitParams p) {
