@@ -176,8 +176,7 @@ __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B
     if constexpr (B >= 3) {  // decision cells (shared table)
       const float z = x[r] * zscale;
       const uint32_t ci = __float_as_uint(z + 8388736.0f) & 0x1FFu;  // round(z) + 128 (2^23 + 128 magic)
-      const float2 e = cells[ci];
-      code = (uint32_t)__float_as_int(e.y) - mask_gt(z, e.x);
+      code = cell_count(cells, ci) - mask_gt(z, cell_boundary(cells, ci));
     } else {
       uint32_t msum = 0u;  // -(number of positive boundaries below |w|)
 #pragma unroll
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) encode_record_kernel(const __grid_co
   float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   __shared__ float2 cells[B >= 3 ? kCells : 1];
   if constexpr (B >= 3) {
-    build_cells(p.c, cells);
+    build_cells<true>(p.c, cells);
     __syncthreads();
   }
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
@@ -328,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) encode_pass_kernel(const __grid_cons
   __shared__ __align__(16) float tbuf[D == 512 ? (kThreads / 32) * 2 * kTVec : 4];
   float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   if constexpr (B >= 3) {
-    build_cells(p.c, cells);
+    build_cells<true>(p.c, cells);
     __syncthreads();
   }
   const EncLane<D, B, false> ln(p.c);
@@ -378,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   __shared__ __align__(16) float tbuf[D == 512 ? (kThreads / 32) * 2 * kTVec : 4];
   float* tb = tbuf + (threadIdx.x >> 5) * 2 * kTVec;
   if constexpr (B >= 3) {
-    build_cells(p.c, cells);
+    build_cells<true>(p.c, cells);
     __syncthreads();
   }
   uint8_t* rec = p.rec + l * p.rec_ls +

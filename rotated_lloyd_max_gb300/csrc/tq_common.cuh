@@ -165,6 +165,11 @@ constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell
 constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
 constexpr float kCellScale = 128.f;
 
+// SPLIT: the table's two planes (boundaries as f32, counts as bytes) in the
+// storage of kCells float2 (the CUDA-core encoder, whose crowded lookups
+// spread over more banks as 4- and 1-byte loads); otherwise float2 entries
+// (boundary, count as int bits), one 8-byte load per lookup.
+template <bool SPLIT = false>
 __device__ __forceinline__ void build_cells(const CodecDev& c, float2* cells) {
   const int nb = (1 << c.bits) - 1;
   for (int i = threadIdx.x; i < kCells; i += kThreads) {
@@ -176,9 +181,22 @@ __device__ __forceinline__ void build_cells(const CodecDev& c, float2* cells) {
       if (t < lo) ++below;
       else if (t < hi) inside = t * kCellScale;
     }
-    cells[i] = make_float2(inside, __int_as_float(below));
-    if (i == kPosCell && c.bits == 2) cells[i].x = c.boundaries[2] * kCellScale;
+    const float bnd = (i == kPosCell && c.bits == 2) ? c.boundaries[2] * kCellScale : inside;
+    if constexpr (SPLIT) {
+      float* bt = reinterpret_cast<float*>(cells);
+      bt[i] = bnd;
+      reinterpret_cast<uint8_t*>(bt + kCells)[i] = (uint8_t)below;
+    } else {
+      cells[i] = make_float2(bnd, __int_as_float(below));
+    }
   }
+}
+// lookups in the SPLIT layout
+__device__ __forceinline__ float cell_boundary(const float2* cells, uint32_t i) {
+  return reinterpret_cast<const float*>(cells)[i];
+}
+__device__ __forceinline__ uint32_t cell_count(const float2* cells, uint32_t i) {
+  return reinterpret_cast<const uint8_t*>(reinterpret_cast<const float*>(cells) + kCells)[i];
 }
 
 }  // namespace tq
