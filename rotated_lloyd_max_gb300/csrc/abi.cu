@@ -178,6 +178,11 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
     if (comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
     if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
   }
+  // at head dim 512 a dense split's partial (512 floats per query head, written
+  // and read back by the merge) outweighs a short run of tail tokens: at least
+  // 128 tokens per split, as on the head-dim 64/128 tensor-core path
+  if ((pl->mma512 || pl->umma512) && a->splits <= 0 && St > 0)
+    St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
   if (pl->umma512 && a->splits <= 0 && comp_tiles > 0) {
     // one CTA per SM: the split count that minimises waves x records per
     // split (plus about two records' worth of per-CTA set-up and partials)
