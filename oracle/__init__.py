@@ -66,8 +66,8 @@ def _load():
             "orc_pack_record": (None, [i32, i32, i32, i32, i32, P, P, P, P, P]),
             "orc_read_code": (i32, [P, i32, i32]),
             "orc_decode_records": (None, [P, i64, i64, i32, i32, i32, i32, P, P, i32, P]),
-            "orc_attention": (None, [P, i32, P, P, i64, i32, f64, P]),
-            "orc_attention_rotated": (None, [P, i32, P, P, i64, P, P, i64, i32, f64, P, P, P]),
+            "orc_attention": (None, [P, i32, P, P, i64, i32, f64, f64, P]),
+            "orc_attention_rotated": (None, [P, i32, P, P, i64, P, P, i64, i32, f64, f64, P, P, P]),
             "orc_retention_floor": (i32, [i32, i32, i32]),
             "orc_chunks_to_evict": (i32, [i32, i32, i32, i32, i32]),
         }
@@ -247,18 +247,19 @@ def decode_records(records: np.ndarray, n: int, codec: Codec, rotated: bool = Fa
 # ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------
-def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
-    """Brute-force softmax attention in fp64.  q [G, d], K/V [n, d] -> [G, d]."""
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, softcap: float = 0.0) -> np.ndarray:
+    """Brute-force softmax attention in fp64.  q [G, d], K/V [n, d] -> [G, d].
+    softcap > 0 caps each logit s = scale * q.k to softcap * tanh(s / softcap)."""
     q = np.ascontiguousarray(q, np.float64)
     K = np.ascontiguousarray(K, np.float64)
     V = np.ascontiguousarray(V, np.float64)
     G, d = q.shape
     out = np.zeros((G, d), np.float64)
-    _load().orc_attention(_p(q), G, _p(K), _p(V), K.shape[0], d, float(scale), _p(out))
+    _load().orc_attention(_p(q), G, _p(K), _p(V), K.shape[0], d, float(scale), float(softcap), _p(out))
     return out
 
 
-def attention_rotated(q, Kr, Vr, Kd, Vd, scale, sk, sv):
+def attention_rotated(q, Kr, Vr, Kd, Vd, scale, sk, sv, softcap=0.0):
     """Rotated-domain evaluation of the same attention (cross-check only)."""
     q = np.ascontiguousarray(q, np.float64)
     G, d = q.shape
@@ -266,14 +267,14 @@ def attention_rotated(q, Kr, Vr, Kd, Vd, scale, sk, sv):
     Kr, Vr, Kd, Vd = f(Kr), f(Vr), f(Kd), f(Vd)
     out = np.zeros((G, d), np.float64)
     _load().orc_attention_rotated(_p(q), G, _p(Kr), _p(Vr), Kr.shape[0], _p(Kd), _p(Vd),
-                                  Kd.shape[0], d, float(scale),
+                                  Kd.shape[0], d, float(scale), float(softcap),
                                   _p(np.ascontiguousarray(sk, np.int8)),
                                   _p(np.ascontiguousarray(sv, np.int8)), _p(out))
     return out
 
 
 def unit_attention(q_bf16, codec_k: Codec | None, codec_v: Codec | None, k_rec, v_rec, n_comp,
-                   k_dense_bf16, v_dense_bf16, scale):
+                   k_dense_bf16, v_dense_bf16, scale, softcap=0.0):
     """Decode-attention output for one (layer, batch, kv-head) unit.
 
     q_bf16 [G, d] uint16; compressed tokens 0..n_comp-1 in k_rec/v_rec (records);
@@ -291,7 +292,7 @@ def unit_attention(q_bf16, codec_k: Codec | None, codec_v: Codec | None, k_rec, 
         Vs.append(bf16_to_f64(v_dense_bf16).reshape(-1, d))
     K = np.concatenate(Ks) if Ks else np.zeros((0, d))
     V = np.concatenate(Vs) if Vs else np.zeros((0, d))
-    return attention(q, K, V, scale)
+    return attention(q, K, V, scale, softcap)
 
 
 # ---------------------------------------------------------------------------

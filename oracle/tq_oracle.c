@@ -22,7 +22,9 @@
  *   [P4] "feat(v4): TurboQuant KV storage for DeepSeek-V4" (arc PR #98),
  *        "What landed" and its bytes-per-token table (256 packed + one f32
  *        norm = 260 B at head_dim 512), "Eviction is chunked, on purpose"
- *        (EVICT_CHUNK = 128, tail bound window + max(t_q-1, margin) + chunk).
+ *        (EVICT_CHUNK = 128, tail bound window + max(t_q-1, margin) + chunk),
+ *        and its softcapping fix (the cap applied after the scale multiply,
+ *        before the logits are stored and their maximum taken).
  *
  * Readings where the pages are silent (each is a stated choice):
  *   - sign diagonal: SplitMix64 (Steele, Lea & Flood, OOPSLA 2014), top bit
@@ -351,12 +353,20 @@ void orc_decode_records(const uint8_t* recs, int64_t rec_bytes, int64_t n, int d
 /* Attention                                                                 */
 /* ------------------------------------------------------------------------- */
 /*
+ * Logit soft cap [P4, the softcapping fix]: s -> cap * tanh(s / cap), applied
+ * to s = scale * q . k before the logit is stored and before the maximum is
+ * taken.  cap = 0 means no cap (the pages' own kernel uses 1.0 as its "off"
+ * value; here 1.0 is an ordinary cap).
+ */
+static double soft_cap(double s, double cap) { return cap > 0.0 ? cap * tanh(s / cap) : s; }
+
+/*
  * Brute-force softmax attention of G query rows over n keys/values, all in the
- * original basis and fp64:  out_g = sum_i softmax_i(scale * q_g . k_i) v_i.
+ * original basis and fp64:  out_g = sum_i softmax_i(cap(scale * q_g . k_i)) v_i.
  * With n = 0 the output is zero.
  */
 void orc_attention(const double* q, int G, const double* K, const double* V, int64_t n, int d,
-                   double scale, double* out) {
+                   double scale, double softcap, double* out) {
 #pragma omp parallel for schedule(static)
   for (int g = 0; g < G; ++g) {
     double* o = out + (int64_t)g * d;
@@ -367,7 +377,7 @@ void orc_attention(const double* q, int G, const double* K, const double* V, int
     for (int64_t i = 0; i < n; ++i) {
       double acc = 0.0;
       for (int j = 0; j < d; ++j) acc += q[(int64_t)g * d + j] * K[i * d + j];
-      logit[i] = scale * acc;
+      logit[i] = soft_cap(scale * acc, softcap);
       if (logit[i] > m) m = logit[i];
     }
     double Z = 0.0;
@@ -393,7 +403,7 @@ void orc_attention(const double* q, int G, const double* K, const double* V, int
  */
 void orc_attention_rotated(const double* q, int G, const double* Kr, const double* Vr, int64_t nc,
                            const double* Kd, const double* Vd, int64_t nd, int d, double scale,
-                           const int8_t* sk, const int8_t* sv, double* out) {
+                           double softcap, const int8_t* sk, const int8_t* sv, double* out) {
   for (int g = 0; g < G; ++g) {
     double qt[512], acc_r[512], acc_d[512];
     for (int j = 0; j < d; ++j) qt[j] = sk[j] * q[(int64_t)g * d + j];
@@ -413,7 +423,7 @@ void orc_attention_rotated(const double* q, int G, const double* Kr, const doubl
         for (int j = 0; j < d; ++j) acc += qt[j] * Kr[i * d + j];
       else
         for (int j = 0; j < d; ++j) acc += q[(int64_t)g * d + j] * Kd[(i - nc) * d + j];
-      logit[i] = scale * acc;
+      logit[i] = soft_cap(scale * acc, softcap);
       if (logit[i] > m) m = logit[i];
     }
     double Z = 0.0;

@@ -84,6 +84,61 @@ def test_query_head_permutation_permutes_outputs(orc):
     np.testing.assert_allclose(b, a[perm], atol=0)
 
 
+def test_softcap_closed_form_position(orc):
+    """Soft cap after the scale multiply (arc PR #98, softcapping fix): with
+    cap 2 and scaled logits 2 atanh(1/2) and -2 atanh(1/2) the capped logits
+    are exactly +1 and -1, so one-hot values return the weights
+    1/(1 + e^-2) and 1/(1 + e^2).  Capping before the scale (scale 1/2 here)
+    or not at all gives other weights."""
+    d, cap, scale = 64, 2.0, 0.5
+    a = 2 * np.arctanh(0.5) / scale          # q.k of token 0
+    q = np.zeros((1, d)); q[0, 0] = 1.0
+    K = np.zeros((2, d)); K[0, 0], K[1, 0] = a, -a
+    V = np.zeros((2, d)); V[0, 3] = V[1, 7] = 1.0
+    out = orc.attention(q, K, V, scale, cap)[0]
+    w0 = 1.0 / (1.0 + np.exp(-2.0))
+    assert abs(out[3] - w0) < 1e-14 and abs(out[7] - (1.0 - w0)) < 1e-14
+    assert abs(orc.attention(q, K, V, scale)[0, 3] - w0) > 0.01        # uncapped: 0.900
+
+
+def test_softcap_bounds_the_weight_ratio(orc):
+    """Capped logits lie in (-cap, cap), so no two softmax weights differ by
+    more than a factor e^(2 cap), however large the raw logits are."""
+    rng = np.random.default_rng(5)
+    d, n, cap = 40, 40, 1.5
+    q = rng.standard_normal((3, d)) * 10
+    K = rng.standard_normal((n, d)) * 10
+    V = np.zeros((n, n)); np.fill_diagonal(V, 1.0)        # one-hot rows: out = weights
+    w = orc.attention(q, K, V, 1.0, cap)
+    assert np.all(w.max(1) / w.min(1) <= np.exp(2 * cap) * (1 + 1e-12))
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-14)
+    raw = orc.attention(q, K, V, 1.0)
+    assert np.all(raw.max(1) > 1e6 * raw.min(1))          # the cap is what bounds it
+
+
+def test_softcap_large_cap_is_no_cap(orc):
+    """cap * tanh(s / cap) -> s as cap -> infinity."""
+    rng = np.random.default_rng(6)
+    q, K, V = rng.standard_normal((4, 64)), rng.standard_normal((20, 64)), rng.standard_normal((20, 64))
+    np.testing.assert_allclose(orc.attention(q, K, V, 0.3, 1e7), orc.attention(q, K, V, 0.3), atol=1e-11)
+
+
+def test_softcap_rotated_form_equals_brute_force(orc):
+    d, nc, nd, G = 64, 200, 30, 4
+    ck, cv = _codec(orc, d, 3), _codec(orc, d, 2)
+    k, v = synth.gaussian_bf16((nc, d), 14), synth.gaussian_bf16((nc, d), 15)
+    kr, vr = orc.encode_records(k, ck), orc.encode_records(v, cv)
+    kd, vd = synth.gaussian_bf16((nd, d), 16), synth.gaussian_bf16((nd, d), 17)
+    q = synth.gaussian_bf16((G, d), 18)
+    brute = orc.unit_attention(q, ck, cv, kr, vr, nc, kd, vd, 0.5, softcap=3.0)
+    rot = orc.attention_rotated(orc.bf16_to_f64(q), orc.decode_records(kr, nc, ck, rotated=True),
+                                orc.decode_records(vr, nc, cv, rotated=True),
+                                orc.bf16_to_f64(kd), orc.bf16_to_f64(vd), 0.5,
+                                orc.signs(1, d), orc.signs(1, d), softcap=3.0)
+    np.testing.assert_allclose(rot, brute, atol=1e-12)
+    assert np.max(np.abs(brute - orc.unit_attention(q, ck, cv, kr, vr, nc, kd, vd, 0.5))) > 1e-2
+
+
 # --------------------------------------------------------------------------- eviction
 
 
