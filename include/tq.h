@@ -172,7 +172,7 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
 /*
  * a6-a10: fused decode attention for one group of layers sharing codecs and
  * geometry.  For layer l, batch b, query head h (kv head h / (Hq/Hkv)):
- *   out = sum_i softmax_i(scale * q . k_i) v_i  over the layer's compressed
+ *   out = sum_i softmax_i(cap(scale * q . k_i)) v_i  over the layer's compressed
  * tokens (records 0..n_chunks-1, scored in the rotated basis against
  * q~ = H(s_k . q)/sqrt(d) from a shared-memory centroid table, values
  * accumulated as sum p_i n_i yhat_i and brought back by one inverse
@@ -214,6 +214,11 @@ typedef struct {
    * 1: always the CUDA-core kernel.  2: as 0 but never tcgen05 (the
    * mma.sync kernels).  All paths meet the same tolerance. */
   int32_t cuda_core_path;
+  /* Logit soft cap (arc PR #98, softcapping fix): each logit s = scale * q . k
+   * becomes softcap * tanh(s / softcap) before it enters the softmax (its
+   * maximum included), for compressed and dense tokens alike.  0 = no cap;
+   * otherwise finite and > 0 (1.0 is an ordinary cap, not "off"). */
+  float softcap;
 } tq_attn_args;
 
 /* Workspace bytes tq_decode_attn needs for these arguments (0 on invalid args). */

@@ -46,7 +46,8 @@ class tq_attn_args(ctypes.Structure):
                 ("v_rec_layer_stride", c_i64), ("rec_cap", c_i32),
                 ("k_tail", c_p), ("v_tail", c_p), ("tail_layer_stride", c_i64), ("tail_cap", c_i32),
                 ("n_chunks", c_p), ("tail_start", c_p), ("tail_len", c_p),
-                ("max_chunks", c_i32), ("max_tail", c_i32), ("splits", c_i32), ("cuda_core_path", c_i32)]
+                ("max_chunks", c_i32), ("max_tail", c_i32), ("splits", c_i32), ("cuda_core_path", c_i32),
+                ("softcap", c_f32)]
 
 
 _SIGS = {
@@ -224,11 +225,11 @@ def tq_evict(k_codec: Codec, v_codec: Codec | None, *, k_rec, v_rec, k_tail, v_t
 def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None, v_tail=None,
                    n_chunks=None, tail_start=None, tail_len=None, max_chunks: int = 0,
                    max_tail: int = 0, splits: int = 0, n_kv_heads: int | None = None,
-                   cuda_core_path: bool | int = False) -> tq_attn_args:
+                   cuda_core_path: bool | int = False, softcap: float = 0.0) -> tq_attn_args:
     """Build tq_attn_args from tensors.
     q: bf16 [L, B, Hq, d] (head and dim axes packed); out: f32 [L, B, Hq, d] contiguous;
     k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, bytes]; k_tail/v_tail: bf16 [L, B, Hkv, cap, d];
-    counters int32 [L, B]."""
+    counters int32 [L, B]; softcap > 0 caps each logit to softcap * tanh(logit / softcap)."""
     L, B, Hq, d = q.shape
     assert q.stride(3) == 1 and q.stride(2) == d, "query heads and dims must be packed"
     assert out.is_contiguous() and tuple(out.shape) == (L, B, Hq, d)
@@ -250,6 +251,7 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     a.tail_len = _ptr(tail_len)
     a.max_chunks, a.max_tail, a.splits = max_chunks, max_tail, splits
     a.cuda_core_path = int(cuda_core_path)  # 0 automatic, 1 CUDA cores, 2 no tcgen05
+    a.softcap = softcap
     # the struct holds raw device pointers: keep the tensors alive with it
     a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len)
     return a

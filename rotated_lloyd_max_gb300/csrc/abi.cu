@@ -99,6 +99,7 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   if (a->q_layer_stride < 0 || a->q_batch_stride < 0 || a->q_layer_stride % 8 || a->q_batch_stride % 8)
     return TQ_ERR_INVALID_ARG;
   if (!(std::isfinite(a->scale))) return TQ_ERR_INVALID_ARG;
+  if (!(std::isfinite(a->softcap)) || a->softcap < 0.f) return TQ_ERR_INVALID_ARG;
   if (a->max_chunks < 0 || a->max_tail < 0 || a->splits < 0) return TQ_ERR_INVALID_ARG;
   pl->D = D;
   pl->G = a->n_q_heads / a->n_kv_heads;
@@ -527,6 +528,8 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.G = pl.G;
   p.n_hg = pl.n_hg;
   p.sscale = (float)((double)a->scale * 1.4426950408889634074);
+  p.scap = a->softcap > 0.f ? (float)((double)a->softcap * 1.4426950408889634074) : 0.f;
+  p.iscap = a->softcap > 0.f ? (float)(1.0 / ((double)a->softcap * 1.4426950408889634074)) : 0.f;
   p.q = (const uint16_t*)a->q;
   p.q_ls = a->q_layer_stride;
   p.q_bs = a->q_batch_stride;

@@ -252,7 +252,11 @@ __device__ __forceinline__ void attn_dense_split(const AttnParams& p, unsigned c
         }
       if (slice == 0 && stok < ntok) {
 #pragma unroll
-        for (int h = 0; h < GT; ++h) logit[stok * GTP + h] = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * p.sscale;
+        for (int h = 0; h < GT; ++h) {
+          float t = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * p.sscale;
+          if (p.scap > 0.f) t = soft_cap(t, p.scap, p.iscap);
+          logit[stok * GTP + h] = t;
+        }
       }
     }
     __syncthreads();
@@ -592,7 +596,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         if (slice == 0) {
           const float f = knorm[tok] * p.sscale;
 #pragma unroll
-          for (int h = 0; h < GT; ++h) logit[tok * GTP + h] = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * f;
+          for (int h = 0; h < GT; ++h) {
+            float t = (h & 1 ? a[h >> 1].y : a[h >> 1].x) * f;
+            if (p.scap > 0.f) t = soft_cap(t, p.scap, p.iscap);
+            logit[tok * GTP + h] = t;
+          }
         }
       }
       __syncthreads();

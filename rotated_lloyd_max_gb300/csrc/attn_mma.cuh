@@ -338,6 +338,10 @@ __device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char*
     sc[1] = (hv1 && va) ? sc[1] * p.sscale : -INFINITY;
     sc[2] = (hv0 && vb) ? sc[2] * p.sscale : -INFINITY;
     sc[3] = (hv1 && vb) ? sc[3] * p.sscale : -INFINITY;
+    if (p.scap > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[e] = soft_cap(sc[e], p.scap, p.iscap);
+    }
     // online softmax (lazy rescale)
     const bool need = (sc[0] > m0 + 8.f) | (sc[2] > m0 + 8.f) | (sc[1] > m1 + 8.f) | (sc[3] > m1 + 8.f);
     if (__any_sync(0xffffffffu, need)) {
@@ -613,6 +617,12 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
       sc[mt][1] = hv1 ? sc[mt][1] * fa : -INFINITY;
       sc[mt][2] = hv0 ? sc[mt][2] * fb : -INFINITY;
       sc[mt][3] = hv1 ? sc[mt][3] * fb : -INFINITY;
+    }
+    if (p.scap > 0.f) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[mt][e] = soft_cap(sc[mt][e], p.scap, p.iscap);
     }
     // ---- online softmax (the max moves only when a logit passes it by 2^8)
     {

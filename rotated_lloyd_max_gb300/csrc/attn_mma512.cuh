@@ -240,10 +240,18 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 8 * nt + 2 * t;
         const bool v0 = h < GT, v1 = h + 1 < GT;
-        lg_s[ta * HN + h] = v0 ? (cc[nt][0] + cl[nt][0] + ch[nt][0]) * fq[nt][0] * fa : -INFINITY;
-        lg_s[ta * HN + h + 1] = v1 ? (cc[nt][1] + cl[nt][1] + ch[nt][1]) * fq[nt][1] * fa : -INFINITY;
-        lg_s[tb * HN + h] = v0 ? (cc[nt][2] + cl[nt][2] + ch[nt][2]) * fq[nt][0] * fb : -INFINITY;
-        lg_s[tb * HN + h + 1] = v1 ? (cc[nt][3] + cl[nt][3] + ch[nt][3]) * fq[nt][1] * fb : -INFINITY;
+        float x[4] = {v0 ? (cc[nt][0] + cl[nt][0] + ch[nt][0]) * fq[nt][0] * fa : -INFINITY,
+                      v1 ? (cc[nt][1] + cl[nt][1] + ch[nt][1]) * fq[nt][1] * fa : -INFINITY,
+                      v0 ? (cc[nt][2] + cl[nt][2] + ch[nt][2]) * fq[nt][0] * fb : -INFINITY,
+                      v1 ? (cc[nt][3] + cl[nt][3] + ch[nt][3]) * fq[nt][1] * fb : -INFINITY};
+        if (p.scap > 0.f) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = soft_cap(x[e], p.scap, p.iscap);
+        }
+        lg_s[ta * HN + h] = x[0];
+        lg_s[ta * HN + h + 1] = x[1];
+        lg_s[tb * HN + h] = x[2];
+        lg_s[tb * HN + h + 1] = x[3];
       }
     }
     __syncthreads();

@@ -342,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
       float lg[GT];
 #pragma unroll
       for (int h = 0; h < GT; ++h) lg[h] = valid ? ((h & 1) ? a[h >> 1].y : a[h >> 1].x) * p.sscale : -INFINITY;
+      if (p.scap > 0.f) {
+#pragma unroll
+        for (int h = 0; h < GT; ++h) lg[h] = soft_cap(lg[h], p.scap, p.iscap);
+      }
       // online softmax (the SL lanes of a token hold the same logits)
       bool need = false;
 #pragma unroll
@@ -459,6 +463,10 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
         const float f = knorm[tloc] * p.sscale;
   #pragma unroll
         for (int h = 0; h < GT; ++h) lg[h] *= f;
+        if (p.scap > 0.f) {
+  #pragma unroll
+          for (int h = 0; h < GT; ++h) lg[h] = soft_cap(lg[h], p.scap, p.iscap);
+        }
       }
 
       // ---- online softmax (warp-local, the max moves only when a logit passes it by 2^8)

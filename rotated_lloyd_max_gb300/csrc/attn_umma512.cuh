@@ -509,6 +509,10 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
           t[16 * x + i] = h < GT ? (__uint_as_float(a[i]) + __uint_as_float(c[i])) * nk * ms.qsc[h] : -INFINITY;
         }
       }
+      if (p.scap > 0.f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[i] = soft_cap(t[i], p.scap, p.iscap);
+      }
     };
     float nk = norm_at(kb0, p.krec_bytes, p.k_off_norm, 0);
     float nv = norm_at(vb0, p.vrec_bytes, p.v_off_norm, 0);

@@ -199,4 +199,14 @@ __device__ __forceinline__ uint32_t cell_count(const float2* cells, uint32_t i) 
   return reinterpret_cast<const uint8_t*>(reinterpret_cast<const float*>(cells) + kCells)[i];
 }
 
+// Logit soft cap (arc PR #98, softcapping fix: cap * tanh(s / cap) on the
+// scaled logit, before it is stored and before the running maximum) in the
+// log2 domain of the attention kernels: with t = s * log2(e) and
+// C = cap * log2(e), log2(e) * cap * tanh(s / cap) = C * tanh(t / C).  A
+// masked slot (-inf) stays masked.  Callers test C > 0 (a launch-uniform
+// branch) before calling.
+__device__ __forceinline__ float soft_cap(float t, float C, float iC) {
+  return t > -INFINITY ? C * tanhf(t * iC) : t;
+}
+
 }  // namespace tq

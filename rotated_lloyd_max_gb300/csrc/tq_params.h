@@ -63,6 +63,7 @@ struct DecodeParams {
 struct AttnParams {
   int L, B, Hq, Hkv, G, n_hg;
   float sscale;  // softmax scale * log2(e)
+  float scap, iscap;  // logit soft cap * log2(e) and its reciprocal; 0, 0 = no cap
   const uint16_t* q;
   int64_t q_ls, q_bs;
   const uint8_t* krec;

@@ -110,6 +110,16 @@ def test_calls_fail_loudly_on_bad_arguments(lib):
     a.k_rec = 0x30000   # records without codecs
     assert L.tq_decode_attn(ctypes.byref(a), None, None, fake, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_decode_attn_workspace_size(ctypes.byref(a), None, None) == 0
+    # soft cap: 0 (off) and positive caps are accepted, negative or non-finite ones rejected
+    a.k_rec = None
+    a.k_tail, a.v_tail, a.tail_cap, a.max_tail, a.tail_layer_stride = 0x30000, 0x40000, 16, 16, 2 * 16 * 128
+    a.tail_start, a.tail_len = 0x50000, 0x60000
+    for cap, ok in [(0.0, True), (30.0, True), (1.0, True), (-1.0, False), (float("nan"), False),
+                    (float("inf"), False)]:
+        a.softcap = cap
+        assert (L.tq_decode_attn_workspace_size(ctypes.byref(a), None, None) > 0) == ok, cap
+        if not ok:
+            assert L.tq_decode_attn(ctypes.byref(a), None, None, fake, 1 << 20, None) == tq.TQ_ERR_INVALID_ARG
     # eviction: null counters
     e = tq.tq_evict_args()
     e.n_layers, e.batch, e.n_kv_heads, e.max_evict, e.rec_cap, e.tail_cap, e.t_q = 1, 1, 1, 1, 4, 272, 1

@@ -36,9 +36,12 @@ def _ocodec(orc, c):
 
 def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=False, dense=False,
              tail_cap=None, splits=0, seed=0, q_pad=0, k_outlier_frac=0.0, end_to_end=True, scale=1.0,
-             cuda_core_path=False, zero_every=0):
+             cuda_core_path=False, zero_every=0, softcap=0.0, oracle_softcap=None):
     """chunks[b], tails[b]: compressed records and dense tail tokens of batch b
-    (the same for every layer).  Returns (gpu_out, oracle_out, oracle_e2e_out)."""
+    (the same for every layer).  softcap: the logit cap of the GPU call and, unless
+    oracle_softcap says otherwise, of the oracle.  Returns (gpu_out, oracle_out,
+    oracle_e2e_out)."""
+    ocap = softcap if oracle_softcap is None else oracle_softcap
     import torch
     dev = "cuda"
     Hq = G * Hkv
@@ -88,7 +91,7 @@ def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=F
                   max_tail=max(tails))
     kw["n_kv_heads"] = Hkv
     tq.decode_attn(k_codec=None if dense else kc, v_codec=None if dense else vc, splits=splits,
-                   cuda_core_path=cuda_core_path, **kw)
+                   cuda_core_path=cuda_core_path, softcap=softcap, **kw)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
 
@@ -103,12 +106,13 @@ def run_case(tq, orc, *, d, G, Hkv, B, L, chunks, tails, kb, vb, T=0.0, shared=F
                 qh = qb[l, b, h * G:(h + 1) * G]
                 kr = rec_np["k"][l, b, h] if not dense else None
                 vr = rec_np["v"][l, b, h] if not dense else None
-                want[l, b, h * G:(h + 1) * G] = orc.unit_attention(qh, okc, ovc, kr, vr, nc * 128, kd, vd, scale)
+                want[l, b, h * G:(h + 1) * G] = orc.unit_attention(qh, okc, ovc, kr, vr, nc * 128, kd, vd, scale,
+                                                                   ocap)
                 if want_e2e is not None:
                     okr = orc.encode_records(kx[l, b, h, :nc * 128], okc) if nc else None
                     ovr = orc.encode_records(vx[l, b, h, :nc * 128], ovc) if nc else None
                     want_e2e[l, b, h * G:(h + 1) * G] = orc.unit_attention(qh, okc, ovc, okr, ovr, nc * 128,
-                                                                           kd, vd, scale)
+                                                                           kd, vd, scale, ocap)
     return got, want, want_e2e
 
 
@@ -212,6 +216,35 @@ def test_tcgen05_d512_matches_mma_sync(tq, orc):
     _assert_close(a, want)
     _assert_close(b, want)
     assert np.max(np.abs(a - b)) <= 1e-4
+
+
+# soft cap 4 on logits of scale 6 (about N(0, 36)): most logits are capped.
+# path: 0 automatic (tensor cores where they apply), 1 CUDA cores, 2 no tcgen05
+SOFTCAP_CASES = [("tiny_gqa4_tail", 0), ("tiny_gqa4_tail", 1), ("qwen_like_gqa6", 0),
+                 ("outliers_gqa4", 0), ("d256_mha_b1", 0), ("gqa3_odd_group", 0),
+                 ("mqa_shared_d512", 0), ("mqa_shared_d512", 1), ("mqa_shared_d512", 2)]
+
+
+@pytest.mark.parametrize("name,path", SOFTCAP_CASES)
+def test_softcap(tq, orc, name, path):
+    """Logit soft cap (arc PR #98, softcapping fix) on every kernel family:
+    compressed and dense tokens, side lists, tcgen05 and mma.sync at d 512."""
+    cfg = dict(CASES[name], scale=6.0, softcap=4.0, end_to_end=False, cuda_core_path=path)
+    got, want, _ = run_case(tq, orc, **cfg)
+    _assert_close(got, want)
+
+
+def test_softcap_is_applied(tq, orc):
+    """The capped GPU output is far from the uncapped oracle (the cap binds)."""
+    cfg = dict(CASES["mqa_shared_d512"], scale=6.0, softcap=4.0, end_to_end=False)
+    got, want, _ = run_case(tq, orc, oracle_softcap=0.0, **cfg)
+    assert np.max(np.abs(got - want)) > 50 * TOL
+
+
+def test_softcap_dense_layers(tq, orc):
+    got, want, _ = run_case(tq, orc, d=128, G=6, Hkv=2, B=1, L=1, chunks=[0], tails=[600], kb=3, vb=2,
+                            dense=True, scale=6.0, softcap=4.0)
+    _assert_close(got, want)
 
 
 def test_dense_boundary_layers(tq, orc):
