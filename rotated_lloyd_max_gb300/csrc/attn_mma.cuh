@@ -91,16 +91,6 @@ __device__ __forceinline__ void load_run(const unsigned char* row, int off, uint
   }
 }
 
-// W bits at bit offset `off` (constant after unrolling) of a word run.
-template <int NW>
-__device__ __forceinline__ uint32_t run_bits(const uint32_t (&w)[NW], int off, int W) {
-  const int wi = off >> 5, sh = off & 31;
-  uint32_t v;
-  if (sh + W <= 32 || wi + 1 >= NW) v = w[wi] >> sh;
-  else v = __funnelshift_r(w[wi], w[wi + 1], sh);
-  return v & ((1u << W) - 1u);
-}
-
 // Shared-memory byte offset of the pair-table entry named by the W-bit field
 // at bit `off` of a word run: field * 128 + lane_off (lane_off < 128), i.e.
 // the field moved to bit 7 and or-ed with the lane's bank-pair offset.
