@@ -17,7 +17,8 @@ against the measured HBM copy bandwidth, the oracle (CPU) timed on a bounded
 sample, and an end-to-end figure with host buffers copied in and out.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                  [--workload qwen2_1p5b_ctx2048|batched_b32_ctx32768|v4flash_mqa_ctx65536|longctx_b4_ctx262144]
+                  [--workload qwen2_1p5b_ctx2048|batched_b32_ctx32768|v4flash_mqa_ctx65536|longctx_b4_ctx262144
+                              |codec_roundtrip_4096x128_b3|encode_sweep_16M]
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (the path has no cross-GPU exchange); value = total bytes of all ranks / max
 rank time.
@@ -46,7 +47,9 @@ def parse_args():
                     help="timed steps (default 5000 for the Qwen2 cache, 20 for the large caches)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="qwen2_1p5b_ctx2048")
+    ap.add_argument("--workload", default="qwen2_1p5b_ctx2048",
+                    choices=["qwen2_1p5b_ctx2048", "batched_b32_ctx32768", "v4flash_mqa_ctx65536",
+                             "longctx_b4_ctx262144", "codec_roundtrip_4096x128_b3", "encode_sweep_16M"])
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -438,10 +441,255 @@ class BigCache:
         return d
 
 
+
+
+# ---------------------------------------------------------------------------
+# codec workloads: the round trip (tq_encode then tq_decode) and the encode sweep
+# ---------------------------------------------------------------------------
+def codec_items(cfg: dict) -> list:
+    """(head dim, bit width) pairs a codec workload runs, in step order."""
+    if cfg["kind"] == "codec":
+        return [(cfg["d"], cfg["bits"])]
+    return [(d, b) for d in cfg["ds"] for b in cfg["bits"]]
+
+
+def codec_bytes(d: int, bits: int, n: int) -> dict:
+    """Algorithmic bytes of encoding n bf16 vectors of head dim d at b bits
+    (no outlier lists) and of decoding them to f32: encode reads 2d and writes
+    d*b/8 code bytes + one f32 norm per vector; decode reads those record
+    bytes and writes 4d per vector."""
+    rec = n * (d * bits // 8 + 4)
+    return {"enc_in": n * 2 * d, "enc_out": rec, "dec_in": rec, "dec_out": n * 4 * d}
+
+
+class CodecWorkload:
+    """The codec round trip (4096 x 128 vectors, N(0,1) x LogNormal(0, 0.5) per
+    vector, b 3: tq_encode, then tq_decode of the records) and the encode sweep
+    (2^24 N(0,1) vectors at each head dim 64..512 and bit width 2..4, one
+    tq_encode each).  One step runs every item once; inputs, records and
+    decoded rows stay in HBM."""
+
+    def __init__(self, name, device):
+        import torch
+
+        import rotated_lloyd_max_gb300 as tq
+        import synth
+        self.tq, self.torch, self.name = tq, torch, name
+        cfg = dict(synth.CONFIGS[name])
+        self.cfg = cfg
+        self.n = n = cfg["n"]
+        self.with_decode = cfg["kind"] == "codec"
+        self.src = {}
+        for d in sorted({d for d, _ in codec_items(cfg)}):
+            if self.with_decode:   # the round trip's parity inputs (host generator, seed 0)
+                bits = synth.gaussian_bf16((n, d), cfg["data_seed"], lognormal_sigma=cfg["lognormal_sigma"])
+                self.src[d] = torch.from_numpy(bits.view("int16")).view(torch.bfloat16).to(device)
+            else:
+                self.src[d] = synth.torch_gaussian_bf16((n, d), synth.layer_seed(cfg["data_seed"], d, 0), device)
+        n_rec = (n + 127) // 128
+        self.items = []
+        for d, b in codec_items(cfg):
+            c = tq.tq_make_codebook(b, d, sign_seed=cfg["sign_seed"])
+            self.items.append({
+                "d": d, "b": b, "codec": c,
+                "rec": torch.empty((n_rec, c.record_bytes), dtype=torch.uint8, device=device),
+                "dec": torch.empty((n, d), dtype=torch.float32, device=device) if self.with_decode else None,
+                **codec_bytes(d, b, n)})
+        self.launches_per_step = len(self.items) * (2 if self.with_decode else 1)
+        self.enc_bytes = sum(it["enc_in"] + it["enc_out"] for it in self.items)
+        self.dec_bytes = sum(it["dec_in"] + it["dec_out"] for it in self.items) if self.with_decode else 0
+        self.step_bytes = self.enc_bytes + self.dec_bytes
+
+    def encode(self, it):
+        self.tq.tq_encode(it["codec"], self.src[it["d"]], it["rec"])
+
+    def decode(self, it):
+        self.tq.tq_decode(it["codec"], it["rec"], it["dec"])
+
+    def step(self):
+        for it in self.items:
+            self.encode(it)
+            if self.with_decode:
+                self.decode(it)
+
+
+def run_codec(args, world, rank, local, pg):
+    """Timed steps of a codec workload: each kernel launch bracketed by CUDA
+    events on the launching stream, L2 flushed before every step (the sweep's
+    inputs, 2-16 GiB per item, exceed L2 on their own)."""
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from rotated_lloyd_max_gb300 import build as b
+    b.build()
+    import rotated_lloyd_max_gb300 as tq
+    tq.load()
+    wl = CodecWorkload(args.workload, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        wl.step()
+    torch.cuda.synchronize()
+    # every launch is captured once and replayed: the round trip's kernels run
+    # for microseconds, less than the host's argument marshalling per call
+    graphs = []
+    for it in wl.items:
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, capture_error_mode="relaxed"):
+            wl.encode(it)
+        gd = None
+        if wl.with_decode:
+            gd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gd, capture_error_mode="relaxed"):
+                wl.decode(it)
+        graphs.append((ge, gd))
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        for ge, gd in graphs:
+            ge.replay()
+            if gd is not None:
+                gd.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    n_it = len(wl.items)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_it)] for _ in range(K)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    barrier(pg)
+    torch.cuda.synchronize()
+    for s in range(K):
+        flush.zero_()
+        for i, (ge, gd) in enumerate(graphs):
+            e = ev[s][i]
+            e[0].record(stream)
+            ge.replay()
+            e[1].record(stream)
+            if gd is not None:
+                gd.replay()
+            e[2].record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop()
+    t_enc = [[ev[s][i][0].elapsed_time(ev[s][i][1]) / 1e3 for s in range(K)] for i in range(n_it)]
+    t_dec = [[ev[s][i][1].elapsed_time(ev[s][i][2]) / 1e3 for s in range(K)] for i in range(n_it)]
+    total = sum(map(sum, t_enc)) + (sum(map(sum, t_dec)) if wl.with_decode else 0.0)
+    total_max = max_over_ranks(pg, total, dev)
+    bytes_all = sum_over_ranks(pg, wl.step_bytes * K, dev)
+    value = bytes_all / total_max / 1e9
+    hbm, _, peak_kind = peaks()
+    enc_s, dec_s = sum(map(sum, t_enc)) / K, sum(map(sum, t_dec)) / K
+    dominant = "tq_decode" if wl.with_decode and dec_s > enc_s else "tq_encode"
+    dom_bytes, dom_s = (wl.dec_bytes, dec_s) if dominant == "tq_decode" else (wl.enc_bytes, enc_s)
+    achieved = dom_bytes / dom_s / 1e9            # = bytes per launch / mean launch time, summed over items
+    per_item = []
+    for i, it in enumerate(wl.items):
+        te = sum(t_enc[i]) / K
+        row = {"d": it["d"], "bits": it["b"], "encode_us": round(te * 1e6, 2),
+               "encode_gbs": round((it["enc_in"] + it["enc_out"]) / te / 1e9, 1),
+               "encode_frac": round((it["enc_in"] + it["enc_out"]) / te / 1e9 / hbm, 4)}
+        if wl.with_decode:
+            td = sum(t_dec[i]) / K
+            row.update({"decode_us": round(td * 1e6, 2),
+                        "decode_gbs": round((it["dec_in"] + it["dec_out"]) / td / 1e9, 1)})
+        per_item.append(row)
+    line = {
+        "metric": "decode-attn KV GB/s & tok/s; encode Mvec/s; % of GB300 HBM roofline",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_max / K * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, packed codes, f32 math" + (", f32 out" if wl.with_decode else ""),
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "vectors": wl.n,
+                   "items": [f"d{d}/b{b}" for d, b in codec_items(wl.cfg)],
+                   "step": "tq_encode" + (" then tq_decode" if wl.with_decode else "") + " of every item",
+                   "l2": "flushed (256 MiB write) before each step", "parallelism": f"replicas x{world}"},
+        "breakdown": {"encode_mvec_s": round(wl.n * n_it / enc_s / 1e6, 1),
+                      "encode_gbs": round(wl.enc_bytes / enc_s / 1e9, 1),
+                      **({"decode_gbs": round(wl.dec_bytes / dec_s / 1e9, 1)} if wl.with_decode else {}),
+                      "items": per_item, "step_algorithmic_bytes": wl.step_bytes},
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "per_step_bytes": dom_bytes,
+                     "traffic": None},
+        "gpu_launches": wl.launches_per_step * K,
+    }
+    if clk:
+        line["clocks"] = clk
+    if not args.no_e2e:
+        line["e2e"] = codec_e2e(wl, max(3, min(20, K)))
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        nbytes, secs, sample = codec_oracle_sample(wl.cfg)
+        import oracle
+        line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+                                "cores": oracle.threads(), "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def codec_e2e(wl, steps: int):
+    """The codec step through the public API with host buffers: each item's
+    bf16 rows copied in from pinned memory, encoded (and decoded), and its
+    product (decoded rows, or the records) copied back, all timed."""
+    import torch
+    pin_in = {d: t.cpu().pin_memory() for d, t in wl.src.items()}
+    prod = [it["dec"] if wl.with_decode else it["rec"] for it in wl.items]
+    pin_out = [torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in prod]
+    h2d = sum(t.numel() * t.element_size() for t in pin_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pin_out)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for d, t in pin_in.items():
+            wl.src[d].copy_(t, non_blocking=True)
+        for it, p, h in zip(wl.items, prod, pin_out):
+            wl.encode(it)
+            if wl.with_decode:
+                wl.decode(it)
+            h.copy_(p, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    secs = (time.perf_counter() - t0) / steps
+    return {"value": round(wl.step_bytes / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(secs * 1e3, 4)}
+
+
+def codec_oracle_sample(cfg: dict, n_max: int = 4096):
+    """The oracle (fp64 C) on the workload's items with at most n_max vectors
+    each (the round trip in full): (algorithmic bytes, seconds, description)."""
+    import oracle
+    import synth
+    oracle.build()
+    n = min(cfg["n"], n_max)
+    decode = cfg["kind"] == "codec"
+    nbytes, secs = 0, 0.0
+    for d, b in codec_items(cfg):
+        if decode:
+            x = synth.gaussian_bf16((n, d), cfg["data_seed"], lognormal_sigma=cfg["lognormal_sigma"])
+        else:
+            x = synth.gaussian_bf16((n, d), synth.layer_seed(cfg["data_seed"], d, 0))
+        oc = oracle.Codec(d=d, bits=b, seed=cfg["sign_seed"])
+        t0 = time.perf_counter()
+        rec = oracle.encode_records(x, oc)
+        if decode:
+            oracle.decode_records(rec, n, oc)
+        secs += time.perf_counter() - t0
+        by = codec_bytes(d, b, n)
+        nbytes += by["enc_in"] + by["enc_out"] + ((by["dec_in"] + by["dec_out"]) if decode else 0)
+    what = "encode + decode" if decode else "encode"
+    return nbytes, secs, f"{what} of {n} vectors per item ({len(codec_items(cfg))} items), fp64 C oracle"
+
+
 WORKLOADS = {"qwen2_1p5b_ctx2048": QwenCache,
              "batched_b32_ctx32768": BigCache,
              "v4flash_mqa_ctx65536": BigCache,
-             "longctx_b4_ctx262144": BigCache}
+             "longctx_b4_ctx262144": BigCache,
+             "codec_roundtrip_4096x128_b3": CodecWorkload,
+             "encode_sweep_16M": CodecWorkload}
 
 
 def encode_all(wl):
@@ -706,16 +954,52 @@ def run_reference(args, world, rank, local, pg):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_codec(args, world, rank, local, pg):
+    """The oracle on a codec workload: each step encodes (and for the round
+    trip decodes) at most 4096 vectors of every item, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    for _ in range(min(max(args.warmup, 3), 3)):
+        codec_oracle_sample(cfg)
+    budget = 150.0
+    nbytes, one, sample = codec_oracle_sample(cfg)
+    K = args.steps
+    n_run = K if one * K <= budget else max(1, int(budget / one))
+    total, secs = 0, 0.0
+    for _ in range(n_run):
+        b, t, _ = codec_oracle_sample(cfg)
+        total += b
+        secs += t
+    value = total / secs / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "decode-attn KV GB/s & tok/s; encode Mvec/s; % of GB300 HBM roofline",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(secs / n_run * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "sample": sample, "steps_run": n_run},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{n_run} steps: {sample}"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.steps is None:
-        args.steps = 5000 if args.workload == "qwen2_1p5b_ctx2048" else 20
+        args.steps = {"qwen2_1p5b_ctx2048": 5000, "codec_roundtrip_4096x128_b3": 2000,
+                      "encode_sweep_16M": 5}.get(args.workload, 20)
     world, rank, local, pg = dist_init(args.gpus)
     try:
+        codec = WORKLOADS[args.workload] is CodecWorkload
         if args.impl == "reference":
-            run_reference(args, world, rank, local, pg)
+            (run_reference_codec if codec else run_reference)(args, world, rank, local, pg)
         else:
-            run_native(args, world, rank, local, pg)
+            (run_codec if codec else run_native)(args, world, rank, local, pg)
     finally:
         if pg is not None:
             pg.destroy_process_group()
