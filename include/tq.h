@@ -221,6 +221,41 @@ typedef struct {
   float softcap;
 } tq_attn_args;
 
+/* Kernels that run split-K decode attention (tq_attn_plan). */
+typedef enum {
+  TQ_ATTN_KERNEL_NONE = 0,           /* no split of this kind */
+  TQ_ATTN_KERNEL_CUDA_CORE = 1,      /* f32 FMA from the centroid table, CTA-wide softmax per tile */
+  TQ_ATTN_KERNEL_CUDA_CORE_WARP = 2, /* f32 FMA, warp-local softmax (head dims 64/128; outlier side lists) */
+  TQ_ATTN_KERNEL_MMA = 3,            /* mma.sync f16 hi/lo splits, head dims 64/128 */
+  TQ_ATTN_KERNEL_MMA512 = 4,         /* mma.sync f16 hi/lo splits, head dim 512 */
+  TQ_ATTN_KERNEL_TCGEN05 = 5         /* tcgen05 with tensor-memory accumulators, head dim 512 */
+} tq_attn_kernel;
+
+/* What tq_decode_attn launches for given arguments.  Splits are per
+ * (layer, batch, kv head, head group); a head group is the query heads one
+ * CTA serves. */
+typedef struct {
+  int32_t compressed_kernel;      /* tq_attn_kernel of the splits over records */
+  int32_t dense_kernel;           /* tq_attn_kernel of the splits over dense tokens */
+  int32_t compressed_splits;
+  int32_t dense_splits;
+  int32_t records_per_split;      /* at most; 0 without compressed splits */
+  int32_t dense_tokens_per_split; /* at most; 0 without dense splits */
+  int32_t heads_per_cta;          /* query heads per CTA of the compressed splits */
+  int32_t dense_heads_per_cta;    /* query heads per CTA of the dense splits */
+  int32_t launches;               /* kernel launches of the call, the merge included */
+  int32_t reserved;
+  uint64_t workspace_bytes;       /* = tq_decode_attn_workspace_size */
+} tq_attn_plan;
+
+/* Fills *plan with the kernels, split counts and launches tq_decode_attn
+ * would use for these arguments.  Host only: no device work, no allocation;
+ * it plans with the current device's SM count and shared memory (GB300's 152
+ * SMs and 227 KB when no device is visible).  Errors as tq_decode_attn's
+ * argument checks; TQ_ERR_INVALID_ARG when plan is NULL. */
+tq_status tq_decode_attn_plan(const tq_attn_args* args, const tq_codec* k_codec, const tq_codec* v_codec,
+                              tq_attn_plan* plan);
+
 /* Workspace bytes tq_decode_attn needs for these arguments (0 on invalid args). */
 size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k_codec,
                                      const tq_codec* v_codec);

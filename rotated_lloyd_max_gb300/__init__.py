@@ -50,6 +50,15 @@ class tq_attn_args(ctypes.Structure):
                 ("softcap", c_f32)]
 
 
+class tq_attn_plan(ctypes.Structure):
+    _fields_ = [("compressed_kernel", c_i32), ("dense_kernel", c_i32), ("compressed_splits", c_i32),
+                ("dense_splits", c_i32), ("records_per_split", c_i32), ("dense_tokens_per_split", c_i32),
+                ("heads_per_cta", c_i32), ("dense_heads_per_cta", c_i32), ("launches", c_i32),
+                ("reserved", c_i32), ("workspace_bytes", c_u64)]
+
+
+ATTN_KERNELS = {0: "none", 1: "cuda_core", 2: "cuda_core_warp", 3: "mma", 4: "mma512", 5: "tcgen05"}
+
 _SIGS = {
     "tq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tq_version": (ctypes.c_int, []),
@@ -71,6 +80,8 @@ _SIGS = {
                                       ctypes.POINTER(tq_codec), c_p, ctypes.c_size_t, c_p]),
     "tq_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(tq_attn_args), ctypes.POINTER(tq_codec),
                                               ctypes.POINTER(tq_codec), c_p]),
+    "tq_decode_attn_plan": (ctypes.c_int, [ctypes.POINTER(tq_attn_args), ctypes.POINTER(tq_codec),
+                                           ctypes.POINTER(tq_codec), ctypes.POINTER(tq_attn_plan)]),
 }
 
 NOALLOC_WORKSPACE_BYTES = 8 << 20
@@ -255,6 +266,19 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     # the struct holds raw device pointers: keep the tensors alive with it
     a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len)
     return a
+
+
+def tq_decode_attn_plan(args: tq_attn_args, k_codec, v_codec) -> dict:
+    """The kernels, split counts and launches tq_decode_attn would use (host
+    only).  Codecs are Codec objects or raw tq_codec structs."""
+    raw = lambda c: None if c is None else ctypes.byref(c.c if isinstance(c, Codec) else c)
+    p = tq_attn_plan()
+    _check("tq_decode_attn_plan", load().tq_decode_attn_plan(ctypes.byref(args), raw(k_codec), raw(v_codec),
+                                                             ctypes.byref(p)))
+    d = {f: getattr(p, f) for f, _ in tq_attn_plan._fields_ if f != "reserved"}
+    d["compressed_kernel"] = ATTN_KERNELS[d["compressed_kernel"]]
+    d["dense_kernel"] = ATTN_KERNELS[d["dense_kernel"]]
+    return d
 
 
 def tq_decode_attn_workspace_size(args: tq_attn_args, k_codec: Codec | None, v_codec: Codec | None) -> int:

@@ -219,6 +219,20 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   return TQ_OK;
 }
 
+// The launch sequence a plan takes: one kernel over every split at head dims
+// 64/128 on the tensor cores; a head-dim-512 tensor-core kernel over the
+// compressed splits plus the general kernel over the dense ones; the
+// warp-local CUDA-core kernel at head dims 64/128 when there are records; the
+// general CUDA-core kernel otherwise.  The merge follows each.
+enum class Route { kMma, kD512, kWarp, kGeneral };
+
+Route route_of(const Plan& pl) {
+  if (pl.mma) return Route::kMma;
+  if ((pl.mma512 || pl.umma512) && pl.Sc > 0) return Route::kD512;
+  if ((pl.D == 64 || pl.D == 128) && pl.Sc > 0) return Route::kWarp;
+  return Route::kGeneral;
+}
+
 }  // namespace
 
 namespace tq {
@@ -512,6 +526,43 @@ size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k
   return pl.ws_bytes;
 }
 
+tq_status tq_decode_attn_plan(const tq_attn_args* args, const tq_codec* k_codec, const tq_codec* v_codec,
+                              tq_attn_plan* plan) {
+  if (!plan) return TQ_ERR_INVALID_ARG;
+  Plan pl;
+  const tq_status st = make_plan(args, k_codec, v_codec, &pl);
+  if (st != TQ_OK) return st;
+  std::memset(plan, 0, sizeof(*plan));
+  const int St = pl.S - pl.Sc;
+  int ck = TQ_ATTN_KERNEL_CUDA_CORE, dk = TQ_ATTN_KERNEL_CUDA_CORE, dense_gt = pl.GT, launches = 2;
+  switch (route_of(pl)) {
+    case Route::kMma:
+      ck = dk = TQ_ATTN_KERNEL_MMA;
+      break;
+    case Route::kD512:
+      ck = pl.umma512 ? TQ_ATTN_KERNEL_TCGEN05 : TQ_ATTN_KERNEL_MMA512;
+      dense_gt = std::min(pl.GT, 8);
+      if (St > 0) ++launches;
+      break;
+    case Route::kWarp:
+      ck = dk = TQ_ATTN_KERNEL_CUDA_CORE_WARP;
+      break;
+    case Route::kGeneral:
+      break;
+  }
+  plan->compressed_kernel = pl.Sc > 0 ? ck : TQ_ATTN_KERNEL_NONE;
+  plan->dense_kernel = St > 0 ? dk : TQ_ATTN_KERNEL_NONE;
+  plan->compressed_splits = pl.Sc;
+  plan->dense_splits = St;
+  plan->records_per_split = pl.Sc > 0 ? pl.cps : 0;
+  plan->dense_tokens_per_split = St > 0 ? pl.tps : 0;
+  plan->heads_per_cta = pl.GT;
+  plan->dense_heads_per_cta = dense_gt;
+  plan->launches = launches;
+  plan->workspace_bytes = pl.ws_bytes;
+  return TQ_OK;
+}
+
 tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const tq_codec* v_codec,
                          void* workspace, size_t workspace_bytes, void* stream) {
   Plan pl;
@@ -577,16 +628,16 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.ws_ml = (float*)((char*)workspace + pl.ws_acc_bytes);
   cudaStream_t s = (cudaStream_t)stream;
   const int units_y = a->batch * a->n_kv_heads * pl.n_hg;
-  const bool rec_kernel = (pl.D == 64 || pl.D == 128) && pl.Sc > 0;
+  const Route route = route_of(pl);
   const int* status = nullptr;
-  if (pl.mma) {
+  if (route == Route::kMma) {
     // tensor cores: compressed and dense splits in one launch
     AttnParams pm = p;
     if (!pl.has_rec) pm.kb = pm.vb = 1;  // dense only: any instantiation (its tables go unused)
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
     if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
-  } else if ((pl.mma512 || pl.umma512) && pl.Sc > 0) {
+  } else if (route == Route::kD512) {
     // compressed splits on a d-512 tensor-core kernel, dense splits (if any)
     // on the general kernel in a second launch (groups of at most 8 heads)
     AttnParams pm = p;
@@ -613,7 +664,7 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
       const int uy = a->batch * a->n_kv_heads * pd.n_hg;
       if (launch_attn(pd, pl.D, gt, dim3(pl.S - pl.Sc, uy, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
     }
-  } else if (rec_kernel) {
+  } else if (route == Route::kWarp) {
     // compressed splits on the warp-local path, dense splits on the general
     // dense path, one launch
     attn_rec_smem_layout(p, pl.D, pl.GT);

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_calls():
     names = declared_functions()
     for want in ["tq_make_codebook", "tq_encode", "tq_decode", "tq_evict", "tq_decode_attn",
-                 "tq_decode_attn_workspace_size", "tq_record_bytes", "tq_status_string"]:
+                 "tq_decode_attn_workspace_size", "tq_decode_attn_plan", "tq_record_bytes",
+                 "tq_status_string"]:
         assert want in names
 
 
@@ -131,7 +132,8 @@ def test_struct_layouts_match_header(lib, tmp_path):
     offsets (checked by compiling a probe against include/tq.h with gcc)."""
     import subprocess
     tq, _ = lib
-    structs = {"tq_codec": tq.tq_codec, "tq_evict_args": tq.tq_evict_args, "tq_attn_args": tq.tq_attn_args}
+    structs = {"tq_codec": tq.tq_codec, "tq_evict_args": tq.tq_evict_args, "tq_attn_args": tq.tq_attn_args,
+               "tq_attn_plan": tq.tq_attn_plan}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
