@@ -241,7 +241,9 @@ class QwenCache:
             ws = max(ws, tq.tq_decode_attn_workspace_size(a, *codecs))
             self.args_layer.append((a, codecs))
         self.ws = torch.empty(ws, dtype=u8, device=device)
-        self.launches_per_step = 4
+        # kernels per step: the two encodes + what the attention call launches
+        self.plan = tq.tq_decode_attn_plan(self.args_all, self.kc, self.vc)
+        self.launches_per_step = 2 + self.plan["launches"]
         # algorithmic bytes
         nc, nd = len(self.comp), len(self.dense)
         d2 = d * 2
@@ -390,7 +392,9 @@ class BigCache:
         self.args_all = tq.make_attn_args(**kw)
         self.ws = torch.empty(tq.tq_decode_attn_workspace_size(self.args_all, self.kc, self.vc), dtype=u8,
                               device=device)
-        self.launches_per_step = (1 if self.shared else 2) + 2
+        # kernels per step: one encode per stream + what the attention call launches
+        self.plan = tq.tq_decode_attn_plan(self.args_all, self.kc, self.vc)
+        self.launches_per_step = (1 if self.shared else 2) + self.plan["launches"]
         # algorithmic bytes: inputs read, records written/read as used (codes,
         # norms, counts and the entries actually stored), tail, q, out
         self.encode_k(); self.encode_v()
@@ -816,7 +820,8 @@ def run_native(args, world, rank, local, pg):
                    "v_bits": wl.cfg["vb"], "bf16_layers": wl.dense, "l2": "flushed (256 MiB write) before each step",
                    "tail_tokens": getattr(wl, "tail", 0),
                    "step": f"encode whole cache ({n_enc} launch(es){', K and V concurrent on two streams' if concurrent_enc else ''})"
-                           f" + decode attention of all {wl.L} layers in one tq_decode_attn call (2 launches)",
+                           f" + decode attention of all {wl.L} layers in one tq_decode_attn call"
+                           f" ({wl.plan['launches']} launches)",
                    "parallelism": f"replicas x{world}"},
         "breakdown": {
             "encode_mvec_s": round(wl.vectors_per_step / (sum(t_enc) / K) / 1e6, 1),
@@ -827,6 +832,7 @@ def run_native(args, world, rank, local, pg):
             "decode_attn_per_layer_calls_us_per_step": round(per_layer * 1e6, 2),
             "encode_us_per_step": round(sum(t_enc) / K * 1e6, 2),
             "step_algorithmic_bytes": wl.step_bytes,
+            "attention_plan": wl.plan,
         },
         "roofline": {"kernel": dominant + (" (K and V launches, concurrent)" if concurrent_enc and dominant == "tq_encode" else ""),
                      **roof, "traffic": MEASURED_TRAFFIC.get((wl.name, dominant))},

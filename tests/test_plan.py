@@ -125,6 +125,14 @@ def test_head_dim_256_runs_on_cuda_cores(orc):
     assert p["compressed_kernel"] == p["dense_kernel"] == "cuda_core"
 
 
+def test_codec_objects_are_accepted(orc, c4_512):
+    """The binding takes Codec objects (as tq_make_codebook returns them) as
+    well as raw tq_codec structs, with the same plan."""
+    a = args_for(L=43, B=1, Hq=64, Hkv=1, d=512, records=510, tail=256, shared=True, rec_bytes=128 * 260)
+    wrapped = tq.Codec(c=c4_512, mse=0.0)
+    assert tq.tq_decode_attn_plan(a, wrapped, wrapped) == tq.tq_decode_attn_plan(a, c4_512, c4_512)
+
+
 def test_empty_context_is_one_dense_split():
     a = args_for(L=1, B=2, Hq=4, Hkv=2, d=128, tail=0)
     p = plan(a, None, None)
