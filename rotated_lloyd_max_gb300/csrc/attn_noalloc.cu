@@ -42,9 +42,10 @@ tq_status scratch_address(void** out) {
 
 extern "C" tq_status tq_decode_attn_noalloc(const tq_attn_args* args, const tq_codec* k_codec,
                                             const tq_codec* v_codec, void* stream) {
-  const size_t need = tq_decode_attn_workspace_size(args, k_codec, v_codec);
-  if (need == 0) return TQ_ERR_INVALID_ARG;
-  if (need > (size_t)TQ_NOALLOC_WORKSPACE_BYTES) return TQ_ERR_WORKSPACE;
+  tq_attn_plan plan;  // the planner's own status: invalid vs unsupported arguments
+  const tq_status ps = tq_decode_attn_plan(args, k_codec, v_codec, &plan);
+  if (ps != TQ_OK) return ps;
+  if (plan.workspace_bytes > (uint64_t)TQ_NOALLOC_WORKSPACE_BYTES) return TQ_ERR_WORKSPACE;
   void* ws = nullptr;
   const tq_status st = scratch_address(&ws);
   if (st != TQ_OK) return st;

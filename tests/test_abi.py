@@ -127,6 +127,26 @@ def test_calls_fail_loudly_on_bad_arguments(lib):
     assert L.tq_evict(ctypes.byref(good), ctypes.byref(good), ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARG
 
 
+def test_noalloc_rejections_need_no_device(lib):
+    """The allocation-free entry point returns the planner's status (invalid
+    vs unsupported) and rejects a workspace above its fixed array before it
+    touches a device."""
+    tq, L = lib
+    a = tq.tq_attn_args()
+    a.n_layers, a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim, a.scale = 1, 1, 6, 4, 128, 1.0
+    a.q, a.out = 0x10000, 0x20000
+    a.k_tail, a.v_tail, a.tail_cap, a.max_tail, a.tail_layer_stride = 0x30000, 0x40000, 8, 8, 8 * 128
+    a.tail_start, a.tail_len = 0x50000, 0x60000
+    assert L.tq_decode_attn_noalloc(ctypes.byref(a), None, None, None) == tq.TQ_ERR_INVALID_ARG   # 6 % 4
+    a.n_kv_heads, a.head_dim = 2, 96
+    assert L.tq_decode_attn_noalloc(ctypes.byref(a), None, None, None) == tq.TQ_ERR_UNSUPPORTED
+    a.head_dim = 512
+    a.n_layers, a.batch, a.n_q_heads, a.n_kv_heads = 64, 64, 64, 1   # 64^3 rows x 512 floats > 8 MiB
+    a.tail_layer_stride = 64 * 8 * 512
+    assert L.tq_decode_attn_workspace_size(ctypes.byref(a), None, None) > tq.NOALLOC_WORKSPACE_BYTES
+    assert L.tq_decode_attn_noalloc(ctypes.byref(a), None, None, None) == tq.TQ_ERR_WORKSPACE
+
+
 def test_struct_layouts_match_header(lib, tmp_path):
     """The ctypes mirrors of the C structs have the C compiler's size and field
     offsets (checked by compiling a probe against include/tq.h with gcc)."""
