@@ -145,6 +145,8 @@ tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, in
  * encoded into record n + e of every kv head, then n += k, start advances by
  * 128k (mod tail_cap), len -= 128k.  Records that would reach rec_cap are not
  * written and the counters of that (layer, batch) are left unchanged.
+ * tail_cap must be at least floor + 128 (otherwise the tail could never reach
+ * the eviction bound): TQ_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t n_layers, batch, n_kv_heads;

@@ -478,11 +478,11 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
     return TQ_ERR_INVALID_ARG;
   if (a->rec_cap <= 0 || a->tail_cap <= 0 || a->window < 0 || a->margin < 0 || a->t_q < 1)
     return TQ_ERR_INVALID_ARG;
-  if (kc.has_outl || vc.has_outl) {
-    // records of outlier codecs are always written whole, so nothing more to check
-  }
+  // the retention floor; a ring that cannot hold floor + one chunk never evicts
+  const int64_t floor64 = (int64_t)a->window + std::max<int64_t>((int64_t)a->t_q - 1, a->margin);
+  if ((int64_t)a->tail_cap < floor64 + TQ_CHUNK) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  const int floor_ = a->window + std::max(a->t_q - 1, a->margin);
+  const int floor_ = (int)floor64;
   EvictParams p;
   p.rec_cap = a->rec_cap;
   p.tail_ls = a->tail_layer_stride;

@@ -127,6 +127,24 @@ def test_calls_fail_loudly_on_bad_arguments(lib):
     assert L.tq_evict(ctypes.byref(good), ctypes.byref(good), ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARG
 
 
+def test_evict_rejects_a_tail_that_cannot_reach_the_bound(lib):
+    """The tail ring must hold window + max(t_q - 1, margin) + 128 tokens (272
+    at window 128, margin 16, t_q 1); smaller rings are rejected on the host."""
+    tq, L = lib
+    good = tq.tq_codec()
+    good.head_dim, good.bits = 128, 1
+    good.centroids[0], good.centroids[1], good.boundaries[0] = -0.07, 0.07, 0.0
+    e = tq.tq_evict_args()
+    e.n_layers, e.batch, e.n_kv_heads, e.max_evict, e.rec_cap, e.t_q = 1, 1, 1, 1, 4, 1
+    e.k_rec = e.v_rec = 0x10000
+    e.k_tail = e.v_tail = 0x20000
+    e.n_chunks, e.tail_start, e.tail_len = 0x30000, 0x40000, 0x50000
+    e.window, e.margin, e.tail_cap = 128, 16, 271
+    assert L.tq_evict(ctypes.byref(good), ctypes.byref(good), ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARG
+    e.window, e.margin, e.t_q, e.tail_cap = 0x7FFFFFFF, 0, 1, 0x7FFFFFFF    # floor + 128 overflows int32
+    assert L.tq_evict(ctypes.byref(good), ctypes.byref(good), ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARG
+
+
 def test_noalloc_rejections_need_no_device(lib):
     """The allocation-free entry point returns the planner's status (invalid
     vs unsupported) and rejects a workspace above its fixed array before it
