@@ -187,3 +187,52 @@ def test_struct_layouts_match_header(lib, tmp_path):
         assert int(got[name]) == ctypes.sizeof(cls), name
         for fname, _ in cls._fields_:
             assert int(got[f"{name}.{fname}"]) == getattr(cls, fname).offset, f"{name}.{fname}"
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "tq.h"
+
+/* A plain C caller of the boundary: host-only calls, fake aligned device
+ * addresses that are never dereferenced.  The 6 bf16 layers of the
+ * Qwen2-shaped cache as one dense call. */
+int main(void) {
+  tq_attn_args a;
+  tq_attn_plan p;
+  memset(&a, 0, sizeof(a));
+  a.n_layers = 6; a.batch = 1; a.n_q_heads = 12; a.n_kv_heads = 2; a.head_dim = 128; a.scale = 1.0f;
+  a.q = (const void*)0x100000; a.out = (float*)0x200000;
+  a.q_layer_stride = 12 * 128; a.q_batch_stride = 12 * 128;
+  a.k_tail = (const void*)0x300000; a.v_tail = (const void*)0x400000;
+  a.tail_layer_stride = 2 * 2048 * 128; a.tail_cap = 2048; a.max_tail = 2048;
+  a.tail_start = (const int32_t*)0x500000; a.tail_len = (const int32_t*)0x600000;
+  if (tq_version() < 10000) return 2;
+  tq_status st = tq_decode_attn_plan(&a, NULL, NULL, &p);
+  if (st != TQ_OK) { printf("%s\n", tq_status_string(st)); return 3; }
+  if ((size_t)p.workspace_bytes != tq_decode_attn_workspace_size(&a, NULL, NULL)) return 4;
+  printf("%d %d %d %d %d\n", p.compressed_kernel, p.dense_kernel, p.dense_splits, p.dense_tokens_per_split,
+         p.launches);
+  a.head_dim = 96;
+  return tq_decode_attn_plan(&a, NULL, NULL, &p) == TQ_ERR_UNSUPPORTED ? 0 : 5;
+}
+"""
+
+
+def test_plain_c_client_links_and_plans(lib, tmp_path):
+    """The library serves a C program (gcc, no Python): it links against
+    libtq_gb300.so with include/tq.h and gets the planner's answer: 6 layers x 2 kv
+    heads want ceil(16 x 152 / 12) = 203 splits, capped at the 64 tiles of 32
+    tokens and then at 128 tokens per split: 16 dense splits on mma.sync."""
+    import subprocess
+    from rotated_lloyd_max_gb300 import build
+    so = build.build()
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(so)
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(so), "-Wl,-rpath," + libdir])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.split() == ["0", "3", "16", "128", "2"]
