@@ -18,7 +18,7 @@ sample, and an end-to-end figure with host buffers copied in and out.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                   [--workload qwen2_1p5b_ctx2048|batched_b32_ctx32768|v4flash_mqa_ctx65536|longctx_b4_ctx262144
-                              |codec_roundtrip_4096x128_b3|encode_sweep_16M]
+                              |codec_roundtrip_4096x128_b3|encode_sweep_16M] [--splits N]
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (the path has no cross-GPU exchange); value = total bytes of all ranks / max
 rank time.
@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="large workloads: layers to instantiate")
     ap.add_argument("--batch", type=int, default=None, help="large workloads: batch to instantiate")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="cache workloads: splits per (layer, batch, kv head) of tq_decode_attn (0 = its planner)")
     return ap.parse_args()
 
 
@@ -185,7 +187,7 @@ class QwenCache:
 
     name = "qwen2_1p5b_ctx2048"
 
-    def __init__(self, device, seed_offset: int = 0):
+    def __init__(self, device, seed_offset: int = 0, splits: int = 0):
         import torch
 
         import rotated_lloyd_max_gb300 as tq
@@ -224,19 +226,19 @@ class QwenCache:
         self.dense_len = torch.where(comp_mask, 0, ctx).to(i32).contiguous()
         self.args_all = tq.make_attn_args(q=self.q, out=self.out, scale=1.0, k_rec=self.krec, v_rec=self.vrec,
                                           n_chunks=self.n_chunks, max_chunks=self.n_rec, k_tail=self.kx,
-                                          v_tail=self.vx, tail_len=self.dense_len, max_tail=ctx)
+                                          v_tail=self.vx, tail_len=self.dense_len, max_tail=ctx, splits=splits)
         ws = tq.tq_decode_attn_workspace_size(self.args_all, self.kc, self.vc)
         self.args_layer = []
         for l in range(L):
             if l in self.dense:
                 a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
                                       k_tail=self.kx[l:l + 1], v_tail=self.vx[l:l + 1],
-                                      tail_len=self.dense_len[l:l + 1], max_tail=ctx)
+                                      tail_len=self.dense_len[l:l + 1], max_tail=ctx, splits=splits)
                 codecs = (None, None)
             else:
                 a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
                                       k_rec=self.krec[l:l + 1], v_rec=self.vrec[l:l + 1],
-                                      n_chunks=self.n_chunks[l:l + 1], max_chunks=self.n_rec)
+                                      n_chunks=self.n_chunks[l:l + 1], max_chunks=self.n_rec, splits=splits)
                 codecs = (self.kc, self.vc)
             ws = max(ws, tq.tq_decode_attn_workspace_size(a, *codecs))
             self.args_layer.append((a, codecs))
@@ -335,7 +337,7 @@ class BigCache:
     tq_encode per stream) + decode attention of every layer in one
     tq_decode_attn call over the records and the dense tail."""
 
-    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0):
+    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0, splits: int = 0):
         import torch
 
         import rotated_lloyd_max_gb300 as tq
@@ -383,7 +385,7 @@ class BigCache:
         self.out = torch.empty((L, B, Hq, d), dtype=torch.float32, device=device)
         self.n_chunks = torch.full((L, B), self.n_rec, dtype=i32, device=device)
         kw = dict(q=self.q, out=self.out, scale=1.0, k_rec=self.krec, v_rec=self.vrec, n_chunks=self.n_chunks,
-                  max_chunks=self.n_rec)
+                  max_chunks=self.n_rec, splits=splits)
         if tail:
             self.tail_len = torch.full((L, B), tail, dtype=i32, device=device)
             self.tail_start = torch.zeros((L, B), dtype=i32, device=device)
@@ -714,9 +716,9 @@ def run_native(args, world, rank, local, pg):
     import rotated_lloyd_max_gb300 as tq
     tq.load()
     if args.workload == "qwen2_1p5b_ctx2048":
-        wl = QwenCache(dev)
+        wl = QwenCache(dev, splits=args.splits)
     else:
-        wl = BigCache(args.workload, dev, layers=args.layers, batch=args.batch)
+        wl = BigCache(args.workload, dev, layers=args.layers, batch=args.batch, splits=args.splits)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -819,6 +821,7 @@ def run_native(args, world, rank, local, pg):
                    "q_heads": wl.Hq, "head_dim": wl.d, "ctx": wl.ctx, "k_bits": wl.cfg["kb"],
                    "v_bits": wl.cfg["vb"], "bf16_layers": wl.dense, "l2": "flushed (256 MiB write) before each step",
                    "tail_tokens": getattr(wl, "tail", 0),
+                   "attention_splits": args.splits or "planner",
                    "step": f"encode whole cache ({n_enc} launch(es){', K and V concurrent on two streams' if concurrent_enc else ''})"
                            f" + decode attention of all {wl.L} layers in one tq_decode_attn call"
                            f" ({wl.plan['launches']} launches)",
