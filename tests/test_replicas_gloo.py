@@ -46,3 +46,23 @@ def test_two_rank_reduction_on_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched by torchrun with two ranks (gloo
+    here): rank 0 alone times the oracle and prints one JSON line; both ranks
+    exit 0."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, TQ_BENCH_BACKEND="gloo")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "1", "--workload", "codec_roundtrip_4096x128_b3"]
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
