@@ -78,6 +78,22 @@ def test_record_bytes_and_rejections(lib):
     assert L.tq_record_bytes(ctypes.byref(bad_cap)) == 0
 
 
+def test_record_bytes_match_the_oracle_layout(lib, orc):
+    """The library's record size equals the oracle's (an independent
+    implementation of the same layout) at every head dim and bit width, with
+    and without outlier side lists (the default capacity and an odd one)."""
+    import math
+    tq, _ = lib
+    L = tq.load()
+    for d in (64, 128, 256, 512):
+        for bits in (1, 2, 3, 4):
+            for T, cap in ((0.0, 0), (2.0, 4 * math.ceil(0.08 * 128 * d / 4)), (1.5, 100)):
+                got = L.tq_record_bytes(ctypes.byref(_codec(tq, d, bits, T, cap)))
+                want = orc.Codec(d=d, bits=bits, T=T, cap=cap).record_bytes
+                assert got == want, (d, bits, T, cap, got, want)
+                assert got % 16 == 0
+
+
 def test_calls_fail_loudly_on_bad_arguments(lib):
     tq, _ = lib
     L = tq.load()
