@@ -252,3 +252,23 @@ def test_plain_c_client_links_and_plans(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.split() == ["0", "3", "16", "128", "2"]
+
+
+def test_no_cpu_fallback_without_the_library(tmp_path):
+    """Without libtq_gb300.so every entry point raises (no silent CPU path):
+    a fresh interpreter whose package points at a missing library."""
+    import subprocess
+    import sys
+    code = (
+        "import rotated_lloyd_max_gb300 as tq\n"
+        "tq.LIB_PATH = %r\n"
+        "for call in (lambda: tq.load(), lambda: tq.tq_record_bytes(tq.Codec(c=tq.tq_codec(), mse=0.0))):\n"
+        "    try:\n"
+        "        call()\n"
+        "    except ImportError as e:\n"
+        "        assert 'no CPU fallback' in str(e)\n"
+        "    else:\n"
+        "        raise SystemExit('no error')\n"
+        "print('ok')\n" % str(tmp_path / "absent" / "libtq_gb300.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.stdout, r.stderr[-2000:])
