@@ -87,7 +87,7 @@ typedef struct {
 size_t tq_codebook_scratch_bytes(void);
 
 /*
- * a1/a2: Gaussian Lloyd-Max table and sign diagonal.  Runs the 1-D Lloyd
+ * Codebook and signs: Gaussian Lloyd-Max table and sign diagonal.  Runs the 1-D Lloyd
  * iteration t_k = (c_k + c_{k+1})/2, c_k = E[X | t_{k-1} < X <= t_k] on the
  * N(0,1) density in fp64 on the device until no centroid moves by more than
  * 1e-14, scales by 1/sqrt(d), rounds to f32 and derives the f32 midpoints;
@@ -106,7 +106,7 @@ tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float out
 size_t tq_record_bytes(const tq_codec* codec);
 
 /*
- * a3: encode.  n_groups independent streams of n_vec bf16 vectors each;
+ * Encode.  n_groups independent streams of n_vec bf16 vectors each;
  * vector i of group g is read at src + g*src_group_stride + i*src_vec_stride
  * (elements) and written as token first_vec + i of the record array at
  * dst + g*dst_group_stride (bytes).
@@ -121,7 +121,7 @@ tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, in
                     int64_t dst_group_stride, int64_t first_vec, void* stream);
 
 /*
- * a5: decode.  Tokens [first_vec, first_vec + n_vec) of each group's record
+ * Decode.  Tokens [first_vec, first_vec + n_vec) of each group's record
  * array (at src + g*src_group_stride bytes) to f32 vectors
  *   xhat = n * s . H(yhat) / sqrt(d),  yhat_j = centroid[code_j], replaced by
  *   the stored value at outlier coordinates,
@@ -134,7 +134,7 @@ tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, in
                     int64_t dst_vec_stride, int64_t dst_group_stride, void* stream);
 
 /*
- * a4: chunked eviction from dense bf16 ring-buffer tails into records, for
+ * Chunked eviction from dense bf16 ring-buffer tails into records, for
  * n_layers x batch x n_kv_heads streams in one launch (plus one small
  * bookkeeping launch), with every decision taken on the device (no host
  * synchronisation).  For each (layer, batch) with counters
@@ -172,7 +172,9 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
                    void* stream);
 
 /*
- * a6-a10: fused decode attention for one group of layers sharing codecs and
+ * Fused decode attention (query rotation, scoring of the compressed keys,
+ * online softmax, values in the rotated basis, dense tail, split-K merge
+ * with one inverse transform) for one group of layers sharing codecs and
  * geometry.  For layer l, batch b, query head h (kv head h / (Hq/Hkv)):
  *   out = sum_i softmax_i(cap(scale * q . k_i)) v_i  over the layer's compressed
  * tokens (records 0..n_chunks-1, scored in the rotated basis against

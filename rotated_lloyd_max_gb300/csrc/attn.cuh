@@ -1,4 +1,4 @@
-// a6-a9: fused split-K decode attention over rotated Lloyd-Max records and a
+// Fused split-K decode attention over rotated Lloyd-Max records and a
 // dense bf16 tail (or a whole bf16 layer).
 //
 // The query is rotated once per CTA, q~ = H(s_k . q)/sqrt(d); since H is

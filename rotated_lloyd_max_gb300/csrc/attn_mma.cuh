@@ -1,4 +1,4 @@
-// a6-a8 on the tensor cores: decode attention over the compressed records
+// Decode attention on the tensor cores over the compressed records
 // (head dims 64 and 128, up to 8 query heads of one kv head per CTA).
 //
 // Same quantities as the warp-local kernel (q~ = H(s_k . q)/sqrt(d) once per

@@ -1,4 +1,4 @@
-// a6-a8 on the tensor cores at head dim 512 (many query heads per kv head,
+// Decode attention on the tensor cores at head dim 512 (many query heads per kv head,
 // e.g. MQA with 64 query heads): decode attention over the compressed records
 // of codecs without outlier side lists.
 //

@@ -1,4 +1,4 @@
-// a6-a8: decode attention over the compressed records (head dims 64 and 128),
+// Decode attention over the compressed records (head dims 64 and 128),
 // warp-local variant.
 //
 // Dense splits of the same call (tail tokens, bf16 layers) run the general

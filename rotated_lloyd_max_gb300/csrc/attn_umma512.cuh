@@ -1,4 +1,4 @@
-// a6-a10 at head dim 512 on the fifth-generation tensor cores (tcgen05.mma,
+// Decode attention at head dim 512 on the fifth-generation tensor cores (tcgen05.mma,
 // accumulators in tensor memory), for compressed records of codecs without
 // outlier side lists and groups of up to 64 query heads per kv head (MQA).
 //

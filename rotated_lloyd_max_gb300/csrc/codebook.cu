@@ -1,4 +1,4 @@
-// a1/a2: Gaussian Lloyd-Max table and SplitMix64 sign diagonal, on the device.
+// Gaussian Lloyd-Max table and SplitMix64 sign diagonal, on the device.
 //
 // One warp; lane k owns centroid k.  The Lloyd iteration for N(0,1)
 // ("centroids_gaussian(bits)" in the M4 commits of "v1.3 PPL on vLLM";

@@ -1,4 +1,4 @@
-// a5: decode records back to f32 head vectors ("v1.3 PPL on vLLM", M5 commit:
+// Decode records back to f32 head vectors ("v1.3 PPL on vLLM", M5 commit:
 // dequantise through the centroid table, replace outlier coordinates by their
 // stored values, inverse WHT, rescale by the norm):
 //   xhat = n * s . H(yhat) / sqrt(d).

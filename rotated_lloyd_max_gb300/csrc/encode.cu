@@ -1,4 +1,4 @@
-// a3/a4: encode bf16 head vectors into 128-token records, and chunked
+// Encode bf16 head vectors into 128-token records, and chunked
 // eviction from dense ring-buffer tails into records.
 //
 // Per vector ("v1.3 PPL on vLLM", M4 Phase A/B commits: rotate = H.D.x,

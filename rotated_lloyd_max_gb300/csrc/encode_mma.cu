@@ -1,4 +1,4 @@
-// a3 at head dim 128 with the Hadamard transform on the tensor cores.
+// Encode at head dim 128 with the Hadamard transform on the tensor cores.
 //
 // Same codes as the CUDA-core encoder (n = ||x||; w = H(s . x), the
 // unnormalised Sylvester transform; y = w / (n sqrt(d)); code_j = #{k : y_j > t_k},

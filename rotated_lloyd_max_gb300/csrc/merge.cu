@@ -1,4 +1,4 @@
-// a10: merge of the split-K partials and the single inverse transform.
+// Merge of the split-K partials and the single inverse transform.
 //
 // Each split left (m_s, l_s, acc_s) in the log2 domain.  With M = max m_s and
 // w_s = 2^(m_s - M):  out = [ s_v . H(sum_{compressed s} w_s acc_s)/sqrt(d)
