@@ -149,7 +149,8 @@ def f64_to_bf16(y: float) -> int:
 # ---------------------------------------------------------------------------
 def default_outlier_cap(d: int) -> int:
     """Entries per 128-token record: 8% of the record's coordinates, rounded up
-    to a multiple of 4 (the 8% sizing is the precedent P1's vLLM slot uses)."""
+    to a multiple of 4 (the 8% slot sizing of "v1.3 PPL on vLLM: production cell +
+    per-channel attribution", M6 Phase A, is the precedent)."""
     return 4 * ((8 * CHUNK * d + 399) // 400)
 
 
