@@ -905,9 +905,11 @@ def e2e_leg(wl, dev, steps: int):
 
 
 def run_reference(args, world, rank, local, pg):
-    """The oracle (fp64 C, OpenMP) on the host cores: each step attends one
-    (layer, kv head) unit of a compressed layer and one of a bf16 layer and
-    encodes that unit's K/V, so K steps finish within minutes."""
+    """The oracle (fp64 C, OpenMP) on the host cores: each step encodes one
+    (layer, kv head) unit of a compressed layer (its packed tokens, one record
+    stream when keys and values share records) and attends it with the unit's
+    dense tail, plus one unit of a bf16 layer where the workload has them, so
+    K steps finish within minutes."""
     if rank != 0:
         return
     import numpy as np
@@ -919,20 +921,32 @@ def run_reference(args, world, rank, local, pg):
     cfg = synth.CONFIGS[args.workload]
     d, ctx, Hkv, Hq = cfg["d"], cfg["ctx"], cfg["Hkv"], cfg["Hq"]
     G = Hq // Hkv
-    okc = oracle.Codec(d=d, bits=cfg["kb"], seed=cfg["sign_seed"])
-    ovc = oracle.Codec(d=d, bits=cfg["vb"], seed=cfg["sign_seed"])
-    k = synth.gaussian_bf16((ctx, d), synth.layer_seed(cfg["data_seed"], 3, 0), fixed_channels=0)
-    v = synth.gaussian_bf16((ctx, d), synth.layer_seed(cfg["data_seed"], 3, 1))
-    kd = synth.gaussian_bf16((ctx, d), synth.layer_seed(cfg["data_seed"], 0, 0))
-    vd = synth.gaussian_bf16((ctx, d), synth.layer_seed(cfg["data_seed"], 0, 1))
-    q = synth.gaussian_bf16((G, d), synth.layer_seed(cfg["data_seed"], 3, 2), scale=cfg["q_scale"])
+    T, shared, tail = cfg["T"], cfg["shared_kv"], cfg.get("tail", 0)
+    nc = (ctx - tail) // 128 * 128                                   # tokens held in records
+    okc = oracle.Codec(d=d, bits=cfg["kb"], seed=cfg["sign_seed"], T=T)
+    ovc = okc if shared else oracle.Codec(d=d, bits=cfg["vb"], seed=cfg["sign_seed"], T=T)
+    seed = cfg["data_seed"]
+    k = synth.gaussian_bf16((ctx, d), synth.layer_seed(seed, 3, 0), **synth.kv_recipe(cfg, "k"))
+    v = k if shared else synth.gaussian_bf16((ctx, d), synth.layer_seed(seed, 3, 1))
+    q = synth.gaussian_bf16((G, d), synth.layer_seed(seed, 3, 2), scale=cfg["q_scale"])
+    dense = bool(cfg["dense_layers"])
+    if dense:
+        kd = synth.gaussian_bf16((ctx, d), synth.layer_seed(seed, 0, 0), **synth.kv_recipe(cfg, "k"))
+        vd = synth.gaussian_bf16((ctx, d), synth.layer_seed(seed, 0, 1))
+    streams = 1 if shared else 2
 
     def step():
-        kr = oracle.encode_records(k, okc)
-        vr = oracle.encode_records(v, ovc)
-        oracle.unit_attention(q, okc, ovc, kr, vr, ctx, None, None, 1.0)
-        oracle.unit_attention(q, None, None, None, None, 0, kd, vd, 1.0)
-        return 2 * ctx * d * 2 + 2 * (kr.nbytes + vr.nbytes) + 2 * ctx * d * 2 + 2 * G * d * 6
+        kr = oracle.encode_records(k[:nc], okc)
+        vr = kr if shared else oracle.encode_records(v[:nc], ovc)
+        kt, vt = (k[nc:], v[nc:]) if tail else (None, None)
+        oracle.unit_attention(q, okc, ovc, kr, vr, nc, kt, vt, 1.0)
+        rec = kr.nbytes + (0 if shared else vr.nbytes)
+        nb = streams * nc * d * 2 + rec                              # encode: bf16 in, records out
+        nb += rec + streams * tail * d * 2 + G * d * 6               # attention: records, tail, q, out
+        if dense:
+            oracle.unit_attention(q, None, None, None, None, 0, kd, vd, 1.0)
+            nb += 2 * ctx * d * 2 + G * d * 6
+        return nb
 
     budget = 150.0
     for _ in range(max(args.warmup, 3) if args.warmup < 1000 else 3):
@@ -954,10 +968,12 @@ def run_reference(args, world, rank, local, pg):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(secs / n_run * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": args.workload, "sample": "per step: encode one (layer, kv head) unit's K/V "
-                   f"({ctx} tokens each) and attend it, plus one bf16-layer unit", "steps_run": n_run},
+        "config": {"workload": args.workload, "sample": f"per step: encode one (layer, kv head) unit "
+                   f"({nc} packed tokens, {streams} stream(s)) and attend it with its {tail}-token dense tail"
+                   + (", plus one bf16-layer unit" if dense else ""), "steps_run": n_run},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{n_run} steps of one compressed + one bf16 (layer, kv head) unit"},
+                         "sample": f"{n_run} steps of one compressed (layer, kv head) unit"
+                                   + (" + one bf16-layer unit" if dense else "")},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
