@@ -845,14 +845,21 @@ def run_native(args, world, rank, local, pg):
         line["clocks"] = clk
     if not args.no_e2e:
         line["e2e"] = e2e_leg(wl, dev, max(3, min(50, K)))
-    if rank == 0 and not args.no_cpu_baseline and world == 1 and isinstance(wl, QwenCache):
-        hin = wl.host_inputs()
-        nbytes, secs = oracle_step(wl, hin)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
         import oracle
+        if isinstance(wl, QwenCache):
+            hin = wl.host_inputs()
+            nbytes, secs = oracle_step(wl, hin)
+            sample = ("one full step (all 28 layers: encode of the 22 compressed layers + attention of every "
+                      "layer), fp64 C oracle")
+        else:
+            step, sample = oracle_unit_sample(wl.cfg)
+            step()                                   # warm-up
+            t0 = time.perf_counter()
+            nbytes = step()
+            secs = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
-                                "cores": oracle.threads(), "kind": "oracle",
-                                "sample": "one full step (all 28 layers: encode of the 22 compressed layers "
-                                          "+ attention of every layer), fp64 C oracle"}
+                                "cores": oracle.threads(), "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -904,21 +911,15 @@ def e2e_leg(wl, dev, steps: int):
             "d2h_bytes_per_step": d2h, "ms_per_step": round(secs * 1e3, 4)}
 
 
-def run_reference(args, world, rank, local, pg):
-    """The oracle (fp64 C, OpenMP) on the host cores: each step encodes one
-    (layer, kv head) unit of a compressed layer (its packed tokens, one record
-    stream when keys and values share records) and attends it with the unit's
-    dense tail, plus one unit of a bf16 layer where the workload has them, so
-    K steps finish within minutes."""
-    if rank != 0:
-        return
-    import numpy as np
-    import torch
-
+def oracle_unit_sample(cfg: dict):
+    """The oracle's bounded sample of a cache workload: one (layer, kv head)
+    unit of a compressed layer (its packed tokens encoded, one record stream
+    when keys and values share records, then attended with the unit's dense
+    tail) plus one unit of a bf16 layer where the workload has them.
+    Returns (step() -> algorithmic bytes, description)."""
     import oracle
     import synth
     oracle.build()
-    cfg = synth.CONFIGS[args.workload]
     d, ctx, Hkv, Hq = cfg["d"], cfg["ctx"], cfg["Hkv"], cfg["Hq"]
     G = Hq // Hkv
     T, shared, tail = cfg["T"], cfg["shared_kv"], cfg.get("tail", 0)
@@ -947,6 +948,23 @@ def run_reference(args, world, rank, local, pg):
             oracle.unit_attention(q, None, None, None, None, 0, kd, vd, 1.0)
             nb += 2 * ctx * d * 2 + G * d * 6
         return nb
+    sample = (f"one (layer, kv head) unit ({nc} packed tokens, {streams} stream(s)) attended with its "
+              f"{tail}-token dense tail" + (", plus one bf16-layer unit" if dense else "") + ", fp64 C oracle")
+    return step, sample
+
+
+def run_reference(args, world, rank, local, pg):
+    """The oracle (fp64 C, OpenMP) on the host cores: each step encodes one
+    (layer, kv head) unit of a compressed layer (its packed tokens, one record
+    stream when keys and values share records) and attends it with the unit's
+    dense tail, plus one unit of a bf16 layer where the workload has them, so
+    K steps finish within minutes."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    step, sample = oracle_unit_sample(cfg)
 
     budget = 150.0
     for _ in range(max(args.warmup, 3) if args.warmup < 1000 else 3):
@@ -968,12 +986,9 @@ def run_reference(args, world, rank, local, pg):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(secs / n_run * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": args.workload, "sample": f"per step: encode one (layer, kv head) unit "
-                   f"({nc} packed tokens, {streams} stream(s)) and attend it with its {tail}-token dense tail"
-                   + (", plus one bf16-layer unit" if dense else ""), "steps_run": n_run},
+        "config": {"workload": args.workload, "sample": "per step: " + sample, "steps_run": n_run},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{n_run} steps of one compressed (layer, kv head) unit"
-                                   + (" + one bf16-layer unit" if dense else "")},
+                         "sample": f"{n_run} steps of: " + sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
