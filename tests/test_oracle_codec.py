@@ -87,6 +87,28 @@ def test_zero_vector(orc):
     assert np.all(orc.decode_records(rec, 1, cod) == 0.0)
 
 
+@pytest.mark.parametrize("d", [64, 512])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_exact_ties_take_the_lower_code(orc, d, bits):
+    """x = e_i + e_j with equal signs s_i = s_j: the rotated coordinate m is
+    s_i (H_mi + H_mj) / sqrt(2 d), exactly 0 wherever H_mi != H_mj (half of
+    them).  0 is the middle boundary of every table, and a value on a
+    boundary takes the lower code: 2^(b-1) - 1.  Elsewhere |y| = sqrt(2/d)."""
+    s = orc.signs(1, d)
+    i, j = 0, next(k for k in range(1, d) if s[k] == s[0])
+    x = np.zeros((1, d), np.uint16)
+    x[0, i] = x[0, j] = 0x3F80                     # bf16 1.0
+    enc = orc.encode_vectors(x, _codec(orc, d, bits), want_y=True)
+    y = enc["y"][0]
+    H = np.array([[(-1) ** bin(m & k).count("1") for k in (i, j)] for m in range(d)])
+    zero = H[:, 0] != H[:, 1]
+    assert zero.sum() == d // 2 and np.all(y[zero] == 0.0)
+    np.testing.assert_allclose(np.abs(y[~zero]), np.sqrt(2.0 / d), rtol=1e-15)
+    assert np.all(enc["codes"][0][zero] == (1 << (bits - 1)) - 1)
+    t = orc.codebook_f32(bits, d)[1]
+    assert t[(1 << (bits - 1)) - 1] == 0.0
+
+
 def test_double_to_bf16_rounding(orc):
     """Round to nearest, ties to even, from the exact value (hand cases)."""
     one = 0x3F80
