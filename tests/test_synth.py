@@ -78,3 +78,28 @@ def test_same_seed_same_draw():
     c = synth.torch_gaussian_bf16((64, 64), 7, "cpu")
     d = synth.torch_gaussian_bf16((64, 64), 7, "cpu")
     assert torch.equal(c, d)
+
+
+def test_workload_geometries_and_byte_counts(orc):
+    """The workload table holds the stated geometries (28 layers of 2 kv and 12
+    query heads at d 128 with layers 0-2 and 25-27 in bf16; 43 MQA layers of
+    64 query heads at d 512 over 65,280 packed + 256 dense tokens; ...) and
+    their record sizes give the stated bytes per token: 52 / 36 (K 3 / V 2
+    bits at d 128), 260 at d 512 and 4 bits, and 730 MB of records per step
+    for the V4-Flash-like cache."""
+    C = synth.CONFIGS
+    q = C["qwen2_1p5b_ctx2048"]
+    assert (q["L"], q["Hkv"], q["Hq"], q["d"], q["ctx"], q["kb"], q["vb"]) == (28, 2, 12, 128, 2048, 3, 2)
+    assert q["dense_layers"] == (0, 1, 2, 25, 26, 27)
+    v = C["v4flash_mqa_ctx65536"]
+    assert (v["L"], v["Hkv"], v["Hq"], v["d"], v["ctx"], v["tail"], v["kb"], v["shared_kv"]) == \
+        (43, 1, 64, 512, 65536, 256, 4, True)
+    assert (v["ctx"] - v["tail"]) % 128 == 0 and (v["ctx"] - v["tail"]) == 65280
+    b = C["batched_b32_ctx32768"]
+    assert (b["L"], b["B"], b["Hkv"], b["Hq"], b["ctx"], b["kb"], b["vb"], b["T"]) == \
+        (32, 32, 8, 32, 32768, 4, 3, 2.0)
+    lc = C["longctx_b4_ctx262144"]
+    assert (lc["L"], lc["B"], lc["ctx"], lc["tail"]) == (8, 4, 262144, 1024)
+    per_tok = lambda d, bits: orc.Codec(d=d, bits=bits).record_bytes // 128
+    assert (per_tok(128, 3), per_tok(128, 2), per_tok(512, 4)) == (52, 36, 260)
+    assert v["L"] * 65280 * per_tok(512, 4) == 729_830_400
