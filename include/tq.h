@@ -21,7 +21,10 @@
  * Conventions for every call:
  *  - Pointers named d_* or documented "device" are device addresses; the
  *    caller owns every buffer (inputs, outputs, workspaces).  The library
- *    allocates no memory and keeps no state between calls.
+ *    allocates no memory and keeps no state between calls, with one
+ *    exception: tq_decode_attn_noalloc's fixed device workspace (a static
+ *    array of the library) and the per-device address of that array, which
+ *    it looks up once and caches.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *    asynchronous on that stream unless stated otherwise.
  *  - Arguments are validated on the host before anything is launched; on an
@@ -288,7 +291,9 @@ tq_status tq_decode_attn(const tq_attn_args* args, const tq_codec* k_codec,
  *   with TQ_ERR_WORKSPACE; lower `splits` or use tq_decode_attn.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
- *   stream capture.  Nothing in the array needs to start at zero, and each
+ *   stream capture.  The cached address does not survive cudaDeviceReset:
+ *   after a reset of a device, do not call this entry point on it again in
+ *   the same process.  Nothing in the array needs to start at zero, and each
  *   call overwrites what the previous one left.  All calls share the one
  *   array: calls whose executions overlap on the GPU (different streams,
  *   concurrent graph branches) race and corrupt each other's results.

@@ -23,8 +23,10 @@ std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device; looked up once per
-// device (with that device current) and cached.  In host code the symbol
-// itself is only a host-side stand-in and must never be passed to a kernel.
+// device (with that device current) and cached for the life of the process
+// (a cudaDeviceReset invalidates it; the header tells callers not to call
+// again after one).  In host code the symbol itself is only a host-side
+// stand-in and must never be passed to a kernel.
 tq_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TQ_ERR_CUDA;
