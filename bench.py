@@ -1,24 +1,31 @@
 #!/usr/bin/env python
 """Benchmark of the rotated Lloyd-Max KV-cache path on GB300.
 
-Default workload: the Qwen2-1.5B-shaped cache (28 layers, 2 KV heads, 12 query
-heads, head_dim 128, batch 1, ctx 2048; K 3 bits, V 2 bits; layers 0-2 and
-25-27 kept bf16).  One step = encode the whole compressed cache (K and V of 22
-layers, two tq_encode launches) + one decode step of every layer (all 28 layers
-in one tq_decode_attn call: attention + merge kernels; 28 per-layer calls
-replayed from a CUDA graph are timed alongside).  Inputs are synthetic, generated on the
-device from fixed seeds, resident in HBM before timing.  L2 is flushed (a
-256 MiB write) before every timed step; each step is timed with CUDA events.
+Default workload: the batched decode cache (32 layers, batch 32, 8 KV heads,
+32 query heads, head_dim 128, ctx 32,768; K 4 bits, V 3 bits, outlier side
+lists at T = 2 on both), the largest configuration that fits one GPU (about
+193 GB resident).  One step = three phases, each replayed from a CUDA graph
+and timed with CUDA events on the launching stream, with L2 flushed (a 256 MiB
+write) before each phase outside its events:
+  encode     tq_encode of the whole compressed cache (K and V),
+  eviction   one tq_evict call moving one 128-token chunk per (layer, batch,
+             kv head) from its dense ring into a record,
+  attention  one decode step of every layer in one tq_decode_attn call.
+Inputs are synthetic, generated on the device from fixed seeds, resident in
+HBM before timing.
 
 value = algorithmic HBM bytes of the step (bytes each kernel must read and
 write by the record layout) / device time, in GB/s.  Also reported: encode
-Mvec/s, decode-attention KV GB/s and tok/s, the roofline of the dominant kernel
-against the measured HBM copy bandwidth, the oracle (CPU) timed on a bounded
-sample, and an end-to-end figure with host buffers copied in and out.
+Mvec/s, eviction Mvec/s, decode-attention KV GB/s and tok/s, the roofline of
+every phase against the measured HBM copy bandwidth (attention above the
+ridge point against the measured bf16 tensor peak) with the dominant phase as
+`roofline`, the oracle (CPU) timed on a bounded sample, and an end-to-end
+figure with host buffers copied in and out.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                  [--workload qwen2_1p5b_ctx2048|batched_b32_ctx32768|v4flash_mqa_ctx65536|longctx_b4_ctx262144
-                              |codec_roundtrip_4096x128_b3|encode_sweep_16M] [--splits N]
+                  [--workload batched_b32_ctx32768|qwen2_1p5b_ctx2048|v4flash_mqa_ctx65536
+                              |longctx_b4_ctx262144|codec_roundtrip_4096x128_b3|encode_sweep_16M]
+                  [--splits N] [--layers L] [--batch B]
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (the path has no cross-GPU exchange); value = total bytes of all ranks / max
 rank time.
@@ -44,17 +51,18 @@ def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default 5000 for the Qwen2 cache, 20 for the large caches)")
+                    help="timed steps (default 20 for the large caches, 5000 for the Qwen2 cache)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="qwen2_1p5b_ctx2048",
-                    choices=["qwen2_1p5b_ctx2048", "batched_b32_ctx32768", "v4flash_mqa_ctx65536",
+    ap.add_argument("--workload", default="batched_b32_ctx32768",
+                    choices=["batched_b32_ctx32768", "qwen2_1p5b_ctx2048", "v4flash_mqa_ctx65536",
                              "longctx_b4_ctx262144", "codec_roundtrip_4096x128_b3", "encode_sweep_16M"])
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layers", type=int, default=None, help="large workloads: layers to instantiate")
-    ap.add_argument("--batch", type=int, default=None, help="large workloads: batch to instantiate")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="cache workloads: instantiate only the first L layers (small profiling cases)")
+    ap.add_argument("--batch", type=int, default=None, help="cache workloads: instantiate batch B")
     ap.add_argument("--splits", type=int, default=0,
                     help="cache workloads: splits per (layer, batch, kv head) of tq_decode_attn (0 = its planner)")
     return ap.parse_args()
@@ -156,15 +164,44 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-# DRAM bytes (read + write) per launch of the dominant kernel: the
-# dram__bytes_read/write counters of an ncu capture of the kernel as it is now
-# built (the Qwen2-shaped step's launch list); None where no such capture
-# exists.  The V4-Flash attention's capture (140.1 MB on 8 layers, equal to the
-# records it reads) predates the tcgen05 kernel's logit soft-cap branch, so
-# that workload reports None until it is captured again.
-MEASURED_TRAFFIC = {
-    ("qwen2_1p5b_ctx2048", "tq_encode"): 23_103_488 + 23_101_184,  # K and V launches of the phase
+# Eviction bound of the cache workloads: window + max(t_q - 1, margin) + 128
+# ("feat(v4): TurboQuant KV storage for DeepSeek-V4", "Eviction is chunked, on
+# purpose"); the V4-Flash-like config states window 128, the others take the
+# same values.
+EVICT_WINDOW, EVICT_MARGIN, EVICT_TQ = 128, 16, 1
+
+# DRAM bytes (read + write) per step of a phase, from dram__bytes_read.sum +
+# dram__bytes_write.sum of a one-kernel ncu capture, keyed by the SHA-256
+# (first 16 hex digits) of the phase's kernel sources at capture time; a
+# phase whose sources have changed since reports null.  Captures of a reduced
+# layer count are scaled to the full workload by layers (the phase's traffic
+# is a sum over layers).
+MEASURED_TRAFFIC: dict = {}
+
+PHASE_SOURCES = {
+    "tq_encode": ["encode_mma.cu", "encode.cu", "tq_common.cuh", "tq_params.h", "abi.cu"],
+    "tq_evict": ["encode.cu", "tq_common.cuh", "tq_params.h", "abi.cu"],
+    "tq_decode_attn": ["abi.cu", "merge.cu", "umma.cuh", "tq_common.cuh", "tq_params.h",
+                       "attn.cuh", "attn_rec.cuh", "attn_mma.cuh", "attn_mma512.cuh", "attn_umma512.cuh"],
 }
+
+
+def phase_sources_sha(phase: str) -> str:
+    """SHA-256 (16 hex digits) of the library sources a phase's kernels are built from."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rotated_lloyd_max_gb300", "csrc")
+    for name in PHASE_SOURCES[phase]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, phase: str):
+    e = MEASURED_TRAFFIC.get((workload, phase))
+    if e is None or e["sources"] != phase_sources_sha(phase):
+        return None
+    return e["bytes"]
 
 
 def peaks():
@@ -177,103 +214,231 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-class QwenCache:
-    """Qwen2-1.5B-shaped cache: encode the whole cache, then one decode step of
-    every layer.  All 28 layers share one argument block: the 22 compressed
-    layers have records and no dense tokens, the 6 bf16 layers have no records
-    and their whole cache as dense tokens, so one tq_decode_attn call (two
-    kernels) serves the step; a per-layer variant (28 calls, CUDA graph) is
-    timed alongside."""
+def used_record_bytes(torch, rec, codec, d: int) -> int:
+    """Algorithmic bytes of a record array [..., record_bytes]: codes and norms
+    of every record, plus the outlier counts and the entries actually stored."""
+    base = 128 * (d * codec.bits // 8) + 512
+    flat = rec.reshape(-1, codec.record_bytes)
+    n = flat.shape[0]
+    if not codec.c.outlier_T:
+        return n * base
+    entries = int(flat[:, base:base + 128].to(torch.int64).sum().item())
+    return n * (base + 128) + 4 * entries
 
-    name = "qwen2_1p5b_ctx2048"
 
-    def __init__(self, device, seed_offset: int = 0, splits: int = 0):
+class EvictPhase:
+    """One tq_evict call that evicts one 128-token chunk for every compressed
+    (layer, batch, kv head) of a cache: each stream gets a 272-slot bf16 ring
+    (window 128 + margin 16 + one chunk) whose oldest 128 slots hold the
+    tokens of the stream's last record and whose other 144 slots hold newer
+    tokens; its counters (n_chunks = records - 1, start 0, length 272) are
+    reset from device templates before every call, so each call re-evicts
+    that record with the same tokens, as a decode step that fills a chunk
+    does."""
+
+    def __init__(self, wl, layers: slice, next_k, next_v):
+        torch = wl.torch
+        self.wl, self.tq, self.torch = wl, wl.tq, torch
+        cap = EVICT_WINDOW + max(EVICT_TQ - 1, EVICT_MARGIN) + 128
+        self.cap = cap
+        kx = wl.kx[layers]
+        Lc, B, Hkv = kx.shape[:3]
+        d, nt = wl.d, wl.n_rec * 128
+        self.krec, self.vrec = wl.krec[layers], wl.vrec[layers]
+        self.kt = torch.cat([kx[:, :, :, nt - 128:nt], next_k], dim=3).contiguous()
+        assert self.kt.shape[3] == cap
+        if wl.shared:
+            self.vt = self.kt
+        else:
+            self.vt = torch.cat([wl.vx[layers][:, :, :, nt - 128:nt], next_v], dim=3).contiguous()
+        i32 = torch.int32
+        dev = kx.device
+        self.tmpl = [torch.full((Lc, B), v, dtype=i32, device=dev) for v in (wl.n_rec - 1, 0, cap)]
+        self.n_chunks, self.tail_start, self.tail_len = [t.clone() for t in self.tmpl]
+        self.streams = 1 if wl.shared else 2
+        self.launches = self.streams + 1                          # encoders + the counter commit
+        self.vectors = self.streams * Lc * B * Hkv * 128
+        self.Lc = Lc
+
+    def reset(self):
+        for w, t in zip((self.n_chunks, self.tail_start, self.tail_len), self.tmpl):
+            w.copy_(t)
+
+    def run(self):
+        wl = self.wl
+        self.tq.tq_evict(wl.kc, wl.vc, k_rec=self.krec, v_rec=self.vrec, k_tail=self.kt, v_tail=self.vt,
+                         n_chunks=self.n_chunks, tail_start=self.tail_start, tail_len=self.tail_len,
+                         window=EVICT_WINDOW, margin=EVICT_MARGIN, t_q=EVICT_TQ, max_evict=1)
+
+    def account(self):
+        """Algorithmic bytes of one call: the evicted tokens read (bf16), the
+        records written (codes, norms, counts and stored entries)."""
+        torch, wl = self.torch, self.wl
+        n = wl.n_rec - 1
+        out = used_record_bytes(torch, self.krec[:, :, :, n], wl.kc, wl.d)
+        if not wl.shared:
+            out += used_record_bytes(torch, self.vrec[:, :, :, n], wl.vc, wl.d)
+        self.bytes_in = self.vectors * wl.d * 2
+        self.bytes_out = out
+        self.bytes = self.bytes_in + self.bytes_out
+
+
+class CacheWorkload:
+    """A KV-cache workload.  One step = three phases, each replayed from its
+    own CUDA graph and timed with CUDA events, L2 flushed before each:
+      encode     tq_encode of every compressed layer's packed region (K and V)
+      eviction   one tq_evict call moving one chunk per (layer, batch, kv head)
+                 from the dense ring into its last record (EvictPhase)
+      attention  one decode step of every layer in one tq_decode_attn call
+                 over the records and the dense part (tail ring, or the
+                 whole cache of a bf16 layer)."""
+
+    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0, splits: int = 0):
         import torch
 
         import rotated_lloyd_max_gb300 as tq
         import synth
-        self.tq, self.torch, self.dev = tq, torch, device
-        cfg = dict(synth.CONFIGS[self.name])
+        self.tq, self.torch, self.dev, self.name = tq, torch, device, name
+        cfg = dict(synth.CONFIGS[name])
         self.cfg = cfg
-        L, B, Hkv, Hq, d, ctx = cfg["L"], cfg["B"], cfg["Hkv"], cfg["Hq"], cfg["d"], cfg["ctx"]
+        L = layers or cfg["L"]
+        B = batch or cfg["B"]
+        Hkv, Hq, d, ctx = cfg["Hkv"], cfg["Hq"], cfg["d"], cfg["ctx"]
         self.L, self.B, self.Hkv, self.Hq, self.d, self.ctx = L, B, Hkv, Hq, d, ctx
-        self.dense = list(cfg["dense_layers"])
+        self.dense = [l for l in cfg.get("dense_layers", ()) if l < L]
         self.comp = [l for l in range(L) if l not in self.dense]
         assert self.comp == list(range(self.comp[0], self.comp[-1] + 1)), "compressed layers are contiguous"
         self.c0, self.c1 = self.comp[0], self.comp[-1] + 1
+        tail = cfg.get("tail", 0)
+        self.tail, self.n_rec = tail, (ctx - tail) // 128
+        self.shared = cfg["shared_kv"]
         seed = cfg["data_seed"] + seed_offset
-        self.kc = tq.tq_make_codebook(cfg["kb"], d, sign_seed=cfg["sign_seed"])
-        self.vc = tq.tq_make_codebook(cfg["vb"], d, sign_seed=cfg["sign_seed"])
-        bf = torch.bfloat16
-        # bf16 K/V of every layer: encode source of the compressed layers, the
-        # attended cache of the bf16 layers
-        self.kx = torch.empty((L, B, Hkv, ctx, d), dtype=bf, device=device)
-        self.vx = torch.empty_like(self.kx)
+        T = cfg["T"]
+        self.kc = tq.tq_make_codebook(cfg["kb"], d, sign_seed=cfg["sign_seed"], outlier_T=T)
+        self.vc = self.kc if self.shared else tq.tq_make_codebook(cfg["vb"], d, sign_seed=cfg["sign_seed"],
+                                                                  outlier_T=T)
+        bf, u8, i32 = torch.bfloat16, torch.uint8, torch.int32
+        # bf16 layers attend their whole cache as the dense part: their rows are ctx long
+        ntok = ctx if self.dense else self.n_rec * 128
+        self.ntok = ntok
+        self.kx = torch.empty((L, B, Hkv, ntok, d), dtype=bf, device=device)
+        self.vx = self.kx if self.shared else torch.empty_like(self.kx)
         self.q = torch.empty((L, B, Hq, d), dtype=bf, device=device)
+        if tail:
+            self.kt = torch.empty((L, B, Hkv, tail, d), dtype=bf, device=device)
+            self.vt = self.kt if self.shared else torch.empty_like(self.kt)
         for l in range(L):
             synth.torch_gaussian_bf16(self.kx[l].shape, synth.layer_seed(seed, l, 0), device,
-                                      fixed_channels=cfg["k_fixed_channels"], out=self.kx[l])
-            synth.torch_gaussian_bf16(self.vx[l].shape, synth.layer_seed(seed, l, 1), device, out=self.vx[l])
+                                      out=self.kx[l], **synth.kv_recipe(cfg, "k"))
+            if not self.shared:
+                synth.torch_gaussian_bf16(self.vx[l].shape, synth.layer_seed(seed, l, 1), device,
+                                          out=self.vx[l], **synth.kv_recipe(cfg, "v"))
             synth.torch_gaussian_bf16(self.q[l].shape, synth.layer_seed(seed, l, 2), device,
                                       scale=cfg["q_scale"], out=self.q[l])
-        self.n_rec = ctx // 128
-        u8, i32 = torch.uint8, torch.int32
+            if tail:
+                synth.torch_gaussian_bf16(self.kt[l].shape, synth.layer_seed(seed, l, 3), device,
+                                          out=self.kt[l], **synth.kv_recipe(cfg, "k"))
+                if not self.shared:
+                    synth.torch_gaussian_bf16(self.vt[l].shape, synth.layer_seed(seed, l, 4), device,
+                                              out=self.vt[l], **synth.kv_recipe(cfg, "v"))
         self.krec = torch.empty((L, B, Hkv, self.n_rec, self.kc.record_bytes), dtype=u8, device=device)
-        self.vrec = torch.empty((L, B, Hkv, self.n_rec, self.vc.record_bytes), dtype=u8, device=device)
+        self.vrec = self.krec if self.shared else torch.empty((L, B, Hkv, self.n_rec, self.vc.record_bytes),
+                                                              dtype=u8, device=device)
         self.out = torch.empty((L, B, Hq, d), dtype=torch.float32, device=device)
         comp_mask = torch.tensor([l in self.comp for l in range(L)], device=device)[:, None].expand(L, B)
         self.n_chunks = torch.where(comp_mask, self.n_rec, 0).to(i32).contiguous()
-        self.dense_len = torch.where(comp_mask, 0, ctx).to(i32).contiguous()
-        self.args_all = tq.make_attn_args(q=self.q, out=self.out, scale=1.0, k_rec=self.krec, v_rec=self.vrec,
-                                          n_chunks=self.n_chunks, max_chunks=self.n_rec, k_tail=self.kx,
-                                          v_tail=self.vx, tail_len=self.dense_len, max_tail=ctx, splits=splits)
+        kw = dict(q=self.q, out=self.out, scale=1.0, k_rec=self.krec, v_rec=self.vrec, n_chunks=self.n_chunks,
+                  max_chunks=self.n_rec, splits=splits)
+        if self.dense:
+            self.dense_len = torch.where(comp_mask, 0, ctx).to(i32).contiguous()
+            kw.update(k_tail=self.kx, v_tail=self.vx, tail_len=self.dense_len, max_tail=ctx)
+        elif tail:
+            self.tail_len = torch.full((L, B), tail, dtype=i32, device=device)
+            self.tail_start = torch.zeros((L, B), dtype=i32, device=device)
+            kw.update(k_tail=self.kt, v_tail=self.vt, tail_len=self.tail_len, tail_start=self.tail_start,
+                      max_tail=tail)
+        self.args_all = tq.make_attn_args(**kw)
         ws = tq.tq_decode_attn_workspace_size(self.args_all, self.kc, self.vc)
-        self.args_layer = []
-        for l in range(L):
-            if l in self.dense:
-                a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
-                                      k_tail=self.kx[l:l + 1], v_tail=self.vx[l:l + 1],
-                                      tail_len=self.dense_len[l:l + 1], max_tail=ctx, splits=splits)
-                codecs = (None, None)
-            else:
-                a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
-                                      k_rec=self.krec[l:l + 1], v_rec=self.vrec[l:l + 1],
-                                      n_chunks=self.n_chunks[l:l + 1], max_chunks=self.n_rec, splits=splits)
-                codecs = (self.kc, self.vc)
-            ws = max(ws, tq.tq_decode_attn_workspace_size(a, *codecs))
-            self.args_layer.append((a, codecs))
+        self.args_layer = None
+        if self.dense:          # the per-layer variant a model's layer loop issues (timed alongside)
+            self.args_layer = []
+            for l in range(L):
+                if l in self.dense:
+                    a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
+                                          k_tail=self.kx[l:l + 1], v_tail=self.vx[l:l + 1],
+                                          tail_len=self.dense_len[l:l + 1], max_tail=ctx, splits=splits)
+                    codecs = (None, None)
+                else:
+                    a = tq.make_attn_args(q=self.q[l:l + 1], out=self.out[l:l + 1], scale=1.0,
+                                          k_rec=self.krec[l:l + 1], v_rec=self.vrec[l:l + 1],
+                                          n_chunks=self.n_chunks[l:l + 1], max_chunks=self.n_rec, splits=splits)
+                    codecs = (self.kc, self.vc)
+                ws = max(ws, tq.tq_decode_attn_workspace_size(a, *codecs))
+                self.args_layer.append((a, codecs))
         self.ws = torch.empty(ws, dtype=u8, device=device)
-        # kernels per step: the two encodes + what the attention call launches
         self.plan = tq.tq_decode_attn_plan(self.args_all, self.kc, self.vc)
-        self.launches_per_step = 2 + self.plan["launches"]
-        # algorithmic bytes
-        nc, nd = len(self.comp), len(self.dense)
-        d2 = d * 2
-        n_vec_stream = nc * B * Hkv * ctx
-        self.enc_in = 2 * n_vec_stream * d2
-        self.enc_out = nc * B * Hkv * self.n_rec * (self.kc.record_bytes + self.vc.record_bytes)
-        self.attn_bytes = (self.enc_out + nd * B * Hkv * ctx * 2 * d2 + L * B * Hq * d * 2
-                           + L * B * Hq * d * 4)
+        # eviction: the 144 tokens after the last record's are the dense tail's
+        # first tokens where the workload has a tail, else a fresh draw
+        lay = slice(self.c0, self.c1)
+        Lc = self.c1 - self.c0
+        if tail >= 144:
+            nk = self.kt[lay, :, :, :144]
+            nv = None if self.shared else self.vt[lay, :, :, :144]
+        else:
+            nk = torch.empty((Lc, B, Hkv, 144, d), dtype=bf, device=device)
+            nv = None if self.shared else torch.empty_like(nk)
+            for i in range(Lc):
+                synth.torch_gaussian_bf16(nk[i].shape, synth.layer_seed(seed, self.c0 + i, 5), device, out=nk[i],
+                                          **synth.kv_recipe(cfg, "k"))
+                if nv is not None:
+                    synth.torch_gaussian_bf16(nv[i].shape, synth.layer_seed(seed, self.c0 + i, 6), device,
+                                              out=nv[i], **synth.kv_recipe(cfg, "v"))
+        self.ev = EvictPhase(self, lay, nk, nv)
+        del nk, nv
+        # launches per step: one encode per stream, the eviction's, the attention call's
+        streams = 1 if self.shared else 2
+        self.enc_launches = streams
+        self.launches_per_step = streams + self.ev.launches + self.plan["launches"]
+        # algorithmic bytes (records counted as used: codes, norms, counts, stored entries)
+        self.encode_k(); self.encode_v()
+        self.ev.reset(); self.ev.run()
+        torch.cuda.synchronize()
+        self.ev.account()
+        nc = len(self.comp)
+        n_vec = nc * B * Hkv * self.n_rec * 128
+        self.enc_in = streams * n_vec * d * 2
+        self.enc_out = used_record_bytes(torch, self.krec[lay], self.kc, d) + (
+            0 if self.shared else used_record_bytes(torch, self.vrec[lay], self.vc, d))
+        dense_tok = len(self.dense) * B * Hkv * ctx + nc * B * Hkv * tail
+        self.attn_bytes = (self.enc_out + streams * dense_tok * d * 2 + L * B * Hq * d * 2 + L * B * Hq * d * 4)
         # plain attention arithmetic: q.k and p.v per (query head, token), 2 flops per MAC
         self.attn_flops = 4 * L * B * Hq * d * ctx
-        self.step_bytes = self.enc_in + self.enc_out + self.attn_bytes
-        self.vectors_per_step = 2 * n_vec_stream
-        self.tokens_per_step = B  # one decode token per sequence through all layers
+        self.step_bytes = self.enc_in + self.enc_out + self.ev.bytes + self.attn_bytes
+        self.concurrent_enc = self.enc_in < (256 << 20)
+        self.vectors_per_step = streams * n_vec
+        self.tokens_per_step = B          # one decode token per sequence through all layers
 
     def _enc(self, codec, src, rec):
-        n = len(self.comp) * self.B * self.Hkv
-        self.tq.tq_encode(codec, src[self.c0:self.c1].view(n, self.ctx, self.d),
+        n = (self.c1 - self.c0) * self.B * self.Hkv
+        nt = self.n_rec * 128
+        self.tq.tq_encode(codec, src[self.c0:self.c1, :, :, :nt].view(n, nt, self.d),
                           rec[self.c0:self.c1].view(n, self.n_rec, -1))
 
     def encode_k(self):
         self._enc(self.kc, self.kx, self.krec)
 
     def encode_v(self):
-        self._enc(self.vc, self.vx, self.vrec)
+        if not self.shared:
+            self._enc(self.vc, self.vx, self.vrec)
 
-    def encode_both(self):
-        """K and V encodes on two streams (fork/join through events): each one
-        is a single launch wave that leaves most of the GPU idle at this size."""
+    def encode(self):
+        """K and V encodes; when the cache is small (each launch a single wave
+        that leaves most of the GPU idle) V's runs on a side stream, forked
+        and joined through events."""
+        if self.shared or not self.concurrent_enc:
+            self.encode_k()
+            self.encode_v()
+            return
         torch = self.torch
         cur = torch.cuda.current_stream()
         if not hasattr(self, "_side"):
@@ -295,17 +460,26 @@ class QwenCache:
             self.tq.tq_decode_attn(a, kc, vc, self.ws)
 
     def inputs(self):
-        return {"kx": self.kx, "vx": self.vx, "q": self.q}
+        """Device tensors a step consumes from the host (leading axis: layer)."""
+        d = {"kx": self.kx, "q": self.q, "evict_k": self.ev.kt}
+        if not self.shared:
+            d.update(vx=self.vx, evict_v=self.ev.vt)
+        if self.tail:
+            d["kt"] = self.kt
+            if not self.shared:
+                d["vt"] = self.vt
+        return d
 
     def host_inputs(self):
         import numpy as np
         f = lambda t: t.contiguous().view(self.torch.int16).cpu().numpy().view(np.uint16)
-        return {k: f(v) for k, v in self.inputs().items()}
+        return {k: f(v) for k, v in (("kx", self.kx), ("vx", self.vx), ("q", self.q))}
 
 
-def oracle_step(wl: QwenCache, hin: dict, layers=None):
-    """The oracle on (a subset of) one step: encode the compressed layers' K/V
-    and attend every listed layer.  Returns (algorithmic bytes, seconds)."""
+def oracle_step(wl: CacheWorkload, hin: dict, layers=None):
+    """The oracle on (a subset of) one step of a cache without a dense tail:
+    encode the compressed layers' K/V, evict one chunk per stream (its
+    encode), attend every listed layer.  Returns (algorithmic bytes, seconds)."""
     import oracle
     cfg = wl.cfg
     d, B, Hkv, Hq, ctx = wl.d, wl.B, wl.Hkv, wl.Hq, wl.ctx
@@ -325,128 +499,13 @@ def oracle_step(wl: QwenCache, hin: dict, layers=None):
                 else:
                     kr = oracle.encode_records(hin["kx"][l, b, h], okc)
                     vr = oracle.encode_records(hin["vx"][l, b, h], ovc)
+                    ke = oracle.encode_records(hin["kx"][l, b, h, ctx - 128:], okc)
+                    ve = oracle.encode_records(hin["vx"][l, b, h, ctx - 128:], ovc)
                     oracle.unit_attention(q, okc, ovc, kr, vr, ctx, None, None, 1.0)
                     nbytes += 2 * ctx * d * 2 + 2 * (kr.nbytes + vr.nbytes)
+                    nbytes += 2 * 128 * d * 2 + ke.nbytes + ve.nbytes
                 nbytes += G * d * 6
     return nbytes, time.perf_counter() - t0
-
-
-class BigCache:
-    """The large single-GPU caches (batched with outliers, V4-Flash-like MQA,
-    long context): one step = encode of the packed region of every layer (one
-    tq_encode per stream) + decode attention of every layer in one
-    tq_decode_attn call over the records and the dense tail."""
-
-    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0, splits: int = 0):
-        import torch
-
-        import rotated_lloyd_max_gb300 as tq
-        import synth
-        self.tq, self.torch, self.dev, self.name = tq, torch, device, name
-        cfg = dict(synth.CONFIGS[name])
-        self.cfg = cfg
-        L = layers or cfg["L"]
-        B = batch or cfg["B"]
-        Hkv, Hq, d, ctx = cfg["Hkv"], cfg["Hq"], cfg["d"], cfg["ctx"]
-        self.L, self.B, self.Hkv, self.Hq, self.d, self.ctx = L, B, Hkv, Hq, d, ctx
-        self.dense = []
-        tail = cfg.get("tail", 0)
-        self.tail, self.n_rec = tail, (ctx - tail) // 128
-        ntok = self.n_rec * 128
-        self.shared = cfg["shared_kv"]
-        seed = cfg["data_seed"] + seed_offset
-        T = cfg["T"]
-        self.kc = tq.tq_make_codebook(cfg["kb"], d, sign_seed=cfg["sign_seed"], outlier_T=T)
-        self.vc = self.kc if self.shared else tq.tq_make_codebook(cfg["vb"], d, sign_seed=cfg["sign_seed"],
-                                                                  outlier_T=T)
-        bf, u8, i32 = torch.bfloat16, torch.uint8, torch.int32
-        self.kx = torch.empty((L, B, Hkv, ntok, d), dtype=bf, device=device)
-        self.vx = self.kx if self.shared else torch.empty_like(self.kx)
-        self.q = torch.empty((L, B, Hq, d), dtype=bf, device=device)
-        tail_cap = max(tail, 1)
-        self.kt = torch.empty((L, B, Hkv, tail_cap, d), dtype=bf, device=device)
-        self.vt = self.kt if self.shared else torch.empty_like(self.kt)
-        for l in range(L):
-            synth.torch_gaussian_bf16(self.kx[l].shape, synth.layer_seed(seed, l, 0), device,
-                                      out=self.kx[l], **synth.kv_recipe(cfg, "k"))
-            if not self.shared:
-                synth.torch_gaussian_bf16(self.vx[l].shape, synth.layer_seed(seed, l, 1), device,
-                                          out=self.vx[l], **synth.kv_recipe(cfg, "v"))
-            synth.torch_gaussian_bf16(self.kt[l].shape, synth.layer_seed(seed, l, 3), device,
-                                      out=self.kt[l], **synth.kv_recipe(cfg, "k"))
-            if not self.shared:
-                synth.torch_gaussian_bf16(self.vt[l].shape, synth.layer_seed(seed, l, 4), device,
-                                          out=self.vt[l], **synth.kv_recipe(cfg, "v"))
-            synth.torch_gaussian_bf16(self.q[l].shape, synth.layer_seed(seed, l, 2), device,
-                                      scale=cfg["q_scale"], out=self.q[l])
-        self.krec = torch.empty((L, B, Hkv, self.n_rec, self.kc.record_bytes), dtype=u8, device=device)
-        self.vrec = self.krec if self.shared else torch.empty((L, B, Hkv, self.n_rec, self.vc.record_bytes),
-                                                              dtype=u8, device=device)
-        self.out = torch.empty((L, B, Hq, d), dtype=torch.float32, device=device)
-        self.n_chunks = torch.full((L, B), self.n_rec, dtype=i32, device=device)
-        kw = dict(q=self.q, out=self.out, scale=1.0, k_rec=self.krec, v_rec=self.vrec, n_chunks=self.n_chunks,
-                  max_chunks=self.n_rec, splits=splits)
-        if tail:
-            self.tail_len = torch.full((L, B), tail, dtype=i32, device=device)
-            self.tail_start = torch.zeros((L, B), dtype=i32, device=device)
-            kw.update(k_tail=self.kt, v_tail=self.vt, tail_len=self.tail_len, tail_start=self.tail_start,
-                      max_tail=tail)
-        self.args_all = tq.make_attn_args(**kw)
-        self.ws = torch.empty(tq.tq_decode_attn_workspace_size(self.args_all, self.kc, self.vc), dtype=u8,
-                              device=device)
-        # kernels per step: one encode per stream + what the attention call launches
-        self.plan = tq.tq_decode_attn_plan(self.args_all, self.kc, self.vc)
-        self.launches_per_step = (1 if self.shared else 2) + self.plan["launches"]
-        # algorithmic bytes: inputs read, records written/read as used (codes,
-        # norms, counts and the entries actually stored), tail, q, out
-        self.encode_k(); self.encode_v()
-        torch.cuda.synchronize()
-        n_vec = L * B * Hkv * ntok
-        streams = 1 if self.shared else 2
-        self.enc_in = streams * n_vec * d * 2
-        self.enc_out = self._used_record_bytes(self.krec, self.kc) + (
-            0 if self.shared else self._used_record_bytes(self.vrec, self.vc))
-        self.attn_bytes = (self.enc_out + streams * L * B * Hkv * tail * d * 2 + L * B * Hq * d * 2
-                           + L * B * Hq * d * 4)
-        self.attn_flops = 4 * L * B * Hq * d * (self.n_rec * 128 + tail)
-        self.step_bytes = self.enc_in + self.enc_out + self.attn_bytes
-        self.vectors_per_step = streams * n_vec
-        self.tokens_per_step = B
-
-    def _used_record_bytes(self, rec, codec):
-        torch = self.torch
-        d, b = self.d, codec.bits
-        base = 128 * (d * b // 8) + 512
-        n = rec.shape[0] * rec.shape[1] * rec.shape[2] * rec.shape[3]
-        if not codec.c.outlier_T:
-            return n * base
-        counts = rec.view(-1, codec.record_bytes)[:, base:base + 128]
-        entries = int(counts.to(torch.int64).sum().item())
-        return n * (base + 128) + 4 * entries
-
-    def encode_k(self):
-        n = self.L * self.B * self.Hkv
-        self.tq.tq_encode(self.kc, self.kx.view(n, -1, self.d), self.krec.view(n, self.n_rec, -1))
-
-    def encode_v(self):
-        if self.shared:
-            return
-        n = self.L * self.B * self.Hkv
-        self.tq.tq_encode(self.vc, self.vx.view(n, -1, self.d), self.vrec.view(n, self.n_rec, -1))
-
-    def attention(self):
-        self.tq.tq_decode_attn(self.args_all, self.kc, self.vc, self.ws)
-
-    def attention_per_layer(self):
-        self.attention()
-
-    def inputs(self):
-        d = {"kx": self.kx, "q": self.q}
-        if not self.shared:
-            d["vx"] = self.vx
-        return d
-
-
 
 
 # ---------------------------------------------------------------------------
@@ -690,21 +749,36 @@ def codec_oracle_sample(cfg: dict, n_max: int = 4096):
     return nbytes, secs, f"{what} of {n} vectors per item ({len(codec_items(cfg))} items), fp64 C oracle"
 
 
-WORKLOADS = {"qwen2_1p5b_ctx2048": QwenCache,
-             "batched_b32_ctx32768": BigCache,
-             "v4flash_mqa_ctx65536": BigCache,
-             "longctx_b4_ctx262144": BigCache,
+WORKLOADS = {"qwen2_1p5b_ctx2048": CacheWorkload,
+             "batched_b32_ctx32768": CacheWorkload,
+             "v4flash_mqa_ctx65536": CacheWorkload,
+             "longctx_b4_ctx262144": CacheWorkload,
              "codec_roundtrip_4096x128_b3": CodecWorkload,
              "encode_sweep_16M": CodecWorkload}
 
 
-def encode_all(wl):
-    """Encode the step's K and V: concurrently where the workload offers it."""
-    if hasattr(wl, "encode_both"):
-        wl.encode_both()
+def roofline_entry(kernel: str, nbytes: int, secs: float, launches: int, flops: int | None = None):
+    """The roofline of one phase: algorithmic bytes (or flops) per step over
+    the phase's CUDA-event time; attention whose plain arithmetic intensity
+    exceeds the ridge point is reported against the tensor peak."""
+    hbm, tflops, peak_kind = peaks()
+    gbs = nbytes / secs / 1e9
+    e = {"kernel": kernel, "launches_per_step": launches}
+    ridge = tflops * 1e12 / (hbm * 1e9)
+    if flops is not None and flops / nbytes > ridge:
+        tf = flops / secs / 1e12
+        e.update({"bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
+                  "frac": round(tf / tflops, 4),
+                  "peak_kind": f"{peak_kind} dense bf16 GEMM (burst); the kernel's f16 MMAs run at the same rate",
+                  "per_step_flops": flops, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)})
     else:
-        wl.encode_k()
-        wl.encode_v()
+        e.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                  "frac": round(gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth"})
+    e["per_step_bytes"] = nbytes
+    if flops is not None:
+        e.update({"intensity_flop_per_byte": round(flops / nbytes, 1), "ridge_flop_per_byte": round(ridge, 1)})
+    e["time_us"] = round(secs * 1e6, 2)
+    return e
 
 
 def run_native(args, world, rank, local, pg):
@@ -715,95 +789,81 @@ def run_native(args, world, rank, local, pg):
     b.build()
     import rotated_lloyd_max_gb300 as tq
     tq.load()
-    if args.workload == "qwen2_1p5b_ctx2048":
-        wl = QwenCache(dev, splits=args.splits)
-    else:
-        wl = BigCache(args.workload, dev, layers=args.layers, batch=args.batch, splits=args.splits)
+    wl = CacheWorkload(args.workload, dev, layers=args.layers, batch=args.batch, splits=args.splits)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    def step_eager():
+        flush.zero_(); wl.encode()
+        wl.ev.reset(); flush.zero_(); wl.ev.run()
+        flush.zero_(); wl.attention()
+
     for _ in range(max(args.warmup, 3)):
-        flush.zero_(); encode_all(wl); wl.attention()
+        step_eager()
     torch.cuda.synchronize()
     # each phase is captured once and replayed, so the timed region measures
     # device work, not the host's per-call argument marshalling
     graphs = []
-    concurrent_enc = hasattr(wl, "encode_both")
-    enc_fns = ([wl.encode_both] if concurrent_enc else
-               [wl.encode_k] + ([] if getattr(wl, "shared", False) else [wl.encode_v]))
-    n_enc_launches = 1 if getattr(wl, "shared", False) else 2
-    for fn in (*enc_fns, wl.attention):
+    for fn in (wl.encode, wl.ev.reset, wl.ev.run, wl.attention):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="relaxed"):
             fn()
         graphs.append(g)
-    for _ in range(max(args.warmup, 3)):
+    g_enc, g_reset, g_ev, g_attn = graphs
+
+    def step(e=None):
         flush.zero_()
-        for g in graphs:
-            g.replay()
+        if e: e[0].record(stream)
+        g_enc.replay()
+        if e: e[1].record(stream)
+        g_reset.replay()                  # counter templates (three 4-byte-per-unit copies), untimed
+        flush.zero_()
+        if e: e[2].record(stream)
+        g_ev.replay()
+        if e: e[3].record(stream)
+        flush.zero_()
+        if e: e[4].record(stream)
+        g_attn.replay()
+        if e: e[5].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     barrier(pg)
     torch.cuda.synchronize()
     for s in range(K):
-        flush.zero_()                     # L2 flush, outside the timed events
-        e = ev[s]
-        e[0].record(stream)
-        graphs[0].replay()
-        e[1].record(stream)
-        if len(graphs) == 3:
-            graphs[1].replay()
-        e[2].record(stream)
-        graphs[-1].replay()
-        e[3].record(stream)
+        step(ev[s])
     torch.cuda.synchronize()
     barrier(pg)
     clk = clocks.stop()
-    t_step = [e[0].elapsed_time(e[3]) / 1e3 for e in ev]
-    t_enc = [(e[0].elapsed_time(e[2])) / 1e3 for e in ev]
-    t_attn = [e[2].elapsed_time(e[3]) / 1e3 for e in ev]
-    total = sum(t_step)
+    t_enc = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3 / K
+    t_ev = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3 / K
+    t_attn = sum(e[4].elapsed_time(e[5]) for e in ev) / 1e3 / K
+    total = (t_enc + t_ev + t_attn) * K
     total_max = max_over_ranks(pg, total, dev)
     bytes_all = sum_over_ranks(pg, wl.step_bytes * K, dev)
     value = bytes_all / total_max / 1e9
-    n_enc = n_enc_launches
-    if concurrent_enc:
-        # the two launches overlap: the phase (both launches' bytes over the
-        # phase time) stands for the encode kernel
-        enc_launch = sum(t_enc) / K
-        enc_bytes_per_launch = wl.enc_in + wl.enc_out
-    else:
-        enc_launch = sum(t_enc) / (n_enc * K)    # average encode launch
-        enc_bytes_per_launch = (wl.enc_in + wl.enc_out) / n_enc
-    attn_region = sum(t_attn) / K
-    hbm, tflops, peak_kind = peaks()
-    enc_gbs = enc_bytes_per_launch / enc_launch / 1e9
-    attn_gbs = wl.attn_bytes / attn_region / 1e9
-    dominant = "tq_encode" if sum(t_enc) >= sum(t_attn) else "tq_decode_attn"
-    # attention is bound by the tensor cores when its arithmetic intensity
-    # (plain q.k + p.v flops per algorithmic byte) exceeds the ridge point
-    intensity = wl.attn_flops / wl.attn_bytes
-    ridge = tflops * 1e12 / (hbm * 1e9)
-    if dominant == "tq_encode":
-        roof = {"bound": "hbm", "achieved": round(enc_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(enc_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                "per_launch_bytes": enc_bytes_per_launch}
-    elif intensity <= ridge:
-        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(attn_gbs / hbm, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                "per_launch_bytes": wl.attn_bytes}
-    else:
-        attn_tf = wl.attn_flops / attn_region / 1e12
-        roof = {"bound": "tensor", "achieved": round(attn_tf, 2), "peak": tflops, "unit": "TFLOP/s",
-                "frac": round(attn_tf / tflops, 4),
-                "peak_kind": f"{peak_kind} dense bf16 GEMM (burst); the kernel's f16 MMAs run at the same rate",
-                "per_launch_flops": wl.attn_flops, "hbm_frac": round(attn_gbs / hbm, 4)}
-    roof.update({"intensity_flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1)})
-    per_layer = (per_layer_attention(wl, stream, flush, max(3, min(200, K)))
-                 if isinstance(wl, QwenCache) else attn_region)
+    phases = {
+        "tq_encode": roofline_entry("tq_encode" + ("" if wl.shared else " (K and V concurrent on two streams)"
+                                                   if wl.concurrent_enc else " (K then V)"),
+                                    wl.enc_in + wl.enc_out, t_enc, wl.enc_launches),
+        "tq_evict": roofline_entry("tq_evict (one chunk per layer, batch and kv head)", wl.ev.bytes, t_ev,
+                                   wl.ev.launches),
+        "tq_decode_attn": roofline_entry(f"tq_decode_attn ({wl.plan['compressed_kernel']} + "
+                                         f"{wl.plan['dense_kernel']} dense splits + merge)",
+                                         wl.attn_bytes, t_attn, wl.plan["launches"], flops=wl.attn_flops),
+    }
+    for name, e in phases.items():
+        t = measured_traffic(wl.name if wl.L == wl.cfg["L"] and wl.B == wl.cfg["B"] else "", name)
+        e["traffic"] = t
+        e["traffic_sources_sha"] = phase_sources_sha(name)
+    dominant = max(phases, key=lambda k: phases[k]["time_us"])
+    per_layer = per_layer_attention(wl, stream, flush, max(3, min(200, K))) if wl.args_layer else None
+    cfg = wl.cfg
     line = {
         "metric": "decode-attn KV GB/s & tok/s; encode Mvec/s; % of GB300 HBM roofline",
         "value": round(value, 2),
@@ -818,45 +878,49 @@ def run_native(args, world, rank, local, pg):
         "dtype": "bf16 in, packed codes, f32 math",
         "data": "synthetic (seeded, generated on device)",
         "config": {"workload": wl.name, "layers": wl.L, "batch": wl.B, "kv_heads": wl.Hkv,
-                   "q_heads": wl.Hq, "head_dim": wl.d, "ctx": wl.ctx, "k_bits": wl.cfg["kb"],
-                   "v_bits": wl.cfg["vb"], "bf16_layers": wl.dense, "l2": "flushed (256 MiB write) before each step",
-                   "tail_tokens": getattr(wl, "tail", 0),
+                   "q_heads": wl.Hq, "head_dim": wl.d, "ctx": wl.ctx, "k_bits": cfg["kb"],
+                   "v_bits": cfg["vb"], "outlier_T": cfg["T"], "bf16_layers": wl.dense,
+                   "tail_tokens": wl.tail, "full_size": wl.L == cfg["L"] and wl.B == cfg["B"],
+                   "l2": "flushed (256 MiB write) before each phase, outside its events",
                    "attention_splits": args.splits or "planner",
-                   "step": f"encode whole cache ({n_enc} launch(es){', K and V concurrent on two streams' if concurrent_enc else ''})"
-                           f" + decode attention of all {wl.L} layers in one tq_decode_attn call"
-                           f" ({wl.plan['launches']} launches)",
+                   "step": (f"encode whole cache ({wl.enc_launches} launch(es)) + evict one chunk per "
+                            f"(layer, batch, kv head) ({wl.ev.launches} launches) + decode attention of all "
+                            f"{wl.L} layers in one tq_decode_attn call ({wl.plan['launches']} launches)"),
+                   "eviction": {"window": EVICT_WINDOW, "margin": EVICT_MARGIN, "t_q": EVICT_TQ,
+                                "ring_slots": wl.ev.cap, "chunks_per_call": 1},
                    "parallelism": f"replicas x{world}"},
         "breakdown": {
-            "encode_mvec_s": round(wl.vectors_per_step / (sum(t_enc) / K) / 1e6, 1),
-            "encode_gbs": round(enc_gbs, 1),
-            "decode_attn_kv_gbs": round(attn_gbs, 1),
-            "decode_attn_tok_s": round(wl.tokens_per_step / attn_region, 1),
-            "decode_attn_us_per_step": round(attn_region * 1e6, 2),
-            "decode_attn_per_layer_calls_us_per_step": round(per_layer * 1e6, 2),
-            "encode_us_per_step": round(sum(t_enc) / K * 1e6, 2),
+            "encode_mvec_s": round(wl.vectors_per_step / t_enc / 1e6, 1),
+            "encode_us_per_step": round(t_enc * 1e6, 2),
+            "evict_mvec_s": round(wl.ev.vectors / t_ev / 1e6, 1),
+            "evict_us_per_step": round(t_ev * 1e6, 2),
+            "decode_attn_kv_gbs": round(wl.attn_bytes / t_attn / 1e9, 1),
+            "decode_attn_tok_s": round(wl.tokens_per_step / t_attn, 1),
+            "decode_attn_us_per_step": round(t_attn * 1e6, 2),
+            **({"decode_attn_per_layer_calls_us_per_step": round(per_layer * 1e6, 2)} if per_layer else {}),
             "step_algorithmic_bytes": wl.step_bytes,
             "attention_plan": wl.plan,
         },
-        "roofline": {"kernel": dominant + (" (K and V launches, concurrent)" if concurrent_enc and dominant == "tq_encode" else ""),
-                     **roof, "traffic": MEASURED_TRAFFIC.get((wl.name, dominant))},
+        "roofline": {**phases[dominant], "phase": dominant},
+        "roofline_phases": phases,
         "gpu_launches": wl.launches_per_step * K,
     }
     if clk:
         line["clocks"] = clk
     if not args.no_e2e:
-        line["e2e"] = e2e_leg(wl, dev, max(3, min(50, K)))
+        line["e2e"] = e2e_leg(wl, max(3, min(50 if wl.step_bytes < (1 << 30) else 3, K)))
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         import oracle
-        if isinstance(wl, QwenCache):
+        if wl.dense:
             hin = wl.host_inputs()
             nbytes, secs = oracle_step(wl, hin)
-            sample = ("one full step (all 28 layers: encode of the 22 compressed layers + attention of every "
-                      "layer), fp64 C oracle")
+            sample = (f"one full step (all {wl.L} layers: encode of the {len(wl.comp)} compressed layers, one "
+                      "evicted chunk per stream, attention of every layer), fp64 C oracle")
         else:
-            step, sample = oracle_unit_sample(wl.cfg)
-            step()                                   # warm-up
+            step_o, sample = oracle_unit_sample(wl.cfg)
+            step_o()                                   # warm-up
             t0 = time.perf_counter()
-            nbytes = step()
+            nbytes = step_o()
             secs = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
                                 "cores": oracle.threads(), "kind": "oracle", "sample": sample}
@@ -865,8 +929,8 @@ def run_native(args, world, rank, local, pg):
 
 
 def per_layer_attention(wl, stream, flush, steps: int) -> float:
-    """Decode attention as 28 per-layer tq_decode_attn calls replayed from a
-    CUDA graph (the shape a model's layer loop issues); mean seconds per step."""
+    """Decode attention as per-layer tq_decode_attn calls replayed from a CUDA
+    graph (the shape a model's layer loop issues); mean seconds per step."""
     import torch
     graph = torch.cuda.CUDAGraph()
     wl.attention_per_layer()
@@ -879,7 +943,6 @@ def per_layer_attention(wl, stream, flush, steps: int) -> float:
     tot = 0.0
     for _ in range(steps):
         flush.zero_()
-        wl.encode_k(); wl.encode_v()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         graph.replay()
@@ -889,21 +952,37 @@ def per_layer_attention(wl, stream, flush, steps: int) -> float:
     return tot / steps
 
 
-def e2e_leg(wl, dev, steps: int):
-    """Same step through the public API with host buffers: pinned host inputs
-    copied in, the step, the output copied back, all inside the timed region."""
+E2E_PIN_LIMIT = 2 << 30   # larger inputs are staged from one pinned layer slice
+
+
+def e2e_leg(wl, steps: int):
+    """The step through the public API with host buffers: every input of the
+    step (the bf16 K/V the encode reads, the ring tokens the eviction reads,
+    q and the dense tail) copied in from pinned host memory, the three phases
+    run eagerly, the attention output copied back, all inside the timed
+    region.  An input larger than 2 GiB is copied layer by layer from one
+    pinned layer-sized host buffer (every layer receives the same host bytes:
+    the copied volume is the full input, the host memory pinned is one layer)."""
     import torch
     srcs = wl.inputs()
-    pin = {k: t.cpu().pin_memory() for k, t in srcs.items()}
+    plan = []
+    for name, t in srcs.items():
+        if t.numel() * t.element_size() > E2E_PIN_LIMIT:
+            h = t[0].cpu().pin_memory()
+            plan += [(t[l], h) for l in range(t.shape[0])]
+        else:
+            plan.append((t, t.cpu().pin_memory()))
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    h2d = sum(dv.numel() * dv.element_size() for dv, _ in plan)
     d2h = out_h.numel() * out_h.element_size()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for k, t in pin.items():
-            srcs[k].copy_(t, non_blocking=True)
-        encode_all(wl); wl.attention()
+        for dv, h in plan:
+            dv.copy_(h, non_blocking=True)
+        wl.encode()
+        wl.ev.reset(); wl.ev.run()
+        wl.attention()
         out_h.copy_(wl.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     secs = (time.perf_counter() - t0) / steps
@@ -914,8 +993,9 @@ def e2e_leg(wl, dev, steps: int):
 def oracle_unit_sample(cfg: dict):
     """The oracle's bounded sample of a cache workload: one (layer, kv head)
     unit of a compressed layer (its packed tokens encoded, one record stream
-    when keys and values share records, then attended with the unit's dense
-    tail) plus one unit of a bf16 layer where the workload has them.
+    when keys and values share records; its last chunk encoded again as the
+    eviction phase does; then attended with the unit's dense tail) plus one
+    unit of a bf16 layer where the workload has them.
     Returns (step() -> algorithmic bytes, description)."""
     import oracle
     import synth
@@ -939,17 +1019,21 @@ def oracle_unit_sample(cfg: dict):
     def step():
         kr = oracle.encode_records(k[:nc], okc)
         vr = kr if shared else oracle.encode_records(v[:nc], ovc)
+        ke = oracle.encode_records(k[nc - 128:nc], okc)
+        ve = ke if shared else oracle.encode_records(v[nc - 128:nc], ovc)
         kt, vt = (k[nc:], v[nc:]) if tail else (None, None)
         oracle.unit_attention(q, okc, ovc, kr, vr, nc, kt, vt, 1.0)
         rec = kr.nbytes + (0 if shared else vr.nbytes)
         nb = streams * nc * d * 2 + rec                              # encode: bf16 in, records out
+        nb += streams * 128 * d * 2 + ke.nbytes + (0 if shared else ve.nbytes)   # eviction of one chunk
         nb += rec + streams * tail * d * 2 + G * d * 6               # attention: records, tail, q, out
         if dense:
             oracle.unit_attention(q, None, None, None, None, 0, kd, vd, 1.0)
             nb += 2 * ctx * d * 2 + G * d * 6
         return nb
-    sample = (f"one (layer, kv head) unit ({nc} packed tokens, {streams} stream(s)) attended with its "
-              f"{tail}-token dense tail" + (", plus one bf16-layer unit" if dense else "") + ", fp64 C oracle")
+    sample = (f"one (layer, kv head) unit ({nc} packed tokens, {streams} stream(s), its last chunk evicted "
+              f"again) attended with its {tail}-token dense tail" + (", plus one bf16-layer unit" if dense else "")
+              + ", fp64 C oracle")
     return step, sample
 
 

@@ -26,7 +26,7 @@ def test_reference_arm_json_line(workload):
               "scaling", "vs_baseline", "dtype", "data", "config"):
         assert k in d, k
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
-    assert d["config"]["workload"] == (workload or "qwen2_1p5b_ctx2048")
+    assert d["config"]["workload"] == (workload or "batched_b32_ctx32768")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
