@@ -53,6 +53,7 @@ tq_status resolve_codec(const tq_codec* c, CodecDev* o) {
   o->rec_bytes = record_layout(d, b, outl, o->cap, &o->off_norm, &o->off_count, &o->off_entries);
   o->thr_out = outl ? (float)((double)c->outlier_T / std::sqrt((double)d)) : INFINITY;
   o->inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  o->inv_sqrt_d_lo = (float)(1.0 / std::sqrt((double)d) - (double)o->inv_sqrt_d);
   o->sqrt_d = (float)std::sqrt((double)d);
   for (int k = 0; k < 16; ++k) o->centroids[k] = c->centroids[k & (K - 1)];
   for (int k = 0; k < 15; ++k) o->boundaries[k] = k + 1 < K ? c->boundaries[k] : 0.f;

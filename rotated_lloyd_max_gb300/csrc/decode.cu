@@ -9,6 +9,10 @@
 
 namespace tq {
 
+// Adding and subtracting 1.5 * 2^9 rounds an f32 of magnitude below 2^9 to
+// the nearest multiple of 2^-14.
+constexpr float kSplitMagic = 768.0f;
+
 template <int D, int B, bool OUTL>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int L = D / 32, VPW = 32 / L, VPC = 4 * VPW, RB = D * B / 8;
@@ -77,19 +81,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
           }
         }
       }
+      // Split transform: yhat = hi + lo with hi on the 2^-14 grid (|yhat| <= 1,
+      // so every partial sum of at most 512 hi values is an integer multiple of
+      // 2^-14 below 2^9 and exact in f32) and lo = yhat - hi exact; H(hi) is
+      // exact and H(lo), at most 2^-15 d, carries f32 rounding only relative to
+      // its own small size.
+      float lo[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        const float h = (x[r] + kSplitMagic) - kSplitMagic;
+        lo[r] = x[r] - h;
+        x[r] = h;
+      }
       fwht_regs<32>(x);
       fwht_lanes<32>(x, lane, L);
+      fwht_regs<32>(lo);
+      fwht_lanes<32>(lo, lane, L);
       if (valid) {
-        const float f = n * scale;
+        // n * (H(hi) + H(lo)) / sqrt(d) rounded once: f = n / sqrt(d) is carried
+        // as fh + fl (fl: the product's rounding error plus n times the error
+        // of the f32 constant 1/sqrt(d)), and the small terms fh * H(lo) and
+        // fl * H(hi) enter the last fused multiply-add of fh * H(hi).
+        const float fh = n * scale;
+        const float fl = fmaf(n, scale, -fh) + n * p.c.inv_sqrt_d_lo;
         float4* dst = reinterpret_cast<float4*>(dst_g + (ci * kChunk + slot - p.first_vec) * p.dst_vs + lg * 32);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          float4 o;
-          o.x = (((sbits >> (4 * k + 0)) & 1u) ? -f : f) * x[4 * k + 0];
-          o.y = (((sbits >> (4 * k + 1)) & 1u) ? -f : f) * x[4 * k + 1];
-          o.z = (((sbits >> (4 * k + 2)) & 1u) ? -f : f) * x[4 * k + 2];
-          o.w = (((sbits >> (4 * k + 3)) & 1u) ? -f : f) * x[4 * k + 3];
-          dst[k] = o;
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * k + e;
+            const float v = fmaf(fh, x[r], fmaf(fh, lo[r], fl * x[r]));
+            o[e] = ((sbits >> r) & 1u) ? -v : v;
+          }
+          dst[k] = make_float4(o[0], o[1], o[2], o[3]);
         }
       }
     }

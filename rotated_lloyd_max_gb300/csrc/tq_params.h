@@ -13,6 +13,7 @@ struct CodecDev {
   int rec_bytes, off_norm, off_count, off_entries;
   float thr_out;     // T / sqrt(d) in f32 (+inf when T is +inf)
   float inv_sqrt_d;  // f32(1/sqrt(d))
+  float inv_sqrt_d_lo;  // 1/sqrt(d) - f32(1/sqrt(d)), rounded to f32
   float sqrt_d;      // f32(sqrt(d))
   float centroids[16];
   float boundaries[15];
