@@ -62,7 +62,8 @@ def _load():
             "orc_bf16_to_double": (f64, [ctypes.c_uint16]),
             "orc_double_to_bf16": (ctypes.c_uint16, [f64]),
             "orc_record_layout": (i64, [i32, i32, i32, i32, P, P, P]),
-            "orc_encode_vectors": (None, [P, i64, i32, i64, i32, P, P, f64, P, P, P, P, P]),
+            "orc_encode_vectors": (None, [P, i64, i32, i64, i32, P, P, P, f64, i32, P, P, P, P, P]),
+            "orc_midpoints_f32": (None, [i32, P, P]),
             "orc_pack_record": (None, [i32, i32, i32, i32, i32, P, P, P, P, P]),
             "orc_read_code": (i32, [P, i32, i32]),
             "orc_decode_records": (None, [P, i64, i64, i32, i32, i32, i32, P, P, i32, P]),
@@ -112,6 +113,14 @@ def codebook_f32(bits: int, d: int):
     return c, t[:K - 1]
 
 
+def midpoints_f32(bits: int, c32: np.ndarray) -> np.ndarray:
+    """f32 midpoints of an ascending f32 centroid table (its decision boundaries)."""
+    c = np.ascontiguousarray(c32, np.float32)
+    t = np.zeros(max((1 << bits) - 1, 1), np.float32)
+    _load().orc_midpoints_f32(bits, _p(c), _p(t))
+    return t[:(1 << bits) - 1]
+
+
 def splitmix64(seed: int, n: int) -> np.ndarray:
     st = (ctypes.c_uint64 * 1)(seed)
     lib = _load()
@@ -154,6 +163,9 @@ def default_outlier_cap(d: int) -> int:
     return 4 * ((8 * CHUNK * d + 399) // 400)
 
 
+SCALE_MODES = {"norm": 0, "matched_norm": 1, "inner_product": 2, "least_squares": 3}
+
+
 @dataclass(frozen=True)
 class Codec:
     d: int
@@ -161,6 +173,8 @@ class Codec:
     seed: int = 1
     T: float = 0.0          # 0: no outlier section
     cap: int = 0            # entries per record (0: default)
+    centroids: tuple = ()   # caller-supplied ascending f32 table (2^bits values); () = the Gaussian table
+    scale: str = "norm"     # stored per-vector scale (see orc_encode_vector)
 
     @property
     def has_outliers(self) -> bool:
@@ -185,7 +199,12 @@ class Codec:
         return self.layout()["size"]
 
     def tables(self):
-        c, t = codebook_f32(self.bits, self.d)
+        if self.centroids:
+            c = np.array(self.centroids, np.float32)
+            assert c.shape == (1 << self.bits,)
+            t = midpoints_f32(self.bits, c)
+        else:
+            c, t = codebook_f32(self.bits, self.d)
         return c, t, signs(self.seed, self.d)
 
 
@@ -196,14 +215,15 @@ def encode_vectors(x_bf16: np.ndarray, codec: Codec, want_y: bool = False):
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     n, d = x.shape
     assert d == codec.d
-    _, t, s = codec.tables()
+    c, t, s = codec.tables()
     codes = np.zeros((n, d), np.uint8)
     norms = np.zeros(n, np.float32)
     is_out = np.zeros((n, d), np.uint8)
     oval = np.zeros((n, d), np.uint16)
     y = np.zeros((n, d), np.float64) if want_y else None
     T = codec.T if codec.has_outliers else 0.0
-    _load().orc_encode_vectors(_p(x), n, d, d, codec.bits, _p(np.ascontiguousarray(t)), _p(s), T,
+    _load().orc_encode_vectors(_p(x), n, d, d, codec.bits, _p(np.ascontiguousarray(c)),
+                               _p(np.ascontiguousarray(t)), _p(s), T, SCALE_MODES[codec.scale],
                                _p(codes), _p(norms), _p(is_out), _p(oval),
                                _p(y) if y is not None else None)
     return dict(codes=codes, norms=norms, is_out=is_out, oval=oval, y=y)

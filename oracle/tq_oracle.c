@@ -113,6 +113,17 @@ int orc_lloyd_max_gaussian(int bits, double* c, double* t, double* mse) {
 }
 
 /*
+ * Boundaries of a caller-supplied ascending f32 centroid table (a calibrated
+ * table, P1's calibrated Lloyd-Max commit: a 2^b sorted f32 table loaded in
+ * place of the Gaussian one): the f32 midpoints of consecutive centroids,
+ * computed in fp64 and rounded, as for the Gaussian table below.
+ */
+void orc_midpoints_f32(int bits, const float* c32, float* t32) {
+  const int K = 1 << bits;
+  for (int k = 0; k + 1 < K; ++k) t32[k] = (float)(0.5 * ((double)c32[k] + (double)c32[k + 1]));
+}
+
+/*
  * The table a codec of head dimension d uses: the unit-variance table scaled
  * by 1/sqrt(d) [P3], rounded to f32; boundaries are the f32 midpoints of the
  * f32 centroids (computed in fp64, then rounded).
@@ -215,10 +226,25 @@ int64_t orc_record_layout(int d, int bits, int has_outliers, int cap, int64_t* o
  *   code_j = #{k : y_j > t_k};
  *   outlier_j = (T > 0) and |y_j| > T / sqrt(d), value bf16(y_j).
  * A zero vector gives y = 0.  y (fp64) is returned for boundary accounting.
+ *
+ * The stored per-vector scale S (the record's f32 "norm" field, by which
+ * decode multiplies H(yhat)) is chosen by scale_mode [P2, the EDEN-scale
+ * commits and their Appendix A note; P1's matched-norm operating point].
+ * With chat the dequantised rotated vector (centroids c32[code_j], replaced by
+ * the bf16 value at every outlier coordinate of the vector) and the decoded
+ * vector xhat = S s.H(chat)/sqrt(d):
+ *   0  S = ||x||                                    (the plain codec)
+ *   1  S = ||x|| / ||chat||                         matched norm: ||xhat|| = ||x||
+ *   2  S = ||x|| / <chat, y>  = ||x||^2 / <c, x>    inner-product preserving: <xhat, x> = ||x||^2
+ *   3  S = ||x|| <chat, y> / ||chat||^2 = <c, x> / ||c||^2
+ *                                                   least squares: min over S of ||x - xhat||^2
+ * (c = s.H(chat)/sqrt(d), the unit-scale reconstruction in the original basis;
+ * the transform is orthonormal, so <c, x> = ||x|| <chat, y> and ||c|| = ||chat||.)
+ * Modes 2 and 3 multiply to the square of mode 1.  A zero vector stores 0.
  */
-void orc_encode_vector(const uint16_t* x, int d, int bits, const float* t32, const int8_t* s,
-                       double T, uint8_t* code, float* norm, uint8_t* is_out, uint16_t* oval,
-                       double* y_out) {
+void orc_encode_vector(const uint16_t* x, int d, int bits, const float* c32, const float* t32,
+                       const int8_t* s, double T, int scale_mode, uint8_t* code, float* norm,
+                       uint8_t* is_out, uint16_t* oval, double* y_out) {
   double y[512];
   double ss = 0.0;
   for (int j = 0; j < d; ++j) {
@@ -241,15 +267,28 @@ void orc_encode_vector(const uint16_t* x, int d, int bits, const float* t32, con
     oval[j] = o ? orc_double_to_bf16(y[j]) : 0;
     if (y_out) y_out[j] = y[j];
   }
+  if (scale_mode != 0 && n > 0.0) {
+    double cc = 0.0, cy = 0.0;
+    for (int j = 0; j < d; ++j) {
+      const double cj = is_out[j] ? orc_bf16_to_double(oval[j]) : (double)c32[code[j]];
+      cc += cj * cj;
+      cy += cj * y[j];
+    }
+    double S = n;
+    if (scale_mode == 1) S = n / sqrt(cc);
+    else if (scale_mode == 2) S = n / cy;
+    else if (scale_mode == 3) S = n * cy / cc;
+    *norm = (float)S;
+  }
 }
 
 /* Encode n vectors (row stride in elements) into per-coordinate arrays. */
 void orc_encode_vectors(const uint16_t* x, int64_t n, int d, int64_t stride, int bits,
-                        const float* t32, const int8_t* s, double T, uint8_t* codes, float* norms,
-                        uint8_t* is_out, uint16_t* oval, double* y) {
+                        const float* c32, const float* t32, const int8_t* s, double T, int scale_mode,
+                        uint8_t* codes, float* norms, uint8_t* is_out, uint16_t* oval, double* y) {
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; ++i)
-    orc_encode_vector(x + i * stride, d, bits, t32, s, T, codes + i * d, norms + i,
+    orc_encode_vector(x + i * stride, d, bits, c32, t32, s, T, scale_mode, codes + i * d, norms + i,
                       is_out + i * d, oval + i * d, y ? y + i * d : NULL);
 }
 
