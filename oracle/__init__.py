@@ -71,6 +71,8 @@ def _load():
             "orc_attention_rotated": (None, [P, i32, P, P, i64, P, P, i64, i32, f64, f64, P, P, P]),
             "orc_retention_floor": (i32, [i32, i32, i32]),
             "orc_chunks_to_evict": (i32, [i32, i32, i32, i32, i32]),
+            "orc_bf16_round_array": (None, [P, i64, P]),
+            "orc_rollback_counts": (i32, [i32, i32, i32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -345,3 +347,44 @@ def evict(tail_k, tail_v, start: int, length: int, n_chunks: int, k_rec, v_rec, 
             if v_rec is not None:
                 v_rec[h, n_chunks + e] = encode_records(tail_v[h, slots], codec_v)[0]
     return (start + k * CHUNK) % cap, length - k * CHUNK, n_chunks + k
+
+
+# ---------------------------------------------------------------------------
+# Rollback
+# ---------------------------------------------------------------------------
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """bf16 bits (nearest, ties to even) of every value of a fp64 array."""
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.zeros(x.shape, np.uint16)
+    _load().orc_bf16_round_array(_p(x), x.size, _p(out))
+    return out
+
+
+def rollback_counts(n_chunks: int, tail_len: int, new_len: int):
+    """(n_chunks', tail_len', start reset?, tokens to decode) of a rollback."""
+    n, ln, rs = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    m = _load().orc_rollback_counts(n_chunks, tail_len, new_len, ctypes.byref(n), ctypes.byref(ln),
+                                    ctypes.byref(rs))
+    return n.value, ln.value, bool(rs.value), m
+
+
+def rollback(tail_k, tail_v, start: int, length: int, n_chunks: int, k_rec, v_rec, codec_k: Codec,
+             codec_v: Codec | None, new_len: int):
+    """Rollback of one (layer, batch) unit, every kv head (see orc_rollback_counts).
+
+    tail_k/tail_v: bf16 ring buffers [Hkv, cap, d] (uint16, modified in place;
+    tail_v None when keys and values share records and ring); k_rec/v_rec:
+    record arrays [Hkv, rec_cap, bytes] (read only).  On a deep rollback the m
+    remaining tokens of record n' are decoded (fp64) and rounded to bf16 into
+    ring slots 0..m-1.  Returns (start, length, n_chunks)."""
+    n2, len2, reset, m = rollback_counts(n_chunks, length, new_len)
+    if not reset:
+        return start, len2, n2
+    for h in range(tail_k.shape[0]):
+        for tail, rec, cod in ((tail_k, k_rec, codec_k), (tail_v, v_rec, codec_v)):
+            if tail is None or m == 0:
+                continue
+            x = decode_records(rec[h, n2:n2 + 1], m, cod)
+            tail[h, :m] = bf16_round(x)
+    return 0, len2, n2
+

@@ -191,6 +191,11 @@ uint16_t orc_double_to_bf16(double y) {
   return (uint16_t)(u >> 16);
 }
 
+/* bf16 of each of n doubles (orc_double_to_bf16 applied elementwise). */
+void orc_bf16_round_array(const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_double_to_bf16(x[i]);
+}
+
 /* ------------------------------------------------------------------------- */
 /* Record layout                                                             */
 /* ------------------------------------------------------------------------- */
@@ -490,6 +495,33 @@ void orc_attention_rotated(const double* q, int G, const double* Kr, const doubl
  * Number of whole chunks that leave a tail of `tail_len` tokens: the largest
  * k with tail_len - k * chunk >= retention floor (0 when none).
  */
+/*
+ * Rollback of one stream to new_len tokens [P4 "What landed": the cache reports
+ * its length in tokens and maps truncation onto both time bases, the packed
+ * records and the dense tail; a deep rollback has to dequantise].  Given
+ * n_chunks, tail_len and new_len, writes the new counters and the number of
+ * leading tokens of record n_chunks' that must be decoded into the tail:
+ *   T = clamp(new_len, 0, 128 n + len);
+ *   T >= 128 n: n' = n, len' = T - 128 n, start kept, nothing decoded;
+ *   T <  128 n: n' = T / 128, len' = T mod 128, start' = 0, len' tokens of
+ *               record n' decoded.
+ * Returns the number of tokens to decode.
+ */
+int orc_rollback_counts(int n_chunks, int tail_len, int new_len, int* n_out, int* len_out, int* start_reset) {
+  const int total = ORC_CHUNK * n_chunks + tail_len;
+  const int T = new_len < 0 ? 0 : (new_len > total ? total : new_len);
+  if (T >= ORC_CHUNK * n_chunks) {
+    *n_out = n_chunks;
+    *len_out = T - ORC_CHUNK * n_chunks;
+    *start_reset = 0;
+    return 0;
+  }
+  *n_out = T / ORC_CHUNK;
+  *len_out = T % ORC_CHUNK;
+  *start_reset = 1;
+  return *len_out;
+}
+
 int orc_retention_floor(int window, int t_q, int margin) {
   return window + ((t_q - 1) > margin ? (t_q - 1) : margin);
 }
