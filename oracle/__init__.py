@@ -72,6 +72,8 @@ def _load():
             "orc_retention_floor": (i32, [i32, i32, i32]),
             "orc_chunks_to_evict": (i32, [i32, i32, i32, i32, i32]),
             "orc_bf16_round_array": (None, [P, i64, P]),
+            "orc_attention_sparse_v": (None, [P, i32, P, P, i64, i32, f64, f64, f64, i32, P, P, P, i32, i32, P,
+                                              P]),
             "orc_rollback_counts": (i32, [i32, i32, i32, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -280,6 +282,57 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, softcap
     out = np.zeros((G, d), np.float64)
     _load().orc_attention(_p(q), G, _p(K), _p(V), K.shape[0], d, float(scale), float(softcap), _p(out))
     return out
+
+
+def attention_sparse_v(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, eps: float, group: int,
+                       blocks, softcap: float = 0.0):
+    """Attention with sparse-V skipping (see orc_attention_sparse_v) in fp64.
+    blocks: list of (begin, end, sequence) token ranges, each sequence's
+    blocks in visiting order.  Returns (out [G, d], skipped (group, token) pairs)."""
+    q = np.ascontiguousarray(q, np.float64)
+    K = np.ascontiguousarray(K, np.float64)
+    V = np.ascontiguousarray(V, np.float64)
+    G, d = q.shape
+    bb = np.ascontiguousarray([b[0] for b in blocks] or [0], np.int64)
+    be = np.ascontiguousarray([b[1] for b in blocks] or [0], np.int64)
+    bs = np.ascontiguousarray([b[2] for b in blocks] or [0], np.int32)
+    n_seq = (max(b[2] for b in blocks) + 1) if blocks else 0
+    out = np.zeros((G, d), np.float64)
+    sk = np.zeros(1, np.int64)
+    _load().orc_attention_sparse_v(_p(q), G, _p(K), _p(V), K.shape[0], d, float(scale), float(softcap),
+                                   float(eps), int(group), _p(bb), _p(be), _p(bs), len(blocks), n_seq, _p(out),
+                                   _p(sk))
+    return out, int(sk[0])
+
+
+def sparse_v_blocks(n_records: int, records_per_split: int, warps: int = 4):
+    """The blocks of the tensor-core decode kernel's schedule: split s covers
+    records [s cps, (s+1) cps); within it, warp w visits the tokens
+    [128 r + 32 w, 128 r + 32 w + 32) of its records in order, sharing one
+    running maximum (a sequence per (split, warp))."""
+    blocks = []
+    span = 128 // warps
+    n_split = (n_records + records_per_split - 1) // records_per_split if n_records else 0
+    for s_ in range(n_split):
+        for w in range(warps):
+            for r in range(s_ * records_per_split, min((s_ + 1) * records_per_split, n_records)):
+                blocks.append((128 * r + span * w, 128 * r + span * (w + 1), s_ * warps + w))
+    return blocks
+
+
+def unit_attention_sparse_v(q_bf16, codec_k: Codec, codec_v: Codec, k_rec, v_rec, n_comp, k_dense_bf16,
+                            v_dense_bf16, scale, eps, records_per_split, heads_per_cta, softcap=0.0):
+    """unit_attention with sparse-V skipping over the compressed tokens, on the
+    tensor-core kernel's schedule (sparse_v_blocks); dense tokens are never
+    skipped.  Returns (out, skipped (group, token) pairs)."""
+    q = bf16_to_f64(q_bf16)
+    d = q.shape[1]
+    Ks, Vs = [decode_records(k_rec, n_comp, codec_k)], [decode_records(v_rec, n_comp, codec_v)]
+    if k_dense_bf16 is not None and len(k_dense_bf16):
+        Ks.append(bf16_to_f64(k_dense_bf16).reshape(-1, d))
+        Vs.append(bf16_to_f64(v_dense_bf16).reshape(-1, d))
+    blocks = sparse_v_blocks(n_comp // 128, records_per_split)
+    return attention_sparse_v(q, np.concatenate(Ks), np.concatenate(Vs), scale, eps, heads_per_cta, blocks, softcap)
 
 
 def attention_rotated(q, Kr, Vr, Kd, Vd, scale, sk, sv, softcap=0.0):

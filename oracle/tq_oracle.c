@@ -436,6 +436,78 @@ void orc_attention(const double* q, int G, const double* K, const double* V, int
 }
 
 /*
+ * Attention with sparse-V dequantisation [P2, turboquant_plus commit log:
+ * "safer-asym + sparse-V dequant", value work skipped where the post-softmax
+ * weight is negligible].  Tokens 0 .. n_blk_tokens-1 are partitioned into
+ * blocks [blk_begin[b], blk_end[b]); each block belongs to sequence blk_seq[b],
+ * and the blocks of a sequence are visited in the order they are listed,
+ * sharing per query head the running maximum M_h of the logits of the blocks
+ * visited before (-inf at the start).  Query heads are taken in groups of
+ * `group` consecutive heads; a block's values are skipped for a group when
+ * every logit of every head of the group in the block lies below
+ * M_h + ln(eps).  Skipped tokens still count in the softmax denominator; tokens
+ * outside the blocks are never skipped.  Every logit is computed in fp64 as in
+ * orc_attention.  Writes the number of (group, token) pairs skipped.
+ */
+void orc_attention_sparse_v(const double* q, int G, const double* K, const double* V, int64_t n, int d,
+                            double scale, double softcap, double eps, int group, const int64_t* blk_begin,
+                            const int64_t* blk_end, const int* blk_seq, int n_blk, int n_seq, double* out,
+                            int64_t* skipped) {
+  const int n_grp = (G + group - 1) / group;
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)G);
+  unsigned char* skip = (unsigned char*)calloc((size_t)n_grp * (size_t)(n > 0 ? n : 1), 1);
+  for (int g = 0; g < G; ++g)
+    for (int64_t i = 0; i < n; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < d; ++j) acc += q[(int64_t)g * d + j] * K[i * d + j];
+      logit[(int64_t)g * n + i] = soft_cap(scale * acc, softcap);
+    }
+  int64_t n_skip = 0;
+  const double lne = eps > 0.0 ? log(eps) : -INFINITY;
+  double* M = (double*)malloc(sizeof(double) * (size_t)G);
+  for (int sq = 0; sq < n_seq; ++sq) {
+    for (int g = 0; g < G; ++g) M[g] = -INFINITY;
+    for (int b = 0; b < n_blk; ++b) {
+      if (blk_seq[b] != sq) continue;
+      for (int hg = 0; hg < n_grp; ++hg) {
+        int all_low = 1;
+        for (int g = hg * group; g < G && g < (hg + 1) * group; ++g)
+          for (int64_t i = blk_begin[b]; i < blk_end[b]; ++i)
+            if (!(logit[(int64_t)g * n + i] < M[g] + lne)) all_low = 0;
+        if (all_low && eps > 0.0)
+          for (int64_t i = blk_begin[b]; i < blk_end[b]; ++i) {
+            skip[(int64_t)hg * n + i] = 1;
+            ++n_skip;
+          }
+      }
+      for (int g = 0; g < G; ++g)
+        for (int64_t i = blk_begin[b]; i < blk_end[b]; ++i)
+          if (logit[(int64_t)g * n + i] > M[g]) M[g] = logit[(int64_t)g * n + i];
+    }
+  }
+  for (int g = 0; g < G; ++g) {
+    double* o = out + (int64_t)g * d;
+    for (int j = 0; j < d; ++j) o[j] = 0.0;
+    if (n == 0) continue;
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i)
+      if (logit[(int64_t)g * n + i] > m) m = logit[(int64_t)g * n + i];
+    double Z = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+      const double p = exp(logit[(int64_t)g * n + i] - m);
+      Z += p;
+      if (skip[(int64_t)(g / group) * n + i]) continue;
+      for (int j = 0; j < d; ++j) o[j] += p * V[i * d + j];
+    }
+    for (int j = 0; j < d; ++j) o[j] /= Z;
+  }
+  if (skipped) *skipped = n_skip;
+  free(M);
+  free(skip);
+  free(logit);
+}
+
+/*
  * The same attention evaluated the way the fused kernel organises it (a
  * cross-check of the oracle, not a second reference): the query is rotated
  * once, q~ = H(s_k . q)/sqrt(d); a compressed key scores as n_i * q~ . yhat_i;
