@@ -72,6 +72,26 @@ const char* tq_status_string(int status);
 int tq_version(void);
 
 /*
+ * Per-vector scale stored in a record's f32 "norm" field (decode multiplies
+ * H(yhat) by it).  With chat the dequantised rotated unit vector (centroids,
+ * outlier values at the vector's outlier coordinates) and c = s.H(chat)/sqrt(d)
+ * its image in the original basis (turboquant_plus commit log: the
+ * EDEN-scale commits and their Appendix A note):
+ *   TQ_SCALE_NORM           ||x||                 (the plain codec)
+ *   TQ_SCALE_MATCHED_NORM   ||x|| / ||chat||      the decoded vector keeps ||x||
+ *   TQ_SCALE_INNER_PRODUCT  ||x||^2 / <c, x>      <xhat, x> = ||x||^2
+ *   TQ_SCALE_LEAST_SQUARES  <c, x> / ||c||^2      minimises ||x - xhat||^2
+ * The last two multiply to the square of the matched norm.  Codes and
+ * outlier lists do not depend on the mode; a zero vector stores 0.
+ */
+typedef enum {
+  TQ_SCALE_NORM = 0,
+  TQ_SCALE_MATCHED_NORM = 1,
+  TQ_SCALE_INNER_PRODUCT = 2,
+  TQ_SCALE_LEAST_SQUARES = 3
+} tq_scale_mode;
+
+/*
  * Codec description, passed by pointer and read on the host at every call.
  * Filled by tq_make_codebook; plain data, copy freely.
  */
@@ -81,9 +101,11 @@ typedef struct {
   uint64_t sign_seed;     /* seed of the SplitMix64 sign diagonal */
   float outlier_T;        /* 0: no outlier section; > 0: keep |y_j| > T/sqrt(d) (may be +inf) */
   int32_t outlier_cap;    /* outlier entries per record (multiple of 4) */
-  float centroids[16];    /* 2^b ascending f32 centroids of N(0, 1/d) */
+  float centroids[16];    /* 2^b ascending f32 centroids (the Gaussian N(0, 1/d) table, or a
+                             caller's table set by tq_codec_set_centroids) */
   float boundaries[15];   /* 2^b - 1 f32 midpoints of consecutive centroids */
   uint32_t sign_bits[16]; /* bit j%32 of word j/32 set <=> s_j = -1 */
+  int32_t scale_mode;     /* tq_scale_mode; tq_make_codebook sets TQ_SCALE_NORM */
 } tq_codec;
 
 /* Device scratch tq_make_codebook needs (bytes). */
@@ -104,6 +126,21 @@ size_t tq_codebook_scratch_bytes(void);
 tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float outlier_T,
                            int outlier_cap, void* d_scratch, size_t scratch_bytes, tq_codec* out,
                            double* mse_out, void* stream);
+
+/*
+ * Replace a codec's table by a caller's ascending f32 centroid table of 2^b
+ * values (a calibrated table: "v1.3 PPL on vLLM" (PR #15), the calibrated
+ * Lloyd-Max commit, loads a sorted 2^b f32 table in place of the Gaussian
+ * one).  Host only.  Sets centroids[] and boundaries[] (f32 midpoints of
+ * consecutive centroids, computed in double); every other field is kept.
+ * The table must be strictly ascending and symmetric (c_k = -c_{2^b-1-k}),
+ * with |c_k| < 0.999 (the tensor-core attention holds centroids x 2^16 in
+ * f16), and for b >= 3 consecutive boundaries at least 1/128 apart (the
+ * encoders decide codes through 1/128-wide cells holding one boundary each):
+ * TQ_ERR_INVALID_ARG for an unordered or non-finite table, TQ_ERR_UNSUPPORTED
+ * for one breaking the other conditions; the codec is unchanged on error.
+ */
+tq_status tq_codec_set_centroids(tq_codec* codec, const float* centroids, int n_centroids);
 
 /* Bytes of one 128-token record of this codec; 0 if the codec is invalid. */
 size_t tq_record_bytes(const tq_codec* codec);
@@ -169,10 +206,43 @@ typedef struct {
   int32_t* tail_len;   /* device [L][B] */
   int32_t window, margin, t_q;
   int32_t max_evict;   /* upper bound on records written per (layer, batch) per call */
+  /* Paged records (optional; NULL = the contiguous layout above).  With a block
+   * table the record arrays are per-layer pools of rec_cap blocks, each block
+   * holding one record per kv head: record r of (l, b, h) sits at
+   *   k_rec + l*k_rec_layer_stride + (block_table[b*table_stride + r]*n_kv_heads + h)*record_bytes
+   * (likewise v_rec).  block_table: device int32 [batch][table_stride], shared
+   * by every layer and by keys and values; a sequence holds at most
+   * table_stride records.  The caller fills block_table[b][n_chunks[l][b] + e]
+   * before a call can evict into it; entries outside [0, rec_cap) are clamped
+   * into the pool (never an out-of-bounds access). */
+  const int32_t* block_table;
+  int32_t table_stride;
 } tq_evict_args;
 
 tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_evict_args* args,
                    void* stream);
+
+/*
+ * Rollback: truncate every (layer, batch) stream of a cache to new_len[l][b]
+ * tokens, mapping the truncation onto both time bases ("feat(v4): TurboQuant
+ * KV storage for DeepSeek-V4", "What landed": length reported in tokens,
+ * truncation mapped onto the packed records and the dense tail; a deep
+ * rollback dequantises).  With n = n_chunks, len = tail_len and
+ * T = min(max(new_len, 0), 128 n + len):
+ *   T >= 128 n: tail_len = T - 128 n (the newest tail tokens go; start kept);
+ *   T <  128 n: records r = T / 128 and later go; the m = T - 128 r tokens of
+ *               record r that remain are decoded (as tq_decode computes them)
+ *               and rounded to bf16 (nearest, ties to even) into ring slots
+ *               0 .. m-1 of every kv head (K and V), then n_chunks = r,
+ *               tail_start = 0, tail_len = m.
+ * Records are only read; the dropped ones keep their bytes and are
+ * overwritten by later evictions.  Every decision runs on the device (two
+ * launches per stream kind plus one bookkeeping launch, no host sync).
+ *   args: the cache as for tq_evict (window, margin, t_q and max_evict are
+ *   not used); new_len: device int32 [n_layers][batch].
+ */
+tq_status tq_rollback(const tq_codec* k_codec, const tq_codec* v_codec, const tq_evict_args* args,
+                      const int32_t* new_len, void* stream);
 
 /*
  * Fused decode attention (query rotation, scoring of the compressed keys,
@@ -226,6 +296,25 @@ typedef struct {
    * maximum included), for compressed and dense tokens alike.  0 = no cap;
    * otherwise finite and > 0 (1.0 is an ordinary cap, not "off"). */
   float softcap;
+  /* Paged records, as in tq_evict_args (NULL = contiguous): record r of
+   * (l, b, h) is block block_table[b*table_stride + r] of layer l's pool of
+   * rec_cap blocks of n_kv_heads records; max_chunks <= table_stride. */
+  const int32_t* block_table;
+  int32_t table_stride;
+  /* Sparse-V (turboquant_plus commit log, "safer-asym + sparse-V dequant":
+   * value dequantisation skipped where the post-softmax weight is
+   * negligible).  0 = off.  With 0 < eps < 1, the tensor-core kernel for head
+   * dims 64/128 skips the value work of a warp's 32 tokens of a record when,
+   * for every query head of its CTA, each of their logits lies below
+   * (the maximum logit of the warp's earlier records of the same split) +
+   * ln(eps); their weights still count in the softmax denominator, so each
+   * output coordinate moves by at most eps * (skipped tokens) * max|v|.
+   * Which blocks a warp visits follows the plan (records_per_split,
+   * heads_per_cta of tq_decode_attn_plan; warp w holds tokens 32w..32w+31 of
+   * each record).  Dense tokens are never skipped.  Another kernel route for
+   * the compressed tokens (outlier side lists, head dims 256/512,
+   * cuda_core_path != 0) with eps > 0: TQ_ERR_UNSUPPORTED. */
+  float sparse_v_eps;
 } tq_attn_args;
 
 /* Kernels that run split-K decode attention (tq_attn_plan). */

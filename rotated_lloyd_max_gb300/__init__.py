@@ -25,7 +25,7 @@ c_i32, c_i64, c_u64, c_f32, c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint6
 class tq_codec(ctypes.Structure):
     _fields_ = [("head_dim", c_i32), ("bits", c_i32), ("sign_seed", c_u64), ("outlier_T", c_f32),
                 ("outlier_cap", c_i32), ("centroids", c_f32 * 16), ("boundaries", c_f32 * 15),
-                ("sign_bits", ctypes.c_uint32 * 16)]
+                ("sign_bits", ctypes.c_uint32 * 16), ("scale_mode", c_i32)]
 
 
 class tq_evict_args(ctypes.Structure):
@@ -34,7 +34,8 @@ class tq_evict_args(ctypes.Structure):
                 ("v_rec_layer_stride", c_i64), ("rec_cap", c_i32),
                 ("k_tail", c_p), ("v_tail", c_p), ("tail_layer_stride", c_i64), ("tail_cap", c_i32),
                 ("n_chunks", c_p), ("tail_start", c_p), ("tail_len", c_p),
-                ("window", c_i32), ("margin", c_i32), ("t_q", c_i32), ("max_evict", c_i32)]
+                ("window", c_i32), ("margin", c_i32), ("t_q", c_i32), ("max_evict", c_i32),
+                ("block_table", c_p), ("table_stride", c_i32)]
 
 
 class tq_attn_args(ctypes.Structure):
@@ -47,7 +48,7 @@ class tq_attn_args(ctypes.Structure):
                 ("k_tail", c_p), ("v_tail", c_p), ("tail_layer_stride", c_i64), ("tail_cap", c_i32),
                 ("n_chunks", c_p), ("tail_start", c_p), ("tail_len", c_p),
                 ("max_chunks", c_i32), ("max_tail", c_i32), ("splits", c_i32), ("cuda_core_path", c_i32),
-                ("softcap", c_f32)]
+                ("softcap", c_f32), ("block_table", c_p), ("table_stride", c_i32), ("sparse_v_eps", c_f32)]
 
 
 class tq_attn_plan(ctypes.Structure):
@@ -67,12 +68,15 @@ _SIGS = {
                                         ctypes.c_size_t, ctypes.POINTER(tq_codec),
                                         ctypes.POINTER(ctypes.c_double), c_p]),
     "tq_record_bytes": (ctypes.c_size_t, [ctypes.POINTER(tq_codec)]),
+    "tq_codec_set_centroids": (ctypes.c_int, [ctypes.POINTER(tq_codec), ctypes.POINTER(c_f32), ctypes.c_int]),
     "tq_encode": (ctypes.c_int, [ctypes.POINTER(tq_codec), c_p, c_i64, c_i64, c_i64, c_i64, c_p, c_i64,
                                  c_i64, c_p]),
     "tq_decode": (ctypes.c_int, [ctypes.POINTER(tq_codec), c_p, c_i64, c_i64, c_i64, c_i64, c_p, c_i64,
                                  c_i64, c_p]),
     "tq_evict": (ctypes.c_int, [ctypes.POINTER(tq_codec), ctypes.POINTER(tq_codec),
                                 ctypes.POINTER(tq_evict_args), c_p]),
+    "tq_rollback": (ctypes.c_int, [ctypes.POINTER(tq_codec), ctypes.POINTER(tq_codec),
+                                   ctypes.POINTER(tq_evict_args), c_p, c_p]),
     "tq_decode_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(tq_attn_args),
                                                         ctypes.POINTER(tq_codec),
                                                         ctypes.POINTER(tq_codec)]),
@@ -179,6 +183,25 @@ def tq_make_codebook(bits: int, head_dim: int, sign_seed: int = 1, outlier_T: fl
     return Codec(out, mse.value)
 
 
+SCALE_MODES = {"norm": 0, "matched_norm": 1, "inner_product": 2, "least_squares": 3}
+
+
+def tq_codec_set_centroids(codec: Codec, centroids) -> Codec:
+    """A copy of `codec` using the caller's ascending f32 table (2^bits values)."""
+    vals = [float(v) for v in centroids]
+    out = Codec(tq_codec.from_buffer_copy(codec.c), codec.mse)
+    arr = (c_f32 * len(vals))(*vals)
+    _check("tq_codec_set_centroids", load().tq_codec_set_centroids(ctypes.byref(out.c), arr, len(vals)))
+    return out
+
+
+def with_scale(codec: Codec, mode: str) -> Codec:
+    """A copy of `codec` storing the per-vector scale `mode` (see SCALE_MODES)."""
+    out = Codec(tq_codec.from_buffer_copy(codec.c), codec.mse)
+    out.c.scale_mode = SCALE_MODES[mode]
+    return out
+
+
 def tq_record_bytes(codec: Codec) -> int:
     n = load().tq_record_bytes(ctypes.byref(codec.c))
     if n == 0:
@@ -218,34 +241,63 @@ def tq_decode(codec: Codec, src, dst, first_vec: int = 0, stream=None):
                                          vs, gs, _stream(stream)))
 
 
-def tq_evict(k_codec: Codec, v_codec: Codec | None, *, k_rec, v_rec, k_tail, v_tail, n_chunks,
-             tail_start, tail_len, window: int, margin: int, t_q: int = 1, max_evict: int = 1,
-             stream=None):
-    """Chunked eviction.  k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, record_bytes] (v_rec may be
-    k_rec for shared keys/values); k_tail/v_tail: bf16 [L, B, Hkv, tail_cap, d];
-    counters: int32 [L, B] (updated on the device)."""
-    L, B, Hkv, rec_cap = k_rec.shape[:4]
+def make_evict_args(*, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len, window: int, margin: int,
+                    t_q: int = 1, max_evict: int = 1, block_table=None) -> tq_evict_args:
+    """tq_evict_args from tensors.  k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, record_bytes]
+    (v_rec may be k_rec for shared keys/values) or, with block_table (int32
+    [B, table_stride]), per-layer pools uint8 [L, n_blocks, Hkv, record_bytes];
+    k_tail/v_tail: bf16 [L, B, Hkv, tail_cap, d]; counters: int32 [L, B]."""
+    if block_table is None:
+        L, B, Hkv, rec_cap = k_rec.shape[:4]
+        table, stride = None, 0
+    else:
+        L, rec_cap, Hkv = k_rec.shape[:3]
+        B, stride = block_table.shape
+        table = block_table.data_ptr()
     a = tq_evict_args(L, B, Hkv, k_rec.data_ptr(), v_rec.data_ptr(), k_rec.stride(0), v_rec.stride(0),
                       rec_cap, k_tail.data_ptr(), v_tail.data_ptr(), k_tail.stride(0), k_tail.shape[3],
                       n_chunks.data_ptr(), tail_start.data_ptr(), tail_len.data_ptr(), window, margin,
-                      t_q, max_evict)
+                      t_q, max_evict, table, stride)
+    a._tensors = (k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len, block_table)
+    return a
+
+
+def tq_evict(k_codec: Codec, v_codec: Codec | None, *, stream=None, **kw):
+    """Chunked eviction (arguments as make_evict_args; counters updated on the device)."""
+    a = make_evict_args(**kw)
     vc = ctypes.byref(v_codec.c) if v_codec is not None else None
     _check("tq_evict", load().tq_evict(ctypes.byref(k_codec.c), vc, ctypes.byref(a), _stream(stream)))
+
+
+def tq_rollback(k_codec: Codec, v_codec: Codec | None, new_len, *, stream=None, **kw):
+    """Truncate every (layer, batch) stream to new_len (int32 [L, B], device) tokens; the
+    cache as for tq_evict (window/margin/t_q are not used).  Counters and rings are
+    updated on the device."""
+    kw.setdefault("window", 0)
+    kw.setdefault("margin", 0)
+    a = make_evict_args(**kw)
+    vc = ctypes.byref(v_codec.c) if v_codec is not None else None
+    _check("tq_rollback", load().tq_rollback(ctypes.byref(k_codec.c), vc, ctypes.byref(a), _ptr(new_len),
+                                             _stream(stream)))
 
 
 def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None, v_tail=None,
                    n_chunks=None, tail_start=None, tail_len=None, max_chunks: int = 0,
                    max_tail: int = 0, splits: int = 0, n_kv_heads: int | None = None,
-                   cuda_core_path: bool | int = False, softcap: float = 0.0) -> tq_attn_args:
+                   cuda_core_path: bool | int = False, softcap: float = 0.0, block_table=None,
+                   sparse_v_eps: float = 0.0) -> tq_attn_args:
     """Build tq_attn_args from tensors.
     q: bf16 [L, B, Hq, d] (head and dim axes packed); out: f32 [L, B, Hq, d] contiguous;
-    k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, bytes]; k_tail/v_tail: bf16 [L, B, Hkv, cap, d];
+    k_rec/v_rec: uint8 [L, B, Hkv, rec_cap, bytes], or with block_table (int32 [B, table_stride])
+    per-layer pools uint8 [L, n_blocks, Hkv, bytes]; k_tail/v_tail: bf16 [L, B, Hkv, cap, d];
     counters int32 [L, B]; softcap > 0 caps each logit to softcap * tanh(logit / softcap)."""
     L, B, Hq, d = q.shape
     assert q.stride(3) == 1 and q.stride(2) == d, "query heads and dims must be packed"
     assert out.is_contiguous() and tuple(out.shape) == (L, B, Hq, d)
     src = k_rec if k_rec is not None else k_tail
-    Hkv = n_kv_heads if n_kv_heads is not None else src.shape[2]
+    paged = block_table is not None
+    Hkv = n_kv_heads if n_kv_heads is not None else (src.shape[2] if not (paged and k_rec is not None)
+                                                     else k_rec.shape[2])
     a = tq_attn_args()
     a.n_layers, a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim, a.scale = L, B, Hq, Hkv, d, scale
     a.q, a.q_layer_stride, a.q_batch_stride = q.data_ptr(), q.stride(0), q.stride(1)
@@ -253,7 +305,9 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     if k_rec is not None:
         a.k_rec, a.v_rec = k_rec.data_ptr(), v_rec.data_ptr()
         a.k_rec_layer_stride, a.v_rec_layer_stride = k_rec.stride(0), v_rec.stride(0)
-        a.rec_cap = k_rec.shape[3]
+        a.rec_cap = k_rec.shape[1] if paged else k_rec.shape[3]
+    if paged:
+        a.block_table, a.table_stride = block_table.data_ptr(), block_table.shape[1]
     if k_tail is not None:
         a.k_tail, a.v_tail = k_tail.data_ptr(), v_tail.data_ptr()
         a.tail_layer_stride, a.tail_cap = k_tail.stride(0), k_tail.shape[3]
@@ -263,8 +317,9 @@ def make_attn_args(*, q, out, scale: float, k_rec=None, v_rec=None, k_tail=None,
     a.max_chunks, a.max_tail, a.splits = max_chunks, max_tail, splits
     a.cuda_core_path = int(cuda_core_path)  # 0 automatic, 1 CUDA cores, 2 no tcgen05
     a.softcap = softcap
+    a.sparse_v_eps = sparse_v_eps
     # the struct holds raw device pointers: keep the tensors alive with it
-    a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len)
+    a._tensors = (q, out, k_rec, v_rec, k_tail, v_tail, n_chunks, tail_start, tail_len, block_table)
     return a
 
 

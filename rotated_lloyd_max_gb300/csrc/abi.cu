@@ -31,6 +31,23 @@ int record_layout(int d, int bits, bool outl, int cap, int* off_norm, int* off_c
   return outl ? *off_ent + 4 * cap : *off_count;
 }
 
+// What the kernels need of any table: centroids below 0.999 in magnitude (the
+// tensor-core attention holds centroid x 2^16 as f16 hi/lo halves) and, at
+// b >= 3, consecutive boundaries at least one decision cell (1/128) apart with
+// every boundary inside (-1, 1) (the encoders' cell table holds one boundary
+// per cell of width 1/128 over |y| <= 1).
+tq_status table_supported(const float* cent, const float* bnd, int b) {
+  const int K = 1 << b;
+  for (int k = 0; k < K; ++k)
+    if (!(std::fabs(cent[k]) < 0.999f)) return TQ_ERR_UNSUPPORTED;
+  if (b >= 3)
+    for (int k = 0; k + 1 < K; ++k) {
+      if (!(std::fabs(bnd[k]) < 1.0f)) return TQ_ERR_UNSUPPORTED;
+      if (k + 2 < K && (double)bnd[k + 1] - (double)bnd[k] < 1.0 / 128.0) return TQ_ERR_UNSUPPORTED;
+    }
+  return TQ_OK;
+}
+
 tq_status resolve_codec(const tq_codec* c, CodecDev* o) {
   if (!c) return TQ_ERR_INVALID_ARG;
   const int d = c->head_dim, b = c->bits;
@@ -45,11 +62,15 @@ tq_status resolve_codec(const tq_codec* c, CodecDev* o) {
       return TQ_ERR_INVALID_ARG;  // not ascending / boundaries not between centroids
     if (c->boundaries[k] != -c->boundaries[K - 2 - k]) return TQ_ERR_UNSUPPORTED;  // asymmetric table
   }
+  const tq_status tab = table_supported(c->centroids, c->boundaries, b);
+  if (tab != TQ_OK) return tab;
+  if (c->scale_mode < TQ_SCALE_NORM || c->scale_mode > TQ_SCALE_LEAST_SQUARES) return TQ_ERR_INVALID_ARG;
   std::memset(o, 0, sizeof(*o));
   o->d = d;
   o->bits = b;
   o->has_outl = outl ? 1 : 0;
   o->cap = outl ? c->outlier_cap : 0;
+  o->scale_mode = c->scale_mode;
   o->rec_bytes = record_layout(d, b, outl, o->cap, &o->off_norm, &o->off_count, &o->off_entries);
   o->thr_out = outl ? (float)((double)c->outlier_T / std::sqrt((double)d)) : INFINITY;
   o->inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
@@ -121,10 +142,13 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
     pl->shared = a->v_rec == a->k_rec;
     if (pl->shared && std::memcmp(kcod, vcod, sizeof(tq_codec)) != 0) return TQ_ERR_INVALID_ARG;
     if (!aligned(a->k_rec, 16) || !aligned(a->v_rec, 16) || a->k_rec_layer_stride % 16 ||
-        a->v_rec_layer_stride % 16 || a->rec_cap <= 0 || a->max_chunks > a->rec_cap || !a->n_chunks)
+        a->v_rec_layer_stride % 16 || a->rec_cap <= 0 || !a->n_chunks)
       return TQ_ERR_INVALID_ARG;
+    // the records a stream may hold: rec_cap, or the block table's row length
+    if (a->block_table && (!aligned(a->block_table, 4) || a->table_stride <= 0)) return TQ_ERR_INVALID_ARG;
+    if (a->max_chunks > (a->block_table ? a->table_stride : a->rec_cap)) return TQ_ERR_INVALID_ARG;
   } else {
-    if (a->v_rec || a->n_chunks) return TQ_ERR_INVALID_ARG;
+    if (a->v_rec || a->n_chunks || a->block_table) return TQ_ERR_INVALID_ARG;
     if (vcod) {  // the merge uses the value codec's signs only for compressed splits
       tq_status st = resolve_codec(vcod, &pl->vc);
       if (st != TQ_OK) return st;
@@ -150,6 +174,9 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   // splits' 8-head CTAs need) or multiples of 64: one CTA keeps 64 heads
   pl->umma512 = pl->mma512 && a->cuda_core_path == 0 && pl->G % 8 == 0 && pl->G >= 16 &&
                 (pl->G <= 64 || pl->G % 64 == 0) && tq::attn_umma512_smem() <= max_dyn_smem();
+  // sparse-V runs on the tensor-core kernel of head dims 64/128 only
+  if (!(a->sparse_v_eps >= 0.f && a->sparse_v_eps < 1.f)) return TQ_ERR_INVALID_ARG;
+  if (a->sparse_v_eps > 0.f && pl->has_rec && !pl->mma) return TQ_ERR_UNSUPPORTED;
   if (pl->umma512) {
     pl->mma512 = false;
     pl->GT = std::min(pl->G, 64);
@@ -394,6 +421,30 @@ tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float out
   return TQ_OK;
 }
 
+tq_status tq_codec_set_centroids(tq_codec* codec, const float* centroids, int n_centroids) {
+  if (!codec || !centroids) return TQ_ERR_INVALID_ARG;
+  const int b = codec->bits;
+  if (b < 1 || b > 4) return TQ_ERR_UNSUPPORTED;
+  const int K = 1 << b;
+  if (n_centroids != K) return TQ_ERR_INVALID_ARG;
+  float c[16], t[15];
+  for (int k = 0; k < K; ++k) {
+    if (!std::isfinite(centroids[k])) return TQ_ERR_INVALID_ARG;
+    if (k && !(centroids[k - 1] < centroids[k])) return TQ_ERR_INVALID_ARG;
+    c[k] = centroids[k];
+  }
+  for (int k = 0; k < K; ++k)
+    if (c[k] != -c[K - 1 - k]) return TQ_ERR_UNSUPPORTED;
+  for (int k = 0; k + 1 < K; ++k) t[k] = (float)(0.5 * ((double)c[k] + (double)c[k + 1]));
+  for (int k = 0; k + 1 < K; ++k)  // the midpoint must fall strictly between its centroids
+    if (!(c[k] < t[k] && t[k] < c[k + 1])) return TQ_ERR_UNSUPPORTED;
+  const tq_status st = table_supported(c, t, b);
+  if (st != TQ_OK) return st;
+  for (int k = 0; k < 16; ++k) codec->centroids[k] = k < K ? c[k] : 0.f;
+  for (int k = 0; k < 15; ++k) codec->boundaries[k] = k + 1 < K ? t[k] : 0.f;
+  return TQ_OK;
+}
+
 size_t tq_record_bytes(const tq_codec* codec) {
   CodecDev c;
   if (resolve_codec(codec, &c) != TQ_OK) return 0;
@@ -423,6 +474,9 @@ tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, in
   p.first_vec = first_vec;
   p.first_chunk = first_vec / TQ_CHUNK;
   p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
+  // task indices: at most 8 per record (16-vector tiles), plus a grid's lookahead
+  p.small_tasks = p.chunks_per_group < (1ll << 31) && n_groups * p.chunks_per_group * 8 + (1ll << 24) < (1ll << 32);
+  p.cpg = make_fast_div(p.small_tasks ? (uint32_t)p.chunks_per_group : 1u);
   // the launcher caps the grid at the number of tasks of the kernel it picks
   return launch_encode(p, 8 * num_sms(), (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
@@ -479,6 +533,7 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
     return TQ_ERR_INVALID_ARG;
   if (a->rec_cap <= 0 || a->tail_cap <= 0 || a->window < 0 || a->margin < 0 || a->t_q < 1)
     return TQ_ERR_INVALID_ARG;
+  if (a->block_table && (!aligned(a->block_table, 4) || a->table_stride <= 0)) return TQ_ERR_INVALID_ARG;
   // the retention floor; a ring that cannot hold floor + one chunk never evicts
   const int64_t floor64 = (int64_t)a->window + std::max<int64_t>((int64_t)a->t_q - 1, a->margin);
   if ((int64_t)a->tail_cap < floor64 + TQ_CHUNK) return TQ_ERR_INVALID_ARG;
@@ -486,6 +541,9 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
   const int floor_ = (int)floor64;
   EvictParams p;
   p.rec_cap = a->rec_cap;
+  p.table = a->block_table;
+  p.table_stride = a->block_table ? a->table_stride : 0;
+  p.rec_limit = a->block_table ? a->table_stride : a->rec_cap;
   p.tail_ls = a->tail_layer_stride;
   p.tail_cap = a->tail_cap;
   p.n_chunks = a->n_chunks;
@@ -516,8 +574,66 @@ tq_status tq_evict(const tq_codec* k_codec, const tq_codec* v_codec, const tq_ev
   cp.floor_ = floor_;
   cp.max_evict = a->max_evict;
   cp.tail_cap = a->tail_cap;
-  cp.rec_cap = a->rec_cap;
+  cp.rec_limit = p.rec_limit;
   return launch_evict_commit(cp, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_rollback(const tq_codec* k_codec, const tq_codec* v_codec, const tq_evict_args* a,
+                      const int32_t* new_len, void* stream) {
+  if (!a || !new_len || !aligned(new_len, 4)) return TQ_ERR_INVALID_ARG;
+  CodecDev kc, vc;
+  tq_status st = resolve_codec(k_codec, &kc);
+  if (st != TQ_OK) return st;
+  const bool shared = a->v_rec == a->k_rec;
+  if (shared) {
+    if (v_codec && std::memcmp(k_codec, v_codec, sizeof(tq_codec)) != 0) return TQ_ERR_INVALID_ARG;
+    if (a->v_tail != a->k_tail) return TQ_ERR_INVALID_ARG;  // shared records come from one ring
+    vc = kc;
+  } else {
+    st = resolve_codec(v_codec, &vc);
+    if (st != TQ_OK) return st;
+  }
+  if (vc.d != kc.d) return TQ_ERR_INVALID_ARG;
+  if (a->n_layers <= 0 || a->n_layers > 65535 || a->batch <= 0 || a->n_kv_heads <= 0 ||
+      (int64_t)a->batch * a->n_kv_heads > 2147483647ll)
+    return TQ_ERR_INVALID_ARG;
+  if (!a->k_rec || !a->v_rec || !a->k_tail || !a->v_tail || !a->n_chunks || !a->tail_start || !a->tail_len)
+    return TQ_ERR_INVALID_ARG;
+  if (!aligned(a->k_rec, 16) || !aligned(a->v_rec, 16) || !aligned(a->k_tail, 16) || !aligned(a->v_tail, 16) ||
+      a->k_rec_layer_stride % 16 || a->v_rec_layer_stride % 16 || a->tail_layer_stride % 8)
+    return TQ_ERR_INVALID_ARG;
+  // the decoded tokens of one record (at most 127) must fit the ring
+  if (a->rec_cap <= 0 || a->tail_cap < TQ_CHUNK) return TQ_ERR_INVALID_ARG;
+  if (a->block_table && (!aligned(a->block_table, 4) || a->table_stride <= 0)) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  RollbackParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.rec_cap = a->rec_cap;
+  p.table = a->block_table;
+  p.table_stride = a->block_table ? a->table_stride : 0;
+  p.rec_limit = a->block_table ? a->table_stride : a->rec_cap;
+  p.tail_ls = a->tail_layer_stride;
+  p.tail_cap = a->tail_cap;
+  p.n_chunks = a->n_chunks;
+  p.tail_start = a->tail_start;
+  p.tail_len = a->tail_len;
+  p.new_len = new_len;
+  p.L = a->n_layers;
+  p.B = a->batch;
+  p.Hkv = a->n_kv_heads;
+  p.c = kc;
+  p.rec = (const uint8_t*)a->k_rec;
+  p.rec_ls = a->k_rec_layer_stride;
+  p.tail = (uint16_t*)a->k_tail;
+  if (launch_rollback(p, s) != cudaSuccess) return TQ_ERR_CUDA;
+  if (!shared) {
+    p.c = vc;
+    p.rec = (const uint8_t*)a->v_rec;
+    p.rec_ls = a->v_rec_layer_stride;
+    p.tail = (uint16_t*)a->v_tail;
+    if (launch_rollback(p, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  return launch_rollback_commit(p, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 size_t tq_decode_attn_workspace_size(const tq_attn_args* args, const tq_codec* k_codec,
@@ -581,6 +697,7 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   p.n_hg = pl.n_hg;
   p.sscale = (float)((double)a->scale * 1.4426950408889634074);
   p.scap = a->softcap > 0.f ? (float)((double)a->softcap * 1.4426950408889634074) : 0.f;
+  p.sv_log2eps = a->sparse_v_eps > 0.f ? (float)std::log2((double)a->sparse_v_eps) : 0.f;
   p.iscap = a->softcap > 0.f ? (float)(1.0 / ((double)a->softcap * 1.4426950408889634074)) : 0.f;
   p.q = (const uint16_t*)a->q;
   p.q_ls = a->q_layer_stride;
@@ -591,6 +708,9 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     p.krec_ls = a->k_rec_layer_stride;
     p.vrec_ls = a->v_rec_layer_stride;
     p.rec_cap = a->rec_cap;
+    p.table = a->block_table;
+    p.table_stride = a->block_table ? a->table_stride : 0;
+    p.rec_limit = a->block_table ? a->table_stride : a->rec_cap;
     p.krec_bytes = pl.kc.rec_bytes;
     p.vrec_bytes = pl.vc.rec_bytes;
     p.kb = pl.kc.bits;

@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   // device counters are clamped to the buffers they index, so a corrupt
   // counter can never move a copy outside the caller's arrays
   if (comp) {
-    const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
+    const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_limit);
     t_begin = split * p.cps;
     t_end = min(t_begin + p.cps, nch);
   } else {
@@ -382,9 +382,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 
   const int n_tiles_c = t_end - t_begin;
   // ---- compressed splits: record staging (3-deep cp.async ring)
-  const uint8_t* kb0 = !comp ? nullptr : p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = (!comp || p.shared_kv) ? kb0
-                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  // record c of this unit (contiguous, or through the block table)
+  const uint8_t* kl0 = p.krec + l * p.krec_ls;
+  const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
+  auto krec_at = [&](int64_t c) {
+    return kl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.krec_bytes);
+  };
+  auto vrec_at = [&](int64_t c) {
+    return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
+  };
   const bool anyout = p.kout || p.vout;
   const int vcap = p.shared_kv ? p.kcap : p.vcap;
   auto stage = [&](int i) { return mainb + (i % 3) * p.sm_stage; };
@@ -392,8 +398,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   auto issue_main = [&](int i) {
     if (i < n_tiles_c) {
       const int64_t c = t_begin + i;
-      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
-      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+      cta_copy_async(stage(i), krec_at(c), p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vrec_at(c), p.v_main);
     }
     cp_async_commit();
   };
@@ -435,11 +441,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       uint32_t* eb = entb(i);
       if (p.kout) {
         const int E = min(pre[((i & 1) * 2) * 129 + 128], p.kcap);
-        cta_copy_async(eb, kb0 + c * p.krec_bytes + p.k_off_ent, (E * 4 + 15) & ~15);
+        cta_copy_async(eb, krec_at(c) + p.k_off_ent, (E * 4 + 15) & ~15);
       }
       if (p.vout && !p.shared_kv) {
         const int E = min(pre[((i & 1) * 2 + 1) * 129 + 128], p.vcap);
-        cta_copy_async(eb + p.kcap * p.kout, vb0 + c * p.vrec_bytes + p.v_off_ent, (E * 4 + 15) & ~15);
+        cta_copy_async(eb + p.kcap * p.kout, vrec_at(c) + p.v_off_ent, (E * 4 + 15) & ~15);
       }
     }
     cp_async_commit();

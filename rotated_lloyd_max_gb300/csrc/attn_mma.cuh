@@ -283,6 +283,10 @@ __device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char*
   }
   const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // sparse-V: exact running maxima of the lane's two heads over the warp's
+  // earlier 32-token blocks of this split (the lazy m0/m1 may trail them)
+  float tm0 = -INFINITY, tm1 = -INFINITY;
+  const bool sparse_v = p.sv_log2eps < 0.f;
   float acc[KS][4];
 #pragma unroll
   for (int mc = 0; mc < KS; ++mc)
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
                        split);
     return;
   }
-  const int nch = min(p.n_chunks[lb], p.rec_cap);
+  const int nch = min(p.n_chunks[lb], p.rec_limit);
   const int c_begin = split * p.cps;
   const int c_end = min(c_begin + p.cps, nch);
   if (c_begin >= c_end) {
@@ -437,15 +441,21 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
     return;
   }
   const int n = c_end - c_begin;
-  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = p.shared_kv ? kb0
-                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  // record c of this unit (contiguous, or through the block table)
+  const uint8_t* kl0 = p.krec + l * p.krec_ls;
+  const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
+  auto krec_at = [&](int64_t c) {
+    return kl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.krec_bytes);
+  };
+  auto vrec_at = [&](int64_t c) {
+    return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
+  };
   auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
   auto issue_main = [&](int i) {
     if (i < n) {
       const int64_t c = c_begin + i;
-      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
-      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+      cta_copy_async(stage(i), krec_at(c), p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vrec_at(c), p.v_main);
     }
     cp_async_commit();
   };
@@ -537,6 +547,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   auto vpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + VP_OFF + o); };
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // sparse-V: exact running maxima of the lane's two heads over the warp's
+  // earlier 32-token blocks of this split (the lazy m0/m1 may trail them)
+  float tm0 = -INFINITY, tm1 = -INFINITY;
+  const bool sparse_v = p.sv_log2eps < 0.f;
   float acc[KS][4];
 #pragma unroll
   for (int mc = 0; mc < KS; ++mc)
@@ -614,6 +628,25 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[mt][e] = soft_cap(sc[mt][e], p.scap, p.iscap);
     }
+    // ---- sparse-V (turboquant_plus commit log, "sparse-V dequant"): the
+    // values of the warp's 32 tokens of this record are skipped when, for
+    // every head of the CTA, each of their logits lies below the exact
+    // maximum of the warp's earlier blocks plus log2(eps); their weights
+    // still enter the denominators
+    bool skip_v = false;
+    if (sparse_v) {
+      float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+      float x1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, m));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, m));
+      }
+      const bool low = (!hv0 || x0 < tm0 + p.sv_log2eps) && (!hv1 || x1 < tm1 + p.sv_log2eps);
+      skip_v = __all_sync(0xffffffffu, low);
+      tm0 = fmaxf(tm0, x0);
+      tm1 = fmaxf(tm1, x1);
+    }
     // ---- online softmax (the max moves only when a logit passes it by 2^8)
     {
       bool need = false;
@@ -673,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
       }
     }
     const float psc = pow2i(kx);
+    if (skip_v) continue;
     // ---- values: k-step mt = the 16 tokens of score tile mt
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {

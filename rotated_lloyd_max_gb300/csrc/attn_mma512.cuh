@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
-  const int nch = min(p.n_chunks[lb], p.rec_cap);
+  const int nch = min(p.n_chunks[lb], p.rec_limit);
   const int c_begin = split * p.cps;
   const int c_end = min(c_begin + p.cps, nch);
   if (c_begin >= c_end) {
@@ -73,15 +73,21 @@ __global__ void __launch_bounds__(kT512, 1) attn_mma512_kernel(const __grid_cons
     return;
   }
   const int n = c_end - c_begin;
-  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = p.shared_kv ? kb0
-                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  // record c of this unit (contiguous, or through the block table)
+  const uint8_t* kl0 = p.krec + l * p.krec_ls;
+  const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
+  auto krec_at = [&](int64_t c) {
+    return kl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.krec_bytes);
+  };
+  auto vrec_at = [&](int64_t c) {
+    return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
+  };
   auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
   auto issue_main = [&](int i) {
     if (i < n) {
       const int64_t c = c_begin + i;
-      cta256_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
-      if (!p.shared_kv) cta256_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+      cta256_copy_async(stage(i), krec_at(c), p.k_main);
+      if (!p.shared_kv) cta256_copy_async(stage(i) + p.k_main, vrec_at(c), p.v_main);
     }
     cp_async_commit();
   };

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     t_begin = (split - p.Sc) * p.tps;
     t_end = min(t_begin + p.tps, len);
   } else {
-    const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_cap);
+    const int nch = min(p.n_chunks ? p.n_chunks[lb] : 0, p.rec_limit);
     t_begin = split * p.cps;
     t_end = min(t_begin + p.cps, nch);
   }
@@ -179,17 +179,23 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     return;
   }
   const int n = t_end - t_begin;
-  const uint8_t* kb0 = dense ? nullptr : p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = (dense || p.shared_kv) ? kb0
-                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  // record c of this unit (contiguous, or through the block table)
+  const uint8_t* kl0 = p.krec + l * p.krec_ls;
+  const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
+  auto krec_at = [&](int64_t c) {
+    return kl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.krec_bytes);
+  };
+  auto vrec_at = [&](int64_t c) {
+    return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
+  };
   const int kcap = p.kcap, vcap = p.shared_kv ? p.kcap : p.vcap;
   const bool kout = p.kout && !dense, vout = p.vout && !dense;
   auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
   auto issue_main = [&](int i) {
     if (i < n) {
       const int64_t c = t_begin + i;
-      cta_copy_async(stage(i), kb0 + c * p.krec_bytes, p.k_main);
-      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vb0 + c * p.vrec_bytes, p.v_main);
+      cta_copy_async(stage(i), krec_at(c), p.k_main);
+      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vrec_at(c), p.v_main);
     }
     cp_async_commit();
   };
@@ -407,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
       // fetched now so that their latency overlaps the scores
       int ke0 = 0, kec = 0, ve0 = 0, vec = 0;
       uint32_t kent[8], vent[8];
-      const uint32_t* kge = reinterpret_cast<const uint32_t*>(kb0 + c * p.krec_bytes + p.k_off_ent);
-      const uint32_t* vge = reinterpret_cast<const uint32_t*>(vb0 + c * p.vrec_bytes + p.v_off_ent);
+      const uint32_t* kge = reinterpret_cast<const uint32_t*>(krec_at(c) + p.k_off_ent);
+      const uint32_t* vge = reinterpret_cast<const uint32_t*>(vrec_at(c) + p.v_off_ent);
       if (kout) {
         token_entries(st + p.k_off_count, kcap, ke0, kec);
   #pragma unroll

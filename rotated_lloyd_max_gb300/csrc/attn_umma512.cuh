@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
-  const int nch = min(p.n_chunks[lb], p.rec_cap);
+  const int nch = min(p.n_chunks[lb], p.rec_limit);
   const int c_begin = split * p.cps;
   const int c_end = min(c_begin + p.cps, nch);
   if (c_begin >= c_end) {
@@ -238,9 +238,15 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
     return;
   }
   const int n = c_end - c_begin;
-  const uint8_t* kb0 = p.krec + l * p.krec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.krec_bytes;
-  const uint8_t* vb0 = p.shared_kv ? kb0
-                                   : p.vrec + l * p.vrec_ls + (int64_t)(b * p.Hkv + kvh) * p.rec_cap * p.vrec_bytes;
+  // record c of this unit (contiguous, or through the block table)
+  const uint8_t* kl0 = p.krec + l * p.krec_ls;
+  const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
+  auto krec_at = [&](int64_t c) {
+    return kl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.krec_bytes);
+  };
+  auto vrec_at = [&](int64_t c) {
+    return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
+  };
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -404,11 +410,11 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
       int kind, rec;
       umma_phase(ph, n, kind, rec);
       if (kind == 0) {
-        const uint8_t* row = kb0 + (int64_t)(c_begin + rec) * p.krec_bytes + tkn * (D * KB / 8);
+        const uint8_t* row = krec_at(c_begin + rec) + tkn * (D * KB / 8);
 #pragma unroll
         for (int i = 0; i < 8; ++i) load_unit<KB>(w[i], row, 4 * i + sub);
       } else {
-        const uint8_t* row = vb0 + (int64_t)(c_begin + rec) * p.vrec_bytes + tkn * (D * VB / 8);
+        const uint8_t* row = vrec_at(c_begin + rec) + tkn * (D * VB / 8);
 #pragma unroll
         for (int i = 0; i < 8; ++i) load_unit<VB>(w[i], row, 4 * i + sub);
       }
@@ -492,8 +498,9 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
     float lacc[2] = {0.f, 0.f};  // softmax denominators of heads lane and 32 + lane over this warp's tokens
     int kx = 127;                // P' scale exponent (only decreases)
-    auto norm_at = [&](const uint8_t* base, int bytes, int off, int rec) {
-      return __ldg(reinterpret_cast<const float*>(base + (int64_t)(c_begin + rec) * bytes + off) + tok);
+    auto norm_at = [&](bool key, int rec) {
+      const uint8_t* r = key ? krec_at(c_begin + rec) + p.k_off_norm : vrec_at(c_begin + rec) + p.v_off_norm;
+      return __ldg(reinterpret_cast<const float*>(r) + tok);
     };
     // logits of heads 32 hh .. 32 hh + 31 of this token (-inf past the group)
     auto logits = [&](uint32_t tSr, int hh, float nk, float (&t)[32]) {
@@ -514,13 +521,13 @@ __global__ void __launch_bounds__(kU512Threads, 1) attn_umma512_kernel(const __g
         for (int i = 0; i < 32; ++i) t[i] = soft_cap(t[i], p.scap, p.iscap);
       }
     };
-    float nk = norm_at(kb0, p.krec_bytes, p.k_off_norm, 0);
-    float nv = norm_at(vb0, p.vrec_bytes, p.v_off_norm, 0);
+    float nk = norm_at(true, 0);
+    float nv = norm_at(false, 0);
     for (int r = 0; r < n; ++r) {
       float nk1 = 0.f, nv1 = 0.f;
       if (r + 1 < n) {
-        nk1 = norm_at(kb0, p.krec_bytes, p.k_off_norm, r + 1);
-        nv1 = norm_at(vb0, p.vrec_bytes, p.v_off_norm, r + 1);
+        nk1 = norm_at(true, r + 1);
+        nv1 = norm_at(false, r + 1);
       }
       mbar_wait(&ms.s_full[r & 1], (r >> 1) & 1, abort_f);
       tc_fence_after();

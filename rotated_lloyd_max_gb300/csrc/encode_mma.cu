@@ -206,9 +206,13 @@ __device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint
 // Codes of the lane's 32 coordinates of one vector (x: unnormalised
 // transform, scale = 128 / (n sqrt(d)) or 0 for a zero vector), packed
 // LSB-first into B words; (OUTL) the outlier mask |y| > T / sqrt(d).
-template <int B, bool OUTL>
+// (SCALE) the lane's parts of ||chat||^2 and <chat, x> over its coordinates,
+// chat_j = cent[code_j] or, at an outlier coordinate, the stored bf16 value.
+template <int B, bool OUTL, bool SCALE = false>
 __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2* cells, float scale,
-                                              float thr_out, uint32_t (&wd)[B], uint32_t& omask) {
+                                              float thr_out, uint32_t (&wd)[B], uint32_t& omask,
+                                              const float* cent = nullptr, float* cc = nullptr,
+                                              float* cx = nullptr) {
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
@@ -242,6 +246,12 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2
       wd[bit >> 5] += code[k] << (bit & 31);
       if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code[k] >> (32 - (bit & 31));
       if (OUTL) omask |= mask_gt(fabsf(x[r + k]), Tox) & (1u << (r + k));
+      if constexpr (SCALE) {
+        float cj = cent[code[k]];
+        if (OUTL && ((omask >> (r + k)) & 1u)) cj = bf16_to_f32(f32_to_bf16_rne(x[r + k] * (scale * (1.f / kCellScale))));
+        *cc = fmaf(cj, cj, *cc);
+        *cx = fmaf(cj, x[r + k], *cx);
+      }
     }
   }
 }
@@ -258,15 +268,32 @@ __device__ __forceinline__ void encm_store_row(uint8_t* row, const uint32_t (&wd
   }
 }
 
+// The stored scales of a lane pair's two vectors from the quad sums of
+// ||chat||^2 and <chat, x> (z = 128 / (n sqrt(d)), so <chat, y> = <chat, x> z / 128).
+__device__ __forceinline__ void encm_scales(int mode, float na, float nb, float za, float zb, float cca, float cxa,
+                                            float ccb, float cxb, float& sa, float& sb) {
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {
+    cca += __shfl_xor_sync(0xffffffffu, cca, m);
+    cxa += __shfl_xor_sync(0xffffffffu, cxa, m);
+    ccb += __shfl_xor_sync(0xffffffffu, ccb, m);
+    cxb += __shfl_xor_sync(0xffffffffu, cxb, m);
+  }
+  sa = vector_scale(mode, na, cca, cxa * (za * (1.f / kCellScale)));
+  sb = vector_scale(mode, nb, ccb, cxb * (zb * (1.f / kCellScale)));
+}
+
 // Encode without outliers: every (group, record, 16-vector tile) is a task of
 // one warp; warps stride over the tasks with the next task's rows in flight
 // (cp.async, two buffers per warp).
-template <int B>
+template <int B, bool SCALE>
 __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_constant__ EncodeParams p) {
   using E = EncM<B>;
   __shared__ float2 cells[kCells];
   __shared__ EncTile tiles[4][2];
+  __shared__ float cent[16];
   build_cells(p.c, cells);
+  if (threadIdx.x < 16) cent[threadIdx.x] = p.c.centroids[threadIdx.x];
   __syncthreads();
   const EncMLane<B> ln(p.c);
   const int64_t per_group = p.chunks_per_group * 8;
@@ -279,8 +306,15 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
   };
   auto locate = [&](int64_t task) {
     Task k;
-    k.grp = task / per_group;
-    const int64_t r = task % per_group;
+    int64_t r;
+    if (p.small_tasks) {  // 32-bit multiply-shift division instead of a 64-bit divide
+      const uint32_t rec = (uint32_t)task >> 3, grp = fast_div(rec, p.cpg);
+      k.grp = grp;
+      r = (int64_t)((uint32_t)task - grp * (uint32_t)per_group);
+    } else {
+      k.grp = task / per_group;
+      r = task % per_group;
+    }
     k.chunk = p.first_chunk + r / 8;
     k.slot_a = (int)(r % 8) * 16 + ln.g;
     k.slot_b = k.slot_a + 8;
@@ -317,49 +351,64 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
     encm_transform<B>(ln, wa, wb, xa, xb);
     uint8_t* rec = p.dst + cur.grp * p.dst_gs + cur.chunk * (int64_t)p.c.rec_bytes;
     uint32_t wd[B], om;
-    encm_quantize<B, false>(xa, cells, na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f, 0.f, wd, om);
+    const float za = na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f;
+    const float zb = nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f;
+    float cca = 0.f, cxa = 0.f, ccb = 0.f, cxb = 0.f;
+    encm_quantize<B, false, SCALE>(xa, cells, za, 0.f, wd, om, cent, &cca, &cxa);
     if (cur.va) encm_store_row<B>(rec + (size_t)cur.slot_a * E::RB + ln.t * 4 * B, wd);
-    encm_quantize<B, false>(xb, cells, nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f, 0.f, wd, om);
+    encm_quantize<B, false, SCALE>(xb, cells, zb, 0.f, wd, om, cent, &ccb, &cxb);
     if (cur.vb) encm_store_row<B>(rec + (size_t)cur.slot_b * E::RB + ln.t * 4 * B, wd);
+    float sca = na, scb = nb;
+    if constexpr (SCALE) encm_scales(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
     if (ln.t == 0) {
       float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
-      if (cur.va) nrm[cur.slot_a] = na;
-      if (cur.vb) nrm[cur.slot_b] = nb;
+      if (cur.va) nrm[cur.slot_a] = sca;
+      if (cur.vb) nrm[cur.slot_b] = scb;
     }
     cur = nxt;
   }
   cp_async_wait<0>();
 }
 
-// Encode with outliers: one CTA per record (grid-stride), two passes of 64
-// slots (warp w: tile w of the pass); entries land in (slot, index) order via
-// a quad prefix (a vector's lanes) and a CTA prefix over the pass's slots.
-template <int B>
+// Encode with outliers: a warp owns a whole record and encodes its 8 tiles of
+// 16 slots in slot order (the next tile, of this record or the warp's next
+// one, in flight through cp.async as in the kernel above).  Entries land in
+// (slot, index) order without any CTA barrier: a vector's lanes take their
+// places by a quad prefix, a tile's 16 vectors by a warp prefix, and a running
+// warp-uniform offset carries the record's entry count from tile to tile.
+template <int B, bool SCALE>
 __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __grid_constant__ EncodeParams p) {
   using E = EncM<B>;
-  __shared__ int cnt_s[64];
-  __shared__ int off_s[64];
-  __shared__ int run_s;
   __shared__ float2 cells[kCells];
   __shared__ EncTile tiles[4][2];
+  __shared__ float cent[16];
   build_cells(p.c, cells);
+  if (threadIdx.x < 16) cent[threadIdx.x] = p.c.centroids[threadIdx.x];
+  __syncthreads();
   const EncMLane<B> ln(p.c);
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   const int64_t v_end = p.first_vec + p.n_vec;
-  // units u = (record task, pass): task blockIdx.x + (u / 2) gridDim.x, pass u % 2;
-  // warp w encodes slots 64 pass + 16 w + g (+ 8) of the record
+  const int64_t warps = (int64_t)gridDim.x * 4;
+  // unit u of this warp: record task warp_id + (u / 8) * warps, tile u % 8
   struct Unit {
     int64_t task, grp, chunk, ta, tb;
-    int pass, slot_a, slot_b;
+    int tile, slot_a, slot_b;
     bool va, vb;
   };
-  auto locate = [&](int u) {
+  const int64_t wid = (int64_t)blockIdx.x * 4 + ln.warp;
+  auto locate = [&](int64_t u) {
     Unit k;
-    k.task = blockIdx.x + (int64_t)(u >> 1) * gridDim.x;
-    k.pass = u & 1;
-    k.grp = k.task / p.chunks_per_group;
-    k.chunk = p.first_chunk + k.task % p.chunks_per_group;
-    k.slot_a = 64 * k.pass + 16 * ln.warp + ln.g;
+    k.task = wid + (u >> 3) * warps;
+    k.tile = (int)(u & 7);
+    if (p.small_tasks) {  // 32-bit multiply-shift division instead of a 64-bit divide
+      const uint32_t grp = fast_div((uint32_t)k.task, p.cpg);
+      k.grp = grp;
+      k.chunk = p.first_chunk + ((uint32_t)k.task - grp * (uint32_t)p.chunks_per_group);
+    } else {
+      k.grp = k.task / p.chunks_per_group;
+      k.chunk = p.first_chunk + k.task % p.chunks_per_group;
+    }
+    k.slot_a = 16 * k.tile + ln.g;
     k.slot_b = k.slot_a + 8;
     k.ta = k.chunk * kChunk + k.slot_a;
     k.tb = k.chunk * kChunk + k.slot_b;
@@ -375,104 +424,94 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
   };
   Unit cur = locate(0);
   issue(cur, 0);
-  for (int u = 0; cur.task < n_tasks; ++u) {
+  int run = 0;  // entries of the current record written so far (warp-uniform)
+  for (int64_t u = 0; cur.task < n_tasks; ++u) {
     const Unit nxt = locate(u + 1);
-    issue(nxt, (u + 1) & 1);
-    if (cur.pass == 0 && threadIdx.x == 0) run_s = 0;
-    cp_async_wait<1>();
-    __syncthreads();  // run_s reset visible; the previous unit's off_s reads are done
+    issue(nxt, (int)((u + 1) & 1));
+    if (cur.tile == 0) run = 0;
+    cp_async_wait<1>();  // this lane's copies of the current tile are in
+    EncTile& tl = tiles[ln.warp][u & 1];
     uint8_t* rec = p.dst + cur.grp * p.dst_gs + cur.chunk * (int64_t)p.c.rec_bytes;
-    {
-      const int pa = 16 * ln.warp + ln.g, pb = pa + 8;  // slots within the pass
-      const int slot_a = cur.slot_a, slot_b = cur.slot_b;
-      const bool va = cur.va, vb = cur.vb;
-      uint32_t wa[16], wb[16];
-      encm_read(tiles[ln.warp][u & 1], ln.g, ln.g, ln.t, va, ln.smask, wa);
-      encm_read(tiles[ln.warp][u & 1], ln.g + 8, ln.g, ln.t, vb, ln.smask, wb);
-      float sa = encm_sq(wa), sb = encm_sq(wb);
-      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
-      const float na = sqrtf(sa), nb = sqrtf(sb);
-      float xa[32], xb[32];
-      encm_transform<B>(ln, wa, wb, xa, xb);
-      uint32_t wd[B], oma, omb;
-      encm_quantize<B, true>(xa, cells, na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f, p.c.thr_out, wd, oma);
-      if (va) encm_store_row<B>(rec + (size_t)slot_a * E::RB + ln.t * 4 * B, wd);
-      encm_quantize<B, true>(xb, cells, nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f, p.c.thr_out, wd, omb);
-      if (vb) encm_store_row<B>(rec + (size_t)slot_b * E::RB + ln.t * 4 * B, wd);
-      if (!va) oma = 0u;
-      if (!vb) omb = 0u;
-      // the lane's y values as bf16 (the stored outlier value), kept in its own
-      // chunks of the tile buffer it has just read, for the entry writes below
-      const float inva = na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f;
-      const float invb = nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f;
-      EncTile& tl = tiles[ln.warp][u & 1];
-      if (oma) encm_stash(tl, ln.g, ln.g, ln.t, xa, inva);
-      if (omb) encm_stash(tl, ln.g + 8, ln.g, ln.t, xb, invb);
-      if (ln.t == 0) {
-        float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
-        if (va) nrm[slot_a] = na;
-        if (vb) nrm[slot_b] = nb;
-      }
-      // entries before this lane within its vector (quad prefix over t)
-      const int ca = __popc(oma), cb = __popc(omb);
-      int ia = ca, ib = cb;
+    const bool va = cur.va, vb = cur.vb;
+    uint32_t wa[16], wb[16];
+    encm_read(tl, ln.g, ln.g, ln.t, va, ln.smask, wa);
+    encm_read(tl, ln.g + 8, ln.g, ln.t, vb, ln.smask, wb);
+    float sa = encm_sq(wa), sb = encm_sq(wb);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+    sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+    sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+    const float na = sqrtf(sa), nb = sqrtf(sb);
+    float xa[32], xb[32];
+    encm_transform<B>(ln, wa, wb, xa, xb);
+    uint32_t wd[B], oma, omb;
+    const float za = na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f;
+    const float zb = nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f;
+    float cca = 0.f, cxa = 0.f, ccb = 0.f, cxb = 0.f;
+    encm_quantize<B, true, SCALE>(xa, cells, za, p.c.thr_out, wd, oma, cent, &cca, &cxa);
+    if (va) encm_store_row<B>(rec + (size_t)cur.slot_a * E::RB + ln.t * 4 * B, wd);
+    encm_quantize<B, true, SCALE>(xb, cells, zb, p.c.thr_out, wd, omb, cent, &ccb, &cxb);
+    if (vb) encm_store_row<B>(rec + (size_t)cur.slot_b * E::RB + ln.t * 4 * B, wd);
+    float sca = na, scb = nb;
+    if constexpr (SCALE) encm_scales(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
+    if (!va) oma = 0u;
+    if (!vb) omb = 0u;
+    // the lane's y values as bf16 (the stored outlier value), kept in its own
+    // chunks of the tile buffer it has just read, for the entry writes below
+    if (oma) encm_stash(tl, ln.g, ln.g, ln.t, xa, na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f);
+    if (omb) encm_stash(tl, ln.g + 8, ln.g, ln.t, xb, nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f);
+    if (ln.t == 0) {
+      float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
+      if (va) nrm[cur.slot_a] = sca;
+      if (vb) nrm[cur.slot_b] = scb;
+    }
+    // entries before this lane within its vector (quad prefix over t)
+    const int ca = __popc(oma), cb = __popc(omb);
+    int ia = ca, ib = cb;
 #pragma unroll
-      for (int m = 1; m < 4; m <<= 1) {
-        const int oa = __shfl_up_sync(0xffffffffu, ia, m, 4);
-        const int ob = __shfl_up_sync(0xffffffffu, ib, m, 4);
-        if (ln.t >= m) {
-          ia += oa;
-          ib += ob;
-        }
+    for (int m = 1; m < 4; m <<= 1) {
+      const int oa = __shfl_up_sync(0xffffffffu, ia, m, 4);
+      const int ob = __shfl_up_sync(0xffffffffu, ib, m, 4);
+      if (ln.t >= m) {
+        ia += oa;
+        ib += ob;
       }
-      const int tota = __shfl_sync(0xffffffffu, ia, 3, 4), totb = __shfl_sync(0xffffffffu, ib, 3, 4);
-      const int nsa = min(tota, 255), nsb = min(totb, 255);
-      if (ln.t == 0) {
-        cnt_s[pa] = va ? nsa : 0;
-        cnt_s[pb] = vb ? nsb : 0;
-      }
-      __syncthreads();
-      if (ln.warp == 0) {
-        const int run = run_s;
-        int v0 = cnt_s[ln.lane], v1 = cnt_s[32 + ln.lane];
-        int i0 = v0, i1 = v1;
+    }
+    const int nsa = min(__shfl_sync(0xffffffffu, ia, 3, 4), 255);
+    const int nsb = min(__shfl_sync(0xffffffffu, ib, 3, 4), 255);
+    // the tile's 16 vectors in slot order (the a rows g = 0..7, then the b
+    // rows): a warp prefix over the quads; the lanes of a quad contribute at
+    // t = 0 only, so all four read their quad's inclusive sum
+    int pa = ln.t == 0 ? nsa : 0, pb = ln.t == 0 ? nsb : 0;
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-          const int o0 = __shfl_up_sync(0xffffffffu, i0, m), o1 = __shfl_up_sync(0xffffffffu, i1, m);
-          if (ln.lane >= m) {
-            i0 += o0;
-            i1 += o1;
-          }
-        }
-        const int half = __shfl_sync(0xffffffffu, i0, 31);
-        const int tot1 = __shfl_sync(0xffffffffu, i1, 31);  // all lanes: a full-mask shuffle
-        off_s[ln.lane] = run + i0 - v0;
-        off_s[32 + ln.lane] = run + half + i1 - v1;
-        __syncwarp();
-        if (ln.lane == 0) run_s = run + half + tot1;
+    for (int m = 1; m < 32; m <<= 1) {
+      const int oa = __shfl_up_sync(0xffffffffu, pa, m);
+      const int ob = __shfl_up_sync(0xffffffffu, pb, m);
+      if (ln.lane >= m) {
+        pa += oa;
+        pb += ob;
       }
-      __syncthreads();
-      uint32_t* ent = reinterpret_cast<uint32_t*>(rec + p.c.off_entries);
+    }
+    const int tot_a = __shfl_sync(0xffffffffu, pa, 31), tot_b = __shfl_sync(0xffffffffu, pb, 31);
+    const int off_a = run + pa - nsa, off_b = run + tot_a + pb - nsb;
+    run += tot_a + tot_b;
+    uint32_t* ent = reinterpret_cast<uint32_t*>(rec + p.c.off_entries);
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        const bool valid = v ? vb : va;
-        if (!valid) continue;
-        const int off = off_s[v ? pb : pa];
-        const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));
-        uint32_t om = v ? omb : oma;
-        int k = (v ? ib - cb : ia - ca);
-        const int row = v ? ln.g + 8 : ln.g;
-        while (om) {
-          const int r = __ffs(om) - 1;
-          om &= om - 1;
-          if (k < stored) ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)encm_stashed(tl, row, ln.g, ln.t, r) << 16);
-          ++k;
-        }
-        if (ln.t == 0) rec[p.c.off_count + (v ? slot_b : slot_a)] = (uint8_t)stored;
+    for (int v = 0; v < 2; ++v) {
+      const bool valid = v ? vb : va;
+      if (!valid) continue;
+      const int off = v ? off_b : off_a;
+      const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));
+      uint32_t om = v ? omb : oma;
+      int k = v ? ib - cb : ia - ca;
+      const int row = v ? ln.g + 8 : ln.g;
+      while (om) {
+        const int r = __ffs(om) - 1;
+        om &= om - 1;
+        if (k < stored) ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)encm_stashed(tl, row, ln.g, ln.t, r) << 16);
+        ++k;
       }
+      if (ln.t == 0) rec[p.c.off_count + (v ? cur.slot_b : cur.slot_a)] = (uint8_t)stored;
     }
     cur = nxt;
   }
@@ -481,25 +520,26 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
 
 // `grid` is 8 CTAs per SM; these kernels run 4 per SM (registers), so one
 // wave (grid / 2) of persistent CTAs, whose warps then prefetch their next task.
-template <int B>
+template <int B, bool SCALE>
 static cudaError_t encm_launch(const EncodeParams& p, int grid, cudaStream_t s) {
   grid = std::max(1, grid / 2);
   if (p.c.has_outl) {
-    const int64_t tasks = p.n_groups * p.chunks_per_group;
-    encode_mma_outl_kernel<B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+    const int64_t tasks = (p.n_groups * p.chunks_per_group + 3) / 4;   // a warp per record
+    encode_mma_outl_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
   } else {
     const int64_t tasks = (p.n_groups * p.chunks_per_group * 8 + 3) / 4;
-    encode_mma_kernel<B><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+    encode_mma_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_encode_mma(const EncodeParams& p, int grid, cudaStream_t s) {
+  const bool sc = p.c.scale_mode != TQ_SCALE_NORM;
   switch (p.c.bits) {
-    case 1: return encm_launch<1>(p, grid, s);
-    case 2: return encm_launch<2>(p, grid, s);
-    case 3: return encm_launch<3>(p, grid, s);
-    case 4: return encm_launch<4>(p, grid, s);
+    case 1: return sc ? encm_launch<1, true>(p, grid, s) : encm_launch<1, false>(p, grid, s);
+    case 2: return sc ? encm_launch<2, true>(p, grid, s) : encm_launch<2, false>(p, grid, s);
+    case 3: return sc ? encm_launch<3, true>(p, grid, s) : encm_launch<3, false>(p, grid, s);
+    case 4: return sc ? encm_launch<4, true>(p, grid, s) : encm_launch<4, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -101,6 +101,26 @@ __device__ __forceinline__ uint32_t mask_le(float a, float b) {
   return r;
 }
 
+// Byte offset of record c of stream (b, h) within its layer's record array:
+// contiguous [B][Hkv][rec_cap] records, or, with a block table, block
+// table[b][c] of a pool of rec_cap blocks of Hkv records each.  A table entry
+// outside the pool is clamped into it (a wrong table reads a wrong record,
+// never out of bounds).
+__device__ __forceinline__ int64_t rec_offset(const int32_t* table, int table_stride, int rec_cap, int Hkv, int b,
+                                              int h, int c, int rec_bytes) {
+  if (table) {
+    const int blk = min(max(__ldg(table + (int64_t)b * table_stride + c), 0), rec_cap - 1);
+    return ((int64_t)blk * Hkv + h) * rec_bytes;
+  }
+  return (((int64_t)b * Hkv + h) * rec_cap + c) * rec_bytes;
+}
+
+// n / f.d for a FastDiv (tq_params.h)
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 // ------------------------------------------------------------- SplitMix64
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t k) {
   // output k (0-based) of SplitMix64 seeded with `seed`
@@ -197,6 +217,18 @@ __device__ __forceinline__ float cell_boundary(const float2* cells, uint32_t i) 
 }
 __device__ __forceinline__ uint32_t cell_count(const float2* cells, uint32_t i) {
   return reinterpret_cast<const uint8_t*>(reinterpret_cast<const float*>(cells) + kCells)[i];
+}
+
+// Per-vector scale of a record's "norm" field (tq_scale_mode): n = ||x||,
+// cc = ||chat||^2 and cy = <chat, y> of the dequantised rotated vector chat
+// (turboquant_plus commit log, the EDEN-scale commits and their Appendix A
+// note).  A zero vector stores 0.
+__device__ __forceinline__ float vector_scale(int mode, float n, float cc, float cy) {
+  if (!(n > 0.f)) return 0.f;
+  if (mode == TQ_SCALE_MATCHED_NORM) return n / sqrtf(cc);
+  if (mode == TQ_SCALE_INNER_PRODUCT) return n / cy;
+  if (mode == TQ_SCALE_LEAST_SQUARES) return n * cy / cc;
+  return n;
 }
 
 // Logit soft cap (arc PR #98, softcapping fix: cap * tanh(s / cap) on the

@@ -10,6 +10,7 @@ namespace tq {
 // What a kernel needs of a codec, resolved on the host.
 struct CodecDev {
   int d, bits, has_outl, cap;
+  int scale_mode;  // tq_scale_mode of the stored per-vector scale
   int rec_bytes, off_norm, off_count, off_entries;
   float thr_out;     // T / sqrt(d) in f32 (+inf when T is +inf)
   float inv_sqrt_d;  // f32(1/sqrt(d))
@@ -20,6 +21,26 @@ struct CodecDev {
   uint32_t signs[16];
 };
 
+// Unsigned 32-bit division by a run-time constant as a multiply-high, an add
+// and two shifts (Granlund & Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994):  with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1,  n / d = (t + ((n - t) >> 1)) >> (l - 1),
+// t = mulhi(m, n), for every n < 2^32.  d = 1 takes m = 0 and no shifts.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+inline FastDiv make_fast_div(uint32_t d) {
+  FastDiv f{d, 0u, 0u, 0u};
+  if (d > 1) {
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    f.m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    f.s1 = 1;
+    f.s2 = l - 1;
+  }
+  return f;
+}
+
 struct EncodeParams {
   CodecDev c;
   const uint16_t* src;
@@ -28,13 +49,18 @@ struct EncodeParams {
   int64_t dst_gs;  // bytes
   int64_t n_groups, n_vec, first_vec;
   int64_t first_chunk, chunks_per_group;
+  FastDiv cpg;       // division by chunks_per_group
+  int small_tasks;   // every task index the kernels form (with the grid's lookahead) is below 2^32
 };
 
 struct EvictParams {
   CodecDev c;               // codec of the stream this launch encodes
   uint8_t* rec;
   int64_t rec_ls;           // bytes
-  int rec_cap;
+  int rec_cap;              // records per stream, or blocks per layer pool with a block table
+  const int32_t* table;     // block table [B][table_stride] or null (contiguous records)
+  int table_stride;
+  int rec_limit;            // records a stream may hold: rec_cap, or table_stride when paged
   const uint16_t* tail;
   int64_t tail_ls;          // elements
   int tail_cap;
@@ -48,7 +74,25 @@ struct EvictCommitParams {
   int32_t* n_chunks;
   int32_t* tail_start;
   int32_t* tail_len;
-  int LB, floor_, max_evict, tail_cap, rec_cap;
+  int LB, floor_, max_evict, tail_cap, rec_limit;
+};
+
+struct RollbackParams {
+  CodecDev c;               // codec of the stream this launch decodes
+  const uint8_t* rec;
+  int64_t rec_ls;           // bytes
+  int rec_cap;              // records per stream, or blocks per layer pool with a block table
+  const int32_t* table;     // block table [B][table_stride] or null
+  int table_stride;
+  int rec_limit;
+  uint16_t* tail;           // bf16 ring [L][B][Hkv][tail_cap][D]
+  int64_t tail_ls;          // elements
+  int tail_cap;
+  int32_t* n_chunks;
+  int32_t* tail_start;
+  int32_t* tail_len;
+  const int32_t* new_len;   // [L][B]
+  int L, B, Hkv;
 };
 
 struct DecodeParams {
@@ -65,12 +109,16 @@ struct AttnParams {
   int L, B, Hq, Hkv, G, n_hg;
   float sscale;  // softmax scale * log2(e)
   float scap, iscap;  // logit soft cap * log2(e) and its reciprocal; 0, 0 = no cap
+  float sv_log2eps;   // sparse-V threshold log2(eps) (< 0), or 0 = every value accumulated
   const uint16_t* q;
   int64_t q_ls, q_bs;
   const uint8_t* krec;
   const uint8_t* vrec;
   int64_t krec_ls, vrec_ls;
-  int rec_cap;
+  int rec_cap;              // records per stream, or blocks per layer pool with a block table
+  const int32_t* table;     // block table [B][table_stride] or null (contiguous records)
+  int table_stride;
+  int rec_limit;            // records a stream may hold: rec_cap, or table_stride when paged
   int krec_bytes, vrec_bytes;
   int kb, vb, kout, vout, kcap, vcap, shared_kv;
   int k_off_norm, v_off_norm, k_off_count, v_off_count, k_off_ent, v_off_ent;
@@ -111,6 +159,8 @@ cudaError_t launch_encode_mma(const EncodeParams& p, int grid, cudaStream_t s); 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t s);
 cudaError_t launch_evict_commit(const EvictCommitParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_rollback(const RollbackParams& p, cudaStream_t s);
+cudaError_t launch_rollback_commit(const RollbackParams& p, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
 // warp-local kernel for the compressed splits (head dims 64 and 128)
 cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);

@@ -3,6 +3,7 @@ declares; host-side validation rejects bad arguments with a status (no silent
 no-op, no launch).  Runs without a GPU: only calls that fail validation before
 touching the device are made here."""
 import ctypes
+import math
 import os
 import re
 
@@ -272,3 +273,59 @@ def test_no_cpu_fallback_without_the_library(tmp_path):
         "print('ok')\n" % str(tmp_path / "absent" / "libtq_gb300.so"))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.stdout, r.stderr[-2000:])
+
+
+def _gauss_codec(tq, orc, bits, d):
+    c = tq.tq_codec()
+    c.head_dim, c.bits, c.sign_seed = d, bits, 1
+    cent, bnd = orc.codebook_f32(bits, d)
+    for k, v in enumerate(cent):
+        c.centroids[k] = float(v)
+    for k, v in enumerate(bnd):
+        c.boundaries[k] = float(v)
+    return tq.Codec(c, 0.0)
+
+
+def test_set_centroids_fills_midpoints_and_validates(lib, orc):
+    """tq_codec_set_centroids (host only): a caller's symmetric ascending table
+    replaces the Gaussian one with the same f32 midpoints the oracle derives;
+    unordered, non-finite, asymmetric, too-large and too-close tables are
+    rejected and leave the codec unchanged."""
+    import numpy as np
+    tq, _ = lib
+    d, bits = 128, 3
+    base = _gauss_codec(tq, orc, bits, d)
+    half = np.float32(np.array([0.1, 0.35, 0.7, 1.3]) / math.sqrt(d))
+    tab = [float(v) for v in np.concatenate([-half[::-1], half])]
+    c = tq.tq_codec_set_centroids(base, tab)
+    assert c.centroids() == [float(np.float32(v)) for v in tab]
+    np.testing.assert_array_equal(np.array(c.boundaries(), np.float32), orc.midpoints_f32(bits, np.array(tab, np.float32)))
+    assert tq.tq_record_bytes(c) == base.record_bytes
+    bad = {
+        "unordered": tab[:3] + [tab[4], tab[3]] + tab[5:],
+        "nan": tab[:7] + [float("nan")],
+        "asymmetric": tab[:7] + [tab[7] * 1.01],
+        "too large": [v * 12.0 for v in tab],
+        "too close": [v * 0.02 for v in tab],
+        "wrong count": tab[:4],
+    }
+    want = {"unordered": tq.TQ_ERR_INVALID_ARG, "nan": tq.TQ_ERR_INVALID_ARG, "wrong count": tq.TQ_ERR_INVALID_ARG,
+            "asymmetric": tq.TQ_ERR_UNSUPPORTED, "too large": tq.TQ_ERR_UNSUPPORTED,
+            "too close": tq.TQ_ERR_UNSUPPORTED}
+    for name, t in bad.items():
+        with pytest.raises(tq.TqError) as e:
+            tq.tq_codec_set_centroids(base, t)
+        assert e.value.status == want[name], name
+    # two-bit tables have no cell-spacing condition
+    c2 = tq.tq_codec_set_centroids(_gauss_codec(tq, orc, 2, d), [-0.02, -0.001, 0.001, 0.02])
+    assert c2.boundaries()[1] == 0.0
+
+
+def test_scale_mode_is_validated(lib, orc):
+    tq, _ = lib
+    c = _gauss_codec(tq, orc, 3, 128)
+    for m in range(4):
+        c.c.scale_mode = m
+        assert tq.load().tq_record_bytes(ctypes.byref(c.c)) > 0
+    c.c.scale_mode = 4
+    assert tq.load().tq_record_bytes(ctypes.byref(c.c)) == 0

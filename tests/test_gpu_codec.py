@@ -166,3 +166,35 @@ def test_sweep_sample_parity(tq, orc):
             enc = orc.encode_vectors(x, _ocodec(orc, c), want_y=True)
             tl.check_codes(codes, enc, orc.codebook_f32(bits, d)[1], d)
             tl.check_norms(norms, enc)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("mode", ["matched_norm", "inner_product", "least_squares"])
+@pytest.mark.parametrize("T", [0.0, 2.0])
+def test_scale_modes(tq, orc, d, mode, T):
+    """The per-vector scale variants (turboquant_plus commit log, the EDEN-scale
+    commits): codes and outlier lists as in the plain codec, the stored f32
+    scale within 4e-6 relative of the oracle's (f32 sums of at most 512
+    positive terms against fp64) on every vector whose codes match, and the
+    GPU decode of those records within 1e-5 of the oracle's."""
+    import torch
+    bits = 3
+    c = tq.with_scale(tq.tq_make_codebook(bits, d, sign_seed=1, outlier_T=T), mode)
+    oc = orc.Codec(d=d, bits=bits, seed=1, T=T, cap=int(c.c.outlier_cap) if T else 0, scale=mode)
+    n = 300
+    x = synth.gaussian_bf16((n, d), 2000 + d, outlier_frac=0.02 if T else 0.0, lognormal_sigma=0.5)
+    rec = _encode_gpu(tq, c, x)[0]
+    codes, norms, outs = tl.unpack_records(rec, n, d, bits, T != 0.0, oc.outlier_cap if T else 0)
+    enc = orc.encode_vectors(x, oc, want_y=True)
+    band = tl.check_codes(codes, enc, orc.codebook_f32(bits, d)[1], d, total_frac=None)[0]
+    if T:
+        band += tl.check_outliers(outs, enc, d, T)
+    assert band <= max(1, 1e-5 * n * d)
+    same = np.all(codes == enc["codes"], axis=1)
+    if T:
+        same &= np.array([set(o) == set(np.nonzero(enc["is_out"][i])[0]) for i, o in enumerate(outs)])
+    assert same.sum() >= n - 2
+    np.testing.assert_allclose(norms[same], enc["norms"][same], rtol=4e-6)
+    dst = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    tq.tq_decode(c, torch.from_numpy(rec).cuda(), dst)
+    _check_decode(dst.cpu().numpy(), orc.decode_records(rec, n, oc), f"d {d} {mode} T {T}")
