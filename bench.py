@@ -65,6 +65,13 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=None, help="cache workloads: instantiate batch B")
     ap.add_argument("--splits", type=int, default=0,
                     help="cache workloads: splits per (layer, batch, kv head) of tq_decode_attn (0 = its planner)")
+    ap.add_argument("--sparse-v", type=float, default=0.0,
+                    help="cache workloads on the d-64/128 tensor-core route: sparse-V threshold eps (0 = off); "
+                         "the attention phase is also timed without it")
+    ap.add_argument("--sinks", action="store_true",
+                    help="cache workloads: plant an attention-sink key (logit about 40 for every head of its kv "
+                         "head) at the first token of every 32-token block the decode kernel's warps open a "
+                         "split with")
     return ap.parse_args()
 
 
@@ -293,7 +300,8 @@ class CacheWorkload:
                  over the records and the dense part (tail ring, or the
                  whole cache of a bf16 layer)."""
 
-    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0, splits: int = 0):
+    def __init__(self, name, device, layers=None, batch=None, seed_offset: int = 0, splits: int = 0,
+                 sparse_v: float = 0.0, sinks: bool = False):
         import torch
 
         import rotated_lloyd_max_gb300 as tq
@@ -357,7 +365,10 @@ class CacheWorkload:
             self.tail_start = torch.zeros((L, B), dtype=i32, device=device)
             kw.update(k_tail=self.kt, v_tail=self.vt, tail_len=self.tail_len, tail_start=self.tail_start,
                       max_tail=tail)
-        self.args_all = tq.make_attn_args(**kw)
+        self.args_all = tq.make_attn_args(**kw, sparse_v_eps=sparse_v)
+        self.sparse_v = sparse_v
+        if sparse_v:   # the same call without skipping, timed beside it
+            self.args_exact = tq.make_attn_args(**kw)
         ws = tq.tq_decode_attn_workspace_size(self.args_all, self.kc, self.vc)
         self.args_layer = None
         if self.dense:          # the per-layer variant a model's layer loop issues (timed alongside)
@@ -377,6 +388,9 @@ class CacheWorkload:
                 self.args_layer.append((a, codecs))
         self.ws = torch.empty(ws, dtype=u8, device=device)
         self.plan = tq.tq_decode_attn_plan(self.args_all, self.kc, self.vc)
+        self.sinks = sinks
+        if sinks:
+            self._plant_sinks()
         # eviction: the 144 tokens after the last record's are the dense tail's
         # first tokens where the workload has a tail, else a fresh draw
         lay = slice(self.c0, self.c1)
@@ -417,6 +431,26 @@ class CacheWorkload:
         self.concurrent_enc = self.enc_in < (256 << 20)
         self.vectors_per_step = streams * n_vec
         self.tokens_per_step = B          # one decode token per sequence through all layers
+
+    def _plant_sinks(self):
+        """A synthetic attention sink per block sequence of the decode kernel:
+        the key u * 40 / min_h(q_h . u), u the sum of the kv head's queries, at
+        token 128 r + 32 w of the first record r of every split, for each of
+        the kernel's four warps w."""
+        torch = self.torch
+        cps = max(1, self.plan["records_per_split"])
+        pos = torch.tensor([128 * r + 32 * w for r in range(0, self.n_rec, cps) for w in range(4)],
+                           device=self.kx.device)
+        G = self.Hq // self.Hkv
+        for l in self.comp:
+            q = self.q[l].float().view(self.B, self.Hkv, G, self.d)
+            u = q.sum(2)                                                    # [B, Hkv, d]
+            lo = torch.einsum("bhgd,bhd->bhg", q, u).amin(-1).clamp_min(1e-3)
+            sink = (u * (40.0 / lo)[..., None]).to(torch.bfloat16)
+            self.kx[l][:, :, pos] = sink[:, :, None, :]
+
+    def attention_exact(self):
+        self.tq.tq_decode_attn(self.args_exact, self.kc, self.vc, self.ws)
 
     def _enc(self, codec, src, rec):
         n = (self.c1 - self.c0) * self.B * self.Hkv
@@ -789,7 +823,8 @@ def run_native(args, world, rank, local, pg):
     b.build()
     import rotated_lloyd_max_gb300 as tq
     tq.load()
-    wl = CacheWorkload(args.workload, dev, layers=args.layers, batch=args.batch, splits=args.splits)
+    wl = CacheWorkload(args.workload, dev, layers=args.layers, batch=args.batch, splits=args.splits,
+                       sparse_v=args.sparse_v, sinks=args.sinks)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -863,6 +898,7 @@ def run_native(args, world, rank, local, pg):
         e["traffic_sources_sha"] = phase_sources_sha(name)
     dominant = max(phases, key=lambda k: phases[k]["time_us"])
     per_layer = per_layer_attention(wl, stream, flush, max(3, min(200, K))) if wl.args_layer else None
+    exact_attn = exact_attention_time(wl, stream, flush, K) if wl.sparse_v else None
     cfg = wl.cfg
     line = {
         "metric": "decode-attn KV GB/s & tok/s; encode Mvec/s; % of GB300 HBM roofline",
@@ -883,6 +919,9 @@ def run_native(args, world, rank, local, pg):
                    "tail_tokens": wl.tail, "full_size": wl.L == cfg["L"] and wl.B == cfg["B"],
                    "l2": "flushed (256 MiB write) before each phase, outside its events",
                    "attention_splits": args.splits or "planner",
+                   **({"sparse_v_eps": wl.sparse_v} if wl.sparse_v else {}),
+                   **({"sinks": "attention-sink key at the first token of each warp block opening a split"}
+                      if wl.sinks else {}),
                    "step": (f"encode whole cache ({wl.enc_launches} launch(es)) + evict one chunk per "
                             f"(layer, batch, kv head) ({wl.ev.launches} launches) + decode attention of all "
                             f"{wl.L} layers in one tq_decode_attn call ({wl.plan['launches']} launches)"),
@@ -898,6 +937,9 @@ def run_native(args, world, rank, local, pg):
             "decode_attn_tok_s": round(wl.tokens_per_step / t_attn, 1),
             "decode_attn_us_per_step": round(t_attn * 1e6, 2),
             **({"decode_attn_per_layer_calls_us_per_step": round(per_layer * 1e6, 2)} if per_layer else {}),
+            **({"sparse_v": {"eps": wl.sparse_v, "decode_attn_us_per_step": round(t_attn * 1e6, 2),
+                             "decode_attn_us_per_step_without": round(exact_attn * 1e6, 2)}}
+               if wl.sparse_v else {}),
             "step_algorithmic_bytes": wl.step_bytes,
             "attention_plan": wl.plan,
         },
@@ -926,6 +968,30 @@ def run_native(args, world, rank, local, pg):
                                 "cores": oracle.threads(), "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def exact_attention_time(wl, stream, flush, steps: int) -> float:
+    """The attention call without sparse-V skipping, replayed from a CUDA graph
+    with L2 flushed before each replay; mean seconds."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    wl.attention_exact()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        wl.attention_exact()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b) / 1e3
+    return tot / steps
 
 
 def per_layer_attention(wl, stream, flush, steps: int) -> float:
