@@ -183,7 +183,24 @@ EVICT_WINDOW, EVICT_MARGIN, EVICT_TQ = 128, 16, 1
 # phase whose sources have changed since reports null.  Captures of a reduced
 # layer count are scaled to the full workload by layers (the phase's traffic
 # is a sum over layers).
-MEASURED_TRAFFIC: dict = {}
+# Captured at commit 9c37d1d8fe47 (profiles/phase_traffic.md): small cases
+# (batched --layers 2, V4-Flash-like --layers 8, long context --layers 1,
+# Qwen2-shaped in full), mean over the captured steps, scaled by layers.
+_T = {"tq_encode": "a01db87b7565d885", "tq_evict": "8caca9e11f62bd3b", "tq_decode_attn": "930ab8b0b44baaa9"}
+MEASURED_TRAFFIC: dict = {
+    ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_570_415_002, "sources": _T["tq_encode"]},
+    ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_411_008, "sources": _T["tq_evict"]},
+    ("batched_b32_ctx32768", "tq_decode_attn"): {"bytes": 45_205_169_766, "sources": _T["tq_decode_attn"]},
+    ("v4flash_mqa_ctx65536", "tq_encode"): {"bytes": 3_501_147_032, "sources": _T["tq_encode"]},
+    ("v4flash_mqa_ctx65536", "tq_evict"): {"bytes": 5_785_048, "sources": _T["tq_evict"]},
+    ("v4flash_mqa_ctx65536", "tq_decode_attn"): {"bytes": 867_608_110, "sources": _T["tq_decode_attn"]},
+    ("longctx_b4_ctx262144", "tq_encode"): {"bytes": 39_894_601_728, "sources": _T["tq_encode"]},
+    ("longctx_b4_ctx262144", "tq_evict"): {"bytes": 17_120_461, "sources": _T["tq_evict"]},
+    ("longctx_b4_ctx262144", "tq_decode_attn"): {"bytes": 6_103_937_024, "sources": _T["tq_decode_attn"]},
+    ("qwen2_1p5b_ctx2048", "tq_encode"): {"bytes": 46_209_229, "sources": _T["tq_encode"]},
+    ("qwen2_1p5b_ctx2048", "tq_evict"): {"bytes": 2_926_080, "sources": _T["tq_evict"]},
+    ("qwen2_1p5b_ctx2048", "tq_decode_attn"): {"bytes": 22_419_302, "sources": _T["tq_decode_attn"]},
+}
 
 PHASE_SOURCES = {
     "tq_encode": ["encode_mma.cu", "encode.cu", "tq_common.cuh", "tq_params.h", "abi.cu"],
@@ -893,7 +910,8 @@ def run_native(args, world, rank, local, pg):
                                          wl.attn_bytes, t_attn, wl.plan["launches"], flops=wl.attn_flops),
     }
     for name, e in phases.items():
-        t = measured_traffic(wl.name if wl.L == wl.cfg["L"] and wl.B == wl.cfg["B"] else "", name)
+        full = wl.L == wl.cfg["L"] and wl.B == wl.cfg["B"] and not wl.sparse_v and not wl.sinks
+        t = measured_traffic(wl.name if full else "", name)
         e["traffic"] = t
         e["traffic_sources_sha"] = phase_sources_sha(name)
     dominant = max(phases, key=lambda k: phases[k]["time_us"])
