@@ -101,3 +101,51 @@ def test_single_f16_operands_miss_the_tolerance(errors):
     worst = max(single for _, single in errors.values())
     assert worst > TOL, errors
     assert errors["v4flash_like"][1] > TOL
+
+
+def _model_terms(qt, kv, kn, vv, vn, scale, score_terms, value_terms):
+    """_model with a chosen subset of the three split products per contraction:
+    'hh', 'hl' (hi . lo of the second operand), 'lh' (lo of the first . hi)."""
+    K = (kv * np.float32(2.0 ** 16)).astype(np.float32)
+    s = (14 - np.floor(np.log2(np.abs(qt).max(1)))).astype(int)
+    Q = (qt * _pow2(s)[:, None]).astype(np.float32)
+    (Kh, Kl), (Qh, Ql) = _split(K), _split(Q)
+    prod = {"hh": lambda: Kh @ Qh.T, "hl": lambda: Kh @ Ql.T, "lh": lambda: Kl @ Qh.T}
+    acc = sum(prod[t]() for t in score_terms)
+    t = (acc * kn[:, None] * np.float32(scale * LOG2E) * _pow2(-(16 + s))[None, :]).astype(np.float32)
+    p = np.exp2(t - t.max(0)).astype(np.float32)
+    l = p.sum(0, dtype=np.float32)
+    kx = int(15 - np.ceil(np.log2(vn.max())))
+    P = (p * vn[:, None] * _pow2(kx)).astype(np.float32)
+    V = (vv * np.float32(2.0 ** 16)).astype(np.float32)
+    (Vh, Vl), (Ph, Pl) = _split(V), _split(P)
+    vprod = {"hh": lambda: Vh.T @ Ph, "hl": lambda: Vh.T @ Pl, "lh": lambda: Vl.T @ Ph}
+    O = sum(vprod[t]() for t in value_terms)
+    return (O * _pow2(-(16 + kx)) / l).astype(np.float64)
+
+
+@pytest.mark.parametrize("drop", ["score hl", "score lh", "value hl", "value lh"])
+def test_no_two_product_split_holds_on_peaky_v4flash_draws(orc, drop):
+    """Dropping any one of the three products (in the scores or in the values)
+    misses the 2e-3 bar on a V4-Flash-like draw with logits scaled 8x, while
+    the three-product split stays far inside it: the tcgen05 kernel's MMA work
+    cannot be cut by a third without giving up the tolerance."""
+    d, H, n, kb, vb, sigma, scale, seed = 512, 64, 2048, 4, 4, 0.3, 8.0, 6
+    rng = np.random.default_rng(seed)
+    ck = orc.codebook_f32(kb, d)[0].astype(np.float32)
+    cv = orc.codebook_f32(vb, d)[0].astype(np.float32)
+    kv = ck[rng.integers(0, 1 << kb, (n, d))]
+    vv = cv[rng.integers(0, 1 << vb, (n, d))]
+    kn = (np.sqrt(d) * np.exp(sigma * rng.standard_normal(n))).astype(np.float32)
+    vn = (np.sqrt(d) * np.exp(sigma * rng.standard_normal(n))).astype(np.float32)
+    qt = (rng.standard_normal((H, d)) / np.sqrt(d)).astype(np.float32)
+    Hd = scipy.linalg.hadamard(d) / np.sqrt(d)
+    want = Hd @ _fp64(qt, kv, kn, vv, vn, scale)
+    full = ("hh", "hl", "lh")
+    kind, term = drop.split()
+    st = tuple(t for t in full if not (kind == "score" and t == term))
+    vt = tuple(t for t in full if not (kind == "value" and t == term))
+    err = float(np.abs(Hd @ _model_terms(qt, kv, kn, vv, vn, scale, st, vt) - want).max())
+    err3 = float(np.abs(Hd @ _model_terms(qt, kv, kn, vv, vn, scale, full, full) - want).max())
+    assert err3 <= TOL / 20
+    assert err > TOL, (drop, err)
