@@ -201,11 +201,12 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   if (tail_tiles > 0) St = std::max<int64_t>(1, std::min(want, tail_tiles));
   // Tensor-core kernels' CTAs take at least two records each, which amortises
   // their per-CTA set-up (pair tables, query fragments), and dense CTAs at
-  // least 128 tokens (two 16-token tiles per warp), which also keeps the
-  // merge's split count down.
+  // least 256 tokens (four 16-token tiles per warp), which also keeps the
+  // merge's split count down (Qwen2-shaped step: 25.4 us of attention with
+  // 8 dense splits of 256 tokens against 27.1 us with 16 of 128).
   if (pl->mma && a->splits <= 0) {
     if (comp_tiles >= 2) Sc = std::min<int64_t>(Sc, cdiv(comp_tiles, 2));
-    if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 128)));
+    if (St > 0) St = std::max<int64_t>(1, std::min<int64_t>(St, cdiv(max_tail, 256)));
   }
   // at head dim 512 a dense split's partial (512 floats per query head, written
   // and read back by the merge) outweighs a short run of tail tokens: at least

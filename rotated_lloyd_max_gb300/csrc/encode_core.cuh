@@ -184,7 +184,7 @@ __device__ __forceinline__ void enc_vector(const CodecDev& c, const EncLane<D, B
     if constexpr (B >= 3) {  // decision cells (shared table)
       const float z = x[r] * zscale;
       const uint32_t ci = __float_as_uint(z + 8388736.0f) & 0x1FFu;  // round(z) + 128 (2^23 + 128 magic)
-      code = cell_count(cells, ci) - mask_gt(z, cell_boundary(cells, ci));
+      code = cell_count(cells, ci) + (__float_as_uint(cell_boundary(cells, ci) - z) >> 31);  // + (z > boundary)
     } else {
       uint32_t msum = 0u;  // -(number of positive boundaries below |w|)
 #pragma unroll

@@ -237,8 +237,10 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2
       const float2 z = mul2(f2(x[r], x[r + 1]), f2(scale, scale));
       const float2 u = add2(z, f2(8388736.0f, 8388736.0f));  // round(z) + 128 in the low bits (2^23 + 128 magic)
       const float2 e0 = cells[__float_as_uint(u.x) & 0x1FFu], e1 = cells[__float_as_uint(u.y) & 0x1FFu];
-      code[0] = (uint32_t)__float_as_int(e0.y) - mask_gt(z.x, e0.x);
-      code[1] = (uint32_t)__float_as_int(e1.y) - mask_gt(z.y, e1.x);
+      // count below the cell + (z > the cell's boundary): the sign bit of boundary - z
+      // (+0 when equal, so a tie takes the lower code)
+      code[0] = (uint32_t)__float_as_int(e0.y) + (__float_as_uint(e0.x - z.x) >> 31);
+      code[1] = (uint32_t)__float_as_int(e1.y) + (__float_as_uint(e1.x - z.y) >> 31);
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {

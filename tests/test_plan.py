@@ -99,14 +99,14 @@ def test_explicit_splits_are_kept(orc, c4_512):
 def test_qwen2_plan(orc):
     """28 layers (22 with 16 records, 6 bf16 with 2048 dense tokens) in one call:
     56 units want ceil(16 x 152 / 56) = 44 splits; the tensor-core kernel takes
-    at least 2 records and 128 dense tokens per split: 8 x 2 records and
-    16 x 128 tokens, one launch of 6-head CTAs + the merge."""
+    at least 2 records and 256 dense tokens per split: 8 x 2 records and
+    8 x 256 tokens, one launch of 6-head CTAs + the merge."""
     kc, vc = raw_codec(orc, 3, 128), raw_codec(orc, 2, 128)
     a = args_for(L=28, B=1, Hq=12, Hkv=2, d=128, records=16, tail=2048, rec_bytes=128 * 52)
     p = plan(a, kc, vc)
     assert p["compressed_kernel"] == p["dense_kernel"] == "mma"
     assert (p["compressed_splits"], p["records_per_split"]) == (8, 2)
-    assert (p["dense_splits"], p["dense_tokens_per_split"]) == (16, 128)
+    assert (p["dense_splits"], p["dense_tokens_per_split"]) == (8, 256)
     assert (p["heads_per_cta"], p["launches"]) == (6, 2)
 
 
