@@ -240,7 +240,7 @@ def test_plain_c_client_links_and_plans(lib, tmp_path):
     """The library serves a C program (gcc, no Python): it links against
     libtq_gb300.so with include/tq.h and gets the planner's answer: 6 layers x 2 kv
     heads want ceil(16 x 152 / 12) = 203 splits, capped at the 64 tiles of 32
-    tokens and then at 128 tokens per split: 16 dense splits on mma.sync."""
+    tokens and then at 256 tokens per split: 8 dense splits on mma.sync."""
     import subprocess
     from rotated_lloyd_max_gb300 import build
     so = build.build()
@@ -252,7 +252,7 @@ def test_plain_c_client_links_and_plans(lib, tmp_path):
                            "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(so), "-Wl,-rpath," + libdir])
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
-    assert r.stdout.split() == ["0", "3", "16", "128", "2"]
+    assert r.stdout.split() == ["0", "3", "8", "256", "2"]
 
 
 def test_no_cpu_fallback_without_the_library(tmp_path):
