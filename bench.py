@@ -1057,9 +1057,11 @@ def e2e_leg(wl, steps: int):
     input larger than 2 GiB is copied layer by layer from one pinned
     layer-sized host buffer (every layer receives the same host bytes: the
     copied volume is the full input, the host memory pinned is one layer).
-    The copies run on a copy stream, layer by layer, and each compressed
-    layer is encoded as soon as its K/V have arrived, so the encodes overlap
-    the later layers' copies; eviction and attention wait for every copy."""
+    From 1 GiB of inputs per step the copies run on a copy stream, layer by
+    layer, and each compressed layer is encoded as soon as its K/V have
+    arrived, so the encodes overlap the later layers' copies; eviction and
+    attention wait for every copy.  Smaller steps copy everything first and
+    then run the step (per-layer launches would dominate them)."""
     import torch
     srcs = wl.inputs()
     layer_in = {"kx", "vx"}

@@ -17,6 +17,11 @@
 // same 32 coordinates of the output: its 32 codes are b words of the packed
 // row, as in the CUDA-core encoder.  A warp encodes 16 vectors at a time
 // (rows g and g + 8 of the MMA tile).
+//
+// A CTA of 16 warps owns an SM.  Its decision-cell table is replicated 16
+// times, copy j in bank pair j, and lane l reads copy l % 16: the lookups of
+// a half-warp (one shared-memory wavefront) never conflict, whatever cells
+// the 16 coordinates fall in.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -54,6 +59,7 @@ struct EncM {
 template <int B>
 struct EncMLane {
   int lane, warp, g, t;
+  uint32_t cell_lane;  // byte offset of this lane's copy within a replicated cell
   uint32_t smask[16];
   uint32_t hb[2][2];  // [n-tile][b0, b1]
   __device__ __forceinline__ explicit EncMLane(const CodecDev& c) {
@@ -61,6 +67,7 @@ struct EncMLane {
     warp = threadIdx.x >> 5;
     g = lane >> 2;
     t = lane & 3;
+    cell_lane = (uint32_t)(lane & 15) * 8u;
     const uint32_t sb = c.signs[t];
 #pragma unroll
     for (int k = 0; k < 16; ++k) smask[k] = (((sb >> (2 * k)) & 1u) << 15) | (((sb >> (2 * k + 1)) & 1u) << 31);
@@ -124,33 +131,40 @@ __device__ __forceinline__ void encm_read(const EncTile& tile, int r, int g, int
   }
 }
 
-// The lane's 32 values x * inv as bf16 (round to nearest even), into its own
-// chunks of tile row r (which it has read already); and one of them back.
-__device__ __forceinline__ void encm_stash(EncTile& tile, int r, int g, int t, const float (&x)[32], float inv) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(x[8 * k + 2 * j] * inv, x[8 * k + 2 * j + 1] * inv);
-      w[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    tile.row[r][encm_chunk(g, t, k)] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-__device__ __forceinline__ uint16_t encm_stashed(const EncTile& tile, int r, int g, int t, int c) {
-  const uint16_t* ch = reinterpret_cast<const uint16_t*>(&tile.row[r][encm_chunk(g, t, c >> 3)]);
-  return ch[c & 7];
+// A predicated 4-byte global store (no branch around it).
+__device__ __forceinline__ void st_global_if(bool p, uint32_t* dst, uint32_t v) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n @q st.global.u32 [%1], %2;\n}\n" ::"r"((uint32_t)p),
+               "l"(dst), "r"(v)
+               : "memory");
 }
 
-// Sum of squares of 32 bf16 coordinates (exact squares, pairwise f32 tree).
+// a * a + c with a bf16 operand (the low or the high half of w), rounded once
+// to f32 (the square of a bf16 value is exact in f32)
+__device__ __forceinline__ float sq_add_lo(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n fma.rn.f32.bf16 %0, lo, lo, %2;\n}\n" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float sq_add_hi(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n fma.rn.f32.bf16 %0, hi, hi, %2;\n}\n" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ void st_global_u8_if(bool p, uint8_t* dst, uint32_t v) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n @q st.global.u8 [%1], %2;\n}\n" ::"r"((uint32_t)p),
+               "l"(dst), "r"(v)
+               : "memory");
+}
+
+// Sum of squares of 32 bf16 coordinates (exact squares, pairwise f32 tree:
+// pair k holds a^2 + b^2 of words 2k (a) and 2k + 1 (b), element by element).
 __device__ __forceinline__ float encm_sq(const uint32_t (&w)[16]) {
   float2 sq[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const float2 a = f2(__uint_as_float(w[2 * k] << 16), __uint_as_float(w[2 * k] & 0xFFFF0000u));
-    const float2 b = f2(__uint_as_float(w[2 * k + 1] << 16), __uint_as_float(w[2 * k + 1] & 0xFFFF0000u));
-    sq[k] = fma2(a, a, mul2(b, b));
+    sq[k].x = sq_add_lo(w[2 * k], sq_add_lo(w[2 * k + 1], 0.f));
+    sq[k].y = sq_add_hi(w[2 * k], sq_add_hi(w[2 * k + 1], 0.f));
   }
 #pragma unroll
   for (int h = 4; h; h >>= 1)
@@ -203,16 +217,50 @@ __device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint
       }
 }
 
+constexpr int kEncWarps = 16;
+constexpr int kEncThreads = 32 * kEncWarps;
+constexpr int kCellCopies = 16;
+
+// Shared memory of both kernels: the replicated decision cells (cell i, copy
+// j at float2 index 16 i + j), two tile buffers per warp, the centroids.
+struct EncSmem {
+  float2 cells[kCells * kCellCopies];
+  EncTile tiles[kEncWarps][2];
+  float cent[16];
+};
+
+// Cell (i128 >> 7) & 511 as seen by a lane (its copy: bank pair lane % 16);
+// i128 is the cell index times 128 in bits 7..15 (other bits ignored).
+__device__ __forceinline__ float2 encm_cell(const unsigned char* cells, uint32_t i128, uint32_t cell_lane) {
+  return *reinterpret_cast<const float2*>(cells + ((i128 & ((uint32_t)(kCells - 1) << 7)) | cell_lane));
+}
+
+// The table, built once per CTA: plain cells into a scratch tile first, then
+// each cell copied 16 times.
+__device__ __forceinline__ void encm_build(const CodecDev& c, EncSmem& sm) {
+  float2* plain = reinterpret_cast<float2*>(&sm.tiles[0][0]);
+  static_assert(sizeof(EncTile) >= kCells * sizeof(float2), "scratch tile holds the plain table");
+  if (threadIdx.x < kThreads) build_cells<false, true>(c, plain);
+  if (threadIdx.x < 16) sm.cent[threadIdx.x] = c.centroids[threadIdx.x];
+  __syncthreads();
+  for (int i = threadIdx.x; i < kCells * kCellCopies; i += kEncThreads) sm.cells[i] = plain[i / kCellCopies];
+  __syncthreads();
+}
+
 // Codes of the lane's 32 coordinates of one vector (x: unnormalised
 // transform, scale = 128 / (n sqrt(d)) or 0 for a zero vector), packed
 // LSB-first into B words; (OUTL) the outlier mask |y| > T / sqrt(d).
 // (SCALE) the lane's parts of ||chat||^2 and <chat, x> over its coordinates,
 // chat_j = cent[code_j] or, at an outlier coordinate, the stored bf16 value.
+// (OUTL) also the lane's 32 values y = x * inv as bf16 into its chunks of a
+// tile row (srow: its 4 chunks, swizzled by sw as in encm_chunk).
 template <int B, bool OUTL, bool SCALE = false>
-__device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2* cells, float scale,
+__device__ __forceinline__ void encm_quantize(const float (&x)[32], const unsigned char* cells, uint32_t cell_lane,
+                                              float scale,
                                               float thr_out, uint32_t (&wd)[B], uint32_t& omask,
                                               const float* cent = nullptr, float* cc = nullptr,
-                                              float* cx = nullptr) {
+                                              float* cx = nullptr, uint4* srow = nullptr, int sw = 0,
+                                              float inv_y = 0.f) {
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
@@ -220,10 +268,17 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2
   // vector (z = x * scale > t * 128  <=>  x > t * 128 / scale); a zero vector
   // (scale 0) has x = 0 and takes the y = 0 codes against threshold 0
   const float inv = scale > 0.f ? 1.0f / scale : 0.f;
-  const float Tx = B == 2 ? cells[kPosCell].x * inv : 0.f;
+  const float Tx = B == 2 ? encm_cell(cells, (uint32_t)kPosCell << 7, cell_lane).x * inv : 0.f;
   const float Tox = OUTL ? (scale > 0.f ? thr_out * kCellScale * inv : INFINITY) : 0.f;
+  uint32_t yw[4];
 #pragma unroll
   for (int r = 0; r < 32; r += 2) {
+    if constexpr (OUTL) {
+      const float2 yv = mul2(f2(x[r], x[r + 1]), f2(inv_y, inv_y));
+      const __nv_bfloat162 h = __floats2bfloat162_rn(yv.x, yv.y);
+      yw[(r >> 1) & 3] = *reinterpret_cast<const uint32_t*>(&h);
+      if ((r & 7) == 6) srow[(r >> 3) ^ sw] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    }
     uint32_t code[2];
     if constexpr (B <= 2) {
       // at most one positive boundary: compare directly (the mirror of the
@@ -235,8 +290,9 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const float2
       }
     } else {
       const float2 z = mul2(f2(x[r], x[r + 1]), f2(scale, scale));
-      const float2 u = add2(z, f2(8388736.0f, 8388736.0f));  // round(z) + 128 in the low bits (2^23 + 128 magic)
-      const float2 e0 = cells[__float_as_uint(u.x) & 0x1FFu], e1 = cells[__float_as_uint(u.y) & 0x1FFu];
+      const float2 u = add2(z, f2(kCellMagicShifted, kCellMagicShifted));  // the shifted cell index x 128
+      const float2 e0 = encm_cell(cells, __float_as_uint(u.x), cell_lane);
+      const float2 e1 = encm_cell(cells, __float_as_uint(u.y), cell_lane);
       // count below the cell + (z > the cell's boundary): the sign bit of boundary - z
       // (+0 when equal, so a tie takes the lower code)
       code[0] = (uint32_t)__float_as_int(e0.y) + (__float_as_uint(e0.x - z.x) >> 31);
@@ -289,14 +345,14 @@ __device__ __forceinline__ void encm_scales(int mode, float na, float nb, float 
 // one warp; warps stride over the tasks with the next task's rows in flight
 // (cp.async, two buffers per warp).
 template <int B, bool SCALE>
-__global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_constant__ EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, 1) encode_mma_kernel(const __grid_constant__ EncodeParams p) {
   using E = EncM<B>;
-  __shared__ float2 cells[kCells];
-  __shared__ EncTile tiles[4][2];
-  __shared__ float cent[16];
-  build_cells(p.c, cells);
-  if (threadIdx.x < 16) cent[threadIdx.x] = p.c.centroids[threadIdx.x];
-  __syncthreads();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
+  encm_build(p.c, sm);
+  const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
+  const float* cent = sm.cent;
+  auto& tiles = sm.tiles;
   const EncMLane<B> ln(p.c);
   const int64_t per_group = p.chunks_per_group * 8;
   const int64_t n_tasks = p.n_groups * per_group;
@@ -332,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
                src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs, k.vb);
     cp_async_commit();
   };
-  const int64_t stride = (int64_t)gridDim.x * 4;
-  int64_t task = (int64_t)blockIdx.x * 4 + ln.warp;
+  const int64_t stride = (int64_t)gridDim.x * kEncWarps;
+  int64_t task = (int64_t)blockIdx.x * kEncWarps + ln.warp;
   Task cur = locate(task);
   issue(cur, 0);
   for (int it = 0; task < n_tasks; task += stride, ++it) {
@@ -356,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
     const float za = na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f;
     const float zb = nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f;
     float cca = 0.f, cxa = 0.f, ccb = 0.f, cxb = 0.f;
-    encm_quantize<B, false, SCALE>(xa, cells, za, 0.f, wd, om, cent, &cca, &cxa);
+    encm_quantize<B, false, SCALE>(xa, cells, ln.cell_lane, za, 0.f, wd, om, cent, &cca, &cxa);
     if (cur.va) encm_store_row<B>(rec + (size_t)cur.slot_a * E::RB + ln.t * 4 * B, wd);
-    encm_quantize<B, false, SCALE>(xb, cells, zb, 0.f, wd, om, cent, &ccb, &cxb);
+    encm_quantize<B, false, SCALE>(xb, cells, ln.cell_lane, zb, 0.f, wd, om, cent, &ccb, &cxb);
     if (cur.vb) encm_store_row<B>(rec + (size_t)cur.slot_b * E::RB + ln.t * 4 * B, wd);
     float sca = na, scb = nb;
     if constexpr (SCALE) encm_scales(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
@@ -379,25 +435,25 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_kernel(const __grid_co
 // places by a quad prefix, a tile's 16 vectors by a warp prefix, and a running
 // warp-uniform offset carries the record's entry count from tile to tile.
 template <int B, bool SCALE>
-__global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __grid_constant__ EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, 1) encode_mma_outl_kernel(const __grid_constant__ EncodeParams p) {
   using E = EncM<B>;
-  __shared__ float2 cells[kCells];
-  __shared__ EncTile tiles[4][2];
-  __shared__ float cent[16];
-  build_cells(p.c, cells);
-  if (threadIdx.x < 16) cent[threadIdx.x] = p.c.centroids[threadIdx.x];
-  __syncthreads();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
+  encm_build(p.c, sm);
+  const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
+  const float* cent = sm.cent;
+  auto& tiles = sm.tiles;
   const EncMLane<B> ln(p.c);
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   const int64_t v_end = p.first_vec + p.n_vec;
-  const int64_t warps = (int64_t)gridDim.x * 4;
+  const int64_t warps = (int64_t)gridDim.x * kEncWarps;
   // unit u of this warp: record task warp_id + (u / 8) * warps, tile u % 8
   struct Unit {
     int64_t task, grp, chunk, ta, tb;
     int tile, slot_a, slot_b;
     bool va, vb;
   };
-  const int64_t wid = (int64_t)blockIdx.x * 4 + ln.warp;
+  const int64_t wid = (int64_t)blockIdx.x * kEncWarps + ln.warp;
   auto locate = [&](int64_t u) {
     Unit k;
     k.task = wid + (u >> 3) * warps;
@@ -450,87 +506,97 @@ __global__ void __launch_bounds__(kThreads, 4) encode_mma_outl_kernel(const __gr
     const float za = na > 0.f ? kCellScale / (na * p.c.sqrt_d) : 0.f;
     const float zb = nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f;
     float cca = 0.f, cxa = 0.f, ccb = 0.f, cxb = 0.f;
-    encm_quantize<B, true, SCALE>(xa, cells, za, p.c.thr_out, wd, oma, cent, &cca, &cxa);
+    // the quantiser also keeps the lane's y values as bf16 (the stored
+    // outlier value) in its own chunks of the tile buffer it has just read,
+    // for the entry writes below
+    const int sw = (ln.t >> 1) ^ ((ln.g & 1) << 1);
+    encm_quantize<B, true, SCALE>(xa, cells, ln.cell_lane, za, p.c.thr_out, wd, oma, cent, &cca, &cxa,
+                                  &tl.row[ln.g][4 * ln.t], sw, na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f);
     if (va) encm_store_row<B>(rec + (size_t)cur.slot_a * E::RB + ln.t * 4 * B, wd);
-    encm_quantize<B, true, SCALE>(xb, cells, zb, p.c.thr_out, wd, omb, cent, &ccb, &cxb);
+    if (!va) oma = 0u;
+    encm_quantize<B, true, SCALE>(xb, cells, ln.cell_lane, zb, p.c.thr_out, wd, omb, cent, &ccb, &cxb,
+                                  &tl.row[ln.g + 8][4 * ln.t], sw, nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f);
     if (vb) encm_store_row<B>(rec + (size_t)cur.slot_b * E::RB + ln.t * 4 * B, wd);
+    if (!vb) omb = 0u;
     float sca = na, scb = nb;
     if constexpr (SCALE) encm_scales(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
-    if (!va) oma = 0u;
-    if (!vb) omb = 0u;
-    // the lane's y values as bf16 (the stored outlier value), kept in its own
-    // chunks of the tile buffer it has just read, for the entry writes below
-    if (oma) encm_stash(tl, ln.g, ln.g, ln.t, xa, na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f);
-    if (omb) encm_stash(tl, ln.g + 8, ln.g, ln.t, xb, nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f);
     if (ln.t == 0) {
       float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
       if (va) nrm[cur.slot_a] = sca;
       if (vb) nrm[cur.slot_b] = scb;
     }
-    // entries before this lane within its vector (quad prefix over t)
+    // entries before this lane within its vector (quad prefix over t), a in
+    // the low and b in the high half-word (at most 128 per vector)
     const int ca = __popc(oma), cb = __popc(omb);
-    int ia = ca, ib = cb;
+    uint32_t qp = (uint32_t)ca | ((uint32_t)cb << 16);
 #pragma unroll
     for (int m = 1; m < 4; m <<= 1) {
-      const int oa = __shfl_up_sync(0xffffffffu, ia, m, 4);
-      const int ob = __shfl_up_sync(0xffffffffu, ib, m, 4);
-      if (ln.t >= m) {
-        ia += oa;
-        ib += ob;
-      }
+      const uint32_t o = __shfl_up_sync(0xffffffffu, qp, m, 4);
+      if (ln.t >= m) qp += o;
     }
-    const int nsa = min(__shfl_sync(0xffffffffu, ia, 3, 4), 255);
-    const int nsb = min(__shfl_sync(0xffffffffu, ib, 3, 4), 255);
+    const int ia = (int)(qp & 0xFFFFu), ib = (int)(qp >> 16);
+    const uint32_t qs = __shfl_sync(0xffffffffu, qp, 3, 4);
+    const int nsa = (int)(qs & 0xFFFFu), nsb = (int)(qs >> 16);
     // the tile's 16 vectors in slot order (the a rows g = 0..7, then the b
-    // rows): a warp prefix over the quads; the lanes of a quad contribute at
-    // t = 0 only, so all four read their quad's inclusive sum
-    int pa = ln.t == 0 ? nsa : 0, pb = ln.t == 0 ? nsb : 0;
+    // rows): an inclusive prefix over the quads, whose lanes all hold the quad's sums
+    uint32_t wp = qs;
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const int oa = __shfl_up_sync(0xffffffffu, pa, m);
-      const int ob = __shfl_up_sync(0xffffffffu, pb, m);
-      if (ln.lane >= m) {
-        pa += oa;
-        pb += ob;
-      }
+    for (int m = 4; m < 32; m <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, wp, m);
+      if (ln.lane >= m) wp += o;
     }
-    const int tot_a = __shfl_sync(0xffffffffu, pa, 31), tot_b = __shfl_sync(0xffffffffu, pb, 31);
-    const int off_a = run + pa - nsa, off_b = run + tot_a + pb - nsb;
+    const uint32_t tot = __shfl_sync(0xffffffffu, wp, 31);
+    const int tot_a = (int)(tot & 0xFFFFu), tot_b = (int)(tot >> 16);
+    const int off_a = run + (int)(wp & 0xFFFFu) - nsa, off_b = run + tot_a + (int)(wp >> 16) - nsb;
     run += tot_a + tot_b;
+    // entry writes: per vector, a warp-uniform number of rounds (the most
+    // entries a lane holds), in each of which every lane writes its next
+    // entry, if it has one: predicated stores, no divergent loop
     uint32_t* ent = reinterpret_cast<uint32_t*>(rec + p.c.off_entries);
+    const uint32_t swz = (uint32_t)sw << 4;  // the chunk swizzle in bytes
+    const uint32_t idx0 = (uint32_t)ln.t * 32u;
 #pragma unroll
     for (int v = 0; v < 2; ++v) {
-      const bool valid = v ? vb : va;
-      if (!valid) continue;
+      const int c = v ? cb : ca;
       const int off = v ? off_b : off_a;
-      const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));
+      const int stored = max(0, min(v ? nsb : nsa, p.c.cap - off));  // 0 for an invalid vector
+      int k = (v ? ib : ia) - c;
+      const int lim = min(stored, k + c);
       uint32_t om = v ? omb : oma;
-      int k = v ? ib - cb : ia - ca;
-      const int row = v ? ln.g + 8 : ln.g;
-      while (om) {
-        const int r = __ffs(om) - 1;
+      // the lane's stashed values of this vector: value j at byte (2 j) ^ swz of its 64 bytes
+      const unsigned char* sv = reinterpret_cast<const unsigned char*>(&tl.row[v ? ln.g + 8 : ln.g][4 * ln.t]);
+      const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)c);
+      for (int i = 0; i < rounds; ++i) {
+        const uint32_t r = (uint32_t)(__ffs(om) - 1) & 31u;  // a lane without entries left reads value 31, unused
         om &= om - 1;
-        if (k < stored) ent[off + k] = (uint32_t)(ln.t * 32 + r) | ((uint32_t)encm_stashed(tl, row, ln.g, ln.t, r) << 16);
+        const uint32_t val = *reinterpret_cast<const uint16_t*>(sv + ((2u * r) ^ swz));
+        st_global_if(k < lim, ent + off + k, (idx0 + r) | (val << 16));
         ++k;
       }
-      if (ln.t == 0) rec[p.c.off_count + (v ? cur.slot_b : cur.slot_a)] = (uint8_t)stored;
+      st_global_u8_if(ln.t == 0 && (v ? vb : va), rec + p.c.off_count + (v ? cur.slot_b : cur.slot_a), (uint32_t)stored);
     }
     cur = nxt;
   }
   cp_async_wait<0>();
 }
 
-// `grid` is 8 CTAs per SM; these kernels run 4 per SM (registers), so one
-// wave (grid / 2) of persistent CTAs, whose warps then prefetch their next task.
+// `grid` is 8 CTAs per SM; these kernels run one 16-warp CTA per SM (all of
+// its registers and most of its shared memory), so one wave (grid / 8) of
+// persistent CTAs, whose warps then prefetch their next task.
 template <int B, bool SCALE>
 static cudaError_t encm_launch(const EncodeParams& p, int grid, cudaStream_t s) {
-  grid = std::max(1, grid / 2);
+  grid = std::max(1, grid / 8);
+  const int smem = (int)sizeof(EncSmem);
   if (p.c.has_outl) {
-    const int64_t tasks = (p.n_groups * p.chunks_per_group + 3) / 4;   // a warp per record
-    encode_mma_outl_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+    const int64_t tasks = (p.n_groups * p.chunks_per_group + kEncWarps - 1) / kEncWarps;  // a warp per record
+    cudaError_t e = cudaFuncSetAttribute(encode_mma_outl_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    encode_mma_outl_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kEncThreads, smem, s>>>(p);
   } else {
-    const int64_t tasks = (p.n_groups * p.chunks_per_group * 8 + 3) / 4;
-    encode_mma_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kThreads, 0, s>>>(p);
+    const int64_t tasks = (p.n_groups * p.chunks_per_group * 8 + kEncWarps - 1) / kEncWarps;
+    cudaError_t e = cudaFuncSetAttribute(encode_mma_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    encode_mma_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kEncThreads, smem, s>>>(p);
   }
   return cudaGetLastError();
 }

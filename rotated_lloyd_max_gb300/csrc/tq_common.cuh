@@ -184,16 +184,23 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[B], int r) {
 constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell (257.. = top cell's law)
 constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
 constexpr float kCellScale = 128.f;
+// z + 2^16 + 128.5 rounds to the 2^-7 grid, so that bits 7..15 of the sum are
+// floor of the rounded z + 128.5: the SHIFTED cell index, already times 128
+constexpr float kCellMagicShifted = 65664.5f;
 
 // SPLIT: the table's two planes (boundaries as f32, counts as bytes) in the
 // storage of kCells float2 (the CUDA-core encoder, whose crowded lookups
 // spread over more banks as 4- and 1-byte loads); otherwise float2 entries
 // (boundary, count as int bits), one 8-byte load per lookup.
-template <bool SPLIT = false>
+// SHIFTED: cells moved down by 1/256, [i - 128.5 - 2^-8, i - 127.5 - 2^-8),
+// the cells of the index floor(z + 128.5) taken on the 2^-7 grid of an add
+// to 2^16 (kCellMagicShifted), whose bits 7..15 are the index itself.
+template <bool SPLIT = false, bool SHIFTED = false>
 __device__ __forceinline__ void build_cells(const CodecDev& c, float2* cells) {
   const int nb = (1 << c.bits) - 1;
+  constexpr float sh = SHIFTED ? 0.00390625f : 0.f;
   for (int i = threadIdx.x; i < kCells; i += kThreads) {
-    const float lo = ((float)(i - 128) - 0.5f) / kCellScale, hi = ((float)(i - 128) + 0.5f) / kCellScale;
+    const float lo = ((float)(i - 128) - 0.5f - sh) / kCellScale, hi = ((float)(i - 128) + 0.5f - sh) / kCellScale;
     int below = 0;
     float inside = 3.0e38f;
     for (int k = 0; k < nb; ++k) {
