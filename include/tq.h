@@ -286,8 +286,10 @@ typedef struct {
    * accumulation: at head dim 512 with 16-64 query heads per kv head (a
    * multiple of 8) or a multiple of 64, on the fifth-generation tensor cores
    * (tcgen05, accumulators in tensor memory); at head dims 64, 128 and the
-   * other head-dim-512 groups on mma.sync.  Everything else runs on the
-   * CUDA-core kernel (f32 FMA from the centroid table).
+   * other head-dim-512 groups on mma.sync.  With side lists at head dims 64
+   * and 128, the mma.sync kernel (corrections applied beside the MMAs) takes
+   * sparse-V calls.  Everything else runs on the CUDA-core kernel (f32 FMA
+   * from the centroid table).
    * 1: always the CUDA-core kernel.  2: as 0 but never tcgen05 (the
    * mma.sync kernels).  All paths meet the same tolerance. */
   int32_t cuda_core_path;
@@ -312,8 +314,8 @@ typedef struct {
    * Which blocks a warp visits follows the plan (records_per_split,
    * heads_per_cta of tq_decode_attn_plan; warp w holds tokens 32w..32w+31 of
    * each record).  Dense tokens are never skipped.  Another kernel route for
-   * the compressed tokens (outlier side lists, head dims 256/512,
-   * cuda_core_path != 0) with eps > 0: TQ_ERR_UNSUPPORTED. */
+   * the compressed tokens (head dims 256/512, cuda_core_path != 0) with
+   * eps > 0: TQ_ERR_UNSUPPORTED. */
   float sparse_v_eps;
 } tq_attn_args;
 
@@ -322,7 +324,7 @@ typedef enum {
   TQ_ATTN_KERNEL_NONE = 0,           /* no split of this kind */
   TQ_ATTN_KERNEL_CUDA_CORE = 1,      /* f32 FMA from the centroid table, CTA-wide softmax per tile */
   TQ_ATTN_KERNEL_CUDA_CORE_WARP = 2, /* f32 FMA, warp-local softmax (head dims 64/128; outlier side lists) */
-  TQ_ATTN_KERNEL_MMA = 3,            /* mma.sync f16 hi/lo splits, head dims 64/128 */
+  TQ_ATTN_KERNEL_MMA = 3,            /* mma.sync f16 hi/lo splits, head dims 64/128 (side lists: sparse-V) */
   TQ_ATTN_KERNEL_MMA512 = 4,         /* mma.sync f16 hi/lo splits, head dim 512 */
   TQ_ATTN_KERNEL_TCGEN05 = 5         /* tcgen05 with tensor-memory accumulators, head dim 512 */
 } tq_attn_kernel;

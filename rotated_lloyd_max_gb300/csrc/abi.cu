@@ -96,6 +96,15 @@ int max_dyn_smem() {
   return n;
 }
 
+// Bytes of a record the head-dim 64/128 tensor-core kernel stages per CTA
+// iteration: codes and scales, and with side lists the per-slot counts and
+// the first entries of the list (a record's list is about 6 entries per slot
+// at T = 2, 740 of them; entries past the staged ones are read from global memory).
+constexpr int kMmaStagedEntries = 896;
+int mma_stage_bytes(const CodecDev& c) {
+  return c.has_outl ? c.off_entries + 4 * std::min(c.cap, kMmaStagedEntries) : c.off_count;
+}
+
 // ----------------------------------------------------------------- attention plan
 struct Plan {
   int D, G, GT, n_hg, S, Sc, cps, tps;
@@ -162,13 +171,31 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   } else if (a->v_tail || a->tail_len || a->tail_start) {
     return TQ_ERR_INVALID_ARG;
   }
-  // Tensor cores for head dims 64 and 128 unless a codec has outlier side
-  // lists (their corrections are latency-bound scatter work, better
-  // overlapped by the CUDA-core kernel's FMA work) or the caller asks for the
-  // CUDA-core kernel; the same at head dim 512 for the compressed splits, with
-  // CTAs of 16 query heads where the group allows (each dequantised pair then
-  // feeds two n-tiles of MMAs).
-  pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && !(pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl));
+  // Tensor cores for head dims 64 and 128 unless the caller asks for the
+  // CUDA-core kernel; the same at head dim 512 for the compressed splits of
+  // codecs without side lists, with CTAs of 16 query heads where the group
+  // allows (each dequantised pair then feeds two n-tiles of MMAs).  Codecs
+  // with outlier side lists take the tensor-core kernel only for sparse-V
+  // (its corrections' scatter into the value accumulators, through shared
+  // atomics at two CTAs per SM, made it 1.7x slower than the CUDA-core
+  // kernel on the batched cache: 2.56 against 1.47 ms per layer), and only
+  // where its shared memory fits.
+  const bool outl = pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl);
+  pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && (!outl || a->sparse_v_eps > 0.f);
+  if (pl->mma && outl) {
+    tq::AttnParams t{};
+    t.kb = pl->kc.bits;
+    t.vb = pl->vc.bits;
+    t.kout = pl->kc.has_outl;
+    t.vout = pl->vc.has_outl;
+    t.k_main = mma_stage_bytes(pl->kc);
+    t.v_main = mma_stage_bytes(pl->vc);
+    t.shared_kv = pl->shared ? 1 : 0;
+    t.G = pl->G;
+    t.n_hg = pl->n_hg;
+    tq::attn_mma_smem_layout(t, D);
+    if (t.sm_total > max_dyn_smem()) pl->mma = false;
+  }
   pl->mma512 = D == 512 && pl->has_rec && a->cuda_core_path != 1 && !pl->kc.has_outl && !pl->vc.has_outl;
   // tcgen05 for groups of 16-64 heads (multiples of 8, which the dense
   // splits' 8-head CTAs need) or multiples of 64: one CTA keeps 64 heads
@@ -340,7 +367,14 @@ void attn_mma_smem_layout(AttnParams& p, int D) {
   off += 4 * 2 * 8 * 4;
   p.sm_logit = off;  // query fragments [d/16][32 lanes][16 B]
   off = al(off + (D / 16) * 32 * 16, 128);
-  p.sm_lut = p.sm_corr = p.sm_pre = p.sm_ent = off;  // unused by this kernel
+  // side lists: f32 centroids (K, V) and the warps' value corrections
+  // [4 warps][heads rounded up to even][D + 8]
+  p.sm_lut = off;
+  off += (p.kout || p.vout) ? 32 * 4 : 0;
+  p.sm_corr = off;
+  const int GT = p.n_hg > 0 ? p.G / p.n_hg : 8;
+  off = al(off + (p.vout ? 4 * ((GT + 1) & ~1) * (D + 8) * 4 : 0), 128);
+  p.sm_pre = p.sm_ent = off;  // unused by this kernel
   p.sm_ent_stage = 0;
   int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
   stage = std::max(stage, (4 * 8 * (D + D / 8) * 4 + 1) / 2);  // the warps' partials at the end
@@ -756,6 +790,10 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     // tensor cores: compressed and dense splits in one launch
     AttnParams pm = p;
     if (!pl.has_rec) pm.kb = pm.vb = 1;  // dense only: any instantiation (its tables go unused)
+    if (pl.has_rec) {
+      pm.k_main = mma_stage_bytes(pl.kc);
+      pm.v_main = mma_stage_bytes(pl.vc);
+    }
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
     if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;

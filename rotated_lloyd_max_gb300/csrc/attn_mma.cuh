@@ -28,10 +28,16 @@
 // A warp owns 32 of a record's 128 tokens (two m-tiles) end to end; records
 // are staged with cp.async in a two-deep ring, one CTA barrier per record;
 // the online softmax is warp-local (the running max moves only when a logit
-// passes it by 2^8).  Codecs with outlier side lists are not handled here:
-// their corrections are a latency-bound scatter (about 6 entries per token
-// and stream at T = 2) that the CUDA-core kernel overlaps with its FMA work at
-// twice this kernel's occupancy, so the host sends them there.
+// passes it by 2^8).
+// Outlier side lists (OUTL): a record is staged with its per-slot counts and
+// the first entries of its list (the rest, rarely any, are read from global
+// memory).  The MMAs score the centroids; a key entry (slot, j, value) then
+// adds (value - c[code_j]) q~_h[j] to the slot's scores before the softmax,
+// the four lanes of a quad taking every fourth entry of one token for all
+// heads and summing over the quad.  A value entry adds
+// (value - c[code_j]) 2^16 P'(slot, h) to a per-warp shared buffer over
+// (head, coordinate) in the accumulator's units (shared atomics), rescaled
+// with the accumulator and added to it before the merge.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -111,6 +117,35 @@ __device__ __forceinline__ uint32_t spread3(uint32_t x) {
   x = (x & 0x07070707u) | ((x << 1) & 0x70707070u);
   return x;
 }
+
+// Code of coordinate j of a packed row (BITS-bit fields, LSB-first); a 3-bit
+// field may straddle two words (the second read stays inside the staged record).
+template <int BITS>
+__device__ __forceinline__ uint32_t row_code(const unsigned char* row, int j) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
+  const int bit = j * BITS;
+  if constexpr (BITS == 3) return __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) & 7u;
+  else return (w[bit >> 5] >> (bit & 31)) & ((1u << BITS) - 1u);
+}
+
+// Side-list entries of the warp's 32 slots of a staged record (per-slot
+// counts at `counts`): lane l gets (offset of slot 32 w + l's first entry) << 8
+// | its count.
+__device__ __forceinline__ int slot_entries(const unsigned char* counts, int warp, int lane) {
+  const int c = counts[32 * warp + lane];
+  int pre = 0;
+  for (int s = lane; s < 32 * warp; s += 32) pre += counts[s];
+  const int base = (int)__reduce_add_sync(0xffffffffu, (unsigned)pre);
+  int inc = c;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, m);
+    if (lane >= m) inc += o;
+  }
+  return ((base + inc - c) << 8) | c;
+}
+
+constexpr int kMmaHeads = 8;  // query heads per CTA at most
 
 template <int D>
 struct MCfg {
@@ -390,8 +425,8 @@ __device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char*
   mma_split_merge<D>(p, mainb, wml, acc, 1.f, m0, m1, l0, l1, GT, qh0, split);
 }
 
-template <int D, int KB, int VB>
-__global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_constant__ AttnParams p) {
+template <int D, int KB, int VB, bool OUTL>
+__global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = MCfg<D>;
   constexpr int KS = C::KS, KR = C::KR, VR = C::VR;
   constexpr int KNB = KR * KB, VNB = VR * VB;
@@ -411,6 +446,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);  // [KS][32 lanes] (hi b0, hi b1, lo b0, lo b1)
   uint2* cent = reinterpret_cast<uint2*>(sm + p.sm_slot); // [32] (hi|lo f16) of K then V centroids x 2^16
   unsigned char* mainb = sm + p.sm_main;
+  // (OUTL) f32 centroids, K then V; value corrections [warp][head][D + 8]
+  float* kcf = reinterpret_cast<float*>(sm + p.sm_lut);
+  float* vcf = kcf + 16;
+  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);
+  constexpr int CST = D + 8;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -492,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
   // f16 halves of every centroid x 2^16: cent[i] = (hi, lo) of K centroid i,
   // cent[16 + i] of V centroid i
   if (tid < 32) {
+    if constexpr (OUTL) kcf[tid] = tid < 16 ? p.kc[tid] : p.vc[tid - 16];
     const float v = (tid < 16 ? p.kc[tid] : p.vc[tid - 16]) * 65536.f;
     const __half h = __float2half_rn(v);
     const __half r = __float2half_rn(v - __half2float(h));
@@ -558,6 +599,29 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
     for (int e = 0; e < 4; ++e) acc[mc][e] = 0.f;
   int kx = 127;  // P' f16 scale exponent of this warp (only ever decreases)
   const int rbk = D * KB / 8, rbv = D * VB / 8;
+  // (OUTL) the lane's part of the warp's value corrections: heads 2t, 2t + 1,
+  // coordinates (d/8) g + 2 mc (+1), as its accumulator fragments
+  const int GTe = (GT + 1) & ~1;
+  auto corr_at = [&](int e, int mc) -> float& {
+    return corr[(warp * GTe + 2 * t + (e & 1)) * CST + VR * g + 2 * mc + (e >> 1)];
+  };
+  const bool own_corr = OUTL && p.vout && 2 * t < GT;
+  if (own_corr) {
+#pragma unroll
+    for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) corr_at(e, mc) = 0.f;
+  }
+  auto corr_scale = [&](float f0, float f1) {
+    __syncwarp();
+    if (own_corr) {
+#pragma unroll
+      for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) corr_at(e, mc) *= (e & 1) ? f1 : f0;
+    }
+    __syncwarp();
+  };
 
   for (int i = 0; i < n; ++i) {
     cp_async_wait<0>();
@@ -611,6 +675,70 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
         sc[mt][1] = cc[mt][1] * fq1;
         sc[mt][2] = cc[mt][2] * fq0;
         sc[mt][3] = cc[mt][3] * fq1;
+      }
+    }
+    // ---- key side lists: sc (centroid scores, before the norm) += sum over
+    // the token's entries of (value - c[code_j]) q~_h[j].  The lane's four
+    // tokens g + 8 q advance together, one entry each per round (entries
+    // 4 r + t): predicated, no divergent loop.
+    if constexpr (OUTL) {
+      if (p.kout) {
+        const int oc_l = slot_entries(st + p.k_off_count, warp, lane);
+        const uint32_t* ent_s = reinterpret_cast<const uint32_t*>(st + p.k_off_ent);
+        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(krec_at(c_begin + i) + p.k_off_ent);
+        const int nse = (p.k_main - p.k_off_ent) >> 2;  // entries staged
+        const int last = __shfl_sync(0xffffffffu, oc_l, 31);
+        const bool staged = (last >> 8) + (last & 255) <= nse;  // the warp's entries all staged
+        int off[4], cnt[4], mx = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int oc = __shfl_sync(0xffffffffu, oc_l, g + 8 * q);
+          off[q] = oc >> 8;
+          cnt[q] = oc & 255;
+          mx = max(mx, cnt[q]);
+        }
+        const int rounds = ((int)__reduce_max_sync(0xffffffffu, (unsigned)mx) + 3) >> 2;
+        float dk[4][kMmaHeads];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int h = 0; h < kMmaHeads; ++h) dk[q][h] = 0.f;
+        for (int r = 0; r < rounds; ++r) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = 4 * r + t, idx = off[q] + k;
+            const bool ok = k < cnt[q] && idx < p.kcap;  // (a list longer than its capacity reads no further)
+            uint32_t e = ent_s[min(idx, nse - 1)];
+            if (!staged && ok && idx >= nse) e = __ldg(ent_g + idx);
+            const int j = (int)(e & (uint32_t)(D - 1));
+            const float cj = kcf[row_code<KB>(kcodes + (g + 8 * q) * rbk, j)];
+            const float delta = ok ? __uint_as_float(e & 0xFFFF0000u) - cj : 0.f;
+#pragma unroll
+            for (int h = 0; h < kMmaHeads; ++h)
+              if (h < GT) dk[q][h] = fmaf(delta, qf[qidx(h, j)], dk[q][h]);
+          }
+        }
+        // sums over the quad; the lane keeps its heads 2t, 2t + 1
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < kMmaHeads; h += 2) {
+            if (h < GT) {
+              float a = dk[q][h], c = dk[q][h + 1];
+              a += __shfl_xor_sync(0xffffffffu, a, 1);
+              c += __shfl_xor_sync(0xffffffffu, c, 1);
+              a += __shfl_xor_sync(0xffffffffu, a, 2);
+              c += __shfl_xor_sync(0xffffffffu, c, 2);
+              if (h == 2 * t) {
+                d0 = a;
+                d1 = c;
+              }
+            }
+          }
+          sc[q >> 1][2 * (q & 1)] += d0;
+          sc[q >> 1][2 * (q & 1) + 1] += d1;
+        }
       }
     }
     // logits (log2 domain)
@@ -675,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
           acc[mc][2] *= a0;
           acc[mc][3] *= a1;
         }
+        if constexpr (OUTL) corr_scale(a0, a1);
       }
     }
     // p, l, p' = p * n_v (unscaled), in place of the logits
@@ -701,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
           for (int mc = 0; mc < KS; ++mc)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mc][e] *= r;
+          if constexpr (OUTL) corr_scale(r, r);
           kx = kn;
         }
       }
@@ -743,18 +873,78 @@ __global__ void __launch_bounds__(kThreads, 4) attn_mma_kernel(const __grid_cons
         mma_f16(acc[mc], al, pb0h, pb1h);
       }
     }
+    // ---- value side lists: corr[h][j] += (value - c[code_j]) 2^16 P'(token, h),
+    // the lane's four tokens advancing together as for the keys
+    if constexpr (OUTL) {
+      if (p.vout) {
+        const int oc_l = slot_entries(vbase + p.v_off_count, warp, lane);
+        const uint32_t* ent_s = reinterpret_cast<const uint32_t*>(vbase + p.v_off_ent);
+        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(vrec_at(c_begin + i) + p.v_off_ent);
+        const int nse = (p.v_main - p.v_off_ent) >> 2;
+        const int last = __shfl_sync(0xffffffffu, oc_l, 31);
+        const bool staged = (last >> 8) + (last & 255) <= nse;
+        const float fsc = 65536.f * psc;
+        float* cw = corr + warp * GTe * CST;
+        int off[4], cnt[4], mx = 0;
+        float pv[4][kMmaHeads];  // P' of the lane's tokens for every head of the CTA, from the quad
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int oc = __shfl_sync(0xffffffffu, oc_l, g + 8 * q);
+          off[q] = oc >> 8;
+          cnt[q] = oc & 255;
+          mx = max(mx, cnt[q]);
+          const float own0 = sc[q >> 1][2 * (q & 1)] * fsc, own1 = sc[q >> 1][2 * (q & 1) + 1] * fsc;
+#pragma unroll
+          for (int u = 0; u < kMmaHeads / 2; ++u) {
+            if (2 * u < GT) {
+              pv[q][2 * u] = __shfl_sync(0xffffffffu, own0, (lane & ~3) | u);
+              pv[q][2 * u + 1] = __shfl_sync(0xffffffffu, own1, (lane & ~3) | u);
+            }
+          }
+        }
+        const int rounds = ((int)__reduce_max_sync(0xffffffffu, (unsigned)mx) + 3) >> 2;
+        for (int r = 0; r < rounds; ++r) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = 4 * r + t, idx = off[q] + k;
+            const bool ok = k < cnt[q] && idx < p.vcap;
+            uint32_t e = ent_s[min(idx, nse - 1)];
+            if (!staged && ok && idx >= nse) e = __ldg(ent_g + idx);
+            const int j = (int)(e & (uint32_t)(D - 1));
+            const float f = __uint_as_float(e & 0xFFFF0000u) - vcf[row_code<VB>(vcodes + (g + 8 * q) * rbv, j)];
+#pragma unroll
+            for (int h = 0; h < kMmaHeads; ++h)
+              if (h < GT && ok) atomicAdd(cw + h * CST + j, f * pv[q][h]);
+          }
+        }
+      }
+    }
+  }
+  if constexpr (OUTL) {
+    __syncwarp();
+    if (own_corr) {
+#pragma unroll
+      for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mc][e] += corr_at(e, mc);
+    }
   }
 
   mma_split_merge<D>(p, mainb, wml, acc, pow2i(-16 - kx), m0, m1, l0, l1, GT, qh0, split);
 }
 
+template <int D, int KB, int VB, bool OUTL>
+cudaError_t attn_mma_launch_o(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, KB, VB, OUTL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm_total);
+  if (e != cudaSuccess) return e;
+  attn_mma_kernel<D, KB, VB, OUTL><<<grid, kThreads, p.sm_total, s>>>(p);
+  return cudaGetLastError();
+}
 template <int D, int KB, int VB>
 cudaError_t attn_mma_launch_t(const AttnParams& p, dim3 grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       p.sm_total);
-  if (e != cudaSuccess) return e;
-  attn_mma_kernel<D, KB, VB><<<grid, kThreads, p.sm_total, s>>>(p);
-  return cudaGetLastError();
+  return (p.kout || p.vout) ? attn_mma_launch_o<D, KB, VB, true>(p, grid, s)
+                            : attn_mma_launch_o<D, KB, VB, false>(p, grid, s);
 }
 
 }  // namespace tq

@@ -28,13 +28,14 @@ def tq():
     return m
 
 
-@pytest.mark.parametrize("d,G,kb,vb,splits", [(128, 6, 3, 2, 2), (64, 4, 4, 3, 3), (128, 8, 4, 3, 0)])
-def test_sparse_v_matches_oracle_schedule(tq, orc, d, G, kb, vb, splits):
+@pytest.mark.parametrize("d,G,kb,vb,splits,T", [(128, 6, 3, 2, 2, 0.0), (64, 4, 4, 3, 3, 0.0), (128, 8, 4, 3, 0, 0.0),
+                                               (128, 4, 4, 3, 2, 2.0)])
+def test_sparse_v_matches_oracle_schedule(tq, orc, d, G, kb, vb, splits, T):
     import torch
     Hkv, R, tail, eps = 2, 12, 40, 2.0 ** -20
-    kc = tq.tq_make_codebook(kb, d, sign_seed=1)
-    vc = tq.tq_make_codebook(vb, d, sign_seed=1)
-    okc, ovc = orc.Codec(d=d, bits=kb), orc.Codec(d=d, bits=vb)
+    kc = tq.tq_make_codebook(kb, d, sign_seed=1, outlier_T=T)
+    vc = tq.tq_make_codebook(vb, d, sign_seed=1, outlier_T=T)
+    okc, ovc = orc.Codec(d=d, bits=kb, T=T), orc.Codec(d=d, bits=vb, T=T)
     ntok = R * 128
     qb = synth.gaussian_bf16((1, 1, G * Hkv, d), 5 + d, scale=2.0 / math.sqrt(d))
     q64 = synth.bf16_bits_to_f32(qb).astype(np.float64)[0, 0]
@@ -91,7 +92,7 @@ def test_sparse_v_matches_oracle_schedule(tq, orc, d, G, kb, vb, splits):
 def test_sparse_v_other_routes_are_unsupported(tq):
     import torch
     dev = "cuda"
-    for d, T, path in ((128, 2.0, 0), (256, 0.0, 0), (128, 0.0, 1)):
+    for d, T, path in ((128, 2.0, 1), (256, 0.0, 0), (128, 0.0, 1)):
         kc = tq.tq_make_codebook(3, d, sign_seed=1, outlier_T=T)
         rec = torch.zeros((1, 1, 1, 2, kc.record_bytes), dtype=torch.uint8, device=dev)
         q = torch.zeros((1, 1, 4, d), dtype=torch.bfloat16, device=dev)

@@ -110,12 +110,18 @@ def test_qwen2_plan(orc):
     assert (p["heads_per_cta"], p["launches"]) == (6, 2)
 
 
-def test_outlier_codecs_take_the_warp_local_kernel(orc):
+def test_outlier_codecs_take_the_warp_local_kernel_and_sparse_v_the_tensor_cores(orc):
+    """Side lists run on the warp-local CUDA-core kernel; with sparse-V on the
+    tensor-core kernel, whose corrections ride along beside its MMAs (its
+    shared memory fits two CTAs per SM for the batched cache's codecs)."""
     kc, vc = raw_codec(orc, 4, 128, T=2.0), raw_codec(orc, 3, 128, T=2.0)
     a = args_for(L=1, B=32, Hq=32, Hkv=8, d=128, records=256, tail=None, rec_bytes=8192)
     p = plan(a, kc, vc)
     assert p["compressed_kernel"] == "cuda_core_warp" and p["dense_kernel"] == "none"
     assert p["heads_per_cta"] == 4 and p["launches"] == 2
+    a.sparse_v_eps = 1e-3
+    p = plan(a, kc, vc)
+    assert p["compressed_kernel"] == "mma" and p["heads_per_cta"] == 4 and p["launches"] == 2
 
 
 def test_head_dim_256_runs_on_cuda_cores(orc):
