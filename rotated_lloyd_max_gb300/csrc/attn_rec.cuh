@@ -16,9 +16,11 @@
 //    logits), an online softmax whose running max only moves when a logit
 //    exceeds it by 2^8 (warp vote), and the value accumulation (a lane holds 4
 //    coordinates x GT heads in registers);
-//  * outlier entries are applied as deltas (stored value - centroid) through
-//    per-warp shared-memory atomics on the logits and on a value correction
-//    buffer;
+//  * outlier entries are applied as deltas (stored value - centroid): on the
+//    logits by the token's own lane, on the values through per-warp shared
+//    integer atomics in a fixed-point buffer (scaled per record by the warp's
+//    largest weight; integer adds retire about four times faster than f32
+//    ones), folded into the lanes' accumulators after each record;
 //  * at the end the 4 warps' (m, l, acc) are merged in shared memory into the
 //    split's partial.
 #pragma once
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   float* lutk = reinterpret_cast<float*>(sm + p.sm_lut);
   float* lutv = lutk + 16;
   float* pbuf = reinterpret_cast<float*>(sm + p.sm_logit);  // [4][32][GTP]
-  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);   // [4][GTP][D] (head-major: atomics on random coordinates spread over the banks)
+  int* corr = reinterpret_cast<int*>(sm + p.sm_corr);       // [4][GTP][D] fixed point (head-major: atomics on random coordinates spread over the banks)
   unsigned char* mainb = sm + p.sm_main;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     lutv[tid] = p.vc[tid];
   }
   if (vout)
-    for (int i = tid; i < 4 * D * GTP; i += kThreads) corr[i] = 0.f;
+    for (int i = tid; i < 4 * D * GTP; i += kThreads) corr[i] = 0;
 
   // per-warp state
   float m_w[GT], l_ln[GT];
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   const int tl = lane / LPT, g = lane % LPT;       // value phase
   const int tloc = q + QR * s;                     // the token whose logits this lane ends with
   float* pw = pbuf + warp * 32 * GTP;
-  float* cw = corr + warp * D * GTP;
+  int* cw = corr + warp * D * GTP;
   const int rbk = D * p.kb / 8, rbv = D * p.vb / 8;
 
   // Entry range of the lane's token in one stream's side list: a per-warp
@@ -496,11 +498,6 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
   #pragma unroll
             for (int cc = 0; cc < 4; ++cc) acc[cc][k] = mul2(acc[cc][k], a2);
           }
-          if (vout) {
-            for (int j = lane; j < D; j += 32)
-  #pragma unroll
-              for (int h = 0; h < GT; ++h) cw[h * D + j] *= al[h];
-          }
         }
         const float vn = vnorm[tloc];
   #pragma unroll
@@ -515,18 +512,45 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
 
       // ---- values
       if (vout) {
-        // the stored value replaces the centroid: acc_idx += p' (val - c[code])
+        // the stored value replaces the centroid: acc_idx += p' (val - c[code]),
+        // in fixed point S = 2^(23 - floor(log2 max p')): a term is below 2^25
+        // in magnitude (|val - c| < 2) and a (head, coordinate) takes at most
+        // one term per token, 32 per record, so a record's sums stay below 2^30
+        float pmx = 0.f;
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) pmx = fmaxf(pmx, pv[h]);
+        pmx = warp_max(pmx);
+        const int ef = min(254, max(1, 277 - (int)((__float_as_uint(pmx) >> 23) & 0xFFu)));
+        const float S = __uint_as_float((uint32_t)ef << 23), iS = __uint_as_float((uint32_t)(254 - ef) << 23);
         const unsigned char* vrow = vcodes + tloc * rbv;
         auto vfix = [&](uint32_t v) {
           const int idx = (int)(v & 0xFFFFu) & (D - 1);
-          const float delta = bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)];
+          const float delta = (bf16_to_f32((uint16_t)(v >> 16)) - lutv[code_in_row(vrow, idx, p.vb)]) * S;
   #pragma unroll
-          for (int h = 0; h < GT; ++h) atomicAdd(&cw[h * D + idx], pv[h] * delta);
+          for (int h = 0; h < GT; ++h) atomicAdd(&cw[h * D + idx], __float2int_rn(pv[h] * delta));
         };
   #pragma unroll
         for (int k = 0; k < 8; ++k)
           if (k < vec) vfix(vent[k]);
         for (int k = 8; k < vec; ++k) vfix(__ldg(vge + ve0 + k));
+        __syncwarp();
+        // fold the record's sums into the accumulators of the coordinates'
+        // owners (4 g .. 4 g + 3, every head) and clear them
+        if (tl == 0) {
+  #pragma unroll
+          for (int h = 0; h < GT; ++h) {
+            int4* cp = reinterpret_cast<int4*>(cw + h * D + 4 * g);
+            const int4 w = *cp;
+            *cp = make_int4(0, 0, 0, 0);
+            const float f[4] = {(float)w.x * iS, (float)w.y * iS, (float)w.z * iS, (float)w.w * iS};
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (h & 1) acc[c][h >> 1].y += f[c];
+              else acc[c][h >> 1].x += f[c];
+            }
+          }
+        }
+        __syncwarp();
       }
       switch (p.vb) {
         case 1: pv_tokens<1, GT, GTP, TLW>(vcodes, rbv, pw, lutv, g, tl, acc); break;
@@ -559,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(c
     for (int c = 0; c < 4; ++c)
 #pragma unroll
       for (int h = 0; h < GT; ++h) {
-        float v = (h & 1) ? acc[c][h >> 1].y : acc[c][h >> 1].x;
-        if (vout) v += cw[h * D + 4 * g + c];
+        const float v = (h & 1) ? acc[c][h >> 1].y : acc[c][h >> 1].x;
         red[(warp * D + 4 * g + c) * GTP + h] = v;
       }
   }
