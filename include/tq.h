@@ -135,7 +135,7 @@ tq_status tq_make_codebook(int bits, int head_dim, uint64_t sign_seed, float out
  * consecutive centroids, computed in double); every other field is kept.
  * The table must be strictly ascending and symmetric (c_k = -c_{2^b-1-k}),
  * with |c_k| < 0.999 (the tensor-core attention holds centroids x 2^16 in
- * f16), and for b >= 3 consecutive boundaries at least 1/128 apart (the
+ * f16), and for b >= 2 consecutive boundaries at least 1/128 apart (the
  * encoders decide codes through 1/128-wide cells holding one boundary each):
  * TQ_ERR_INVALID_ARG for an unordered or non-finite table, TQ_ERR_UNSUPPORTED
  * for one breaking the other conditions; the codec is unchanged on error.

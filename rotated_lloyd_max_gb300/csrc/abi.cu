@@ -33,14 +33,14 @@ int record_layout(int d, int bits, bool outl, int cap, int* off_norm, int* off_c
 
 // What the kernels need of any table: centroids below 0.999 in magnitude (the
 // tensor-core attention holds centroid x 2^16 as f16 hi/lo halves) and, at
-// b >= 3, consecutive boundaries at least one decision cell (1/128) apart with
+// b >= 2, consecutive boundaries at least one decision cell (1/128) apart with
 // every boundary inside (-1, 1) (the encoders' cell table holds one boundary
 // per cell of width 1/128 over |y| <= 1).
 tq_status table_supported(const float* cent, const float* bnd, int b) {
   const int K = 1 << b;
   for (int k = 0; k < K; ++k)
     if (!(std::fabs(cent[k]) < 0.999f)) return TQ_ERR_UNSUPPORTED;
-  if (b >= 3)
+  if (b >= 2)
     for (int k = 0; k + 1 < K; ++k) {
       if (!(std::fabs(bnd[k]) < 1.0f)) return TQ_ERR_UNSUPPORTED;
       if (k + 2 < K && (double)bnd[k + 1] - (double)bnd[k] < 1.0 / 128.0) return TQ_ERR_UNSUPPORTED;

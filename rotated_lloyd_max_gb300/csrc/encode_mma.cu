@@ -264,11 +264,10 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const unsign
 #pragma unroll
   for (int q = 0; q < B; ++q) wd[q] = 0u;
   omask = 0u;
-  // b <= 2 and the outlier test compare |x| against thresholds scaled once per
-  // vector (z = x * scale > t * 128  <=>  x > t * 128 / scale); a zero vector
-  // (scale 0) has x = 0 and takes the y = 0 codes against threshold 0
+  // the outlier test compares |x| against the threshold scaled once per
+  // vector (|z| = |x| scale > T 128  <=>  |x| > T 128 / scale); a zero vector
+  // (scale 0) has x = 0 and no outliers
   const float inv = scale > 0.f ? 1.0f / scale : 0.f;
-  const float Tx = B == 2 ? encm_cell(cells, (uint32_t)kPosCell << 7, cell_lane).x * inv : 0.f;
   const float Tox = OUTL ? (scale > 0.f ? thr_out * kCellScale * inv : INFINITY) : 0.f;
   uint32_t yw[4];
 #pragma unroll
@@ -280,14 +279,10 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const unsign
       if ((r & 7) == 6) srow[(r >> 3) ^ sw] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
     }
     uint32_t code[2];
-    if constexpr (B <= 2) {
-      // at most one positive boundary: compare directly (the mirror of the
-      // positive side, HALF - 1 for x <= 0)
+    if constexpr (B == 1) {
+      // the one boundary is 0: code 1 for x > 0
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint32_t m = B == 2 ? mask_gt(fabsf(x[r + k]), Tx) : 0u;
-        code[k] = ((uint32_t)(1 << (B - 1)) - m) ^ (mask_le(x[r + k], 0.f) & ((1u << B) - 1u));
-      }
+      for (int k = 0; k < 2; ++k) code[k] = 1u - (mask_le(x[r + k], 0.f) & 1u);
     } else {
       const float2 z = mul2(f2(x[r], x[r + 1]), f2(scale, scale));
       const float2 u = add2(z, f2(kCellMagicShifted, kCellMagicShifted));  // the shifted cell index x 128

@@ -174,7 +174,7 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[B], int r) {
   return (uint32_t)(v >> sh) & ((1u << B) - 1u);
 }
 
-// Decision cells (both encoders, b >= 3): with z = y * 128 (y the normalised rotated value, |y| <= 1)
+// Decision cells (the d-128 encoder at b >= 2, the CUDA-core encoder at b >= 3): with z = y * 128 (y the normalised rotated value, |y| <= 1)
 // and i = round(z) + 128, cell i covers z in [i - 128.5, i - 127.5) and
 // holds (count of boundaries below the cell, the boundary inside it x 128 or
 // +huge); boundaries are >= 1.4/128 apart for b <= 4 at every head dim up to
@@ -182,7 +182,6 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[B], int r) {
 // at most one.  |y| <= 1 keeps i in 0..256.  code = count + (z > boundary): the same code as
 // #{k : y > t_k} except within a couple of f32 ulp of a boundary.
 constexpr int kCells = 512;  // index masked to 9 bits: every value reads a cell (257.. = top cell's law)
-constexpr int kPosCell = 511;  // b = 2: .x holds the positive boundary x 128 (the cell is never indexed then)
 constexpr float kCellScale = 128.f;
 // z + 2^16 + 128.5 rounds to the 2^-7 grid, so that bits 7..15 of the sum are
 // floor of the rounded z + 128.5: the SHIFTED cell index, already times 128
@@ -208,7 +207,7 @@ __device__ __forceinline__ void build_cells(const CodecDev& c, float2* cells) {
       if (t < lo) ++below;
       else if (t < hi) inside = t * kCellScale;
     }
-    const float bnd = (i == kPosCell && c.bits == 2) ? c.boundaries[2] * kCellScale : inside;
+    const float bnd = inside;
     if constexpr (SPLIT) {
       float* bt = reinterpret_cast<float*>(cells);
       bt[i] = bnd;

@@ -1,4 +1,4 @@
-"""The encoders' decision-cell quantiser (3- and 4-bit codes).  With z = 128 y
+"""The encoders' decision-cell quantiser (2-, 3- and 4-bit codes).  With z = 128 y
 (y the normalised rotated coordinate, |y| <= 1) and cell i = rint(z) + 128
 covering z in [i - 128.5, i - 127.5), each cell keeps the count of Lloyd-Max
 boundaries below it and the boundary inside it (if any); the code is
@@ -44,7 +44,7 @@ def cell_index(z, shifted):
 
 @pytest.mark.parametrize("shifted", [False, True])
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_cells_hold_at_most_one_boundary_and_give_the_count(orc, d, bits, shifted):
     t = orc.codebook_f32(bits, d)[1].astype(np.float32)
     below, inside = cell_table(t, shifted)
