@@ -36,8 +36,9 @@
 // the four lanes of a quad taking every fourth entry of one token for all
 // heads and summing over the quad.  A value entry adds
 // (value - c[code_j]) 2^16 P'(slot, h) to a per-warp shared buffer over
-// (head, coordinate) in the accumulator's units (shared atomics), rescaled
-// with the accumulator and added to it before the merge.
+// (head, coordinate) in the accumulator's units, in fixed point through
+// shared integer atomics, which the owning lanes fold into their
+// accumulator fragments after each record.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
   // (OUTL) f32 centroids, K then V; value corrections [warp][head][D + 8]
   float* kcf = reinterpret_cast<float*>(sm + p.sm_lut);
   float* vcf = kcf + 16;
-  float* corr = reinterpret_cast<float*>(sm + p.sm_corr);
+  int* corr = reinterpret_cast<int*>(sm + p.sm_corr);
   constexpr int CST = D + 8;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -599,10 +600,11 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     for (int e = 0; e < 4; ++e) acc[mc][e] = 0.f;
   int kx = 127;  // P' f16 scale exponent of this warp (only ever decreases)
   const int rbk = D * KB / 8, rbv = D * VB / 8;
-  // (OUTL) the lane's part of the warp's value corrections: heads 2t, 2t + 1,
-  // coordinates (d/8) g + 2 mc (+1), as its accumulator fragments
+  // (OUTL) the lane's part of the warp's value corrections (fixed point, one
+  // record at a time): heads 2t, 2t + 1, coordinates (d/8) g + 2 mc (+1), as
+  // its accumulator fragments
   const int GTe = (GT + 1) & ~1;
-  auto corr_at = [&](int e, int mc) -> float& {
+  auto corr_at = [&](int e, int mc) -> int& {
     return corr[(warp * GTe + 2 * t + (e & 1)) * CST + VR * g + 2 * mc + (e >> 1)];
   };
   const bool own_corr = OUTL && p.vout && 2 * t < GT;
@@ -610,18 +612,8 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
 #pragma unroll
     for (int mc = 0; mc < KS; ++mc)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) corr_at(e, mc) = 0.f;
+      for (int e = 0; e < 4; ++e) corr_at(e, mc) = 0;
   }
-  auto corr_scale = [&](float f0, float f1) {
-    __syncwarp();
-    if (own_corr) {
-#pragma unroll
-      for (int mc = 0; mc < KS; ++mc)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) corr_at(e, mc) *= (e & 1) ? f1 : f0;
-    }
-    __syncwarp();
-  };
 
   for (int i = 0; i < n; ++i) {
     cp_async_wait<0>();
@@ -803,7 +795,6 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
           acc[mc][2] *= a0;
           acc[mc][3] *= a1;
         }
-        if constexpr (OUTL) corr_scale(a0, a1);
       }
     }
     // p, l, p' = p * n_v (unscaled), in place of the logits
@@ -830,7 +821,6 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
           for (int mc = 0; mc < KS; ++mc)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mc][e] *= r;
-          if constexpr (OUTL) corr_scale(r, r);
           kx = kn;
         }
       }
@@ -874,7 +864,12 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       }
     }
     // ---- value side lists: corr[h][j] += (value - c[code_j]) 2^16 P'(token, h),
-    // the lane's four tokens advancing together as for the keys
+    // the lane's four tokens advancing together as for the keys; in fixed
+    // point S = 2^(23 - floor(log2 max 2^16 P')) (shared integer atomics
+    // retire about four times faster than f32 ones): a term is below 2^25 in
+    // magnitude (|value - c| < 2) and a (head, coordinate) takes at most one
+    // term per token, so a record's sums stay below 2^30; the owners fold
+    // them into their accumulators after the record
     if constexpr (OUTL) {
       if (p.vout) {
         const int oc_l = slot_entries(vbase + p.v_off_count, warp, lane);
@@ -883,8 +878,13 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
         const int nse = (p.v_main - p.v_off_ent) >> 2;
         const int last = __shfl_sync(0xffffffffu, oc_l, 31);
         const bool staged = (last >> 8) + (last & 255) <= nse;
-        const float fsc = 65536.f * psc;
-        float* cw = corr + warp * GTe * CST;
+        float pmx = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
+                          fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
+        pmx = warp_max(pmx * (65536.f * psc));
+        const int ef = min(254, max(1, 277 - (int)((__float_as_uint(pmx) >> 23) & 0xFFu)));
+        const float S = __uint_as_float((uint32_t)ef << 23), iS = __uint_as_float((uint32_t)(254 - ef) << 23);
+        const float fsc = 65536.f * psc * S;
+        int* cw = corr + warp * GTe * CST;
         int off[4], cnt[4], mx = 0;
         float pv[4][kMmaHeads];  // P' of the lane's tokens for every head of the CTA, from the quad
 #pragma unroll
@@ -914,19 +914,22 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
             const float f = __uint_as_float(e & 0xFFFF0000u) - vcf[row_code<VB>(vcodes + (g + 8 * q) * rbv, j)];
 #pragma unroll
             for (int h = 0; h < kMmaHeads; ++h)
-              if (h < GT && ok) atomicAdd(cw + h * CST + j, f * pv[q][h]);
+              if (h < GT && ok) atomicAdd(cw + h * CST + j, __float2int_rn(f * pv[q][h]));
           }
         }
+        __syncwarp();
+        if (own_corr) {
+#pragma unroll
+          for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              int& v = corr_at(e, mc);
+              acc[mc][e] = fmaf((float)v, iS, acc[mc][e]);
+              v = 0;
+            }
+        }
+        __syncwarp();
       }
-    }
-  }
-  if constexpr (OUTL) {
-    __syncwarp();
-    if (own_corr) {
-#pragma unroll
-      for (int mc = 0; mc < KS; ++mc)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mc][e] += corr_at(e, mc);
     }
   }
 
