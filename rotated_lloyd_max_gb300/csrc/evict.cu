@@ -6,11 +6,18 @@
 
 namespace tq {
 
-// Eviction: CTA (e, b*Hkv + h, l) encodes the e-th due chunk of stream (l, b, h).
+constexpr int kEvictParts = 4;  // CTAs per chunk without outlier lists (32 slots each)
+
+// Eviction: CTA (e * parts + part, b*Hkv + h, l) encodes part `part` of the
+// e-th due chunk of stream (l, b, h).  Without outlier lists the chunk's slots
+// are independent and a chunk is split over parts = gridDim.x / max_evict
+// CTAs (a single chunk per stream is otherwise a few latency-bound CTAs);
+// with them one CTA keeps the chunk, whose entries it orders.
 template <int D, int B, bool OUTL, bool SCALE>
 __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__ EvictParams p) {
   __shared__ EncSmem sm;
-  const int e = blockIdx.x;
+  const int parts = gridDim.x / p.max_evict;
+  const int e = blockIdx.x / parts, part = blockIdx.x % parts;
   const int h = blockIdx.y % p.Hkv, b = blockIdx.y / p.Hkv, l = blockIdx.z;
   const int lb = l * p.B + b;
   const int len = p.tail_len[lb], nch = p.n_chunks[lb];
@@ -30,7 +37,8 @@ __global__ void __launch_bounds__(kThreads) evict_kernel(const __grid_constant__
   const int first = start + e * kChunk;
   const int cap = p.tail_cap;
   auto row = [&](int slot) { return tail + (int64_t)((first + min(slot, kChunk - 1)) % cap) * D; };
-  encode_record<D, B, OUTL, SCALE>(p.c, cells, cent, tb, row, rec, 0, kChunk, &sm);
+  const int per = kChunk / parts;
+  encode_record<D, B, OUTL, SCALE>(p.c, cells, cent, tb, row, rec, part * per, part * per + per, &sm);
 }
 
 __global__ void evict_commit_kernel(const EvictCommitParams p) {
@@ -47,7 +55,7 @@ __global__ void evict_commit_kernel(const EvictCommitParams p) {
 
 template <int D, int B, bool OUTL>
 static cudaError_t ev_launch(const EvictParams& p, cudaStream_t s) {
-  dim3 grid(p.max_evict, p.B * p.Hkv, p.L);
+  dim3 grid(p.max_evict * (OUTL ? 1 : kEvictParts), p.B * p.Hkv, p.L);
   if (p.c.scale_mode != TQ_SCALE_NORM) evict_kernel<D, B, OUTL, true><<<grid, kThreads, 0, s>>>(p);
   else evict_kernel<D, B, OUTL, false><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
