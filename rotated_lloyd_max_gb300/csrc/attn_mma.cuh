@@ -561,10 +561,18 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
 
   // ---- query fragments: head g, coordinates (d/4) t + 4 kk + {0,1} / {2,3},
   // scaled by 2^s_g so that the largest |q~| of the head is in [2^13, 2^14);
-  // stored per lane in shared memory (read once per k-step for both m-tiles)
-  float fq0, fq1;  // 2^-(s_h + 16) for the lane's score heads 2t, 2t+1
+  // stored per lane in shared memory (read once per k-step for both m-tiles).
+  // Packed (at most 4 heads per CTA): column g < 4 holds the hi part of head
+  // g and column g + 4 its lo part, so that one MMA forms hi.hi and hi.lo
+  // (and a second lo.hi and lo.lo): two MMAs per product instead of three,
+  // the halves summed across lanes t and t ^ 2; a lane's heads are then
+  // 2 (t & 1), 2 (t & 1) + 1.
+  const bool pk = GT <= 4;
+  const int th = pk ? (t & 1) : t;  // the lane's head pair in the score fragments
+  float fq0, fq1;  // 2^-(s_h + 16) for the lane's score heads 2th, 2th+1
   {
-    const float* qrow = qf + qidx(g, KR * t);
+    const int hq = pk ? (g & 3) : g;
+    const float* qrow = qf + qidx(hq, KR * t);
     float mx = 0.f;
 #pragma unroll
     for (int j = 0; j < KR; ++j) mx = fmaxf(mx, fabsf(qrow[j]));
@@ -576,14 +584,18 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       uint4 f;
       split_f16x2(qrow[4 * kk] * sc, qrow[4 * kk + 1] * sc, f.x, f.z);
       split_f16x2(qrow[4 * kk + 2] * sc, qrow[4 * kk + 3] * sc, f.y, f.w);
+      if (pk && g >= 4) {
+        f.x = f.z;
+        f.y = f.w;
+      }
       qfrag[kk * 32 + lane] = f;
     }
-    const int s0 = __shfl_sync(0xffffffffu, s, 4 * (2 * t));
-    const int s1 = __shfl_sync(0xffffffffu, s, 4 * (2 * t + 1));
+    const int s0 = __shfl_sync(0xffffffffu, s, 4 * (2 * th));
+    const int s1 = __shfl_sync(0xffffffffu, s, 4 * (2 * th + 1));
     fq0 = pow2i(-s0 - 16);
     fq1 = pow2i(-s1 - 16);
   }
-  const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
+  const bool hv0 = 2 * th < GT, hv1 = 2 * th + 1 < GT;
   const uint32_t loff = (lane & 15) * 8;
   auto kpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + KP_OFF + o); };
   auto vpair_at = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(sm + VP_OFF + o); };
@@ -653,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
             al[2 * hf + 1] = e1.y;
           }
           mma_f16(cc[mt], ah, f.x, f.y);
-          mma_f16(cl[mt], ah, f.z, f.w);
+          if (!pk) mma_f16(cl[mt], ah, f.z, f.w);
           mma_f16(ch[mt], al, f.x, f.y);
         }
       }
@@ -661,6 +673,12 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) cc[mt][e] += cl[mt][e] + ch[mt][e];
+      if (pk) {  // q~ hi columns (t < 2) plus lo columns (t >= 2)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cc[mt][e] += __shfl_xor_sync(0xffffffffu, cc[mt][e], 2);
+      }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         sc[mt][0] = cc[mt][0] * fq0;
@@ -722,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
               c += __shfl_xor_sync(0xffffffffu, c, 1);
               a += __shfl_xor_sync(0xffffffffu, a, 2);
               c += __shfl_xor_sync(0xffffffffu, c, 2);
-              if (h == 2 * t) {
+              if (h == 2 * th) {
                 d0 = a;
                 d1 = c;
               }
@@ -830,15 +848,21 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     // ---- values: k-step mt = the 16 tokens of score tile mt
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      uint32_t th, tl, bhw, blw;  // (p' hi / lo) of tokens g (top) and g + 8 (bottom)
-      split_f16x2(sc[mt][0] * psc, sc[mt][1] * psc, th, tl);
+      uint32_t thw, tlw, bhw, blw;  // (p' hi / lo) of tokens g (top) and g + 8 (bottom)
+      split_f16x2(sc[mt][0] * psc, sc[mt][1] * psc, thw, tlw);
       split_f16x2(sc[mt][2] * psc, sc[mt][3] * psc, bhw, blw);
-      const int sa = 4 * (2 * t) + (g >> 1), sb = sa + 4;
-      const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-      const uint32_t pb0h = __byte_perm(__shfl_sync(0xffffffffu, th, sa), __shfl_sync(0xffffffffu, th, sb), sel);
-      const uint32_t pb0l = __byte_perm(__shfl_sync(0xffffffffu, tl, sa), __shfl_sync(0xffffffffu, tl, sb), sel);
-      const uint32_t pb1h = __byte_perm(__shfl_sync(0xffffffffu, bhw, sa), __shfl_sync(0xffffffffu, bhw, sb), sel);
+      // column g of P'^T: head g, or packed head g & 3, hi for g < 4 and lo beyond
+      const int hb = pk ? (g & 3) : g;
+      const int sa = 4 * (2 * t) + (hb >> 1), sb = sa + 4;
+      const uint32_t sel = (hb & 1) ? 0x7632u : 0x5410u;
+      uint32_t pb0h = __byte_perm(__shfl_sync(0xffffffffu, thw, sa), __shfl_sync(0xffffffffu, thw, sb), sel);
+      const uint32_t pb0l = __byte_perm(__shfl_sync(0xffffffffu, tlw, sa), __shfl_sync(0xffffffffu, tlw, sb), sel);
+      uint32_t pb1h = __byte_perm(__shfl_sync(0xffffffffu, bhw, sa), __shfl_sync(0xffffffffu, bhw, sb), sel);
       const uint32_t pb1l = __byte_perm(__shfl_sync(0xffffffffu, blw, sa), __shfl_sync(0xffffffffu, blw, sb), sel);
+      if (pk && g >= 4) {
+        pb0h = pb0l;
+        pb1h = pb1l;
+      }
       // value runs of tokens 2t, 2t+1 (k columns 2t, 2t+1) and 2t+8, 2t+9
       uint32_t r0[VNW], r1[VNW], r2[VNW], r3[VNW];
       const unsigned char* vt = vcodes + 16 * mt * rbv;
@@ -859,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
         const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x};
         const uint32_t al[4] = {e0.y, e1.y, e2.y, e3.y};
         mma_f16(acc[mc], ah, pb0h, pb1h);
-        mma_f16(acc[mc], ah, pb0l, pb1l);
+        if (!pk) mma_f16(acc[mc], ah, pb0l, pb1l);
         mma_f16(acc[mc], al, pb0h, pb1h);
       }
     }
@@ -933,6 +957,12 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     }
   }
 
+  if (pk) {  // P' hi columns (t < 2) plus lo columns (t >= 2)
+#pragma unroll
+    for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mc][e] += __shfl_xor_sync(0xffffffffu, acc[mc][e], 2);
+  }
   mma_split_merge<D>(p, mainb, wml, acc, pow2i(-16 - kx), m0, m1, l0, l1, GT, qh0, split);
 }
 
