@@ -44,6 +44,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "attn.cuh"
 
 namespace tq {
@@ -648,27 +650,33 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       float cl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       float ch[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // the k loop specialised on packing (a uniform branch, not predicated MMAs)
+      auto score_mmas = [&](auto pkc) {
+        constexpr bool P = decltype(pkc)::value;
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const uint4 f = qfrag[kk * 32 + lane];
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint4 f = qfrag[kk * 32 + lane];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          uint32_t ah[4], al[4];
+          for (int mt = 0; mt < 2; ++mt) {
+            uint32_t ah[4], al[4];
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int off = (4 * kk + 2 * hf) * KB;
-            const uint2 e0 = kpair_at(pair_off(w[2 * mt], off, 2 * KB, loff));
-            const uint2 e1 = kpair_at(pair_off(w[2 * mt + 1], off, 2 * KB, loff));
-            ah[2 * hf] = e0.x;
-            al[2 * hf] = e0.y;
-            ah[2 * hf + 1] = e1.x;
-            al[2 * hf + 1] = e1.y;
+            for (int hf = 0; hf < 2; ++hf) {
+              const int off = (4 * kk + 2 * hf) * KB;
+              const uint2 e0 = kpair_at(pair_off(w[2 * mt], off, 2 * KB, loff));
+              const uint2 e1 = kpair_at(pair_off(w[2 * mt + 1], off, 2 * KB, loff));
+              ah[2 * hf] = e0.x;
+              al[2 * hf] = e0.y;
+              ah[2 * hf + 1] = e1.x;
+              al[2 * hf + 1] = e1.y;
+            }
+            mma_f16(cc[mt], ah, f.x, f.y);
+            if constexpr (!P) mma_f16(cl[mt], ah, f.z, f.w);
+            mma_f16(ch[mt], al, f.x, f.y);
           }
-          mma_f16(cc[mt], ah, f.x, f.y);
-          if (!pk) mma_f16(cl[mt], ah, f.z, f.w);
-          mma_f16(ch[mt], al, f.x, f.y);
         }
-      }
+      };
+      if (pk) score_mmas(std::true_type{});
+      else score_mmas(std::false_type{});
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -873,19 +881,24 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       uint32_t ze01[ZW], zo01[ZW], ze23[ZW], zo23[ZW];
       v_pair_words<VB, VNW>(r0, r1, ze01, zo01);
       v_pair_words<VB, VNW>(r2, r3, ze23, zo23);
+      auto value_mmas = [&](auto pkc) {
+        constexpr bool P = decltype(pkc)::value;
 #pragma unroll
-      for (int mc = 0; mc < KS; ++mc) {
-        const int off = mc * 2 * FW;
-        const uint2 e0 = vpair_at(pair_off(ze01, off, 2 * FW, loff));
-        const uint2 e1 = vpair_at(pair_off(zo01, off, 2 * FW, loff));
-        const uint2 e2 = vpair_at(pair_off(ze23, off, 2 * FW, loff));
-        const uint2 e3 = vpair_at(pair_off(zo23, off, 2 * FW, loff));
-        const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x};
-        const uint32_t al[4] = {e0.y, e1.y, e2.y, e3.y};
-        mma_f16(acc[mc], ah, pb0h, pb1h);
-        if (!pk) mma_f16(acc[mc], ah, pb0l, pb1l);
-        mma_f16(acc[mc], al, pb0h, pb1h);
-      }
+        for (int mc = 0; mc < KS; ++mc) {
+          const int off = mc * 2 * FW;
+          const uint2 e0 = vpair_at(pair_off(ze01, off, 2 * FW, loff));
+          const uint2 e1 = vpair_at(pair_off(zo01, off, 2 * FW, loff));
+          const uint2 e2 = vpair_at(pair_off(ze23, off, 2 * FW, loff));
+          const uint2 e3 = vpair_at(pair_off(zo23, off, 2 * FW, loff));
+          const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x};
+          const uint32_t al[4] = {e0.y, e1.y, e2.y, e3.y};
+          mma_f16(acc[mc], ah, pb0h, pb1h);
+          if constexpr (!P) mma_f16(acc[mc], ah, pb0l, pb1l);
+          mma_f16(acc[mc], al, pb0h, pb1h);
+        }
+      };
+      if (pk) value_mmas(std::true_type{});
+      else value_mmas(std::false_type{});
     }
     // ---- value side lists: corr[h][j] += (value - c[code_j]) 2^16 P'(token, h),
     // the lane's four tokens advancing together as for the keys; in fixed
