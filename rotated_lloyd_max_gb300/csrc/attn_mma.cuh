@@ -320,11 +320,7 @@ __device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char*
     }
   }
   const bool hv0 = 2 * t < GT, hv1 = 2 * t + 1 < GT;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  // sparse-V: exact running maxima of the lane's two heads over the warp's
-  // earlier 32-token blocks of this split (the lazy m0/m1 may trail them)
-  float tm0 = -INFINITY, tm1 = -INFINITY;
-  const bool sparse_v = p.sv_log2eps < 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // (dense tokens are never skipped by sparse-V)
   float acc[KS][4];
 #pragma unroll
   for (int mc = 0; mc < KS; ++mc)
