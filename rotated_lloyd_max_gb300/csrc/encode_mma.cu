@@ -217,17 +217,20 @@ __device__ __forceinline__ void encm_transform(const EncMLane<B>& ln, const uint
       }
 }
 
-constexpr int kEncWarps = 16;
+constexpr int kEncWarps = 16;                   // warps per CTA at most (one CTA per SM)
+constexpr int kEncWarpsSmall = 4;               // small encodes: two CTAs fit one SM
 constexpr int kEncThreads = 32 * kEncWarps;
 constexpr int kCellCopies = 16;
 
 // Shared memory of both kernels: the replicated decision cells (cell i, copy
-// j at float2 index 16 i + j), two tile buffers per warp, the centroids.
+// j at float2 index 16 i + j), the centroids, then two tile buffers per warp
+// (as many warps as the launch has).
 struct EncSmem {
   float2 cells[kCells * kCellCopies];
-  EncTile tiles[kEncWarps][2];
-  float cent[16];
+  float cent[32];
+  EncTile tiles[1][2];  // [warps][2] in the launch's dynamic shared memory
 };
+constexpr int enc_smem_bytes(int warps) { return (int)(sizeof(EncSmem) + (warps - 1) * 2 * sizeof(EncTile)); }
 
 // Cell (i128 >> 7) & 511 as seen by a lane (its copy: bank pair lane % 16);
 // i128 is the cell index times 128 in bits 7..15 (other bits ignored).
@@ -243,7 +246,7 @@ __device__ __forceinline__ void encm_build(const CodecDev& c, EncSmem& sm) {
   if (threadIdx.x < kThreads) build_cells<false, true>(c, plain);
   if (threadIdx.x < 16) sm.cent[threadIdx.x] = c.centroids[threadIdx.x];
   __syncthreads();
-  for (int i = threadIdx.x; i < kCells * kCellCopies; i += kEncThreads) sm.cells[i] = plain[i / kCellCopies];
+  for (int i = threadIdx.x; i < kCells * kCellCopies; i += blockDim.x) sm.cells[i] = plain[i / kCellCopies];
   __syncthreads();
 }
 
@@ -347,7 +350,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_mma_kernel(const __grid
   encm_build(p.c, sm);
   const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
   const float* cent = sm.cent;
-  auto& tiles = sm.tiles;
+  EncTile (*tiles)[2] = sm.tiles;
+  const int W = blockDim.x >> 5;  // warps in this CTA
   const EncMLane<B> ln(p.c);
   const int64_t per_group = p.chunks_per_group * 8;
   const int64_t n_tasks = p.n_groups * per_group;
@@ -383,8 +387,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_mma_kernel(const __grid
                src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs, k.vb);
     cp_async_commit();
   };
-  const int64_t stride = (int64_t)gridDim.x * kEncWarps;
-  int64_t task = (int64_t)blockIdx.x * kEncWarps + ln.warp;
+  const int64_t stride = (int64_t)gridDim.x * W;
+  int64_t task = (int64_t)blockIdx.x * W + ln.warp;
   Task cur = locate(task);
   issue(cur, 0);
   for (int it = 0; task < n_tasks; task += stride, ++it) {
@@ -437,18 +441,19 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_mma_outl_kernel(const _
   encm_build(p.c, sm);
   const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
   const float* cent = sm.cent;
-  auto& tiles = sm.tiles;
+  EncTile (*tiles)[2] = sm.tiles;
+  const int W = blockDim.x >> 5;  // warps in this CTA
   const EncMLane<B> ln(p.c);
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
   const int64_t v_end = p.first_vec + p.n_vec;
-  const int64_t warps = (int64_t)gridDim.x * kEncWarps;
+  const int64_t warps = (int64_t)gridDim.x * W;
   // unit u of this warp: record task warp_id + (u / 8) * warps, tile u % 8
   struct Unit {
     int64_t task, grp, chunk, ta, tb;
     int tile, slot_a, slot_b;
     bool va, vb;
   };
-  const int64_t wid = (int64_t)blockIdx.x * kEncWarps + ln.warp;
+  const int64_t wid = (int64_t)blockIdx.x * W + ln.warp;
   auto locate = [&](int64_t u) {
     Unit k;
     k.task = wid + (u >> 3) * warps;
@@ -577,21 +582,28 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_mma_outl_kernel(const _
 
 // `grid` is 8 CTAs per SM; these kernels run one 16-warp CTA per SM (all of
 // its registers and most of its shared memory), so one wave (grid / 8) of
-// persistent CTAs, whose warps then prefetch their next task.
+// persistent CTAs, whose warps then prefetch their next task.  An encode of
+// fewer than 4 tile tasks per such warp runs 4-warp CTAs instead (96 KB), so
+// that another encode on a concurrent stream (a small cache's K and V) shares
+// the SMs rather than waiting for them.
 template <int B, bool SCALE>
 static cudaError_t encm_launch(const EncodeParams& p, int grid, cudaStream_t s) {
   grid = std::max(1, grid / 8);
-  const int smem = (int)sizeof(EncSmem);
+  const int64_t tiles = p.n_groups * p.chunks_per_group * 8;
+  const int W = tiles < 4LL * kEncWarps * grid ? kEncWarpsSmall : kEncWarps;
+  const int smem = enc_smem_bytes(W);
   if (p.c.has_outl) {
-    const int64_t tasks = (p.n_groups * p.chunks_per_group + kEncWarps - 1) / kEncWarps;  // a warp per record
-    cudaError_t e = cudaFuncSetAttribute(encode_mma_outl_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int64_t tasks = (p.n_groups * p.chunks_per_group + W - 1) / W;  // a warp per record
+    cudaError_t e = cudaFuncSetAttribute(encode_mma_outl_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         enc_smem_bytes(kEncWarps));
     if (e != cudaSuccess) return e;
-    encode_mma_outl_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kEncThreads, smem, s>>>(p);
+    encode_mma_outl_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), 32 * W, smem, s>>>(p);
   } else {
-    const int64_t tasks = (p.n_groups * p.chunks_per_group * 8 + kEncWarps - 1) / kEncWarps;
-    cudaError_t e = cudaFuncSetAttribute(encode_mma_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int64_t tasks = (tiles + W - 1) / W;
+    cudaError_t e = cudaFuncSetAttribute(encode_mma_kernel<B, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         enc_smem_bytes(kEncWarps));
     if (e != cudaSuccess) return e;
-    encode_mma_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), kEncThreads, smem, s>>>(p);
+    encode_mma_kernel<B, SCALE><<<(int)std::min<int64_t>(tasks, grid), 32 * W, smem, s>>>(p);
   }
   return cudaGetLastError();
 }
