@@ -342,7 +342,7 @@ typedef struct {
   int32_t heads_per_cta;          /* query heads per CTA of the compressed splits */
   int32_t dense_heads_per_cta;    /* query heads per CTA of the dense splits */
   int32_t launches;               /* kernel launches of the call, the merge included */
-  int32_t reserved;
+  int32_t warps_per_cta;          /* warps per CTA of the compressed splits */
   uint64_t workspace_bytes;       /* = tq_decode_attn_workspace_size */
 } tq_attn_plan;
 

@@ -305,23 +305,27 @@ def attention_sparse_v(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float
     return out, int(sk[0])
 
 
-def sparse_v_blocks(n_records: int, records_per_split: int, warps: int = 4):
+def sparse_v_blocks(n_records: int, records_per_split: int, warps: int = 4, groups: int = 1):
     """The blocks of the tensor-core decode kernel's schedule: split s covers
-    records [s cps, (s+1) cps); within it, warp w visits the tokens
-    [128 r + 32 w, 128 r + 32 w + 32) of its records in order, sharing one
-    running maximum (a sequence per (split, warp))."""
+    records [s cps, (s+1) cps); a CTA of `groups` 4-warp groups deals them out
+    round robin (group g takes records s cps + g, s cps + g + groups, ...);
+    within a group, warp w visits the tokens [128 r + 32 w, 128 r + 32 w + 32)
+    of its records in order, sharing one running maximum (a sequence per
+    (split, group, warp))."""
     blocks = []
     span = 128 // warps
     n_split = (n_records + records_per_split - 1) // records_per_split if n_records else 0
     for s_ in range(n_split):
-        for w in range(warps):
-            for r in range(s_ * records_per_split, min((s_ + 1) * records_per_split, n_records)):
-                blocks.append((128 * r + span * w, 128 * r + span * (w + 1), s_ * warps + w))
+        end = min((s_ + 1) * records_per_split, n_records)
+        for g in range(groups):
+            for w in range(warps):
+                for r in range(s_ * records_per_split + g, end, groups):
+                    blocks.append((128 * r + span * w, 128 * r + span * (w + 1), (s_ * groups + g) * warps + w))
     return blocks
 
 
 def unit_attention_sparse_v(q_bf16, codec_k: Codec, codec_v: Codec, k_rec, v_rec, n_comp, k_dense_bf16,
-                            v_dense_bf16, scale, eps, records_per_split, heads_per_cta, softcap=0.0):
+                            v_dense_bf16, scale, eps, records_per_split, heads_per_cta, softcap=0.0, groups=1):
     """unit_attention with sparse-V skipping over the compressed tokens, on the
     tensor-core kernel's schedule (sparse_v_blocks); dense tokens are never
     skipped.  Returns (out, skipped (group, token) pairs)."""
@@ -331,7 +335,7 @@ def unit_attention_sparse_v(q_bf16, codec_k: Codec, codec_v: Codec, k_rec, v_rec
     if k_dense_bf16 is not None and len(k_dense_bf16):
         Ks.append(bf16_to_f64(k_dense_bf16).reshape(-1, d))
         Vs.append(bf16_to_f64(v_dense_bf16).reshape(-1, d))
-    blocks = sparse_v_blocks(n_comp // 128, records_per_split)
+    blocks = sparse_v_blocks(n_comp // 128, records_per_split, groups=groups)
     return attention_sparse_v(q, np.concatenate(Ks), np.concatenate(Vs), scale, eps, heads_per_cta, blocks, softcap)
 
 

@@ -55,7 +55,7 @@ class tq_attn_plan(ctypes.Structure):
     _fields_ = [("compressed_kernel", c_i32), ("dense_kernel", c_i32), ("compressed_splits", c_i32),
                 ("dense_splits", c_i32), ("records_per_split", c_i32), ("dense_tokens_per_split", c_i32),
                 ("heads_per_cta", c_i32), ("dense_heads_per_cta", c_i32), ("launches", c_i32),
-                ("reserved", c_i32), ("workspace_bytes", c_u64)]
+                ("warps_per_cta", c_i32), ("workspace_bytes", c_u64)]
 
 
 ATTN_KERNELS = {0: "none", 1: "cuda_core", 2: "cuda_core_warp", 3: "mma", 4: "mma512", 5: "tcgen05"}
@@ -330,7 +330,7 @@ def tq_decode_attn_plan(args: tq_attn_args, k_codec, v_codec) -> dict:
     p = tq_attn_plan()
     _check("tq_decode_attn_plan", load().tq_decode_attn_plan(ctypes.byref(args), raw(k_codec), raw(v_codec),
                                                              ctypes.byref(p)))
-    d = {f: getattr(p, f) for f, _ in tq_attn_plan._fields_ if f != "reserved"}
+    d = {f: getattr(p, f) for f, _ in tq_attn_plan._fields_}
     d["compressed_kernel"] = ATTN_KERNELS[d["compressed_kernel"]]
     d["dense_kernel"] = ATTN_KERNELS[d["dense_kernel"]]
     return d

@@ -112,7 +112,8 @@ struct Plan {
   size_t ws_acc_bytes, ws_bytes;
   CodecDev kc, vc;
   bool has_rec, has_tail, shared;
-  bool mma;     // tensor-core kernel (head dims 64/128, no outlier side lists)
+  bool mma;     // tensor-core kernel (head dims 64/128)
+  int groups;   // its 4-warp groups per CTA
   bool mma512;  // tensor-core kernel at head dim 512 (mma.sync)
   bool umma512; // tcgen05 kernel at head dim 512 (groups of up to 64 heads per CTA)
   size_t ws_status_off;
@@ -175,14 +176,15 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
   // CUDA-core kernel; the same at head dim 512 for the compressed splits of
   // codecs without side lists, with CTAs of 16 query heads where the group
   // allows (each dequantised pair then feeds two n-tiles of MMAs).  Codecs
-  // with outlier side lists take the tensor-core kernel only for sparse-V
-  // (its corrections' scatter into the value accumulators, through shared
-  // atomics at two CTAs per SM, made it 1.7x slower than the CUDA-core
-  // kernel on the batched cache: 2.56 against 1.47 ms per layer), and only
-  // where its shared memory fits.
+  // with outlier side lists take the tensor-core kernel only for sparse-V:
+  // its per-token corrections (shared-memory loads, lookups and atomics
+  // beside the MMAs, in CTAs of three 4-warp groups) took 2.60 ms on two
+  // layers of the batched cache against 2.19 ms for the CUDA-core kernel,
+  // which overlaps the same work with its FMA work.
   const bool outl = pl->has_rec && (pl->kc.has_outl || pl->vc.has_outl);
   pl->mma = (D == 64 || D == 128) && !a->cuda_core_path && (!outl || a->sparse_v_eps > 0.f);
-  if (pl->mma && outl) {
+  pl->groups = 1;
+  if (pl->mma && pl->has_rec) {
     tq::AttnParams t{};
     t.kb = pl->kc.bits;
     t.vb = pl->vc.bits;
@@ -193,8 +195,8 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
     t.shared_kv = pl->shared ? 1 : 0;
     t.G = pl->G;
     t.n_hg = pl->n_hg;
-    tq::attn_mma_smem_layout(t, D);
-    if (t.sm_total > max_dyn_smem()) pl->mma = false;
+    pl->groups = tq::attn_mma_groups(t, D);
+    if (pl->groups == 0) pl->mma = false;
   }
   pl->mma512 = D == 512 && pl->has_rec && a->cuda_core_path != 1 && !pl->kc.has_outl && !pl->vc.has_outl;
   // tcgen05 for groups of 16-64 heads (multiples of 8, which the dense
@@ -354,6 +356,7 @@ void attn_rec_smem_layout(AttnParams& p, int D, int GT) {
 
 void attn_mma_smem_layout(AttnParams& p, int D) {
   auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  const int NG = std::max(1, p.groups), NW = 4 * NG;  // 4-warp groups, warps
   int off = 0;
   p.sm_kpair = off;  // the kernel addresses both pair tables at these fixed offsets
   off += (1 << (2 * p.kb)) * 128;
@@ -363,25 +366,42 @@ void attn_mma_smem_layout(AttnParams& p, int D) {
   off += 8 * 4 * (std::max(D / 4, 32) + 1) * 4;
   p.sm_slot = off;   // centroid halves
   off += 32 * 8;
-  p.sm_red = off;
-  off += 4 * 2 * 8 * 4;
+  p.sm_red = off;    // the warps' (m, l) at the end
+  off += NW * 2 * 8 * 4;
   p.sm_logit = off;  // query fragments [d/16][32 lanes][16 B]
   off = al(off + (D / 16) * 32 * 16, 128);
-  // side lists: f32 centroids (K, V) and the warps' value corrections
-  // [4 warps][heads rounded up to even][D + 8]
+  // side lists: f32 centroids (K, V), q~ by coordinate [D][8 heads] and the
+  // warps' value corrections [warps][heads rounded up to even][D + D/8 + pad]
   p.sm_lut = off;
   off += (p.kout || p.vout) ? 32 * 4 : 0;
+  p.sm_qi = off;
+  off += p.kout ? D * 8 * 4 : 0;
   p.sm_corr = off;
   const int GT = p.n_hg > 0 ? p.G / p.n_hg : 8;
-  off = al(off + (p.vout ? 4 * ((GT + 1) & ~1) * (D + 8) * 4 : 0), 128);
+  off = al(off + (p.vout ? NW * ((GT + 1) & ~1) * (D == 128 ? 168 : 72) * 4 : 0), 128);
   p.sm_pre = p.sm_ent = off;  // unused by this kernel
   p.sm_ent_stage = 0;
   int stage = p.k_main + (p.shared_kv ? 0 : p.v_main) + 16;  // + the word a run load may read past a row
   stage = std::max(stage, (4 * 8 * (D + D / 8) * 4 + 1) / 2);  // the warps' partials at the end
   p.sm_stage = al(stage, 128);
   p.sm_main = off;
-  off += 2 * p.sm_stage;
+  off += 2 * NG * p.sm_stage;  // a two-deep ring per group
   p.sm_total = off;
+}
+
+// 4-warp groups per CTA of the tensor-core kernel: one for codecs without
+// side lists (up to four such CTAs per SM); with side lists as many as one
+// CTA per SM holds (at most 3), so that the SM keeps 12 warps and one copy
+// of the pair tables (4-bit keys: 32 KB) rather than two 4-warp CTAs with a
+// copy each.  0 if not even one group fits.
+int attn_mma_groups(const AttnParams& base, int D) {
+  AttnParams t = base;
+  for (int ng = (base.kout || base.vout) ? kMmaOutlGroups : 1; ng >= 1; --ng) {
+    t.groups = ng;
+    attn_mma_smem_layout(t, D);
+    if (t.sm_total <= max_dyn_smem()) return ng;
+  }
+  return 0;
 }
 
 void attn_mma512_smem_layout(AttnParams& p) {
@@ -686,10 +706,12 @@ tq_status tq_decode_attn_plan(const tq_attn_args* args, const tq_codec* k_codec,
   if (st != TQ_OK) return st;
   std::memset(plan, 0, sizeof(*plan));
   const int St = pl.S - pl.Sc;
-  int ck = TQ_ATTN_KERNEL_CUDA_CORE, dk = TQ_ATTN_KERNEL_CUDA_CORE, dense_gt = pl.GT, launches = 2;
+  int ck = TQ_ATTN_KERNEL_CUDA_CORE, dk = TQ_ATTN_KERNEL_CUDA_CORE, dense_gt = pl.GT, launches = 2, warps = 4;
   switch (route_of(pl)) {
     case Route::kMma:
       ck = dk = TQ_ATTN_KERNEL_MMA;
+      if (pl.has_rec && pl.groups > 1 && St > 0) ++launches;
+      warps = 4 * (pl.has_rec ? pl.groups : 1);
       break;
     case Route::kD512:
       ck = pl.umma512 ? TQ_ATTN_KERNEL_TCGEN05 : TQ_ATTN_KERNEL_MMA512;
@@ -712,6 +734,7 @@ tq_status tq_decode_attn_plan(const tq_attn_args* args, const tq_codec* k_codec,
   plan->dense_heads_per_cta = dense_gt;
   plan->launches = launches;
   plan->workspace_bytes = pl.ws_bytes;
+  plan->warps_per_cta = warps;
   return TQ_OK;
 }
 
@@ -787,16 +810,32 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
   const Route route = route_of(pl);
   const int* status = nullptr;
   if (route == Route::kMma) {
-    // tensor cores: compressed and dense splits in one launch
+    // tensor cores: compressed and dense splits in one launch of 4-warp
+    // CTAs; with CTAs of several groups the dense splits (4-warp work) take
+    // a second launch of single-group CTAs
     AttnParams pm = p;
     if (!pl.has_rec) pm.kb = pm.vb = 1;  // dense only: any instantiation (its tables go unused)
     if (pl.has_rec) {
       pm.k_main = mma_stage_bytes(pl.kc);
       pm.v_main = mma_stage_bytes(pl.vc);
     }
+    pm.groups = pl.has_rec ? pl.groups : 1;
     attn_mma_smem_layout(pm, pl.D);
     if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
-    if (launch_attn_mma(pm, pl.D, dim3(pl.S, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    const bool wide = pm.groups > 1;
+    const int gx = wide ? pl.Sc : pl.S;
+    if (gx > 0 && launch_attn_mma(pm, pl.D, dim3(gx, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (wide && pl.S > pl.Sc) {
+      AttnParams pd = p;
+      pd.kb = pd.vb = 1;
+      pd.kout = pd.vout = 0;
+      pd.k_main = pd.v_main = 0;
+      pd.groups = 1;
+      pd.split_base = pl.Sc;
+      attn_mma_smem_layout(pd, pl.D);
+      if (pd.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
+      if (launch_attn_mma(pd, pl.D, dim3(pl.S - pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    }
   } else if (route == Route::kD512) {
     // compressed splits on a d-512 tensor-core kernel, dense splits (if any)
     // on the general kernel in a second launch (groups of at most 8 heads)

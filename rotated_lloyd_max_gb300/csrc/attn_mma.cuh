@@ -29,21 +29,27 @@
 // are staged with cp.async in a two-deep ring, one CTA barrier per record;
 // the online softmax is warp-local (the running max moves only when a logit
 // passes it by 2^8).
-// Outlier side lists (OUTL): a record is staged with its per-slot counts and
-// the first entries of its list (the rest, rarely any, are read from global
-// memory).  The MMAs score the centroids; a key entry (slot, j, value) then
-// adds (value - c[code_j]) q~_h[j] to the slot's scores before the softmax,
-// the four lanes of a quad taking every fourth entry of one token for all
-// heads and summing over the quad.  A value entry adds
-// (value - c[code_j]) 2^16 P'(slot, h) to a per-warp shared buffer over
+// Outlier side lists (OUTL, the sparse-V route of such codecs): a CTA is
+// three 4-warp groups (one CTA per SM holding one copy of the pair tables;
+// 4-bit keys take 32 KB), each group with its own staging ring and barrier
+// over every third record of the split.  A record is staged with its per-slot
+// counts and the first entries of its list (the rest, rarely any, are read
+// from global memory).  The MMAs score the centroids; lane l then takes the
+// entries (slot, j, value) of the warp's token l, four at a time with their
+// loads independent, adding (value - c[code_j]) q~_h[j] for every head (q~
+// by coordinate, one 128-bit load) before the sums move to the lanes whose
+// score fragments hold the token.  For the values the same lane adds
+// (value - c[code_j]) 2^16 P'(token, h) to a per-warp shared buffer over
 // (head, coordinate) in the accumulator's units, in fixed point through
-// shared integer atomics, which the owning lanes fold into their
-// accumulator fragments after each record.
+// shared integer atomics; the owning lanes fold it into their accumulator
+// fragments during the next record (folding right after the value MMAs
+// stalls on their results), with 64-bit accesses laid out across all banks.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "attn.cuh"
@@ -149,6 +155,12 @@ __device__ __forceinline__ int slot_entries(const unsigned char* counts, int war
 }
 
 constexpr int kMmaHeads = 8;  // query heads per CTA at most
+// Barrier of the 4 warps of group grp < 3 (named barriers 1-3; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int grp) {
+  if (grp == 0) asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  else if (grp == 1) asm volatile("bar.sync 2, 128;\n" ::: "memory");
+  else asm volatile("bar.sync 3, 128;\n" ::: "memory");
+}
 
 template <int D>
 struct MCfg {
@@ -198,16 +210,17 @@ __device__ __forceinline__ void v_pair_words(const uint32_t (&r0)[NW], const uin
   }
 }
 
-// The 4 warps' (m, l, acc) of a split -> the split's partial in the
+// The CTA's warps' (m, l, acc) of a split -> the split's partial in the
 // workspace.  acc is in the value-fragment layout (coordinate (d/8) g + 2 mc
 // (+1 for elements 2, 3), head 2t (+1 for odd elements)), scaled by 1/un.
-// mainb (the staging ring, free by now) holds the warps' partials.
+// mainb (the staging rings, free by now) holds the warps' partials.
 template <int D>
 __device__ __forceinline__ void mma_split_merge(const AttnParams& p, unsigned char* mainb, float* wml,
                                                 const float (&acc)[D / 16][4], float un, float m0, float m1,
                                                 float l0, float l1, int GT, int64_t qh0, int split) {
   constexpr int KS = D / 16, VR = D / 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  const int NW = blockDim.x >> 5;
 #pragma unroll
   for (int m = 4; m < 32; m <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, m);
@@ -215,8 +228,8 @@ __device__ __forceinline__ void mma_split_merge(const AttnParams& p, unsigned ch
   }
   __syncwarp();
   cp_async_wait<0>();
-  __syncthreads();  // all tokens consumed: the staging ring becomes the merge buffer
-  // merge buffer [4 warps][8 heads][D + D/8]: element (h, j) of a warp at
+  __syncthreads();  // all tokens consumed: the staging rings become the merge buffer
+  // merge buffer [warps][8 heads][D + D/8]: element (h, j) of a warp at
   // h (D + D/8) + j + 4 (j / 32) + h / 2, so that a warp's 32 fragment stores
   // (j = (d/8) g + const, h = 2t + const) hit 32 different banks
   float* red = reinterpret_cast<float*>(mainb);
@@ -236,14 +249,12 @@ __device__ __forceinline__ void mma_split_merge(const AttnParams& p, unsigned ch
     wml[(warp * 2 + 1) * 8 + 2 * t + 1] = l1;
   }
   __syncthreads();
-  for (int idx = tid; idx < GT * D; idx += kThreads) {
+  for (int idx = tid; idx < GT * D; idx += blockDim.x) {
     const int h = idx / D, j = idx % D;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, wml[(w * 2) * 8 + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wml[(w * 2) * 8 + h]);
     float v = 0.f, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float mw = wml[(w * 2) * 8 + h];
       const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
       v = fmaf(f, red[red_at(w, h, j)], v);
@@ -425,7 +436,8 @@ __device__ __noinline__ void mma_dense_split(const AttnParams& p, unsigned char*
 }
 
 template <int D, int KB, int VB, bool OUTL>
-__global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(OUTL ? kMmaOutlGroups * kThreads : kThreads, OUTL ? 1 : 4)
+    attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = MCfg<D>;
   constexpr int KS = C::KS, KR = C::KR, VR = C::VR;
   constexpr int KNB = KR * KB, VNB = VR * VB;
@@ -441,29 +453,41 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
   float* qf = reinterpret_cast<float*>(sm + p.sm_q);
   constexpr int QST = (MCfg<D>::KR > 32 ? MCfg<D>::KR : 32) + 1;
   auto qidx = [](int h, int c) { return h * 4 * QST + (c / MCfg<D>::KR) * QST + (c % MCfg<D>::KR); };
-  float* wml = reinterpret_cast<float*>(sm + p.sm_red);   // [4][2][8]
+  float* wml = reinterpret_cast<float*>(sm + p.sm_red);   // [warps][2][8]
   uint4* qfrag = reinterpret_cast<uint4*>(sm + p.sm_logit);  // [KS][32 lanes] (hi b0, hi b1, lo b0, lo b1)
   uint2* cent = reinterpret_cast<uint2*>(sm + p.sm_slot); // [32] (hi|lo f16) of K then V centroids x 2^16
   unsigned char* mainb = sm + p.sm_main;
-  // (OUTL) f32 centroids, K then V; value corrections [warp][head][D + 8]
+  // (OUTL) f32 centroids, K then V; q~ by coordinate [D][8 heads]; value
+  // corrections [warp][head][D + 8]
   float* kcf = reinterpret_cast<float*>(sm + p.sm_lut);
   float* vcf = kcf + 16;
+  const float4* qi4 = reinterpret_cast<const float4*>(sm + p.sm_qi);
   int* corr = reinterpret_cast<int*>(sm + p.sm_corr);
-  constexpr int CST = D + 8;
+  // corrections of (head h, coordinate j) at h CST + j + 2 (j / 16): a fold's
+  // 64-bit accesses (j = 16 g + 2 mc + {0, 1}, h = 2 t + const) then cover 32
+  // different banks (CST = 8 mod 32)
+  constexpr int CST = D == 128 ? 168 : 72;
+  auto cj = [](int j) { return j + 2 * (j >> 4); };
 
+  // (OUTL) The CTA is one or more groups of 4 warps (blockDim.x / 128).  Each
+  // group stages and scores its own records of the split (records grp,
+  // grp + NG, ...) with its own two-deep ring and barrier; the pair tables,
+  // q~ and the query fragments are shared.  Otherwise one group.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NW = OUTL ? (int)(blockDim.x >> 5) : 4, NG = NW >> 2;
+  const int grp = warp >> 2, wg = warp & 3, gtid = tid & 127;
   const int g = lane >> 2, t = lane & 3;
   const int l = blockIdx.z;
   int rem = blockIdx.y;
   const int hg = rem % p.n_hg;
   rem /= p.n_hg;
   const int kvh = rem % p.Hkv, b = rem / p.Hkv;
-  const int split = blockIdx.x;
+  const int split = blockIdx.x + p.split_base;
   const int GT = p.G / p.n_hg;
   const int h0 = kvh * p.G + hg * GT;
   const int lb = l * p.B + b;
   const int64_t qh0 = (int64_t)lb * p.Hq + h0;
-  if (split >= p.Sc) {  // dense tokens (tail ring or bf16 layer)
+  if (split >= p.Sc) {  // dense tokens (tail ring or bf16 layer); such launches run one group
     mma_dense_split<D>(p, sm + p.sm_main, reinterpret_cast<float*>(sm + p.sm_red), l, b, kvh, GT, h0, qh0, lb,
                        split);
     return;
@@ -480,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     return;
   }
   const int n = c_end - c_begin;
+  const int ng = n > grp ? (n - grp + NG - 1) / NG : 0;  // this group's records
   // record c of this unit (contiguous, or through the block table)
   const uint8_t* kl0 = p.krec + l * p.krec_ls;
   const uint8_t* vl0 = p.shared_kv ? kl0 : p.vrec + l * p.vrec_ls;
@@ -489,19 +514,23 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
   auto vrec_at = [&](int64_t c) {
     return vl0 + rec_offset(p.table, p.table_stride, p.rec_cap, p.Hkv, b, kvh, (int)c, p.vrec_bytes);
   };
-  auto stage = [&](int i) { return mainb + (i & 1) * p.sm_stage; };
+  auto rec_of = [&](int i) { return (int64_t)c_begin + grp + (int64_t)NG * i; };
+  auto stage = [&](int i) { return mainb + (2 * grp + (i & 1)) * p.sm_stage; };
+  auto group_copy = [&](unsigned char* s, const uint8_t* gsrc, int bytes) {
+    for (int off = gtid * 16; off < bytes; off += 128 * 16) cp_async16(s + off, gsrc + off);
+  };
   auto issue_main = [&](int i) {
-    if (i < n) {
-      const int64_t c = c_begin + i;
-      cta_copy_async(stage(i), krec_at(c), p.k_main);
-      if (!p.shared_kv) cta_copy_async(stage(i) + p.k_main, vrec_at(c), p.v_main);
+    if (i < ng) {
+      const int64_t c = rec_of(i);
+      group_copy(stage(i), krec_at(c), p.k_main);
+      if (!p.shared_kv) group_copy(stage(i) + p.k_main, vrec_at(c), p.v_main);
     }
     cp_async_commit();
   };
   issue_main(0);
 
   // ---- q~ = H(s_k . q)/sqrt(d) of the CTA's heads (rows >= GT are zero)
-  for (int hh = warp; hh < 8; hh += 4) {
+  for (int hh = warp; hh < 8; hh += NW) {
     constexpr int R = D / 32;
     float x[R];
     if (hh < GT) {
@@ -527,6 +556,11 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) qf[qidx(hh, lane * R + r)] = x[r];
+    if (OUTL && p.kout) {
+      float* qi = reinterpret_cast<float*>(sm + p.sm_qi);
+#pragma unroll
+      for (int r = 0; r < R; ++r) qi[(lane * R + r) * 8 + hh] = x[r];
+    }
   }
   // f16 halves of every centroid x 2^16: cent[i] = (hi, lo) of K centroid i,
   // cent[16 + i] of V centroid i
@@ -540,12 +574,12 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
   __syncthreads();  // q~ and the centroid halves complete
   // pair tables: entry e at byte e*128 + (lane % 16)*8 holds (hi pair, lo pair)
   // of its two centroids (first in the low half)
-  for (int i = tid; i < EK * 16; i += kThreads) {
+  for (int i = tid; i < EK * 16; i += blockDim.x) {
     const int e = i >> 4;
     const uint2 a = cent[e & ((1 << KB) - 1)], c = cent[e >> KB];
     *reinterpret_cast<uint2*>(sm + KP_OFF + i * 8) = make_uint2(__byte_perm(a.x, c.x, 0x5410), __byte_perm(a.y, c.y, 0x5410));
   }
-  for (int i = tid; i < EV * 16; i += kThreads) {
+  for (int i = tid; i < EV * 16; i += blockDim.x) {
     const int e = i >> 4;
     const int c0 = e & ((1 << FW) - 1), c1 = e >> FW;
     uint2 v = make_uint2(0u, 0u);
@@ -555,7 +589,6 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     }
     *reinterpret_cast<uint2*>(sm + VP_OFF + i * 8) = v;
   }
-  __syncthreads();
 
   // ---- query fragments: head g, coordinates (d/4) t + 4 kk + {0,1} / {2,3},
   // scaled by 2^s_g so that the largest |q~| of the head is in [2^13, 2^14);
@@ -578,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const int s = mx > 0.f ? 13 - exp_of(mx) : 0;
     const float sc = pow2i(s);
-    for (int kk = warp; kk < KS; kk += 4) {
+    for (int kk = warp; kk < KS; kk += NW) {
       uint4 f;
       split_f16x2(qrow[4 * kk] * sc, qrow[4 * kk + 1] * sc, f.x, f.z);
       split_f16x2(qrow[4 * kk + 2] * sc, qrow[4 * kk + 3] * sc, f.y, f.w);
@@ -614,27 +647,54 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
   // record at a time): heads 2t, 2t + 1, coordinates (d/8) g + 2 mc (+1), as
   // its accumulator fragments
   const int GTe = (GT + 1) & ~1;
-  auto corr_at = [&](int e, int mc) -> int& {
-    return corr[(warp * GTe + 2 * t + (e & 1)) * CST + VR * g + 2 * mc + (e >> 1)];
+  // the pair (elements e, e + 2) of m-tile mc: head 2t + e, coordinates
+  // (d/8) g + 2 mc and + 1
+  auto corr_pair = [&](int e, int mc) -> int2& {
+    return *reinterpret_cast<int2*>(corr + (warp * GTe + 2 * t + e) * CST + cj(VR * g + 2 * mc));
   };
   const bool own_corr = OUTL && p.vout && 2 * t < GT;
   if (own_corr) {
 #pragma unroll
     for (int mc = 0; mc < KS; ++mc)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) corr_at(e, mc) = 0;
+      for (int e = 0; e < 2; ++e) corr_pair(e, mc) = make_int2(0, 0);
   }
+  // (OUTL) a record's value corrections are folded into the accumulators
+  // during the next record (before its softmax may rescale them), when the
+  // value MMAs that last wrote them have long completed: folding right after
+  // those MMAs stalls the warp on their results
+  bool fold_pending = false;
+  float fold_iS = 0.f;
+  auto fold = [&]() {
+    __syncwarp();
+    if (own_corr) {
+#pragma unroll
+      for (int mc = 0; mc < KS; ++mc)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          int2& v = corr_pair(e, mc);
+          const int2 w = v;
+          v = make_int2(0, 0);
+          acc[mc][e] = fmaf((float)w.x, fold_iS, acc[mc][e]);
+          acc[mc][e + 2] = fmaf((float)w.y, fold_iS, acc[mc][e + 2]);
+        }
+    }
+    __syncwarp();
+    fold_pending = false;
+  };
+  __syncthreads();  // pair tables and query fragments complete for every group
 
-  for (int i = 0; i < n; ++i) {
+  for (int i = 0; i < ng; ++i) {
     cp_async_wait<0>();
-    __syncthreads();  // record i is in; record i-1 is done with
+    if constexpr (OUTL) group_sync(grp);  // record i is in; record i-1 is done with
+    else __syncthreads();
     issue_main(i + 1);
     const unsigned char* st = stage(i);
-    const unsigned char* kcodes = st + warp * 32 * rbk;
-    const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + warp * 32;
+    const unsigned char* kcodes = st + wg * 32 * rbk;
+    const float* knorm = reinterpret_cast<const float*>(st + p.k_off_norm) + wg * 32;
     const unsigned char* vbase = p.shared_kv ? st : st + p.k_main;
-    const unsigned char* vcodes = vbase + warp * 32 * rbv;
-    const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + warp * 32;
+    const unsigned char* vcodes = vbase + wg * 32 * rbv;
+    const float* vnorm = reinterpret_cast<const float*>(vbase + p.v_off_norm) + wg * 32;
 
     // ---- scores: tile mt holds tokens 16 mt + g (elements 0, 1) and + 8 (2, 3)
     float sc[2][4];
@@ -692,61 +752,67 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       }
     }
     // ---- key side lists: sc (centroid scores, before the norm) += sum over
-    // the token's entries of (value - c[code_j]) q~_h[j].  The lane's four
-    // tokens g + 8 q advance together, one entry each per round (entries
-    // 4 r + t): predicated, no divergent loop.
+    // the token's entries of (value - c[code_j]) q~_h[j].  Lane l takes the
+    // entries of the warp's token l, one per round (as many rounds as the
+    // warp's longest list); the sums then move to the lanes whose score
+    // fragments hold the token.
     if constexpr (OUTL) {
       if (p.kout) {
-        const int oc_l = slot_entries(st + p.k_off_count, warp, lane);
+        const int oc = slot_entries(st + p.k_off_count, wg, lane);
+        const int off = oc >> 8, cnt = max(0, min(oc & 255, p.kcap - off));  // (a list longer than its capacity reads no further)
         const uint32_t* ent_s = reinterpret_cast<const uint32_t*>(st + p.k_off_ent);
-        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(krec_at(c_begin + i) + p.k_off_ent);
         const int nse = (p.k_main - p.k_off_ent) >> 2;  // entries staged
-        const int last = __shfl_sync(0xffffffffu, oc_l, 31);
-        const bool staged = (last >> 8) + (last & 255) <= nse;  // the warp's entries all staged
-        int off[4], cnt[4], mx = 0;
+        const bool staged = __all_sync(0xffffffffu, off + cnt <= nse);
+        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(krec_at(rec_of(i)) + p.k_off_ent);
+        const unsigned char* krow = kcodes + lane * rbk;
+        const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)cnt);
+        float dk[kMmaHeads];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int oc = __shfl_sync(0xffffffffu, oc_l, g + 8 * q);
-          off[q] = oc >> 8;
-          cnt[q] = oc & 255;
-          mx = max(mx, cnt[q]);
-        }
-        const int rounds = ((int)__reduce_max_sync(0xffffffffu, (unsigned)mx) + 3) >> 2;
-        float dk[4][kMmaHeads];
+        for (int h = 0; h < kMmaHeads; ++h) dk[h] = 0.f;
+        // four entries per trip, their loads independent of one another
+        for (int k0 = 0; k0 < rounds; k0 += 4) {
+          uint32_t e[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+          for (int u = 0; u < 4; ++u) {
+            const int idx = k0 + u < cnt ? off + k0 + u : 0;
+            if (staged || idx < nse) e[u] = ent_s[idx];
+            else e[u] = __ldg(ent_g + idx);
+          }
+          float delta[4];
+          int j[4];
 #pragma unroll
-          for (int h = 0; h < kMmaHeads; ++h) dk[q][h] = 0.f;
-        for (int r = 0; r < rounds; ++r) {
+          for (int u = 0; u < 4; ++u) {
+            j[u] = (int)(e[u] & (uint32_t)(D - 1));
+            delta[u] = k0 + u < cnt ? __uint_as_float(e[u] & 0xFFFF0000u) - kcf[row_code<KB>(krow, j[u])] : 0.f;
+          }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = 4 * r + t, idx = off[q] + k;
-            const bool ok = k < cnt[q] && idx < p.kcap;  // (a list longer than its capacity reads no further)
-            uint32_t e = ent_s[min(idx, nse - 1)];
-            if (!staged && ok && idx >= nse) e = __ldg(ent_g + idx);
-            const int j = (int)(e & (uint32_t)(D - 1));
-            const float cj = kcf[row_code<KB>(kcodes + (g + 8 * q) * rbk, j)];
-            const float delta = ok ? __uint_as_float(e & 0xFFFF0000u) - cj : 0.f;
-#pragma unroll
-            for (int h = 0; h < kMmaHeads; ++h)
-              if (h < GT) dk[q][h] = fmaf(delta, qf[qidx(h, j)], dk[q][h]);
+          for (int u = 0; u < 4; ++u) {
+            const float4 qa = qi4[2 * j[u]];
+            dk[0] = fmaf(delta[u], qa.x, dk[0]);
+            dk[1] = fmaf(delta[u], qa.y, dk[1]);
+            dk[2] = fmaf(delta[u], qa.z, dk[2]);
+            dk[3] = fmaf(delta[u], qa.w, dk[3]);
+            if (GT > 4) {
+              const float4 qb = qi4[2 * j[u] + 1];
+              dk[4] = fmaf(delta[u], qb.x, dk[4]);
+              dk[5] = fmaf(delta[u], qb.y, dk[5]);
+              dk[6] = fmaf(delta[u], qb.z, dk[6]);
+              dk[7] = fmaf(delta[u], qb.w, dk[7]);
+            }
           }
         }
-        // sums over the quad; the lane keeps its heads 2t, 2t + 1
+        // token g + 8 q sits in sc[q >> 1][2 (q & 1) + {0, 1}] (heads 2 th, 2 th + 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float d0 = 0.f, d1 = 0.f;
 #pragma unroll
           for (int h = 0; h < kMmaHeads; h += 2) {
             if (h < GT) {
-              float a = dk[q][h], c = dk[q][h + 1];
-              a += __shfl_xor_sync(0xffffffffu, a, 1);
-              c += __shfl_xor_sync(0xffffffffu, c, 1);
-              a += __shfl_xor_sync(0xffffffffu, a, 2);
-              c += __shfl_xor_sync(0xffffffffu, c, 2);
+              const float a = __shfl_sync(0xffffffffu, dk[h], g + 8 * q);
+              const float c2 = __shfl_sync(0xffffffffu, dk[h + 1], g + 8 * q);
               if (h == 2 * th) {
                 d0 = a;
-                d1 = c;
+                d1 = c2;
               }
             }
           }
@@ -755,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
         }
       }
     }
+    if (OUTL && fold_pending) fold();
     // logits (log2 domain)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
@@ -896,75 +963,80 @@ __global__ void __launch_bounds__(kThreads, OUTL ? 2 : 4) attn_mma_kernel(const 
       if (pk) value_mmas(std::true_type{});
       else value_mmas(std::false_type{});
     }
-    // ---- value side lists: corr[h][j] += (value - c[code_j]) 2^16 P'(token, h),
-    // the lane's four tokens advancing together as for the keys; in fixed
-    // point S = 2^(23 - floor(log2 max 2^16 P')) (shared integer atomics
-    // retire about four times faster than f32 ones): a term is below 2^25 in
-    // magnitude (|value - c| < 2) and a (head, coordinate) takes at most one
-    // term per token, so a record's sums stay below 2^30; the owners fold
-    // them into their accumulators after the record
+    // ---- value side lists: corr[h][j] += (value - c[code_j]) 2^16 P'(token, h)
+    // in fixed point S = 2^(23 - floor(log2 max 2^16 P')) (shared integer
+    // atomics retire about four times faster than f32 ones): a term is below
+    // 2^25 in magnitude (|value - c| < 2) and a (head, coordinate) takes at
+    // most one term per token, so a record's sums stay below 2^30.  Lane l
+    // takes the entries of the warp's token l, one per round, with the
+    // token's P' gathered from the score fragments; the owners fold the sums
+    // into their accumulators during the next record.
     if constexpr (OUTL) {
       if (p.vout) {
-        const int oc_l = slot_entries(vbase + p.v_off_count, warp, lane);
+        const int oc = slot_entries(vbase + p.v_off_count, wg, lane);
+        const int off = oc >> 8, cnt = max(0, min(oc & 255, p.vcap - off));
         const uint32_t* ent_s = reinterpret_cast<const uint32_t*>(vbase + p.v_off_ent);
-        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(vrec_at(c_begin + i) + p.v_off_ent);
         const int nse = (p.v_main - p.v_off_ent) >> 2;
-        const int last = __shfl_sync(0xffffffffu, oc_l, 31);
-        const bool staged = (last >> 8) + (last & 255) <= nse;
+        const bool staged = __all_sync(0xffffffffu, off + cnt <= nse);
+        const uint32_t* ent_g = reinterpret_cast<const uint32_t*>(vrec_at(rec_of(i)) + p.v_off_ent);
+        const unsigned char* vrow = vcodes + lane * rbv;
         float pmx = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
                           fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
         pmx = warp_max(pmx * (65536.f * psc));
         const int ef = min(254, max(1, 277 - (int)((__float_as_uint(pmx) >> 23) & 0xFFu)));
         const float S = __uint_as_float((uint32_t)ef << 23), iS = __uint_as_float((uint32_t)(254 - ef) << 23);
         const float fsc = 65536.f * psc * S;
+        // token l = 16 mt + 8 eh + r8 sits in lane 4 r8 + h / 2, sc[mt][2 eh + (h & 1)]
+        float pv[kMmaHeads];
+        {
+          const int mt = lane >> 4, eh = (lane >> 3) & 1, src0 = 4 * (lane & 7);
+#pragma unroll
+          for (int h = 0; h < kMmaHeads; h += 2) {
+            pv[h] = 0.f;
+            pv[h + 1] = 0.f;
+            if (h < GT) {
+              float v[2][4];
+#pragma unroll
+              for (int m2 = 0; m2 < 2; ++m2)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[m2][e] = __shfl_sync(0xffffffffu, sc[m2][e], src0 + (h >> 1));
+              pv[h] = (mt ? (eh ? v[1][2] : v[1][0]) : (eh ? v[0][2] : v[0][0])) * fsc;
+              pv[h + 1] = (mt ? (eh ? v[1][3] : v[1][1]) : (eh ? v[0][3] : v[0][1])) * fsc;
+            }
+          }
+        }
         int* cw = corr + warp * GTe * CST;
-        int off[4], cnt[4], mx = 0;
-        float pv[4][kMmaHeads];  // P' of the lane's tokens for every head of the CTA, from the quad
+        const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)cnt);
+        for (int k0 = 0; k0 < rounds; k0 += 4) {
+          uint32_t e[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int oc = __shfl_sync(0xffffffffu, oc_l, g + 8 * q);
-          off[q] = oc >> 8;
-          cnt[q] = oc & 255;
-          mx = max(mx, cnt[q]);
-          const float own0 = sc[q >> 1][2 * (q & 1)] * fsc, own1 = sc[q >> 1][2 * (q & 1) + 1] * fsc;
+          for (int u = 0; u < 4; ++u) {
+            const int idx = k0 + u < cnt ? off + k0 + u : 0;
+            if (staged || idx < nse) e[u] = ent_s[idx];
+            else e[u] = __ldg(ent_g + idx);
+          }
+          float f[4];
+          int j[4];
 #pragma unroll
-          for (int u = 0; u < kMmaHeads / 2; ++u) {
-            if (2 * u < GT) {
-              pv[q][2 * u] = __shfl_sync(0xffffffffu, own0, (lane & ~3) | u);
-              pv[q][2 * u + 1] = __shfl_sync(0xffffffffu, own1, (lane & ~3) | u);
+          for (int u = 0; u < 4; ++u) {
+            j[u] = (int)(e[u] & (uint32_t)(D - 1));
+            f[u] = __uint_as_float(e[u] & 0xFFFF0000u) - vcf[row_code<VB>(vrow, j[u])];
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (k0 + u < cnt) {
+#pragma unroll
+              for (int h = 0; h < kMmaHeads; ++h)
+                if (h < GT) atomicAdd(cw + h * CST + cj(j[u]), __float2int_rn(f[u] * pv[h]));
             }
           }
         }
-        const int rounds = ((int)__reduce_max_sync(0xffffffffu, (unsigned)mx) + 3) >> 2;
-        for (int r = 0; r < rounds; ++r) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = 4 * r + t, idx = off[q] + k;
-            const bool ok = k < cnt[q] && idx < p.vcap;
-            uint32_t e = ent_s[min(idx, nse - 1)];
-            if (!staged && ok && idx >= nse) e = __ldg(ent_g + idx);
-            const int j = (int)(e & (uint32_t)(D - 1));
-            const float f = __uint_as_float(e & 0xFFFF0000u) - vcf[row_code<VB>(vcodes + (g + 8 * q) * rbv, j)];
-#pragma unroll
-            for (int h = 0; h < kMmaHeads; ++h)
-              if (h < GT && ok) atomicAdd(cw + h * CST + j, __float2int_rn(f * pv[q][h]));
-          }
-        }
-        __syncwarp();
-        if (own_corr) {
-#pragma unroll
-          for (int mc = 0; mc < KS; ++mc)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              int& v = corr_at(e, mc);
-              acc[mc][e] = fmaf((float)v, iS, acc[mc][e]);
-              v = 0;
-            }
-        }
-        __syncwarp();
+        fold_pending = true;
+        fold_iS = iS;
       }
     }
   }
+  if (OUTL && fold_pending) fold();
 
   if (pk) {  // P' hi columns (t < 2) plus lo columns (t >= 2)
 #pragma unroll
@@ -980,7 +1052,7 @@ cudaError_t attn_mma_launch_o(const AttnParams& p, dim3 grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, KB, VB, OUTL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm_total);
   if (e != cudaSuccess) return e;
-  attn_mma_kernel<D, KB, VB, OUTL><<<grid, kThreads, p.sm_total, s>>>(p);
+  attn_mma_kernel<D, KB, VB, OUTL><<<grid, kThreads * std::max(1, p.groups), p.sm_total, s>>>(p);
   return cudaGetLastError();
 }
 template <int D, int KB, int VB>

@@ -134,12 +134,13 @@ struct AttnParams {
   const int32_t* tail_len;
   int S, Sc, cps, tps;
   int split_base;  // index of the first split a launch covers (dense-only launches)
+  int groups;      // tensor-core kernel (head dims 64/128): 4-warp groups per CTA (0 = 1)
   float* ws_acc;
   float* ws_ml;
   int* status;  // sticky launch status in the workspace (nonzero: a bounded wait expired)
   // dynamic shared memory carve-up (bytes)
   int sm_q, sm_lut, sm_red, sm_logit, sm_main, sm_stage, sm_ent, sm_ent_stage, sm_pre, sm_slot,
-      sm_corr, sm_kpair, sm_vpair, sm_total;
+      sm_corr, sm_kpair, sm_vpair, sm_qi, sm_total;
 };
 
 struct MergeParams {
@@ -178,6 +179,8 @@ cudaError_t launch_merge(const MergeParams& p, int D, cudaStream_t s);
 void attn_smem_layout(AttnParams& p, int D, int GT);
 void attn_rec_smem_layout(AttnParams& p, int D, int GT);
 void attn_mma_smem_layout(AttnParams& p, int D);
+int attn_mma_groups(const AttnParams& base, int D);
+constexpr int kMmaOutlGroups = 3;  // tensor-core kernel with side lists: 4-warp groups per CTA at most
 void attn_mma512_smem_layout(AttnParams& p);
 
 // The codebook kernel writes this block into the caller's scratch.

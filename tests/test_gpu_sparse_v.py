@@ -53,15 +53,17 @@ def test_sparse_v_matches_oracle_schedule(tq, orc, d, G, kb, vb, splits, T):
               tail_start=cnt(0), tail_len=cnt(tail), max_tail=tail, splits=splits)
     plan = tq.tq_decode_attn_plan(tq.make_attn_args(**kw, sparse_v_eps=eps), kc, vc)
     assert plan["compressed_kernel"] == "mma"
-    cps, gt = plan["records_per_split"], plan["heads_per_cta"]
+    cps, gt, groups = plan["records_per_split"], plan["heads_per_cta"], plan["warps_per_cta"] // 4
+    assert groups == (3 if T else 1)  # side lists: CTAs of three 4-warp groups
     # an attention sink (logit about 40 for every head of its kv head) opens
-    # every (split, warp) sequence: later blocks fall far below it
+    # every (split, group, warp) sequence: later blocks fall far below it
     for h in range(Hkv):
         u = q64[h * G:(h + 1) * G].sum(0)
         sink = u * (40.0 / np.min(q64[h * G:(h + 1) * G] @ u))
         for s in range(0, R, cps):
-            for w in range(4):
-                k32[h, 128 * s + 32 * w] = sink
+            for g in range(min(groups, R - s, cps)):
+                for w in range(4):
+                    k32[h, 128 * (s + g) + 32 * w] = sink
     kx = synth.f32_to_bf16_bits(k32)
     vx = synth.gaussian_bf16((Hkv, ntok, d), 9 + d)
     tq.tq_encode(kc, tl.to_bf16_tensor(kx, dev), krec.view(Hkv, R, -1))
@@ -77,7 +79,7 @@ def test_sparse_v_matches_oracle_schedule(tq, orc, d, G, kb, vb, splits, T):
     for h in range(Hkv):
         qh = qb[0, 0, h * G:(h + 1) * G]
         want, skipped = orc.unit_attention_sparse_v(qh, okc, ovc, kr[h], vr[h], ntok, kt[h], vt[h], 1.0, eps,
-                                                    cps, gt)
+                                                    cps, gt, groups=groups)
         exact = orc.unit_attention(qh, okc, ovc, kr[h], vr[h], ntok, kt[h], vt[h], 1.0)
         got = outs[eps][h * G:(h + 1) * G]
         assert np.all(np.isfinite(got))

@@ -97,3 +97,21 @@ def test_schedule_blocks(orc):
     assert b[:3] == [(0, 32, 0), (128, 160, 0), (32, 64, 1)]
     assert (4 * 128 + 96, 4 * 128 + 128, 2 * 4 + 3) in b
     assert sorted(t for bb in b for t in range(bb[0], bb[1])) == list(range(5 * 128))
+
+
+def test_schedule_blocks_of_grouped_ctas(orc):
+    """Three 4-warp groups per CTA: split s deals its records out round robin,
+    group g visiting records g, g + 3, ... of the split; one sequence per
+    (split, group, warp)."""
+    b = orc.sparse_v_blocks(7, 5, groups=3)
+    assert len(b) == 7 * 4
+    seq = {}
+    for lo, hi, s in b:
+        seq.setdefault(s, []).append(lo // 128)
+    # split 0 (records 0-4): group 0 takes 0 and 3, group 1 takes 1 and 4, group 2 takes 2
+    assert seq[0 * 4 + 1] == [0, 3] and seq[1 * 4 + 2] == [1, 4] and seq[2 * 4 + 0] == [2]
+    # split 1 (records 5, 6): groups 0 and 1 take one record each, group 2 none
+    assert seq[(3 + 0) * 4 + 3] == [5] and seq[(3 + 1) * 4 + 0] == [6] and (3 + 2) * 4 not in seq
+    assert b[0] == (0, 32, 0) and (3 * 128 + 32, 3 * 128 + 64, 1) in b
+    assert sorted(t for bb in b for t in range(bb[0], bb[1])) == list(range(7 * 128))
+    assert orc.sparse_v_blocks(5, 2, groups=1) == orc.sparse_v_blocks(5, 2)

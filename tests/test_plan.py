@@ -112,16 +112,31 @@ def test_qwen2_plan(orc):
 
 def test_outlier_codecs_take_the_warp_local_kernel_and_sparse_v_the_tensor_cores(orc):
     """Side lists run on the warp-local CUDA-core kernel; with sparse-V on the
-    tensor-core kernel, whose corrections ride along beside its MMAs (its
-    shared memory fits two CTAs per SM for the batched cache's codecs)."""
+    tensor-core kernel in CTAs of three 4-warp groups (one CTA per SM, one
+    copy of the 4-bit pair table: the batched cache's codecs need 220 KB of
+    shared memory for that).  Dense splits of such a call run in a second
+    launch of 4-warp CTAs."""
     kc, vc = raw_codec(orc, 4, 128, T=2.0), raw_codec(orc, 3, 128, T=2.0)
     a = args_for(L=1, B=32, Hq=32, Hkv=8, d=128, records=256, tail=None, rec_bytes=8192)
     p = plan(a, kc, vc)
     assert p["compressed_kernel"] == "cuda_core_warp" and p["dense_kernel"] == "none"
-    assert p["heads_per_cta"] == 4 and p["launches"] == 2
+    assert (p["heads_per_cta"], p["warps_per_cta"], p["launches"]) == (4, 4, 2)
     a.sparse_v_eps = 1e-3
     p = plan(a, kc, vc)
-    assert p["compressed_kernel"] == "mma" and p["heads_per_cta"] == 4 and p["launches"] == 2
+    assert p["compressed_kernel"] == "mma" and p["dense_kernel"] == "none"
+    assert (p["heads_per_cta"], p["warps_per_cta"], p["launches"]) == (4, 12, 2)
+    b = args_for(L=1, B=2, Hq=8, Hkv=2, d=128, records=4, tail=64, rec_bytes=8192)
+    b.sparse_v_eps = 1e-3
+    p = plan(b, kc, vc)
+    assert p["compressed_kernel"] == p["dense_kernel"] == "mma"
+    assert (p["warps_per_cta"], p["launches"]) == (12, 3)
+
+
+def test_codecs_without_side_lists_keep_four_warp_ctas(orc):
+    kc, vc = raw_codec(orc, 4, 128), raw_codec(orc, 3, 128)
+    a = args_for(L=1, B=32, Hq=32, Hkv=8, d=128, records=256, tail=None, rec_bytes=8192)
+    p = plan(a, kc, vc)
+    assert p["compressed_kernel"] == "mma" and p["warps_per_cta"] == 4 and p["launches"] == 2
 
 
 def test_head_dim_256_runs_on_cuda_cores(orc):
