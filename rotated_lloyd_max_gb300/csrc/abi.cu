@@ -529,8 +529,8 @@ tq_status tq_encode(const tq_codec* codec, const void* src, int64_t n_groups, in
   p.first_vec = first_vec;
   p.first_chunk = first_vec / TQ_CHUNK;
   p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
-  // task indices: at most 8 per record (16-vector tiles), plus a grid's lookahead
-  p.small_tasks = p.chunks_per_group < (1ll << 31) && n_groups * p.chunks_per_group * 8 + (1ll << 24) < (1ll << 32);
+  // task indices: at most 32 per record (tiles of 16, 8 or 4 vectors), plus a grid's lookahead
+  p.small_tasks = p.chunks_per_group < (1ll << 31) && n_groups * p.chunks_per_group * 32 + (1ll << 24) < (1ll << 32);
   p.cpg = make_fast_div(p.small_tasks ? (uint32_t)p.chunks_per_group : 1u);
   // the launcher caps the grid at the number of tasks of the kernel it picks
   return launch_encode(p, 8 * num_sms(), (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

@@ -93,7 +93,8 @@ static cudaError_t enc_launch(const EncodeParams& p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, int grid, cudaStream_t s) {
-  if (p.c.d == 128) return launch_encode_mma(p, grid, s);  // Hadamard stage on the tensor cores
+  // head dims 128, 256, 512: the 16-point Hadamard stage on the tensor cores
+  if (p.c.d >= 128) return launch_encode_mma(p, grid, s);
   TQ_DISPATCH_DBO(enc_launch, p.c.d, p.c.bits, p.c.has_outl, p, grid, s);
 }
 
