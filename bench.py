@@ -203,9 +203,9 @@ MEASURED_TRAFFIC: dict = {
 }
 
 PHASE_SOURCES = {
-    "tq_encode": ["encode_mma.cuh", "encode_mma.cu", "encode_mma_d256.cu", "encode_mma_d512.cu", "encode.cu",
+    "tq_encode": ["encode_mma.cuh", "encode_mma.cu", "encode_mma_d64.cu", "encode_mma_d256.cu", "encode_mma_d512.cu",
                   "tq_common.cuh", "tq_params.h", "abi.cu"],
-    "tq_evict": ["encode.cu", "tq_common.cuh", "tq_params.h", "abi.cu"],
+    "tq_evict": ["evict.cu", "encode_core.cuh", "tq_common.cuh", "tq_params.h", "abi.cu"],
     "tq_decode_attn": ["abi.cu", "merge.cu", "umma.cuh", "tq_common.cuh", "tq_params.h",
                        "attn.cuh", "attn_rec.cuh", "attn_mma.cuh", "attn_mma512.cuh", "attn_umma512.cuh"],
 }

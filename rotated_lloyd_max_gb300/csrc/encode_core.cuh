@@ -1,6 +1,6 @@
-// The CUDA-core encoder's device code, shared by the encode kernels
-// (encode.cu) and the eviction kernels (evict.cu): encode bf16 head vectors
-// into 128-token records.
+// The CUDA-core encoder's device code, used by the eviction kernels
+// (evict.cu; tq_encode runs the tensor-core encoders of encode_mma.cuh):
+// encode bf16 head vectors into 128-token records.
 //
 // Per vector ("v1.3 PPL on vLLM", M4 Phase A/B commits: rotate = H.D.x,
 // per-row scale, Lloyd-Max argmin, outliers; larql PR #196 turbo-quant note:

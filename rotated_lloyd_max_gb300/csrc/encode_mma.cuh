@@ -27,6 +27,11 @@
 // butterflies follow: between the lane's two rows, and at d 512 between lanes
 // g and g ^ 4 (lane ^ 16) by shuffles.  A lane ends with 64 outputs of one
 // vector (two runs of 32 coordinates), as many as at d 128.
+// Head dim 64: a 128-coordinate row holds two vectors (coordinate bit 6, the
+// high bit of t, picks the vector), and the 16-point stage leaves that bit
+// alone (its matrix is H8 (x) I2 over (e, h, t & 1) and t >> 1), so a tile
+// carries 32 vectors and lane (g, t) ends with 32 outputs of vector
+// (row, t >> 1); a vector's lanes are pairs (t, t ^ 1) rather than quads.
 //
 // A CTA of 16 warps (12 at d 256/512, whose lanes also hold the signs of two
 // quarters) owns an SM.  Its decision-cell table is replicated 16 times, copy
@@ -54,9 +59,15 @@ __device__ __forceinline__ void mma_bf16_e(float (&c)[4], uint32_t a0, uint32_t 
 
 // bf16 +-1 pair of the permuted H16: entry (input in4, output out4) is
 // (-1)^popcount(in4 & out4), in4 = e | h<<1 | t'<<2, out4 = e' | nt<<1 | t''<<2.
+// (BLOCK, head dim 64) zero where bit 3 of in4 and out4 (t' >> 1, t'' >> 1:
+// the vector of the row) differ.
+template <bool BLOCK = false>
 __device__ __forceinline__ uint32_t h16_pair(int in4a, int in4b, int out4) {
-  const uint32_t lo = (__popc(in4a & out4) & 1) ? 0xBF80u : 0x3F80u;
-  const uint32_t hi = (__popc(in4b & out4) & 1) ? 0xBF80u : 0x3F80u;
+  const int m = BLOCK ? 7 : 15;  // the vector bit never enters the sign
+  uint32_t lo = (__popc(in4a & out4 & m) & 1) ? 0xBF80u : 0x3F80u;
+  uint32_t hi = (__popc(in4b & out4 & m) & 1) ? 0xBF80u : 0x3F80u;
+  if (BLOCK && ((in4a ^ out4) & 8)) lo = 0u;
+  if (BLOCK && ((in4b ^ out4) & 8)) hi = 0u;
   return lo | (hi << 16);
 }
 
@@ -64,23 +75,27 @@ __device__ __forceinline__ uint32_t h16_pair(int in4a, int in4b, int out4) {
 // tile, TPR tiles per 128-slot record; RB bytes per packed row.
 template <int D, int B>
 struct EncM {
-  static constexpr int R = D / 128;
-  static constexpr int VT = 16 / R;
+  static constexpr int R = D >= 128 ? D / 128 : 1;
+  static constexpr int VT = D == 64 ? 32 : 16 / R;
   static constexpr int TPR = kChunk / VT;
   static constexpr int RB = D * B / 8;
 };
 
-// The rows of tile `tile` a lane with group g works on: the slots of rows g
-// and g + 8 and the quarters of their vectors they hold.
+// The rows of tile `tile` a lane (g, t) works on: the slots of its vectors
+// in rows g and g + 8 and the quarters of them it holds.
 struct EncRows {
   int slot_a, slot_b, qa, qb;
 };
 template <int D>
-__device__ __forceinline__ EncRows enc_rows(int tile, int g) {
-  if constexpr (D == 128) return {16 * tile + g, 16 * tile + g + 8, 0, 0};
+__device__ __forceinline__ EncRows enc_rows(int tile, int g, int t) {
+  if constexpr (D == 64) return {32 * tile + 2 * g + (t >> 1), 32 * tile + 16 + 2 * g + (t >> 1), 0, 0};
+  else if constexpr (D == 128) return {16 * tile + g, 16 * tile + g + 8, 0, 0};
   else if constexpr (D == 256) return {8 * tile + g, 8 * tile + g, 0, 1};
   else return {4 * tile + (g & 3), 4 * tile + (g & 3), g >> 2, 2 + (g >> 2)};
 }
+// Element offset of a lane's 32 coordinates within its vector.
+template <int D>
+__device__ __forceinline__ int enc_col(int q, int t) { return D == 64 ? 32 * (t & 1) : 128 * q + 32 * t; }
 
 // Lane state shared by the kernels: sign masks of the lane's 32 coordinates
 // in each of its rows (XOR on packed bf16 pairs; one set at d 128, where both
@@ -89,7 +104,7 @@ template <int D, int B>
 struct EncMLane {
   int lane, warp, g, t;
   uint32_t cell_lane;  // byte offset of this lane's copy within a replicated cell
-  uint32_t smask[D == 128 ? 1 : 2][16];
+  uint32_t smask[D <= 128 ? 1 : 2][16];
   uint32_t hb[2][2];  // [n-tile][b0, b1]
   __device__ __forceinline__ explicit EncMLane(const CodecDev& c) {
     lane = threadIdx.x & 31;
@@ -97,10 +112,10 @@ struct EncMLane {
     g = lane >> 2;
     t = lane & 3;
     cell_lane = (uint32_t)(lane & 15) * 8u;
-    const EncRows rw = enc_rows<D>(0, g);
+    const EncRows rw = enc_rows<D>(0, g, t);
 #pragma unroll
-    for (int s = 0; s < (D == 128 ? 1 : 2); ++s) {
-      const uint32_t sb = c.signs[(s ? rw.qb : rw.qa) * 4 + t];
+    for (int s = 0; s < (D <= 128 ? 1 : 2); ++s) {
+      const uint32_t sb = c.signs[enc_col<D>(s ? rw.qb : rw.qa, t) / 32];
 #pragma unroll
       for (int k = 0; k < 16; ++k)
         smask[s][k] = (((sb >> (2 * k)) & 1u) << 15) | (((sb >> (2 * k + 1)) & 1u) << 31);
@@ -108,8 +123,8 @@ struct EncMLane {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int out4 = (g & 1) | (nt << 1) | ((g >> 1) << 2);
-      hb[nt][0] = h16_pair(0 | (t << 2), 1 | (t << 2), out4);
-      hb[nt][1] = h16_pair(2 | (t << 2), 3 | (t << 2), out4);
+      hb[nt][0] = h16_pair<D == 64>(0 | (t << 2), 1 | (t << 2), out4);
+      hb[nt][1] = h16_pair<D == 64>(2 | (t << 2), 3 | (t << 2), out4);
     }
   }
 };
@@ -233,19 +248,19 @@ __device__ __forceinline__ void encm_transform(const EncMLane<D, B>& ln, const u
 // warps per CTA at most (one CTA per SM): 16, or 12 at d 256/512 (two sets of
 // sign masks per lane); small encodes run 4-warp CTAs so that two fit an SM
 template <int D>
-constexpr int enc_warps() { return D == 128 ? 16 : 12; }
+constexpr int enc_warps() { return D <= 128 ? 16 : 12; }
 constexpr int kEncWarpsSmall = 4;
 constexpr int kCellCopies = 16;
 
 // Shared memory of both kernels: the replicated decision cells (cell i, copy
 // j at float2 index 16 i + j), the centroids, then two tile buffers per warp
 // (as many warps as the launch has).
-struct EncSmem {
+struct EncMSmem {
   float2 cells[kCells * kCellCopies];
   float cent[32];
   EncTile tiles[1][2];  // [warps][2] in the launch's dynamic shared memory
 };
-constexpr int enc_smem_bytes(int warps) { return (int)(sizeof(EncSmem) + (warps - 1) * 2 * sizeof(EncTile)); }
+constexpr int enc_smem_bytes(int warps) { return (int)(sizeof(EncMSmem) + (warps - 1) * 2 * sizeof(EncTile)); }
 
 // Cell (i128 >> 7) & 511 as seen by a lane (its copy: bank pair lane % 16);
 // i128 is the cell index times 128 in bits 7..15 (other bits ignored).
@@ -255,7 +270,7 @@ __device__ __forceinline__ float2 encm_cell(const unsigned char* cells, uint32_t
 
 // The table, built once per CTA: plain cells into a scratch tile first, then
 // each cell copied 16 times.
-__device__ __forceinline__ void encm_build(const CodecDev& c, EncSmem& sm) {
+__device__ __forceinline__ void encm_build(const CodecDev& c, EncMSmem& sm) {
   float2* plain = reinterpret_cast<float2*>(&sm.tiles[0][0]);
   static_assert(sizeof(EncTile) >= kCells * sizeof(float2), "scratch tile holds the plain table");
   if (threadIdx.x < kThreads) build_cells<false, true>(c, plain);
@@ -354,18 +369,21 @@ __device__ __forceinline__ void encm_scales(int mode, float na, float nb, float 
   sb = vector_scale(mode, nb, ccb, cxb * (zb * (1.f / kCellScale)));
 }
 
-// Norms of the lane's vectors: d 128 one per row (quad sums), otherwise one
+// Norms of the lane's vectors: d 64 one per row and pair, d 128 one per row
+// (quad sums), otherwise one
 // per vector over its rows (quad sums, at d 512 also over lane ^ 16).  Every
 // lane of a vector ends with the same value (f32 addition commutes).
-template <int R>
+template <int D, int R>
 __device__ __forceinline__ void encm_norms(const uint32_t (&wa)[16], const uint32_t (&wb)[16], float& na,
                                            float& nb) {
   float sa = encm_sq(wa), sb = encm_sq(wb);
   if constexpr (R == 1) {
     sa += __shfl_xor_sync(0xffffffffu, sa, 1);
     sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-    sa += __shfl_xor_sync(0xffffffffu, sa, 2);
-    sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+    if constexpr (D == 128) {  // at d 64 a vector's lanes are a pair
+      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+    }
     na = sqrtf(sa);
     nb = sqrtf(sb);
   } else {
@@ -412,10 +430,17 @@ __device__ __forceinline__ void encm_quarters(int g, float (&xa)[32], float (&xb
 // The stored scales (scale modes) from the lane's parts of ||chat||^2 and
 // <chat, x> (z = 128 / (n sqrt(d)), so <chat, y> = <chat, x> z / 128): per
 // row at d 128, per vector otherwise.
-template <int R>
+template <int D, int R>
 __device__ __forceinline__ void encm_scales_r(int mode, float na, float nb, float za, float zb, float cca,
                                               float cxa, float ccb, float cxb, float& sa, float& sb) {
-  if constexpr (R == 1) {
+  if constexpr (D == 64) {  // pair sums
+    cca += __shfl_xor_sync(0xffffffffu, cca, 1);
+    cxa += __shfl_xor_sync(0xffffffffu, cxa, 1);
+    ccb += __shfl_xor_sync(0xffffffffu, ccb, 1);
+    cxb += __shfl_xor_sync(0xffffffffu, cxb, 1);
+    sa = vector_scale(mode, na, cca, cxa * (za * (1.f / kCellScale)));
+    sb = vector_scale(mode, nb, ccb, cxb * (zb * (1.f / kCellScale)));
+  } else if constexpr (R == 1) {
     encm_scales(mode, na, nb, za, zb, cca, cxa, ccb, cxb, sa, sb);
   } else {
     float cc = cca + ccb, cx = cxa + cxb;
@@ -432,10 +457,9 @@ __device__ __forceinline__ void encm_scales_r(int mode, float na, float nb, floa
   }
 }
 
-// Byte offset of a lane's 32 codes (quarter q, coordinates 128 q + 32 t ..)
-// within a packed row.
-template <int B>
-__device__ __forceinline__ int encm_run_bytes(int q, int t) { return q * 16 * B + t * 4 * B; }
+// Byte offset of a lane's 32 codes (coordinates enc_col ..) within a packed row.
+template <int D, int B>
+__device__ __forceinline__ int encm_run_bytes(int q, int t) { return enc_col<D>(q, t) / 8 * B; }
 
 // Encode without outliers: every (group, record, tile) is a task of one warp;
 // warps stride over the tasks with the next task's rows in flight (cp.async,
@@ -445,7 +469,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
   using E = EncM<D, B>;
   constexpr int R = E::R, TPR = E::TPR;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
+  EncMSmem& sm = *reinterpret_cast<EncMSmem*>(smem_raw);
   encm_build(p.c, sm);
   const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
   const float* cent = sm.cent;
@@ -472,7 +496,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
       r = task % per_group;
     }
     k.chunk = p.first_chunk + r / TPR;
-    k.rw = enc_rows<D>((int)(r % TPR), ln.g);
+    k.rw = enc_rows<D>((int)(r % TPR), ln.g, ln.t);
     k.ta = k.chunk * kChunk + k.rw.slot_a;
     k.tb = k.chunk * kChunk + k.rw.slot_b;
     k.va = task < n_tasks && k.ta >= p.first_vec && k.ta < v_end;
@@ -480,9 +504,10 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
     return k;
   };
   auto issue = [&](const Task& k, int buf) {
-    const uint16_t* src = p.src + k.grp * p.src_gs + ln.t * 32;
-    encm_issue(tiles[ln.warp][buf], ln.g, ln.t, src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs + 128 * k.rw.qa,
-               k.va, src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs + 128 * k.rw.qb, k.vb);
+    const uint16_t* src = p.src + k.grp * p.src_gs;
+    encm_issue(tiles[ln.warp][buf], ln.g, ln.t,
+               src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs + enc_col<D>(k.rw.qa, ln.t), k.va,
+               src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs + enc_col<D>(k.rw.qb, ln.t), k.vb);
     cp_async_commit();
   };
   const int64_t stride = (int64_t)gridDim.x * W;
@@ -497,7 +522,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
     encm_read(tiles[ln.warp][it & 1], ln.g, ln.g, ln.t, cur.va, ln.smask[0], wa);
     encm_read(tiles[ln.warp][it & 1], ln.g + 8, ln.g, ln.t, cur.vb, ln.smask[R == 1 ? 0 : 1], wb);
     float na, nb;
-    encm_norms<R>(wa, wb, na, nb);
+    encm_norms<D, R>(wa, wb, na, nb);
     float xa[32], xb[32];
     encm_transform<D, B>(ln, wa, wb, xa, xb);
     encm_quarters<R>(ln.g, xa, xb);
@@ -507,12 +532,12 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
     const float zb = nb > 0.f ? kCellScale / (nb * p.c.sqrt_d) : 0.f;
     float cca = 0.f, cxa = 0.f, ccb = 0.f, cxb = 0.f;
     encm_quantize<B, false, SCALE>(xa, cells, ln.cell_lane, za, 0.f, wd, om, cent, &cca, &cxa);
-    if (cur.va) encm_store_row<B>(rec + (size_t)cur.rw.slot_a * E::RB + encm_run_bytes<B>(cur.rw.qa, ln.t), wd);
+    if (cur.va) encm_store_row<B>(rec + (size_t)cur.rw.slot_a * E::RB + encm_run_bytes<D, B>(cur.rw.qa, ln.t), wd);
     encm_quantize<B, false, SCALE>(xb, cells, ln.cell_lane, zb, 0.f, wd, om, cent, &ccb, &cxb);
-    if (cur.vb) encm_store_row<B>(rec + (size_t)cur.rw.slot_b * E::RB + encm_run_bytes<B>(cur.rw.qb, ln.t), wd);
+    if (cur.vb) encm_store_row<B>(rec + (size_t)cur.rw.slot_b * E::RB + encm_run_bytes<D, B>(cur.rw.qb, ln.t), wd);
     float sca = na, scb = nb;
-    if constexpr (SCALE) encm_scales_r<R>(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
-    if (ln.t == 0) {  // one lane per vector writes its scale
+    if constexpr (SCALE) encm_scales_r<D, R>(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
+    if ((D == 64 ? (ln.t & 1) : ln.t) == 0) {  // one lane per vector writes its scale
       float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
       if constexpr (R == 1) {
         if (cur.va) nrm[cur.rw.slot_a] = sca;
@@ -538,7 +563,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
   using E = EncM<D, B>;
   constexpr int R = E::R, TPR = E::TPR;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
+  EncMSmem& sm = *reinterpret_cast<EncMSmem*>(smem_raw);
   encm_build(p.c, sm);
   const unsigned char* cells = reinterpret_cast<const unsigned char*>(sm.cells);
   const float* cent = sm.cent;
@@ -568,7 +593,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
       k.grp = k.task / p.chunks_per_group;
       k.chunk = p.first_chunk + k.task % p.chunks_per_group;
     }
-    k.rw = enc_rows<D>(k.tile, ln.g);
+    k.rw = enc_rows<D>(k.tile, ln.g, ln.t);
     k.ta = k.chunk * kChunk + k.rw.slot_a;
     k.tb = k.chunk * kChunk + k.rw.slot_b;
     k.va = k.task < n_tasks && k.ta >= p.first_vec && k.ta < v_end;
@@ -576,9 +601,10 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
     return k;
   };
   auto issue = [&](const Unit& k, int buf) {
-    const uint16_t* src = p.src + k.grp * p.src_gs + ln.t * 32;
-    encm_issue(tiles[ln.warp][buf], ln.g, ln.t, src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs + 128 * k.rw.qa,
-               k.va, src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs + 128 * k.rw.qb, k.vb);
+    const uint16_t* src = p.src + k.grp * p.src_gs;
+    encm_issue(tiles[ln.warp][buf], ln.g, ln.t,
+               src + (k.va ? k.ta - p.first_vec : 0) * p.src_vs + enc_col<D>(k.rw.qa, ln.t), k.va,
+               src + (k.vb ? k.tb - p.first_vec : 0) * p.src_vs + enc_col<D>(k.rw.qb, ln.t), k.vb);
     cp_async_commit();
   };
   Unit cur = locate(0);
@@ -596,7 +622,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
     encm_read(tl, ln.g, ln.g, ln.t, va, ln.smask[0], wa);
     encm_read(tl, ln.g + 8, ln.g, ln.t, vb, ln.smask[R == 1 ? 0 : 1], wb);
     float na, nb;
-    encm_norms<R>(wa, wb, na, nb);
+    encm_norms<D, R>(wa, wb, na, nb);
     float xa[32], xb[32];
     encm_transform<D, B>(ln, wa, wb, xa, xb);
     encm_quarters<R>(ln.g, xa, xb);
@@ -610,15 +636,15 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
     const int sw = (ln.t >> 1) ^ ((ln.g & 1) << 1);
     encm_quantize<B, true, SCALE>(xa, cells, ln.cell_lane, za, p.c.thr_out, wd, oma, cent, &cca, &cxa,
                                   &tl.row[ln.g][4 * ln.t], sw, na > 0.f ? 1.0f / (na * p.c.sqrt_d) : 0.f);
-    if (va) encm_store_row<B>(rec + (size_t)cur.rw.slot_a * E::RB + encm_run_bytes<B>(cur.rw.qa, ln.t), wd);
+    if (va) encm_store_row<B>(rec + (size_t)cur.rw.slot_a * E::RB + encm_run_bytes<D, B>(cur.rw.qa, ln.t), wd);
     if (!va) oma = 0u;
     encm_quantize<B, true, SCALE>(xb, cells, ln.cell_lane, zb, p.c.thr_out, wd, omb, cent, &ccb, &cxb,
                                   &tl.row[ln.g + 8][4 * ln.t], sw, nb > 0.f ? 1.0f / (nb * p.c.sqrt_d) : 0.f);
-    if (vb) encm_store_row<B>(rec + (size_t)cur.rw.slot_b * E::RB + encm_run_bytes<B>(cur.rw.qb, ln.t), wd);
+    if (vb) encm_store_row<B>(rec + (size_t)cur.rw.slot_b * E::RB + encm_run_bytes<D, B>(cur.rw.qb, ln.t), wd);
     if (!vb) omb = 0u;
     float sca = na, scb = nb;
-    if constexpr (SCALE) encm_scales_r<R>(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
-    if (ln.t == 0) {  // one lane per vector writes its scale
+    if constexpr (SCALE) encm_scales_r<D, R>(p.c.scale_mode, na, nb, za, zb, cca, cxa, ccb, cxb, sca, scb);
+    if ((D == 64 ? (ln.t & 1) : ln.t) == 0) {  // one lane per vector writes its scale
       float* nrm = reinterpret_cast<float*>(rec + p.c.off_norm);
       if constexpr (R == 1) {
         if (va) nrm[cur.rw.slot_a] = sca;
@@ -627,27 +653,30 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
         if (va && (R == 2 || ln.g < 4)) nrm[cur.rw.slot_a] = sca;
       }
     }
-    // entries before this lane within its row (quad prefix over t), a in
-    // the low and b in the high half-word (at most 128 per row)
+    // entries before this lane within its row's vector (prefix over the
+    // VL lanes of the vector: a quad, a pair at d 64), a in the low and b in
+    // the high half-word (at most 128 per row)
+    constexpr int VL = D == 64 ? 2 : 4;
     const int ca = __popc(oma), cb = __popc(omb);
     uint32_t qp = (uint32_t)ca | ((uint32_t)cb << 16);
 #pragma unroll
-    for (int m = 1; m < 4; m <<= 1) {
-      const uint32_t o = __shfl_up_sync(0xffffffffu, qp, m, 4);
-      if (ln.t >= m) qp += o;
+    for (int m = 1; m < VL; m <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, qp, m, VL);
+      if ((ln.t & (VL - 1)) >= m) qp += o;
     }
     const int ia = (int)(qp & 0xFFFFu), ib = (int)(qp >> 16);
-    const uint32_t qs = __shfl_sync(0xffffffffu, qp, 3, 4);
+    const uint32_t qs = __shfl_sync(0xffffffffu, qp, VL - 1, VL);
     const int nsa = (int)(qs & 0xFFFFu), nsb = (int)(qs >> 16);
     // record-list positions of the lane's first row-a and row-b entries and,
     // for the lane that writes it, a vector's stored count
     int pos_a, pos_b, cnt_a = 0, cnt_b = 0;
     if constexpr (R == 1) {
-      // the tile's 16 vectors in slot order (the a rows g = 0..7, then the b
-      // rows): an inclusive prefix over the quads, whose lanes all hold the quad's sums
+      // the tile's vectors in slot order (those of the a rows, then those of
+      // the b rows): an inclusive prefix over the vectors' lane groups, whose
+      // lanes all hold the group's sums
       uint32_t wp = qs;
 #pragma unroll
-      for (int m = 4; m < 32; m <<= 1) {
+      for (int m = VL; m < 32; m <<= 1) {
         const uint32_t o = __shfl_up_sync(0xffffffffu, wp, m);
         if (ln.lane >= m) wp += o;
       }
@@ -704,7 +733,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
       const int c = v ? cb : ca;
       int pos = v ? pos_b : pos_a;
       uint32_t om = v ? omb : oma;
-      const uint32_t idx0 = (uint32_t)(128 * (v ? cur.rw.qb : cur.rw.qa) + 32 * ln.t);
+      const uint32_t idx0 = (uint32_t)enc_col<D>(v ? cur.rw.qb : cur.rw.qa, ln.t);
       // the lane's stashed values of this row: value j at byte (2 j) ^ swz of its 64 bytes
       const unsigned char* sv = reinterpret_cast<const unsigned char*>(&tl.row[v ? ln.g + 8 : ln.g][4 * ln.t]);
       const int rounds = (int)__reduce_max_sync(0xffffffffu, (unsigned)c);
@@ -716,7 +745,7 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_outl_kernel
         ++pos;
       }
     }
-    if (ln.t == 0) {  // one lane per vector writes its stored count
+    if ((D == 64 ? (ln.t & 1) : ln.t) == 0) {  // one lane per vector writes its stored count
       if constexpr (R == 1) {
         st_global_u8_if(va, rec + p.c.off_count + cur.rw.slot_a, (uint32_t)cnt_a);
         st_global_u8_if(vb, rec + p.c.off_count + cur.rw.slot_b, (uint32_t)cnt_b);

@@ -156,7 +156,6 @@ struct MergeParams {
 // launchers (return the launch status)
 cudaError_t launch_codebook(int bits, int d, uint64_t seed, void* scratch, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams& p, int grid, cudaStream_t s);
-cudaError_t launch_encode_mma(const EncodeParams& p, int grid, cudaStream_t s);  // head dims 128, 256, 512
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t s);
 cudaError_t launch_evict_commit(const EvictCommitParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
