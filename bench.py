@@ -183,23 +183,23 @@ EVICT_WINDOW, EVICT_MARGIN, EVICT_TQ = 128, 16, 1
 # phase whose sources have changed since reports null.  Captures of a reduced
 # layer count are scaled to the full workload by layers (the phase's traffic
 # is a sum over layers).
-# Captured at commit 70dbc83 (profiles/phase_traffic.md): small cases
+# Captured at commit b5dcf1a (profiles/phase_traffic.md): small cases
 # (batched --layers 2, V4-Flash-like --layers 8, long context --layers 1,
 # Qwen2-shaped in full), mean over the captured steps, scaled by layers.
-_T = {"tq_encode": "687a49dd6831c80d", "tq_evict": "827eabaa52b22393", "tq_decode_attn": "8c24ff42d56c7855"}
+_T = {"tq_encode": "eed5d9770a69635b", "tq_evict": "a474b3cbee1e2001", "tq_decode_attn": "acedb33b499af94f"}
 MEASURED_TRAFFIC: dict = {
-    ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_453_402_931, "sources": _T["tq_encode"]},
-    ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_397_082, "sources": _T["tq_evict"]},
-    ("batched_b32_ctx32768", "tq_decode_attn"): {"bytes": 45_092_641_997, "sources": _T["tq_decode_attn"]},
-    ("v4flash_mqa_ctx65536", "tq_encode"): {"bytes": 3_499_790_984, "sources": _T["tq_encode"]},
-    ("v4flash_mqa_ctx65536", "tq_evict"): {"bytes": 5_779_544, "sources": _T["tq_evict"]},
-    ("v4flash_mqa_ctx65536", "tq_decode_attn"): {"bytes": 868_125_349, "sources": _T["tq_decode_attn"]},
-    ("longctx_b4_ctx262144", "tq_encode"): {"bytes": 39_865_548_800, "sources": _T["tq_encode"]},
-    ("longctx_b4_ctx262144", "tq_evict"): {"bytes": 17_127_014, "sources": _T["tq_evict"]},
-    ("longctx_b4_ctx262144", "tq_decode_attn"): {"bytes": 6_100_065_075, "sources": _T["tq_decode_attn"]},
-    ("qwen2_1p5b_ctx2048", "tq_encode"): {"bytes": 46_203_494, "sources": _T["tq_encode"]},
-    ("qwen2_1p5b_ctx2048", "tq_evict"): {"bytes": 2_927_718, "sources": _T["tq_evict"]},
-    ("qwen2_1p5b_ctx2048", "tq_decode_attn"): {"bytes": 22_128_486, "sources": _T["tq_decode_attn"]},
+    ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_463_989_453, "sources": _T["tq_encode"]},
+    ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_510_131, "sources": _T["tq_evict"]},
+    ("batched_b32_ctx32768", "tq_decode_attn"): {"bytes": 45_090_189_312, "sources": _T["tq_decode_attn"]},
+    ("v4flash_mqa_ctx65536", "tq_encode"): {"bytes": 3_493_702_528, "sources": _T["tq_encode"]},
+    ("v4flash_mqa_ctx65536", "tq_evict"): {"bytes": 5_780_576, "sources": _T["tq_evict"]},
+    ("v4flash_mqa_ctx65536", "tq_decode_attn"): {"bytes": 867_505_530, "sources": _T["tq_decode_attn"]},
+    ("longctx_b4_ctx262144", "tq_encode"): {"bytes": 39_890_391_040, "sources": _T["tq_encode"]},
+    ("longctx_b4_ctx262144", "tq_evict"): {"bytes": 17_130_291, "sources": _T["tq_evict"]},
+    ("longctx_b4_ctx262144", "tq_decode_attn"): {"bytes": 6_099_550_618, "sources": _T["tq_decode_attn"]},
+    ("qwen2_1p5b_ctx2048", "tq_encode"): {"bytes": 46_203_802, "sources": _T["tq_encode"]},
+    ("qwen2_1p5b_ctx2048", "tq_evict"): {"bytes": 2_926_746, "sources": _T["tq_evict"]},
+    ("qwen2_1p5b_ctx2048", "tq_decode_attn"): {"bytes": 22_128_333, "sources": _T["tq_decode_attn"]},
 }
 
 PHASE_SOURCES = {
