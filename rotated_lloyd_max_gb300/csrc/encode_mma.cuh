@@ -1,4 +1,5 @@
-// Encode at head dim 128 with the Hadamard transform on the tensor cores.
+// tq_encode's kernels: encode with the Hadamard transform on the tensor
+// cores, at every head dim (128 first; the others below).
 //
 // Same codes as the CUDA-core encoder (n = ||x||; w = H(s . x), the
 // unnormalised Sylvester transform; y = w / (n sqrt(d)); code_j = #{k : y_j > t_k},
@@ -19,7 +20,7 @@
 // (rows g and g + 8 of the MMA tile).
 //
 // Head dims 256 and 512 (R = d/128 quarters of 128 coordinates): with the
-// Sylvester ordering H_d = H_R (x) H128 over the top R - 1 index bits, so the
+// Sylvester ordering H_d = H_R (x) H128 over the top log2 R index bits, so the
 // 16 rows of an MMA tile hold quarters rather than whole vectors -- d 256: rows
 // g and g + 8 are the halves of vector g (8 vectors per tile); d 512: rows g
 // and g + 8 are quarters (g >> 2) and 2 + (g >> 2) of vector g & 3 (4 vectors
@@ -129,7 +130,7 @@ struct EncMLane {
   }
 };
 
-// cp.async staging of 16-vector tiles: a lane copies its own 64 bytes of
+// cp.async staging of 16-row tiles: a lane copies its own 64 bytes of
 // rows g and g + 8 and later reads back exactly those, so no other lane is
 // involved; its 4 chunks sit at swizzled positions so that the 16-byte reads
 // of a quarter-warp (g in {2q, 2q+1}, t in 0..3) hit 8 different bank groups.
@@ -354,8 +355,8 @@ __device__ __forceinline__ void encm_store_row(uint8_t* row, const uint32_t (&wd
   }
 }
 
-// The stored scales of a lane pair's two vectors from the quad sums of
-// ||chat||^2 and <chat, x> (z = 128 / (n sqrt(d)), so <chat, y> = <chat, x> z / 128).
+// (d 128) The stored scales of the vectors of a lane's two rows from the quad
+// sums of ||chat||^2 and <chat, x> (z = 128 / (n sqrt(d)), so <chat, y> = <chat, x> z / 128).
 __device__ __forceinline__ void encm_scales(int mode, float na, float nb, float za, float zb, float cca, float cxa,
                                             float ccb, float cxb, float& sa, float& sb) {
 #pragma unroll
@@ -555,7 +556,8 @@ __global__ void __launch_bounds__(32 * enc_warps<D>(), 1) encode_mma_kernel(cons
 // slot order (the next tile, of this record or the warp's next one, in
 // flight through cp.async as in the kernel above).  Entries land in (slot,
 // index) order without any CTA barrier: a row's lanes take their places by a
-// quad prefix, a vector's rows (quarters) in coordinate order, a tile's
+// prefix over the vector's lanes (a quad, a pair at d 64), a vector's rows
+// (quarters) in coordinate order, a tile's
 // vectors by a warp prefix, and a running warp-uniform offset carries the
 // record's entry count from tile to tile.
 template <int D, int B, bool SCALE>
