@@ -186,7 +186,7 @@ EVICT_WINDOW, EVICT_MARGIN, EVICT_TQ = 128, 16, 1
 # Captured at commit b5dcf1a (profiles/phase_traffic.md): small cases
 # (batched --layers 2, V4-Flash-like --layers 8, long context --layers 1,
 # Qwen2-shaped in full), mean over the captured steps, scaled by layers.
-_T = {"tq_encode": "eed5d9770a69635b", "tq_evict": "a474b3cbee1e2001", "tq_decode_attn": "acedb33b499af94f"}
+_T = {"tq_encode": "a9bd005c7f4cf995", "tq_evict": "a474b3cbee1e2001", "tq_decode_attn": "acedb33b499af94f"}
 MEASURED_TRAFFIC: dict = {
     ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_463_989_453, "sources": _T["tq_encode"]},
     ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_510_131, "sources": _T["tq_evict"]},
