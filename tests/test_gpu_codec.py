@@ -138,16 +138,23 @@ def test_encode_decode_parity(tq, orc, d, bits, mode):
         _check_decode(got, full, f"d {d} b {bits} {mode} group {g}")
 
 
-def test_zero_vectors(tq, orc):
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_zero_vectors(tq, orc, d):
+    """Zero vectors beside a nonzero one in the same tile: code of 0, norm 0,
+    no side-list entries, decoded to exact zeros; the nonzero vector as the oracle."""
     import torch
-    c = tq.tq_make_codebook(3, 128, sign_seed=1, outlier_T=2.0)
-    x = np.zeros((130, 128), np.uint16)
-    x[5] = synth.gaussian_bf16((1, 128), 3)[0]
+    c = tq.tq_make_codebook(3, d, sign_seed=1, outlier_T=2.0)
+    x = np.zeros((130, d), np.uint16)
+    x[5] = synth.gaussian_bf16((1, d), 3)[0]
     rec = _encode_gpu(tq, c, x)[0]
-    codes, norms, outs = tl.unpack_records(rec, 130, 128, 3, True, c.c.outlier_cap)
+    codes, norms, outs = tl.unpack_records(rec, 130, d, 3, True, c.c.outlier_cap)
     zero = np.ones(130, bool); zero[5] = False
     assert np.all(codes[zero] == 3) and np.all(norms[zero] == 0) and all(not outs[i] for i in np.nonzero(zero)[0])
-    dst = torch.empty((130, 128), dtype=torch.float32, device="cuda")
+    enc = orc.encode_vectors(x[5:6], _ocodec(orc, c), want_y=True)
+    tl.check_norms(norms[5:6], enc)
+    tl.check_codes(codes[5:6], enc, orc.codebook_f32(3, d)[1], d, total_frac=None)
+    assert tl.check_outliers([outs[5]], enc, d, 2.0) <= 1
+    dst = torch.empty((130, d), dtype=torch.float32, device="cuda")
     tq.tq_decode(c, torch.from_numpy(rec).cuda(), dst)
     assert torch.all(dst[torch.from_numpy(zero).cuda()] == 0)
 
