@@ -207,7 +207,8 @@ PHASE_SOURCES = {
                   "tq_common.cuh", "tq_params.h", "abi.cu"],
     "tq_evict": ["evict.cu", "encode_core.cuh", "tq_common.cuh", "tq_params.h", "abi.cu"],
     "tq_decode_attn": ["abi.cu", "merge.cu", "umma.cuh", "tq_common.cuh", "tq_params.h",
-                       "attn.cuh", "attn_rec.cuh", "attn_mma.cuh", "attn_mma512.cuh", "attn_umma512.cuh"],
+                       "attn.cuh", "attn_rec.cuh", "attn_mma.cuh", "attn_mma512.cuh", "attn_umma512.cuh",
+                       "attn_dense512.cuh"],
 }
 
 

@@ -325,7 +325,7 @@ typedef enum {
   TQ_ATTN_KERNEL_CUDA_CORE = 1,      /* f32 FMA from the centroid table, CTA-wide softmax per tile */
   TQ_ATTN_KERNEL_CUDA_CORE_WARP = 2, /* f32 FMA, warp-local softmax (head dims 64/128; outlier side lists) */
   TQ_ATTN_KERNEL_MMA = 3,            /* mma.sync f16 hi/lo splits, head dims 64/128 (side lists: sparse-V) */
-  TQ_ATTN_KERNEL_MMA512 = 4,         /* mma.sync f16 hi/lo splits, head dim 512 */
+  TQ_ATTN_KERNEL_MMA512 = 4,         /* mma.sync at head dim 512 (records: f16 hi/lo splits; dense: bf16, 16 heads a CTA) */
   TQ_ATTN_KERNEL_TCGEN05 = 5         /* tcgen05 with tensor-memory accumulators, head dim 512 */
 } tq_attn_kernel;
 

@@ -116,6 +116,7 @@ struct Plan {
   int groups;   // its 4-warp groups per CTA
   bool mma512;  // tensor-core kernel at head dim 512 (mma.sync)
   bool umma512; // tcgen05 kernel at head dim 512 (groups of up to 64 heads per CTA)
+  bool dense512; // their dense splits on the tensor cores (groups of 16 heads per CTA)
   size_t ws_status_off;
 };
 
@@ -214,6 +215,7 @@ tq_status make_plan(const tq_attn_args* a, const tq_codec* kcod, const tq_codec*
     pl->GT = 16;
     pl->n_hg = pl->G / 16;
   }
+  pl->dense512 = (pl->mma512 || pl->umma512) && pl->G % 16 == 0 && tq::attn_dense512_smem_bytes() <= max_dyn_smem();
   const int64_t comp_tiles = pl->has_rec ? a->max_chunks : 0;
   const int TT = 4096 / D;
   const int64_t max_tail = pl->has_tail ? a->max_tail : 0;
@@ -715,7 +717,8 @@ tq_status tq_decode_attn_plan(const tq_attn_args* args, const tq_codec* k_codec,
       break;
     case Route::kD512:
       ck = pl.umma512 ? TQ_ATTN_KERNEL_TCGEN05 : TQ_ATTN_KERNEL_MMA512;
-      dense_gt = std::min(pl.GT, 8);
+      if (pl.dense512) dk = TQ_ATTN_KERNEL_MMA512;
+      dense_gt = pl.dense512 ? 16 : std::min(pl.GT, 8);
       if (St > 0) ++launches;
       break;
     case Route::kWarp:
@@ -838,7 +841,8 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
     }
   } else if (route == Route::kD512) {
     // compressed splits on a d-512 tensor-core kernel, dense splits (if any)
-    // on the general kernel in a second launch (groups of at most 8 heads)
+    // in a second launch: on the tensor cores for groups of a multiple of 16
+    // heads, else on the general kernel (groups of at most 8 heads)
     AttnParams pm = p;
     if (pl.umma512) {
       pm.status = (int*)((char*)workspace + pl.ws_status_off);
@@ -850,7 +854,13 @@ tq_status tq_decode_attn(const tq_attn_args* a, const tq_codec* k_codec, const t
       if (pm.sm_total > max_dyn_smem()) return TQ_ERR_UNSUPPORTED;
       if (launch_attn_mma512(pm, dim3(pl.Sc, units_y, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
     }
-    if (pl.S > pl.Sc) {
+    if (pl.S > pl.Sc && pl.dense512) {
+      AttnParams pd = p;
+      pd.split_base = pl.Sc;
+      pd.n_hg = pl.G / 16;
+      const int uy = a->batch * a->n_kv_heads * pd.n_hg;
+      if (launch_attn_dense512(pd, dim3(pl.S - pl.Sc, uy, a->n_layers), s) != cudaSuccess) return TQ_ERR_CUDA;
+    } else if (pl.S > pl.Sc) {
       AttnParams pd = p;
       pd.split_base = pl.Sc;
       int gt = pl.GT;

@@ -1,5 +1,7 @@
-// Decode-attention instantiations for head dim 512 (query-head groups of 1, 2, 4, 6, 8).
+// Decode-attention instantiations for head dim 512 (query-head groups of 1, 2, 4, 6, 8) and the
+// tensor-core dense-split kernel (groups of 16 query heads).
 #include "attn.cuh"
+#include "attn_dense512.cuh"
 
 namespace tq {
 cudaError_t launch_attn_d512(const AttnParams& p, int GT, dim3 grid, cudaStream_t s) {
@@ -12,4 +14,8 @@ cudaError_t launch_attn_d512(const AttnParams& p, int GT, dim3 grid, cudaStream_
     default: return cudaErrorInvalidValue;
   }
 }
+cudaError_t launch_attn_dense512(const AttnParams& p, dim3 grid, cudaStream_t s) {
+  return attn_dense512_launch(p, grid, s);
+}
+int attn_dense512_smem_bytes() { return attn_dense512_smem(); }
 }  // namespace tq

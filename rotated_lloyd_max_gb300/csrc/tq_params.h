@@ -162,6 +162,10 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_rollback(const RollbackParams& p, cudaStream_t s);
 cudaError_t launch_rollback_commit(const RollbackParams& p, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
+// dense splits of head dim 512 on the tensor cores, 16 query heads per CTA
+// (p.n_hg = G / 16, p.split_base = the first dense split)
+cudaError_t launch_attn_dense512(const AttnParams& p, dim3 grid, cudaStream_t s);
+int attn_dense512_smem_bytes();
 // warp-local kernel for the compressed splits (head dims 64 and 128)
 cudaError_t launch_attn_rec(const AttnParams& p, int D, int GT, dim3 grid, cudaStream_t s);
 // tensor-core kernel for the compressed splits (head dims 64 and 128)

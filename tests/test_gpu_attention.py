@@ -218,6 +218,20 @@ def test_tcgen05_d512_matches_mma_sync(tq, orc):
     assert np.max(np.abs(a - b)) <= 1e-4
 
 
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_d512_dense_tail_tensor_cores(tq, orc, splits):
+    """The tail on the tensor cores (16 heads a CTA, tokens in chunks of 32):
+    ragged lengths over several chunks and splits, a ring that wraps, a batch
+    with a one-token tail, a peaky softmax whose running maximum moves between
+    chunks, two kv heads of 32 heads; the CUDA-core kernel gives the same."""
+    cfg = dict(d=512, G=32, Hkv=2, B=3, L=1, chunks=[1, 2, 1], tails=[301, 33, 1], kb=3, vb=2, end_to_end=False,
+               seed=21, scale=8.0, tail_cap=320, splits=splits)
+    got, want, _ = run_case(tq, orc, **cfg)
+    _assert_close(got, want)
+    ref, _, _ = run_case(tq, orc, cuda_core_path=1, **cfg)
+    assert np.max(np.abs(got - ref)) <= 1e-4
+
+
 # soft cap 4 on logits of scale 6 (about N(0, 36)): most logits are capped.
 # path: 0 automatic (tensor cores where they apply), 1 CUDA cores, 2 no tcgen05
 SOFTCAP_CASES = [("tiny_gqa4_tail", 0), ("tiny_gqa4_tail", 1), ("qwen_like_gqa6", 0),

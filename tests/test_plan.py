@@ -66,13 +66,21 @@ def test_v4flash_mqa_plan(orc, c4_512):
     """43 layers x 510 records + 256 tail tokens, 64 heads on one kv head: the
     tcgen05 kernel at 7 splits of 73 records (the one-CTA-per-SM cost model:
     2 waves x 75 = 150 against 156-174 for its neighbours), the tail in 2 splits
-    of 128 tokens on the CUDA-core kernel (8 heads per CTA), then the merge."""
+    of 128 tokens on the mma.sync dense kernel (16 heads per CTA), then the merge."""
     a = args_for(L=43, B=1, Hq=64, Hkv=1, d=512, records=510, tail=256, shared=True, rec_bytes=128 * 260)
     p = plan(a, c4_512, c4_512)
-    assert p["compressed_kernel"] == "tcgen05" and p["dense_kernel"] == "cuda_core"
+    assert p["compressed_kernel"] == "tcgen05" and p["dense_kernel"] == "mma512"
     assert (p["compressed_splits"], p["records_per_split"]) == (7, 73)
     assert (p["dense_splits"], p["dense_tokens_per_split"]) == (2, 128)
-    assert (p["heads_per_cta"], p["dense_heads_per_cta"], p["launches"]) == (64, 8, 3)
+    assert (p["heads_per_cta"], p["dense_heads_per_cta"], p["launches"]) == (64, 16, 3)
+
+
+def test_d512_dense_splits_fall_back_for_groups_off_sixteen(orc, c4_512):
+    """24 heads a kv head: tcgen05 for the records, but the tail's CTAs need
+    groups of 16 heads on the tensor cores, so it runs 8-head CUDA-core CTAs."""
+    a = args_for(L=2, B=1, Hq=24, Hkv=1, d=512, records=20, tail=256, shared=True, rec_bytes=128 * 260)
+    p = plan(a, c4_512, c4_512)
+    assert (p["compressed_kernel"], p["dense_kernel"], p["dense_heads_per_cta"]) == ("tcgen05", "cuda_core", 8)
 
 
 def test_v4flash_mqa_other_paths(orc, c4_512):
