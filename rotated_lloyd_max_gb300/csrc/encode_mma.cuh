@@ -332,7 +332,7 @@ __device__ __forceinline__ void encm_quantize(const float (&x)[32], const unsign
       const int bit = (r + k) * B;
       wd[bit >> 5] += code[k] << (bit & 31);
       if ((bit & 31) + B > 32) wd[(bit >> 5) + 1] += code[k] >> (32 - (bit & 31));
-      if (OUTL) omask |= mask_gt(fabsf(x[r + k]), Tox) & (1u << (r + k));
+      if (OUTL) omask += mask_gt(fabsf(x[r + k]), Tox) * (0u - (1u << (r + k)));  // distinct bits: + is |
       if constexpr (SCALE) {
         float cj = cent[code[k]];
         if (OUTL && ((omask >> (r + k)) & 1u)) cj = bf16_to_f32(f32_to_bf16_rne(x[r + k] * (scale * (1.f / kCellScale))));
