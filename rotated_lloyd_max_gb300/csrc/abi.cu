@@ -561,7 +561,11 @@ tq_status tq_decode(const tq_codec* codec, const void* src, int64_t n_groups, in
   p.first_chunk = first_vec / TQ_CHUNK;
   p.chunks_per_group = (first_vec + n_vec - 1) / TQ_CHUNK - p.first_chunk + 1;
   const int64_t tasks = n_groups * p.chunks_per_group;
-  const int grid = (int)std::min<int64_t>(tasks, 8LL * num_sms());
+  // fewer records than SMs: split each over up to 4 CTAs (the codec round trip's
+  // 32 records then take 128 CTAs instead of 32); head dim 512 keeps one
+  p.log2_parts = 0;
+  while (p.c.d < 512 && p.log2_parts < 2 && (tasks << p.log2_parts) < num_sms()) ++p.log2_parts;
+  const int grid = (int)std::min<int64_t>(tasks << p.log2_parts, 8LL * num_sms());
   return launch_decode(p, grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -12,11 +12,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane % L, vi = lane / L;
   if (threadIdx.x < 16) lut[threadIdx.x] = p.c.centroids[threadIdx.x & ((1 << B) - 1)];
+  // CTA b takes part b % 2^lp (kChunk >> lp slots) of its records; the grid
+  // is a multiple of 2^lp
+  // (head dim 512 keeps one CTA per record: ptxas 13.0 fails register
+  // allocation on its instantiation with a runtime part count)
+  const int lp = D >= 512 ? 0 : p.log2_parts;
+  const int part = (int)blockIdx.x & ((1 << lp) - 1), per = kChunk >> lp;
   const int64_t n_tasks = p.n_groups * p.chunks_per_group;
-  for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+  for (int64_t task = blockIdx.x >> lp; task < n_tasks; task += gridDim.x >> lp) {
     const int64_t g = task / p.chunks_per_group;
     const int64_t ci = p.first_chunk + task % p.chunks_per_group;
-    const int64_t lo = max(p.first_vec, ci * kChunk), hi = min(p.first_vec + p.n_vec, (ci + 1) * kChunk);
+    const int64_t lo = max(p.first_vec, ci * kChunk + part * per);
+    const int64_t hi = min(p.first_vec + p.n_vec, ci * kChunk + (part + 1) * per);
     const uint8_t* rec = p.src + g * p.src_gs + ci * (int64_t)p.c.rec_bytes;
     float* dst_g = p.dst + g * p.dst_gs;
     __syncthreads();  // lut ready; pre[] of the previous task consumed

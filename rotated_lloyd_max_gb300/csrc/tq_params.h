@@ -103,6 +103,7 @@ struct DecodeParams {
   int64_t dst_vs, dst_gs;  // elements
   int64_t n_groups, n_vec, first_vec;
   int64_t first_chunk, chunks_per_group;
+  int log2_parts;  // 2^log2_parts CTAs per record (1, 2 or 4): few records spread their slots over more SMs
 };
 
 struct AttnParams {

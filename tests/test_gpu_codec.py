@@ -138,6 +138,26 @@ def test_encode_decode_parity(tq, orc, d, bits, mode):
         _check_decode(got, full, f"d {d} b {bits} {mode} group {g}")
 
 
+@pytest.mark.parametrize("n_rec,first,T", [(3, 37, 0.0), (3, 0, 2.0), (40, 0, 2.0), (200, 5, 0.0), (200, 0, 2.0)])
+def test_decode_record_splits(tq, orc, n_rec, first, T):
+    """Decodes of fewer records than SMs split each record over 4 CTAs of 32
+    slots (3 and 40 records); 200 records keep one CTA each. Every slot,
+    including a ragged start and end, decodes as the oracle does from the
+    same records (outlier codecs start at a record boundary)."""
+    import torch
+    d, bits = 128, 3
+    c = tq.tq_make_codebook(bits, d, sign_seed=1, outlier_T=T)
+    oc = _ocodec(orc, c)
+    n = n_rec * 128 - first - 11                      # a ragged end in the last record
+    x = synth.gaussian_bf16((1, n, d), 77 + n_rec, outlier_frac=0.02 if T else 0.0, lognormal_sigma=0.5)
+    rec = _encode_gpu(tq, c, x, first_vec=first)[0]
+    dst = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    tq.tq_decode(c, torch.from_numpy(np.ascontiguousarray(rec)).cuda(), dst, first_vec=first)
+    got = dst.cpu().numpy()
+    want = orc.decode_records(rec, first + n, oc)[first:]
+    _check_decode(got, want, f"{n_rec} records from slot {first}")
+
+
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
 def test_zero_vectors(tq, orc, d):
     """Zero vectors beside a nonzero one in the same tile: code of 0, norm 0,
