@@ -138,7 +138,7 @@ __device__ __forceinline__ uint32_t code_in_row(const unsigned char* row, int id
 }
 
 template <int D, int GT>
-__global__ void __launch_bounds__(kThreads, (GT >= 8 ? 3 : 4)) attn_rec_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kThreads, (GT == 2 || GT == 4) ? 5 : (GT >= 8 ? 3 : 4)) attn_rec_kernel(const __grid_constant__ AttnParams p) {
   using C = RCfg<D, GT>;
   constexpr int GTP = C::GTP, GH = C::GH, SL = C::SL, TPL = C::TPL, QR = C::QR, LPT = C::LPT, TLW = C::TLW;
   extern __shared__ __align__(128) unsigned char sm[];
