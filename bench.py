@@ -183,23 +183,23 @@ EVICT_WINDOW, EVICT_MARGIN, EVICT_TQ = 128, 16, 1
 # phase whose sources have changed since reports null.  Captures of a reduced
 # layer count are scaled to the full workload by layers (the phase's traffic
 # is a sum over layers).
-# Captured at commit 2c6cdb0 (profiles/phase_traffic.md): small cases
+# Captured at commit 54b393f (profiles/phase_traffic.md): small cases
 # (batched --layers 2, V4-Flash-like --layers 8, long context --layers 1,
 # Qwen2-shaped in full), mean over the captured steps, scaled by layers.
-_T = {"tq_encode": "f5ad64cd4cecdc57", "tq_evict": "7945a5bf4ff276af", "tq_decode_attn": "5688178c60b057a6"}
+_T = {"tq_encode": "cf493c19144d20f9", "tq_evict": "cb3934c670ca7e8f", "tq_decode_attn": "4990717f4be6d7ec"}
 MEASURED_TRAFFIC: dict = {
-    ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_462_398_566, "sources": _T["tq_encode"]},
-    ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_398_720, "sources": _T["tq_evict"]},
-    ("batched_b32_ctx32768", "tq_decode_attn"): {"bytes": 45_093_619_302, "sources": _T["tq_decode_attn"]},
-    ("v4flash_mqa_ctx65536", "tq_encode"): {"bytes": 3_493_823_960, "sources": _T["tq_encode"]},
-    ("v4flash_mqa_ctx65536", "tq_evict"): {"bytes": 5_781_264, "sources": _T["tq_evict"]},
-    ("v4flash_mqa_ctx65536", "tq_decode_attn"): {"bytes": 867_511_584, "sources": _T["tq_decode_attn"]},
-    ("longctx_b4_ctx262144", "tq_encode"): {"bytes": 39_890_775_654, "sources": _T["tq_encode"]},
-    ("longctx_b4_ctx262144", "tq_evict"): {"bytes": 17_129_472, "sources": _T["tq_evict"]},
-    ("longctx_b4_ctx262144", "tq_decode_attn"): {"bytes": 6_099_648_922, "sources": _T["tq_decode_attn"]},
-    ("qwen2_1p5b_ctx2048", "tq_encode"): {"bytes": 46_205_286, "sources": _T["tq_encode"]},
-    ("qwen2_1p5b_ctx2048", "tq_evict"): {"bytes": 2_928_282, "sources": _T["tq_evict"]},
-    ("qwen2_1p5b_ctx2048", "tq_decode_attn"): {"bytes": 22_128_282, "sources": _T["tq_decode_attn"]},
+    ("batched_b32_ctx32768", "tq_encode"): {"bytes": 181_461_894_758, "sources": _T["tq_encode"]},
+    ("batched_b32_ctx32768", "tq_evict"): {"bytes": 538_411_827, "sources": _T["tq_evict"]},
+    ("batched_b32_ctx32768", "tq_decode_attn"): {"bytes": 45_096_975_565, "sources": _T["tq_decode_attn"]},
+    ("v4flash_mqa_ctx65536", "tq_encode"): {"bytes": 3_494_490_632, "sources": _T["tq_encode"]},
+    ("v4flash_mqa_ctx65536", "tq_evict"): {"bytes": 5_780_232, "sources": _T["tq_evict"]},
+    ("v4flash_mqa_ctx65536", "tq_decode_attn"): {"bytes": 866_984_370, "sources": _T["tq_decode_attn"]},
+    ("longctx_b4_ctx262144", "tq_encode"): {"bytes": 39_890_091_622, "sources": _T["tq_encode"]},
+    ("longctx_b4_ctx262144", "tq_evict"): {"bytes": 17_132_339, "sources": _T["tq_evict"]},
+    ("longctx_b4_ctx262144", "tq_decode_attn"): {"bytes": 6_100_180_992, "sources": _T["tq_decode_attn"]},
+    ("qwen2_1p5b_ctx2048", "tq_encode"): {"bytes": 46_205_952, "sources": _T["tq_encode"]},
+    ("qwen2_1p5b_ctx2048", "tq_evict"): {"bytes": 2_927_667, "sources": _T["tq_evict"]},
+    ("qwen2_1p5b_ctx2048", "tq_decode_attn"): {"bytes": 22_128_998, "sources": _T["tq_decode_attn"]},
 }
 
 PHASE_SOURCES = {
