@@ -296,6 +296,14 @@ class EvictPhase:
                          n_chunks=self.n_chunks, tail_start=self.tail_start, tail_len=self.tail_len,
                          window=EVICT_WINDOW, margin=EVICT_MARGIN, t_q=EVICT_TQ, max_evict=1)
 
+    def run_layer(self, i: int):
+        """The same call restricted to compressed layer i (the end-to-end leg's pipeline)."""
+        wl, sl = self.wl, slice(i, i + 1)
+        self.tq.tq_evict(wl.kc, wl.vc, k_rec=self.krec[sl], v_rec=self.vrec[sl], k_tail=self.kt[sl],
+                         v_tail=self.vt[sl], n_chunks=self.n_chunks[sl], tail_start=self.tail_start[sl],
+                         tail_len=self.tail_len[sl], window=EVICT_WINDOW, margin=EVICT_MARGIN, t_q=EVICT_TQ,
+                         max_evict=1)
+
     def account(self):
         """Algorithmic bytes of one call: the evicted tokens read (bf16), the
         records written (codes, norms, counts and stored entries)."""
@@ -520,6 +528,23 @@ class CacheWorkload:
     def attention_per_layer(self):
         for a, (kc, vc) in self.args_layer:
             self.tq.tq_decode_attn(a, kc, vc, self.ws)
+
+    def attention_layer(self, l: int):
+        """Decode attention of compressed layer l alone (the end-to-end leg's
+        pipeline: a layer's attention starts once its records are encoded)."""
+        if not hasattr(self, "_args_comp"):
+            self._args_comp = {}
+            for c in self.comp:
+                sl = slice(c, c + 1)
+                kw = dict(q=self.q[sl], out=self.out[sl], scale=1.0, k_rec=self.krec[sl], v_rec=self.vrec[sl],
+                          n_chunks=self.n_chunks[sl], max_chunks=self.n_rec)
+                if self.tail:
+                    kw.update(k_tail=self.kt[sl], v_tail=self.vt[sl], tail_len=self.tail_len[sl],
+                              tail_start=self.tail_start[sl], max_tail=self.tail)
+                a = self.tq.make_attn_args(**kw, sparse_v_eps=self.sparse_v)
+                assert self.tq.tq_decode_attn_workspace_size(a, self.kc, self.vc) <= self.ws.numel()
+                self._args_comp[c] = a
+        self.tq.tq_decode_attn(self._args_comp[l], self.kc, self.vc, self.ws)
 
     def inputs(self):
         """Device tensors a step consumes from the host (leading axis: layer)."""
@@ -1060,20 +1085,27 @@ def e2e_leg(wl, steps: int):
     layer-sized host buffer (every layer receives the same host bytes: the
     copied volume is the full input, the host memory pinned is one layer).
     From 1 GiB of inputs per step the copies run on a copy stream, layer by
-    layer, and each compressed layer is encoded as soon as its K/V have
-    arrived, so the encodes overlap the later layers' copies; eviction and
-    attention wait for every copy.  Smaller steps copy everything first and
-    then run the step (per-layer launches would dominate them)."""
+    layer, and each compressed layer is encoded, evicted and attended as soon
+    as its inputs have arrived (one tq_evict and one tq_decode_attn call per
+    layer, as a model's layer loop issues them), so all three phases overlap
+    the later layers' copies; bf16 layers are attended once every copy is in.
+    Smaller steps copy everything first and then run the step (per-layer
+    launches would dominate them)."""
     import torch
     srcs = wl.inputs()
-    layer_in = {"kx", "vx"}
+    pipelined = sum(t.numel() * t.element_size() for t in srcs.values()) >= E2E_PIPELINE_MIN
+    # inputs copied layer by layer, and the absolute layer of their index 0 (the
+    # pipeline also takes each layer's ring and tail tokens with its K/V)
+    layer_axis = {"kx": 0, "vx": 0}
+    if pipelined:
+        layer_axis.update(kt=0, vt=0, evict_k=wl.c0, evict_v=wl.c0)
     small, per_layer = [], [[] for _ in range(wl.L)]
     for name, t in srcs.items():
         big = t.numel() * t.element_size() > E2E_PIN_LIMIT
-        if name in layer_in:
+        if name in layer_axis:
             h = t[0].cpu().pin_memory() if big else t.cpu().pin_memory()
-            for l in range(wl.L):
-                per_layer[l].append((t[l], h if big else h[l]))
+            for i in range(t.shape[0]):
+                per_layer[layer_axis[name] + i].append((t[i], h if big else h[i]))
         elif big:
             h = t[0].cpu().pin_memory()
             small += [(t[l], h) for l in range(t.shape[0])]
@@ -1083,7 +1115,7 @@ def e2e_leg(wl, steps: int):
     h2d = sum(dv.numel() * dv.element_size() for dv, _ in small + [x for lay in per_layer for x in lay])
     d2h = out_h.numel() * out_h.element_size()
     cur = torch.cuda.current_stream()
-    if h2d < E2E_PIPELINE_MIN:
+    if not pipelined:
         # a small step: copies and the whole-cache encode back to back (a
         # per-layer pipeline would be launch-bound)
         torch.cuda.synchronize()
@@ -1102,32 +1134,37 @@ def e2e_leg(wl, steps: int):
                 "pipeline": "copies, then the step (inputs below 1 GiB)"}
     copy = torch.cuda.Stream()
     arrived = [torch.cuda.Event() for _ in range(wl.L)]
-    start, rest = torch.cuda.Event(), torch.cuda.Event()
+    start, first = torch.cuda.Event(), torch.cuda.Event()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
         start.record(cur)
         copy.wait_event(start)
         with torch.cuda.stream(copy):
+            for dv, h in small:                      # q and other small inputs first
+                dv.copy_(h, non_blocking=True)
+            first.record(copy)
             for l in range(wl.L):
                 for dv, h in per_layer[l]:
                     dv.copy_(h, non_blocking=True)
                 arrived[l].record(copy)
-            for dv, h in small:
-                dv.copy_(h, non_blocking=True)
-            rest.record(copy)
+        cur.wait_event(first)
+        wl.ev.reset()
         for l in wl.comp:
             cur.wait_event(arrived[l])
             wl.encode_layer(l)
-        cur.wait_event(rest)
-        wl.ev.reset(); wl.ev.run()
-        wl.attention()
+            wl.ev.run_layer(l - wl.c0)
+            wl.attention_layer(l)
+        if wl.dense:
+            cur.wait_event(arrived[wl.L - 1])
+            for a, (kc, vc) in [wl.args_layer[l] for l in wl.dense]:
+                wl.tq.tq_decode_attn(a, kc, vc, wl.ws)
         out_h.copy_(wl.out, non_blocking=True)
         cur.synchronize()
     secs = (time.perf_counter() - t0) / steps
     return {"value": round(wl.step_bytes / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(secs * 1e3, 4),
-            "pipeline": "layer copies on a copy stream, each layer encoded on arrival"}
+            "pipeline": "layer copies on a copy stream; each layer encoded, evicted and attended on arrival"}
 
 
 def oracle_unit_sample(cfg: dict):
